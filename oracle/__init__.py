@@ -1,0 +1,218 @@
+"""NVFP4 oracle -- TEST INFRASTRUCTURE ONLY.
+
+A ctypes front end over the plain-C oracle in ``oracle.c``.  Only the test
+suite, ``__graft_entry__.smoke()`` and the benchmark's CPU-baseline leg may
+import this package; the GPU library never does, and shares no code with it.
+Inputs are numpy arrays (BF16 as ``uint16`` bit patterns); outputs are numpy
+arrays.  Every function maps one-to-one onto a C function in ``oracle.c``,
+whose comments cite the passage each step follows.
+"""
+import ctypes
+import os
+
+import numpy as np
+
+from .build import build as _build
+
+_LIB = None
+
+OK, ERR_INVALID_ARG, ERR_UNSUPPORTED_SHAPE, ERR_NONFINITE = 0, 1, 2, 6
+
+
+class OracleError(RuntimeError):
+    def __init__(self, status):
+        super().__init__("oracle status %d" % status)
+        self.status = status
+
+
+class _Cfg(ctypes.Structure):
+    _fields_ = [
+        ("block", ctypes.c_int32),
+        ("rounding", ctypes.c_int32),
+        ("rht", ctypes.c_int32),
+        ("transpose", ctypes.c_int32),
+        ("rht_seed", ctypes.c_uint64),
+        ("sr_seed", ctypes.c_uint64),
+        ("sr_offset", ctypes.c_uint64),
+    ]
+
+
+def _lib():
+    global _LIB
+    if _LIB is None:
+        lib = ctypes.CDLL(_build())
+        P = ctypes.c_void_p
+        I64 = ctypes.c_int64
+        lib.oracle_e2m1_value.restype = ctypes.c_double
+        lib.oracle_e2m1_value.argtypes = [ctypes.c_uint8]
+        lib.oracle_e4m3_value.restype = ctypes.c_double
+        lib.oracle_e4m3_value.argtypes = [ctypes.c_uint8]
+        lib.oracle_e4m3_encode.restype = ctypes.c_uint8
+        lib.oracle_e4m3_encode.argtypes = [ctypes.c_float]
+        lib.oracle_e2m1_encode_rne.restype = ctypes.c_uint8
+        lib.oracle_e2m1_encode_rne.argtypes = [ctypes.c_float]
+        lib.oracle_e2m1_encode_sr.restype = ctypes.c_uint8
+        lib.oracle_e2m1_encode_sr.argtypes = [ctypes.c_float, ctypes.c_uint32]
+        lib.oracle_philox4x32_10.restype = None
+        lib.oracle_philox4x32_10.argtypes = [P, P, P]
+        lib.oracle_rht_signs.restype = None
+        lib.oracle_rht_signs.argtypes = [ctypes.c_uint64, P]
+        lib.oracle_rht16.restype = None
+        lib.oracle_rht16.argtypes = [P, P]
+        lib.oracle_quantize.restype = ctypes.c_int
+        lib.oracle_quantize.argtypes = [P, I64, I64, I64, ctypes.POINTER(_Cfg), P, P, P]
+        lib.oracle_amax.restype = ctypes.c_int
+        lib.oracle_amax.argtypes = [P, I64, I64, I64, ctypes.POINTER(_Cfg), P]
+        lib.oracle_sf_mma_offset.restype = I64
+        lib.oracle_sf_mma_offset.argtypes = [I64, I64, I64]
+        lib.oracle_sf_mma_bytes.restype = I64
+        lib.oracle_sf_mma_bytes.argtypes = [I64, I64]
+        lib.oracle_sf_to_mma.restype = None
+        lib.oracle_sf_to_mma.argtypes = [P, I64, I64, P]
+        lib.oracle_dequantize.restype = None
+        lib.oracle_dequantize.argtypes = [P, P, ctypes.c_float, I64, I64, P]
+        lib.oracle_gemm_f64.restype = None
+        lib.oracle_gemm_f64.argtypes = [P, P, ctypes.c_float, P, P, ctypes.c_float, I64, I64, I64, P]
+        lib.oracle_gemm_f64_sampled.restype = None
+        lib.oracle_gemm_f64_sampled.argtypes = [P, P, ctypes.c_float, P, P, ctypes.c_float,
+                                                I64, P, P, I64, P]
+        _LIB = lib
+    return _LIB
+
+
+def _ptr(a):
+    return ctypes.c_void_p(a.ctypes.data)
+
+
+def make_cfg(block=0, rounding=0, rht=0, transpose=0, rht_seed=0, sr_seed=0, sr_offset=0):
+    return dict(block=block, rounding=rounding, rht=rht, transpose=transpose,
+                rht_seed=rht_seed, sr_seed=sr_seed, sr_offset=sr_offset)
+
+
+def _cfg(cfg):
+    c = make_cfg(**(cfg or {}))
+    return _Cfg(c["block"], c["rounding"], c["rht"], c["transpose"],
+                c["rht_seed"], c["sr_seed"], c["sr_offset"])
+
+
+# --- codecs -----------------------------------------------------------------
+def e2m1_value(code):
+    return _lib().oracle_e2m1_value(int(code))
+
+
+def e4m3_value(byte):
+    return _lib().oracle_e4m3_value(int(byte))
+
+
+def e4m3_encode(t):
+    return _lib().oracle_e4m3_encode(float(t))
+
+
+def e2m1_encode_rne(v):
+    return _lib().oracle_e2m1_encode_rne(float(v))
+
+
+def e2m1_encode_sr(v, r):
+    return _lib().oracle_e2m1_encode_sr(float(v), int(r) & 0xFFFFFFFF)
+
+
+def philox4x32_10(ctr, key):
+    c = np.asarray(ctr, dtype=np.uint32).copy()
+    k = np.asarray(key, dtype=np.uint32).copy()
+    out = np.zeros(4, dtype=np.uint32)
+    _lib().oracle_philox4x32_10(_ptr(c), _ptr(k), _ptr(out))
+    return out
+
+
+def rht_signs(seed):
+    sigma = np.zeros(16, dtype=np.float32)
+    _lib().oracle_rht_signs(int(seed), _ptr(sigma))
+    return sigma
+
+
+def rht16(v, sigma):
+    out = np.ascontiguousarray(v, dtype=np.float32).copy()
+    s = np.ascontiguousarray(sigma, dtype=np.float32)
+    _lib().oracle_rht16(_ptr(out), _ptr(s))
+    return out
+
+
+# --- quantisation -----------------------------------------------------------
+def quantize(x_u16, cfg=None):
+    """x_u16: uint16 [rows, cols] BF16 bit patterns (row-major, may be a
+    strided view along rows).  Returns (codes [qr, qk/2] u8, sf [qr, qk/16]
+    u8 row-major, tensor_scale float32)."""
+    x = np.asarray(x_u16)
+    assert x.dtype == np.uint16 and x.ndim == 2
+    if x.strides[1] != 2:
+        x = np.ascontiguousarray(x)
+    rows, cols = x.shape
+    ld = x.strides[0] // 2 if rows > 1 else cols
+    c = _cfg(cfg)
+    qr, qk = (cols, rows) if c.transpose else (rows, cols)
+    codes = np.zeros((qr, max(qk // 2, 0)), dtype=np.uint8)
+    sf = np.zeros((qr, max(qk // 16, 0)), dtype=np.uint8)
+    ts = np.zeros(1, dtype=np.float32)
+    st = _lib().oracle_quantize(_ptr(x), rows, cols, ld, ctypes.byref(c), _ptr(codes), _ptr(sf), _ptr(ts))
+    if st != OK:
+        raise OracleError(st)
+    return codes, sf, ts[0]
+
+
+def amax(x_u16, cfg=None):
+    x = np.ascontiguousarray(x_u16)
+    rows, cols = x.shape
+    c = _cfg(cfg)
+    out = np.zeros(1, dtype=np.float32)
+    st = _lib().oracle_amax(_ptr(x), rows, cols, cols, ctypes.byref(c), _ptr(out))
+    if st != OK:
+        raise OracleError(st)
+    return out[0]
+
+
+def sf_mma_offset(r, kb, qk):
+    return _lib().oracle_sf_mma_offset(int(r), int(kb), int(qk))
+
+
+def sf_mma_bytes(qr, qk):
+    return _lib().oracle_sf_mma_bytes(int(qr), int(qk))
+
+
+def sf_to_mma(sf, qr, qk):
+    sf = np.ascontiguousarray(sf, dtype=np.uint8)
+    out = np.zeros(sf_mma_bytes(qr, qk), dtype=np.uint8)
+    _lib().oracle_sf_to_mma(_ptr(sf), int(qr), int(qk), _ptr(out))
+    return out
+
+
+def dequantize(codes, sf, tensor_scale, qr, qk):
+    codes = np.ascontiguousarray(codes, dtype=np.uint8)
+    sf = np.ascontiguousarray(sf, dtype=np.uint8)
+    out = np.zeros((qr, qk), dtype=np.float64)
+    _lib().oracle_dequantize(_ptr(codes), _ptr(sf), float(tensor_scale), int(qr), int(qk), _ptr(out))
+    return out
+
+
+def gemm_f64(a, b, M, N, K):
+    """a, b: (codes, sf_rowmajor, tensor_scale) of A [M, K] and B [N, K]."""
+    ac, asf, ascale = a
+    bc, bsf, bscale = b
+    ac, asf = np.ascontiguousarray(ac), np.ascontiguousarray(asf)
+    bc, bsf = np.ascontiguousarray(bc), np.ascontiguousarray(bsf)
+    out = np.zeros((M, N), dtype=np.float64)
+    _lib().oracle_gemm_f64(_ptr(ac), _ptr(asf), float(ascale), _ptr(bc), _ptr(bsf), float(bscale),
+                           int(M), int(N), int(K), _ptr(out))
+    return out
+
+
+def gemm_f64_sampled(a, b, K, m_idx, n_idx):
+    ac, asf, ascale = a
+    bc, bsf, bscale = b
+    ac, asf = np.ascontiguousarray(ac), np.ascontiguousarray(asf)
+    bc, bsf = np.ascontiguousarray(bc), np.ascontiguousarray(bsf)
+    mi = np.ascontiguousarray(m_idx, dtype=np.int64)
+    ni = np.ascontiguousarray(n_idx, dtype=np.int64)
+    out = np.zeros(mi.shape[0], dtype=np.float64)
+    _lib().oracle_gemm_f64_sampled(_ptr(ac), _ptr(asf), float(ascale), _ptr(bc), _ptr(bsf), float(bscale),
+                                   int(K), _ptr(mi), _ptr(ni), int(mi.shape[0]), _ptr(out))
+    return out

@@ -1,0 +1,375 @@
+/*
+ * NVFP4 oracle -- TEST INFRASTRUCTURE ONLY (see oracle.h for scope, sources
+ * and the list of pins).  Plain C, single-threaded, no vectorisation tricks.
+ *
+ * Build with contraction disabled (-ffp-contract=off) and without fast-math:
+ * every FP32 step below is one IEEE round-to-nearest-even operation, which is
+ * what makes the quantised codes a deterministic function of the input.
+ */
+#include "oracle.h"
+
+#include <math.h>
+#include <stdlib.h>
+#include <string.h>
+
+/* ------------------------------------------------------------------------- */
+/* E2M1 element codes.                                                        */
+/* The 4-bit grid is sparse ("NVIDIA acelera o pre-treinamento de LLM: NVFP4  */
+/* no Blackwell...", section "Por que cada porcento e importante"); its eight */
+/* magnitudes are 0, 0.5, 1, 1.5, 2, 3, 4, 6.  Bit 3 is the sign, bits 2..0   */
+/* index the magnitude (sign-magnitude, exponent bits 2:1, mantissa bit 0).   */
+/* ------------------------------------------------------------------------- */
+static const double k_e2m1_mag[8] = {0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0};
+
+double oracle_e2m1_value(uint8_t code) {
+  double m = k_e2m1_mag[code & 7];
+  return (code & 8) ? -m : m;
+}
+
+/* E4M3 (FP8, 1 sign, 4 exponent bits with bias 7, 3 mantissa bits, no      */
+/* infinities, S.1111.111 is NaN, largest finite 448, subnormals m * 2^-9).  */
+double oracle_e4m3_value(uint8_t byte) {
+  int sign = (byte >> 7) & 1;
+  int e = (byte >> 3) & 15;
+  int m = byte & 7;
+  double v;
+  if (e == 15 && m == 7) return NAN;
+  if (e == 0)
+    v = ldexp((double)m, -9);
+  else
+    v = ldexp(1.0 + m / 8.0, e - 7);
+  return sign ? -v : v;
+}
+
+/* Nearest candidate to t >= 0 among ascending values[0..n-1] (all finite),
+ * ties going to the candidate whose code has a clear lowest bit ("even
+ * mantissa").  Values above the largest candidate pick the largest, which is
+ * saturation.  Comparisons are done in double, where the two bracketing
+ * candidates and t are exact and their differences are exact. */
+static int nearest_even(double t, const double* values, const uint8_t* codes, int n) {
+  int hi = 0;
+  if (t >= values[n - 1]) return n - 1;
+  while (values[hi] <= t) hi++;          /* values[hi] > t >= values[hi-1] */
+  if (hi == 0) return 0;
+  int lo = hi - 1;
+  double dlo = t - values[lo], dhi = values[hi] - t;
+  if (dlo < dhi) return lo;
+  if (dhi < dlo) return hi;
+  return (codes[lo] & 1) ? hi : lo;
+}
+
+static double k_e4m3_values[127];
+static uint8_t k_e4m3_codes[127];
+static int k_e4m3_ready = 0;
+
+static void e4m3_table(void) {
+  /* Bytes 0x00..0x7E are the non-negative finite E4M3 values in ascending
+   * order (the encoding is monotone in the byte for a fixed sign). */
+  if (k_e4m3_ready) return;
+  for (int b = 0; b < 127; ++b) {
+    k_e4m3_codes[b] = (uint8_t)b;
+    k_e4m3_values[b] = oracle_e4m3_value((uint8_t)b);
+  }
+  k_e4m3_ready = 1;
+}
+
+/* Block-scale encoding: t (>= 0, finite) to the nearest E4M3 value, ties to
+ * even mantissa, saturating at 448, subnormals kept (reading: the format
+ * definition names an E4M3 scale and nothing else; this is the IEEE-style
+ * choice). */
+uint8_t oracle_e4m3_encode(float t) {
+  e4m3_table();
+  if (!(t >= 0.0f)) return 0;            /* never reached for valid input */
+  return k_e4m3_codes[nearest_even((double)t, k_e4m3_values, k_e4m3_codes, 127)];
+}
+
+static const uint8_t k_e2m1_codes[8] = {0, 1, 2, 3, 4, 5, 6, 7};
+
+/* Round-to-nearest-even onto the E2M1 grid.  Ties go to the even code, which
+ * gives 0.25->0, 0.75->1, 1.25->1, 1.75->2, 2.5->2, 3.5->4, 5->4; magnitudes
+ * above 6 saturate to 6.  The sign is the sign bit of v, so a negative value
+ * that rounds to zero is encoded 0x8 (reading: IEEE-style signed zero). */
+uint8_t oracle_e2m1_encode_rne(float v) {
+  double mag = fabs((double)v);
+  uint8_t code = k_e2m1_codes[nearest_even(mag, k_e2m1_mag, k_e2m1_codes, 8)];
+  return (uint8_t)(code | (signbit(v) ? 8 : 0));
+}
+
+/* Stochastic rounding onto the E2M1 grid (reading): for lo <= |v| < hi,
+ * adjacent grid points, f = (|v| - lo) / (hi - lo) computed in FP32 (exact:
+ * hi - lo is a power of two and |v| - lo is exact by Sterbenz' lemma);
+ * u = (r >> 8) * 2^-24 from one 32-bit Philox word; round up iff u < f.
+ * |v| >= 6 gives 6.  The sign is kept as in round-to-nearest. */
+uint8_t oracle_e2m1_encode_sr(float v, uint32_t r) {
+  float mag = fabsf(v);
+  uint8_t code;
+  if (mag >= 6.0f) {
+    code = 7;
+  } else {
+    int lo = 0;
+    while (lo < 7 && k_e2m1_mag[lo + 1] <= (double)mag) lo++;
+    float lo_v = (float)k_e2m1_mag[lo];
+    float step = (float)(k_e2m1_mag[lo + 1] - k_e2m1_mag[lo]);
+    float f = (mag - lo_v) / step;
+    float u = (float)(r >> 8) * 0x1p-24f;
+    code = (uint8_t)((u < f) ? lo + 1 : lo);
+  }
+  return (uint8_t)(code | (signbit(v) ? 8 : 0));
+}
+
+/* ------------------------------------------------------------------------- */
+/* Philox4x32-10 (Salmon, Moraes, Dror, Shaw, "Parallel Random Numbers: As    */
+/* Easy as 1, 2, 3", SC'11): ten rounds of two 32x32->64 multiplies, the      */
+/* key bumped by the Weyl constants between rounds.                          */
+/* ------------------------------------------------------------------------- */
+void oracle_philox4x32_10(const uint32_t ctr[4], const uint32_t key[2], uint32_t out[4]) {
+  uint32_t c0 = ctr[0], c1 = ctr[1], c2 = ctr[2], c3 = ctr[3];
+  uint32_t k0 = key[0], k1 = key[1];
+  for (int round = 0; round < 10; ++round) {
+    uint64_t p0 = (uint64_t)0xD2511F53u * (uint64_t)c0;
+    uint64_t p1 = (uint64_t)0xCD9E8D57u * (uint64_t)c2;
+    uint32_t hi0 = (uint32_t)(p0 >> 32), lo0 = (uint32_t)p0;
+    uint32_t hi1 = (uint32_t)(p1 >> 32), lo1 = (uint32_t)p1;
+    uint32_t n0 = hi1 ^ c1 ^ k0;
+    uint32_t n1 = lo1;
+    uint32_t n2 = hi0 ^ c3 ^ k1;
+    uint32_t n3 = lo0;
+    c0 = n0; c1 = n1; c2 = n2; c3 = n3;
+    k0 += 0x9E3779B9u;
+    k1 += 0xBB67AE85u;
+  }
+  out[0] = c0; out[1] = c1; out[2] = c2; out[3] = c3;
+}
+
+/* ------------------------------------------------------------------------- */
+/* Random Hadamard transform ("Full-Stack FP4...", section 2.2: Hadamard      */
+/* mixing spreads the distribution before quantisation).                     */
+/* Reading: sigma_j = -1 iff bit j of word 0 of Philox(key = seed,           */
+/* counter = 0); x' = 1/4 * H16 * diag(sigma) * x, with H16 the Sylvester    */
+/* Hadamard matrix, evaluated as butterflies of stride 1, 2, 4, 8 (each      */
+/* output a+b or a-b rounded to FP32), then the exact scaling by 1/4.        */
+/* ------------------------------------------------------------------------- */
+void oracle_rht_signs(uint64_t seed, float sigma[16]) {
+  uint32_t ctr[4] = {0, 0, 0, 0};
+  uint32_t key[2] = {(uint32_t)seed, (uint32_t)(seed >> 32)};
+  uint32_t out[4];
+  oracle_philox4x32_10(ctr, key, out);
+  for (int j = 0; j < 16; ++j) sigma[j] = ((out[0] >> j) & 1u) ? -1.0f : 1.0f;
+}
+
+void oracle_rht16(float v[16], const float sigma[16]) {
+  for (int j = 0; j < 16; ++j) v[j] = v[j] * sigma[j];
+  for (int stride = 1; stride < 16; stride *= 2) {
+    for (int i = 0; i < 16; ++i) {
+      if (i & stride) continue;
+      float a = v[i], b = v[i + stride];
+      v[i] = a + b;
+      v[i + stride] = a - b;
+    }
+  }
+  for (int j = 0; j < 16; ++j) v[j] = v[j] * 0.25f;
+}
+
+/* ------------------------------------------------------------------------- */
+/* Quantisation                                                               */
+/* ------------------------------------------------------------------------- */
+static float bf16_to_float(uint16_t b) {
+  uint32_t u = (uint32_t)b << 16;
+  float f;
+  memcpy(&f, &u, 4);
+  return f;
+}
+
+/* Materialise the quantised operand Q [qr, qk] as FP32: Q = x or x^T, then the
+ * optional transform on each run of 16 along K.  Returns NULL on OOM. */
+static float* logical_operand(const uint16_t* x, int64_t rows, int64_t cols, int64_t ld,
+                              const oracle_cfg* cfg, int64_t* qr, int64_t* qk) {
+  int64_t R = cfg->transpose ? cols : rows;
+  int64_t K = cfg->transpose ? rows : cols;
+  *qr = R;
+  *qk = K;
+  float* q = (float*)malloc((size_t)(R * K + 1) * sizeof(float));
+  if (!q) return NULL;
+  for (int64_t i = 0; i < R; ++i)
+    for (int64_t k = 0; k < K; ++k)
+      q[i * K + k] = cfg->transpose ? bf16_to_float(x[k * ld + i]) : bf16_to_float(x[i * ld + k]);
+  if (cfg->rht) {
+    float sigma[16];
+    oracle_rht_signs(cfg->rht_seed, sigma);
+    for (int64_t i = 0; i < R; ++i)
+      for (int64_t k = 0; k < K; k += 16) oracle_rht16(&q[i * K + k], sigma);
+  }
+  return q;
+}
+
+static int check_args(int64_t rows, int64_t cols, int64_t ld, const oracle_cfg* cfg) {
+  if (!cfg || rows < 0 || cols < 0 || ld < cols) return ORACLE_ERR_INVALID_ARG;
+  if (cfg->block < 0 || cfg->block > 1 || cfg->rounding < 0 || cfg->rounding > 1)
+    return ORACLE_ERR_INVALID_ARG;
+  int64_t R = cfg->transpose ? cols : rows;
+  int64_t K = cfg->transpose ? rows : cols;
+  if (K % 16 != 0) return ORACLE_ERR_UNSUPPORTED_SHAPE;
+  if (cfg->block == 1 && R % 16 != 0) return ORACLE_ERR_UNSUPPORTED_SHAPE;
+  return ORACLE_OK;
+}
+
+static float amax_of(const float* q, int64_t n) {
+  float amax = 0.0f;
+  for (int64_t i = 0; i < n; ++i) {
+    float a = fabsf(q[i]);
+    if (isnan(a)) return NAN;
+    if (a > amax) amax = a;
+  }
+  return amax;
+}
+
+int oracle_amax(const uint16_t* x, int64_t rows, int64_t cols, int64_t ld,
+                const oracle_cfg* cfg, float* amax) {
+  int st = check_args(rows, cols, ld, cfg);
+  if (st != ORACLE_OK) return st;
+  int64_t R = 0, K = 0;
+  float* q = logical_operand(x, rows, cols, ld, cfg, &R, &K);
+  if (!q) return ORACLE_ERR_INVALID_ARG;
+  *amax = amax_of(q, R * K);
+  free(q);
+  return ORACLE_OK;
+}
+
+int oracle_quantize(const uint16_t* x, int64_t rows, int64_t cols, int64_t ld,
+                    const oracle_cfg* cfg, uint8_t* codes, uint8_t* sf, float* tensor_scale) {
+  int st = check_args(rows, cols, ld, cfg);
+  if (st != ORACLE_OK) return st;
+  int64_t R = 0, K = 0;
+  float* q = logical_operand(x, rows, cols, ld, cfg, &R, &K);
+  if (!q) return ORACLE_ERR_INVALID_ARG;
+  int64_t KB = K / 16;
+
+  /* Step 1: tensor amax, taken after the transform (reading). */
+  float amax = amax_of(q, R * K);
+  if (!isfinite(amax)) {
+    free(q);
+    return ORACLE_ERR_NONFINITE;
+  }
+  /* Step 2: FP32 tensor (decode) scale s = amax / (6 * 448): the largest
+   * block can then reach both the largest E4M3 scale and the largest E2M1
+   * element (reading).  A zero scale (all-zero or subnormal-tiny tensor)
+   * is replaced by 1, which makes every block scale and every code zero. */
+  float s_dec = amax / 2688.0f;
+  if (s_dec == 0.0f) s_dec = 1.0f;
+  *tensor_scale = s_dec;
+
+  memset(codes, 0, (size_t)(R * (K / 2)));
+  for (int64_t i = 0; i < R; ++i) {
+    for (int64_t b = 0; b < KB; ++b) {
+      /* Step 3: block amax over the 1x16 run, or over the whole 16x16 tile
+       * the run belongs to (its scale is then repeated on the tile's 16 rows). */
+      float bamax = 0.0f;
+      int64_t r0 = (cfg->block == 1) ? (i / 16) * 16 : i;
+      int64_t r1 = (cfg->block == 1) ? r0 + 16 : i + 1;
+      for (int64_t r = r0; r < r1; ++r)
+        for (int64_t k = b * 16; k < b * 16 + 16; ++k) {
+          float a = fabsf(q[r * K + k]);
+          if (a > bamax) bamax = a;
+        }
+      /* Step 4: block scale t = (bamax / 6) / s, two FP32 divisions, then
+       * E4M3 round-to-nearest-even with saturation. */
+      float t = (bamax / 6.0f) / s_dec;
+      uint8_t sfb = oracle_e4m3_encode(t);
+      sf[i * KB + b] = sfb;
+      /* Step 5: elements v = x / (scale * s), one FP32 multiply then one FP32
+       * division, rounded onto the E2M1 grid.  A zero block scale encodes the
+       * whole run as code 0. */
+      float denom = (float)oracle_e4m3_value(sfb) * s_dec;
+      for (int64_t k = b * 16; k < b * 16 + 16; ++k) {
+        uint8_t code = 0;
+        if (sfb != 0) {
+          float v = q[i * K + k] / denom;
+          if (cfg->rounding == 0) {
+            code = oracle_e2m1_encode_rne(v);
+          } else {
+            /* Philox counter for element e = i*K + k of Q: (e >> 2 as a 64-bit
+             * pair, sr_offset as a 64-bit pair), key = sr_seed; word e & 3. */
+            uint64_t e = (uint64_t)(i * K + k);
+            uint32_t ctr[4] = {(uint32_t)(e >> 2), (uint32_t)(e >> 34),
+                               (uint32_t)cfg->sr_offset, (uint32_t)(cfg->sr_offset >> 32)};
+            uint32_t key[2] = {(uint32_t)cfg->sr_seed, (uint32_t)(cfg->sr_seed >> 32)};
+            uint32_t out[4];
+            oracle_philox4x32_10(ctr, key, out);
+            code = oracle_e2m1_encode_sr(v, out[e & 3]);
+          }
+        }
+        /* Packing: element 2j in the low nibble of byte j, 2j+1 in the high. */
+        codes[i * (K / 2) + k / 2] |= (uint8_t)(code << (4 * (k & 1)));
+      }
+    }
+  }
+  free(q);
+  return ORACLE_OK;
+}
+
+/* ------------------------------------------------------------------------- */
+/* Tensor-core scale layout: the operand's scales are cut into atoms of 128  */
+/* rows x 4 scales (64 elements of K), 512 bytes each, atoms ordered by row   */
+/* block then K block; inside an atom, scale (r, j) sits at byte              */
+/* (r % 32) * 16 + (r / 32) * 4 + j.  Rows and scale columns beyond the      */
+/* operand are padding and hold zero.                                        */
+/* ------------------------------------------------------------------------- */
+int64_t oracle_sf_mma_bytes(int64_t qr, int64_t qk) {
+  int64_t row_atoms = (qr + 127) / 128;
+  int64_t k_atoms = (qk / 16 + 3) / 4;
+  return row_atoms * k_atoms * 512;
+}
+
+int64_t oracle_sf_mma_offset(int64_t r, int64_t kb, int64_t qk) {
+  int64_t k_atoms = (qk / 16 + 3) / 4;
+  int64_t atom = (r / 128) * k_atoms + kb / 4;
+  int64_t rr = r % 128;
+  return atom * 512 + (rr % 32) * 16 + (rr / 32) * 4 + (kb % 4);
+}
+
+void oracle_sf_to_mma(const uint8_t* sf, int64_t qr, int64_t qk, uint8_t* out) {
+  memset(out, 0, (size_t)oracle_sf_mma_bytes(qr, qk));
+  for (int64_t r = 0; r < qr; ++r)
+    for (int64_t kb = 0; kb < qk / 16; ++kb) out[oracle_sf_mma_offset(r, kb, qk)] = sf[r * (qk / 16) + kb];
+}
+
+/* ------------------------------------------------------------------------- */
+/* Dequantisation and the reference GEMM (FP64; the accumulators of the NVFP4 */
+/* GEMM are FP32 per "NVIDIA acelera...", "Como o treinamento mixed-precision */
+/* funciona com NVFP4", so FP64 is the exact-enough reference).               */
+/* ------------------------------------------------------------------------- */
+static double deq(const uint8_t* codes, const uint8_t* sf, double s, int64_t qk, int64_t i, int64_t k) {
+  uint8_t byte = codes[i * (qk / 2) + k / 2];
+  uint8_t code = (k & 1) ? (byte >> 4) : (byte & 15);
+  return oracle_e2m1_value(code) * oracle_e4m3_value(sf[i * (qk / 16) + k / 16]) * s;
+}
+
+void oracle_dequantize(const uint8_t* codes, const uint8_t* sf, float tensor_scale,
+                       int64_t qr, int64_t qk, double* out) {
+  for (int64_t i = 0; i < qr; ++i)
+    for (int64_t k = 0; k < qk; ++k) out[i * qk + k] = deq(codes, sf, tensor_scale, qk, i, k);
+}
+
+void oracle_gemm_f64(const uint8_t* a_codes, const uint8_t* a_sf, float a_scale,
+                     const uint8_t* b_codes, const uint8_t* b_sf, float b_scale,
+                     int64_t M, int64_t N, int64_t K, double* out) {
+  for (int64_t m = 0; m < M; ++m)
+    for (int64_t n = 0; n < N; ++n) {
+      double acc = 0.0;
+      for (int64_t k = 0; k < K; ++k)
+        acc += deq(a_codes, a_sf, a_scale, K, m, k) * deq(b_codes, b_sf, b_scale, K, n, k);
+      out[m * N + n] = acc;
+    }
+}
+
+void oracle_gemm_f64_sampled(const uint8_t* a_codes, const uint8_t* a_sf, float a_scale,
+                             const uint8_t* b_codes, const uint8_t* b_sf, float b_scale,
+                             int64_t K, const int64_t* m_idx, const int64_t* n_idx,
+                             int64_t count, double* out) {
+  for (int64_t c = 0; c < count; ++c) {
+    double acc = 0.0;
+    for (int64_t k = 0; k < K; ++k)
+      acc += deq(a_codes, a_sf, a_scale, K, m_idx[c], k) * deq(b_codes, b_sf, b_scale, K, n_idx[c], k);
+    out[c] = acc;
+  }
+}
