@@ -1,0 +1,380 @@
+"""Benchmark: NVFP4 linear layer (quantise + GEMM), fprop + dgrad + wgrad.
+
+One step = one pass of the whole hot path over the 12B-hybrid-shaped MLP
+up-projection (tokens 8192 = 4 x 2048, hidden 5120, FFN 20480): quantise
+X, W, dY in the orientation each GEMM needs (1x16 activations/gradients,
+16x16 weights, transform + stochastic rounding on the wgrad operands), then
+the three block-scaled FP4 GEMMs with BF16 outputs.  Inputs are synthetic
+BF16 tensors resident in HBM (629 MB per step, larger than L2).
+
+Prints one JSON line.  `--impl reference` times the CPU oracle (the plain C
+statement of the same arithmetic) on a bounded sample of the same workload.
+"""
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "NVFP4 linear TFLOP/s (quantize+GEMM) and quantize GB/s, % of GB300 roofline"
+T, HID, FFN = 8192, 5120, 20480
+GEMM_FLOP = 2.0 * T * HID * FFN  # each of fprop, dgrad, wgrad
+STEP_FLOP = 3 * GEMM_FLOP
+FP4_OVER_BF16 = 13.5 / 2.25  # nominal dense FP4 : BF16 tensor ratio on GB300
+QUANT_BYTES_PER_ELT = 2.0 + 0.5 + 1.0 / 16  # read BF16, write codes + block scales
+WORKLOAD = ("12B-hybrid MLP up-projection fprop+dgrad+wgrad, tokens 8192 (4x2048), hidden 5120, FFN 20480; "
+            "X N(0,1), W N(0,0.02), dY N(0,1e-3); W 16x16, X/dY 1x16, wgrad operands RHT+SR")
+
+
+def _config():
+    return {"workload": WORKLOAD, "tokens": T, "hidden": HID, "ffn": FFN, "out_dtype": "bf16",
+            "l2": "inputs larger than L2 (X+W+dY = 629 MB BF16 per step)"}
+
+
+def _peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return p, "measured"
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling during the timed region."""
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), "--query-gpu=" + q,
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        try:
+            with open(self.path) as f:
+                for line in f:
+                    parts = [p.strip() for p in line.split(",")]
+                    if len(parts) < 9:
+                        continue
+                    try:
+                        sm.append(float(parts[1]))
+                        smax.append(float(parts[2]))
+                    except ValueError:
+                        continue
+                    for n, v in zip(names, parts[5:9]):
+                        if v.lower() == "active":
+                            reasons.add(n)
+            os.unlink(self.path)
+        except OSError:
+            pass
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        loaded = sorted(sm)[len(sm) // 4:] or sm  # drop the idle head of the window
+        return {"sm_mhz": statistics.median(loaded), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def _dist():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+# --------------------------------------------------------------------- ours
+def run_ours(args):
+    import torch
+
+    import block_scaled_gemm_nvfp4_gb300 as nv
+    from block_scaled_gemm_nvfp4_gb300 import synthetic as syn
+
+    world, rank, local = _dist()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl", device_id=dev)
+        pg = dist
+    nv.lib()
+
+    x_c, w_c, dy_c = syn.config2()
+    x, w, dy = x_c.to(dev), w_c.to(dev), dy_c.to(dev)
+
+    s = nv.NVFP4_DEFAULT_RHT_SEED
+    roles = {
+        # (source, cfg) for the A and B operands of each GEMM
+        "fprop": ((x, nv.quant_cfg(block=0)), (w, nv.quant_cfg(block=1))),
+        "dgrad": ((dy, nv.quant_cfg(block=0)), (w, nv.quant_cfg(block=1, transpose=1))),
+        "wgrad": ((dy, nv.quant_cfg(rounding=1, rht=1, transpose=1, rht_seed=s, sr_seed=5)),
+                  (x, nv.quant_cfg(rounding=1, rht=1, transpose=1, rht_seed=s, sr_seed=6))),
+    }
+    outs = {"fprop": torch.empty((T, FFN), dtype=torch.bfloat16, device=dev),
+            "dgrad": torch.empty((T, HID), dtype=torch.bfloat16, device=dev),
+            "wgrad": torch.empty((FFN, HID), dtype=torch.bfloat16, device=dev)}
+    # preallocated quantised operands and workspaces (the library never allocates)
+    qbufs, wss = {}, {}
+    for op, pair in roles.items():
+        qbufs[op] = []
+        for src, cfg in pair:
+            r, c = src.shape
+            qr, qk = (c, r) if cfg.transpose else (r, c)
+            qbufs[op].append(nv.NVFP4Tensor(
+                codes=torch.empty((qr, qk // 2), dtype=torch.uint8, device=dev),
+                sf=torch.empty(nv.nvfp4_sf_bytes(qr, qk, nv.NVFP4_SF_MMA), dtype=torch.uint8, device=dev),
+                tensor_scale=torch.empty(1, dtype=torch.float32, device=dev), rows=qr, k=qk,
+                sf_layout=nv.NVFP4_SF_MMA))
+        wss[op] = torch.zeros(nv.nvfp4_quantize_workspace_size(T, FFN, roles[op][0][1]) + (1 << 16),
+                              dtype=torch.uint8, device=dev)
+
+    stream = torch.cuda.current_stream()
+    gemm_events = []
+    quant_events = []
+
+    def step(record):
+        for op, pair in roles.items():
+            if record:
+                q0 = torch.cuda.Event(enable_timing=True)
+                q0.record(stream)
+            for (src, cfg), qb in zip(pair, qbufs[op]):
+                nv.nvfp4_quantize(src, cfg, out=qb, workspace=wss[op])
+            if record:
+                g0 = torch.cuda.Event(enable_timing=True)
+                g1 = torch.cuda.Event(enable_timing=True)
+                g0.record(stream)
+            nv.nvfp4_gemm(qbufs[op][0], qbufs[op][1], out_dtype=nv.NVFP4_OUT_BF16, d=outs[op], workspace=wss[op])
+            if record:
+                g1.record(stream)
+                quant_events.append((q0, g0))
+                gemm_events.append((g0, g1))
+
+    for _ in range(args.warmup):
+        step(False)
+    torch.cuda.synchronize()
+    if pg:
+        pg.barrier()
+    with ClockSampler(local) as clocks:
+        torch.cuda.synchronize()
+        if pg:
+            pg.barrier()
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        t0.record(stream)
+        for _ in range(args.steps):
+            step(True)
+        t1.record(stream)
+        torch.cuda.synchronize()
+        if pg:
+            pg.barrier()
+    ms_total = t0.elapsed_time(t1)
+    for op in roles:
+        st = nv.nvfp4_check_device_status(wss[op])
+        if st != nv.NVFP4_OK:
+            raise RuntimeError("device status %s after %s" % (nv.nvfp4_status_string(st), op))
+    if pg:
+        t = torch.tensor([ms_total], device=dev)
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        ms_total = t.item()
+    ms_step = ms_total / args.steps
+    value = world * STEP_FLOP / (ms_step * 1e-3) / 1e12
+
+    gemm_ms = statistics.mean(a.elapsed_time(b) for a, b in gemm_events)
+    quant_ms = statistics.mean(a.elapsed_time(b) for a, b in quant_events)  # two quantises per GEMM
+    peaks, src = _peaks()
+    peak_fp4 = peaks["bf16_tflops"] * FP4_OVER_BF16
+    achieved = GEMM_FLOP / (gemm_ms * 1e-3) / 1e12
+    # quantised elements per GEMM pass: fprop X + W, dgrad dY + W, wgrad dY + X (same total each pass on average)
+    q_elts = {"fprop": T * HID + FFN * HID, "dgrad": T * FFN + FFN * HID, "wgrad": T * FFN + T * HID}
+    q_bytes = statistics.mean(q_elts.values()) * QUANT_BYTES_PER_ELT
+    quant_gbs = q_bytes / (quant_ms * 1e-3) / 1e9
+    clock = clocks.summary()
+
+    # launches per step: each quantise = amax + encode kernels, each GEMM = 1
+    launches_per_step = 3 * (2 * 2 + 1)
+
+    e2e = run_e2e(args, nv, torch, x_c, w_c, dy_c, dev, world, pg)
+
+    line = {
+        "metric": METRIC, "value": round(value, 3), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms_step, 4), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "nvfp4 (e2m1 codes, e4m3 block scales, fp32 accumulate)",
+        "data": "synthetic", "config": _config(),
+        "roofline": {"bound": "tensor", "kernel": "nvfp4_gemm (tcgen05 mxf4nvf4)", "achieved": round(achieved, 1),
+                     "peak": round(peak_fp4, 1), "unit": "TFLOP/s", "frac": round(achieved / peak_fp4, 4),
+                     "traffic": None,
+                     "peak_source": "%s bf16 %.1f TFLOP/s x nominal FP4/BF16 ratio %.1f" % (
+                         src, peaks["bf16_tflops"], FP4_OVER_BF16),
+                     "gemm_ms": round(gemm_ms, 4)},
+        "quantize": {"bound": "hbm", "achieved": round(quant_gbs, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": round(quant_gbs / peaks["hbm_gbs"], 4), "ms_per_gemm_pass": round(quant_ms, 4),
+                     "bytes_model": "2.5625 B/element (read BF16, write codes + scales)"},
+        "clocks": clock,
+        "gpu_launches": launches_per_step * args.steps,
+        "e2e": e2e,
+    }
+    if rank == 0:
+        line["cpu_baseline"] = cpu_baseline(args)
+        print(json.dumps(line), flush=True)
+    if pg:
+        pg.barrier()
+        pg.destroy_process_group()
+
+
+def run_e2e(args, nv, torch, x_c, w_c, dy_c, dev, world, pg):
+    """The same step through the linear wrappers with pinned host buffers:
+    host->device copies of X, W, dY and device->host copies of Y, dX, dW are
+    inside the timed region."""
+    xh, wh, dyh = x_c.pin_memory(), w_c.pin_memory(), dy_c.pin_memory()
+    yh = torch.empty((T, FFN), dtype=torch.bfloat16).pin_memory()
+    dxh = torch.empty((T, HID), dtype=torch.bfloat16).pin_memory()
+    dwh = torch.empty((FFN, HID), dtype=torch.bfloat16).pin_memory()
+    xd, wd, dyd = torch.empty_like(x_c, device=dev), torch.empty_like(w_c, device=dev), torch.empty_like(dy_c, device=dev)
+    yd = torch.empty((T, FFN), dtype=torch.bfloat16, device=dev)
+    dxd = torch.empty((T, HID), dtype=torch.bfloat16, device=dev)
+    dwd = torch.empty((FFN, HID), dtype=torch.bfloat16, device=dev)
+    ws = {op: torch.zeros(nv.nvfp4_linear_workspace_size(i, T, HID, FFN), dtype=torch.uint8, device=dev)
+          for i, op in enumerate(("fprop", "dgrad", "wgrad"))}
+
+    def step():
+        xd.copy_(xh, non_blocking=True)
+        wd.copy_(wh, non_blocking=True)
+        dyd.copy_(dyh, non_blocking=True)
+        nv.nvfp4_linear_fprop(xd, wd, y=yd, workspace=ws["fprop"])
+        nv.nvfp4_linear_dgrad(dyd, wd, dx=dxd, workspace=ws["dgrad"])
+        nv.nvfp4_linear_wgrad(dyd, xd, dw=dwd, workspace=ws["wgrad"])
+        yh.copy_(yd, non_blocking=True)
+        dxh.copy_(dxd, non_blocking=True)
+        dwh.copy_(dwd, non_blocking=True)
+
+    for _ in range(max(1, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    if pg:
+        pg.barrier()
+    stream = torch.cuda.current_stream()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    n = max(1, min(args.steps, 5))
+    t0.record(stream)
+    for _ in range(n):
+        step()
+    t1.record(stream)
+    torch.cuda.synchronize()
+    ms = t0.elapsed_time(t1)
+    if pg:
+        t = torch.tensor([ms], device=dev)
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        ms = t.item()
+    ms /= n
+    h2d = (T * HID + FFN * HID + T * FFN) * 2
+    d2h = (T * FFN + T * HID + FFN * HID) * 2
+    return {"value": round(world * STEP_FLOP / (ms * 1e-3) / 1e12, 3), "unit": "TFLOP/s",
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(ms, 4),
+            "api": "nvfp4_linear_{fprop,dgrad,wgrad} with pinned host buffers"}
+
+
+# ------------------------------------------------------------- CPU oracle
+def _oracle_sample(rows=64):
+    """The oracle on a bounded sample of the workload: for each of fprop,
+    dgrad and wgrad, quantise the operand rows behind a rows x rows output
+    block (the tensor scale still needs the whole operand) and accumulate
+    that block in FP64.  Returns (flop, seconds)."""
+    import oracle
+    from block_scaled_gemm_nvfp4_gb300 import synthetic as syn
+
+    x, w, dy = syn.config2()
+    xu, wu, dyu = syn.as_u16(x), syn.as_u16(w), syn.as_u16(dy)
+    s = 0x5EEDC0DE0F4
+    jobs = [
+        (xu, oracle.make_cfg(block=0), wu, oracle.make_cfg(block=1), HID),
+        (dyu, oracle.make_cfg(block=0), wu, oracle.make_cfg(block=1, transpose=1), FFN),
+        (dyu, oracle.make_cfg(rounding=1, rht=1, transpose=1, rht_seed=s, sr_seed=5),
+         xu, oracle.make_cfg(rounding=1, rht=1, transpose=1, rht_seed=s, sr_seed=6), T),
+    ]
+    t0 = time.perf_counter()
+    flop = 0.0
+    for a, ca, b, cb, K in jobs:
+        qa = oracle.quantize_rows(a, ca, 0, rows)
+        qb = oracle.quantize_rows(b, cb, 0, rows)
+        oracle.gemm_f64(qa, qb, rows, rows, K)
+        flop += 2.0 * rows * rows * K
+    return flop, time.perf_counter() - t0
+
+
+def cpu_baseline(args, rows=64):
+    flop, sec = _oracle_sample(rows)
+    return {"value": round(flop / sec / 1e12, 9), "unit": "TFLOP/s", "cores": 1, "kind": "oracle",
+            "sample": "fprop+dgrad+wgrad, one %dx%d output block each at full K, with the operand rows "
+                      "quantised from the full tensors (single-threaded C, %.1f s)" % (rows, rows, sec)}
+
+
+def run_reference(args):
+    world, rank, _ = _dist()
+    if rank != 0:
+        return
+    times = []
+    flop = 0.0
+    for _ in range(args.warmup):
+        _oracle_sample(16)
+    for _ in range(args.steps):
+        f, sec = _oracle_sample(16)
+        flop = f
+        times.append(sec)
+    sec = sum(times) / len(times)
+    value = flop / sec / 1e12
+    line = {"metric": METRIC, "value": round(value, 9), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(sec * 1e3, 3), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "nvfp4 (oracle: fp32 encode, fp64 accumulate)",
+            "data": "synthetic", "config": _config(), "impl": "reference",
+            "cpu_baseline": {"value": round(value, 9), "unit": "TFLOP/s", "kind": "oracle", "cores": 1,
+                             "sample": "per step: fprop+dgrad+wgrad, one 16x16 output block each at full K"},
+            "e2e": {"value": round(value, 9), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    args = ap.parse_args()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

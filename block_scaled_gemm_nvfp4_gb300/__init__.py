@@ -1,1 +1,290 @@
-"""libnvfp4: NVFP4 quantisation and block-scaled FP4 GEMM for GB300 (sm_103a)."""
+"""libnvfp4: NVFP4 quantisation and block-scaled FP4 GEMM for GB300 (sm_103a).
+
+A thin ctypes binding over the C ABI declared in ``include/nvfp4.h``.  The
+Python functions carry the C names and only marshal arguments: device
+pointers and sizes from torch tensors, the current CUDA stream, workspaces
+allocated with torch.  Every step of the computation runs in the library's
+CUDA kernels; if the library is not built, every call raises.
+"""
+import ctypes
+import os
+from dataclasses import dataclass
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_lib", "libnvfp4.so")
+
+NVFP4_OK = 0
+NVFP4_ERR_INVALID_ARG = 1
+NVFP4_ERR_UNSUPPORTED_SHAPE = 2
+NVFP4_ERR_WORKSPACE = 3
+NVFP4_ERR_CUDA = 4
+NVFP4_ERR_TIMEOUT = 5
+NVFP4_ERR_NONFINITE = 6
+
+NVFP4_BLOCK_1x16, NVFP4_BLOCK_16x16 = 0, 1
+NVFP4_ROUND_RNE, NVFP4_ROUND_SR = 0, 1
+NVFP4_SF_ROWMAJOR, NVFP4_SF_MMA = 0, 1
+NVFP4_OUT_BF16, NVFP4_OUT_F32 = 0, 1
+NVFP4_LINEAR_FPROP, NVFP4_LINEAR_DGRAD, NVFP4_LINEAR_WGRAD = 0, 1, 2
+
+# Every exported symbol of include/nvfp4.h.
+EXPORTS = [
+    "nvfp4_status_string", "nvfp4_version", "nvfp4_codes_bytes", "nvfp4_sf_bytes",
+    "nvfp4_quantize_workspace_size", "nvfp4_quantize", "nvfp4_dequantize",
+    "nvfp4_gemm_workspace_size", "nvfp4_gemm", "nvfp4_linear_workspace_size",
+    "nvfp4_linear_fprop", "nvfp4_linear_dgrad", "nvfp4_linear_wgrad",
+    "nvfp4_check_device_status", "nvfp4_debug_gemm_skip_load",
+]
+
+
+class Nvfp4Error(RuntimeError):
+    def __init__(self, status, what=""):
+        self.status = status
+        msg = nvfp4_status_string(status) if _LIB is not None else "status %d" % status
+        super().__init__("%s: %s (status %d)" % (what, msg, status) if what else "%s (status %d)" % (msg, status))
+
+
+class QuantCfg(ctypes.Structure):
+    """nvfp4_quant_cfg."""
+    _fields_ = [
+        ("block", ctypes.c_int32),
+        ("rounding", ctypes.c_int32),
+        ("rht", ctypes.c_int32),
+        ("sf_layout", ctypes.c_int32),
+        ("transpose", ctypes.c_int32),
+        ("reserved", ctypes.c_int32),
+        ("rht_seed", ctypes.c_uint64),
+        ("sr_seed", ctypes.c_uint64),
+        ("sr_offset", ctypes.c_uint64),
+    ]
+
+
+def quant_cfg(block=0, rounding=0, rht=0, sf_layout=NVFP4_SF_MMA, transpose=0, rht_seed=0, sr_seed=0,
+              sr_offset=0):
+    return QuantCfg(block, rounding, rht, sf_layout, transpose, 0, rht_seed, sr_seed, sr_offset)
+
+
+class _Tensor(ctypes.Structure):
+    """nvfp4_tensor."""
+    _fields_ = [
+        ("codes", ctypes.c_void_p),
+        ("sf", ctypes.c_void_p),
+        ("tensor_scale", ctypes.c_void_p),
+        ("rows", ctypes.c_int64),
+        ("k", ctypes.c_int64),
+        ("sf_layout", ctypes.c_int32),
+        ("reserved", ctypes.c_int32),
+    ]
+
+
+@dataclass
+class NVFP4Tensor:
+    """A quantised operand Q [rows, k] held in torch device buffers."""
+    codes: torch.Tensor         # uint8 [rows, k/2]
+    sf: torch.Tensor            # uint8, row-major [rows, k/16] or the padded MMA layout
+    tensor_scale: torch.Tensor  # float32 [1]
+    rows: int
+    k: int
+    sf_layout: int
+
+    def _c(self):
+        return _Tensor(self.codes.data_ptr(), self.sf.data_ptr(), self.tensor_scale.data_ptr(),
+                       self.rows, self.k, self.sf_layout, 0)
+
+
+_LIB = None
+
+
+def lib():
+    """Load libnvfp4 (raises if it has not been built)."""
+    global _LIB
+    if _LIB is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError("libnvfp4 is not built (%s missing); run __graft_entry__.build()" % LIB_PATH)
+        L = ctypes.CDLL(LIB_PATH)
+        P, I64, I32, SZ = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.c_size_t
+        PSZ = ctypes.POINTER(ctypes.c_size_t)
+        PCFG = ctypes.POINTER(QuantCfg)
+        PT = ctypes.POINTER(_Tensor)
+        sigs = {
+            "nvfp4_status_string": (ctypes.c_char_p, [I32]),
+            "nvfp4_version": (I32, []),
+            "nvfp4_codes_bytes": (SZ, [I64, I64]),
+            "nvfp4_sf_bytes": (SZ, [I64, I64, I32]),
+            "nvfp4_quantize_workspace_size": (I32, [I64, I64, PCFG, PSZ]),
+            "nvfp4_quantize": (I32, [P, I64, I64, I64, PCFG, P, P, P, P, SZ, P]),
+            "nvfp4_dequantize": (I32, [PT, I32, P, I64, P]),
+            "nvfp4_gemm_workspace_size": (I32, [I64, I64, I64, PSZ]),
+            "nvfp4_gemm": (I32, [PT, PT, I32, P, I64, P, SZ, P]),
+            "nvfp4_linear_workspace_size": (I32, [I32, I64, I64, I64, PSZ]),
+            "nvfp4_linear_fprop": (I32, [P, P, I64, I64, I64, PCFG, PCFG, I32, P, P, SZ, P]),
+            "nvfp4_linear_dgrad": (I32, [P, P, I64, I64, I64, PCFG, PCFG, I32, P, P, SZ, P]),
+            "nvfp4_linear_wgrad": (I32, [P, P, I64, I64, I64, PCFG, PCFG, I32, P, P, SZ, P]),
+            "nvfp4_check_device_status": (I32, [P, P]),
+            "nvfp4_debug_gemm_skip_load": (None, [I32]),
+        }
+        for name, (res, args) in sigs.items():
+            fn = getattr(L, name)
+            fn.restype = res
+            fn.argtypes = args
+        _LIB = L
+    return _LIB
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _check(status, what):
+    if status != NVFP4_OK:
+        raise Nvfp4Error(status, what)
+
+
+def _ptr(t):
+    return ctypes.c_void_p(t.data_ptr() if t is not None else 0)
+
+
+def nvfp4_status_string(status):
+    return lib().nvfp4_status_string(int(status)).decode()
+
+
+def nvfp4_version():
+    return lib().nvfp4_version()
+
+
+def nvfp4_codes_bytes(qr, qk):
+    return lib().nvfp4_codes_bytes(qr, qk)
+
+
+def nvfp4_sf_bytes(qr, qk, sf_layout):
+    return lib().nvfp4_sf_bytes(qr, qk, sf_layout)
+
+
+def _alloc_ws(nbytes, device):
+    # Workspaces are zero-filled once (the status word must start clear).
+    return torch.zeros(max(int(nbytes), 256), dtype=torch.uint8, device=device)
+
+
+def nvfp4_quantize_workspace_size(rows, cols, cfg):
+    n = ctypes.c_size_t(0)
+    _check(lib().nvfp4_quantize_workspace_size(rows, cols, ctypes.byref(cfg), ctypes.byref(n)),
+           "nvfp4_quantize_workspace_size")
+    return n.value
+
+
+def nvfp4_quantize(x, cfg, out=None, workspace=None, stream=None):
+    """x: BF16 CUDA tensor [rows, cols] with unit column stride.  Returns an
+    NVFP4Tensor (allocated unless `out` is given)."""
+    assert x.dtype == torch.bfloat16 and x.dim() == 2 and x.stride(1) == 1
+    rows, cols = x.shape
+    qr, qk = (cols, rows) if cfg.transpose else (rows, cols)
+    if out is None:
+        out = NVFP4Tensor(
+            codes=torch.empty((qr, qk // 2), dtype=torch.uint8, device=x.device),
+            sf=torch.empty(max(nvfp4_sf_bytes(qr, qk, cfg.sf_layout), 1), dtype=torch.uint8, device=x.device),
+            tensor_scale=torch.empty(1, dtype=torch.float32, device=x.device),
+            rows=qr, k=qk, sf_layout=cfg.sf_layout)
+    if workspace is None:
+        workspace = _alloc_ws(nvfp4_quantize_workspace_size(rows, cols, cfg), x.device)
+    ldx = x.stride(0) if rows > 1 else cols
+    st = lib().nvfp4_quantize(_ptr(x), rows, cols, ldx, ctypes.byref(cfg), _ptr(out.codes), _ptr(out.sf),
+                              _ptr(out.tensor_scale), _ptr(workspace), workspace.numel(), _stream(stream))
+    _check(st, "nvfp4_quantize")
+    return out
+
+
+def nvfp4_dequantize(q, out_dtype=NVFP4_OUT_F32, out=None, stream=None):
+    if out is None:
+        dt = torch.float32 if out_dtype == NVFP4_OUT_F32 else torch.bfloat16
+        out = torch.empty((q.rows, q.k), dtype=dt, device=q.codes.device)
+    t = q._c()
+    st = lib().nvfp4_dequantize(ctypes.byref(t), out_dtype, _ptr(out), out.stride(0) if q.rows > 1 else q.k,
+                                _stream(stream))
+    _check(st, "nvfp4_dequantize")
+    return out
+
+
+def nvfp4_gemm_workspace_size(M, N, K):
+    n = ctypes.c_size_t(0)
+    _check(lib().nvfp4_gemm_workspace_size(M, N, K, ctypes.byref(n)), "nvfp4_gemm_workspace_size")
+    return n.value
+
+
+def nvfp4_gemm(a, b, out_dtype=NVFP4_OUT_BF16, d=None, workspace=None, stream=None):
+    """D [a.rows, b.rows] = A * B^T on NVFP4 operands."""
+    if d is None:
+        dt = torch.float32 if out_dtype == NVFP4_OUT_F32 else torch.bfloat16
+        d = torch.empty((a.rows, b.rows), dtype=dt, device=a.codes.device)
+    if workspace is None:
+        workspace = _alloc_ws(nvfp4_gemm_workspace_size(a.rows, b.rows, a.k), a.codes.device)
+    ta, tb = a._c(), b._c()
+    ldd = d.stride(0) if d.dim() == 2 and d.shape[0] > 1 else b.rows
+    st = lib().nvfp4_gemm(ctypes.byref(ta), ctypes.byref(tb), out_dtype, _ptr(d), ldd, _ptr(workspace),
+                          workspace.numel(), _stream(stream))
+    _check(st, "nvfp4_gemm")
+    return d
+
+
+def nvfp4_linear_workspace_size(op, tokens, din, dout):
+    n = ctypes.c_size_t(0)
+    _check(lib().nvfp4_linear_workspace_size(op, tokens, din, dout, ctypes.byref(n)),
+           "nvfp4_linear_workspace_size")
+    return n.value
+
+
+def _linear(fn, op, a, b, tokens, din, dout, cfg_a, cfg_b, out_dtype, out, out_shape, workspace, stream):
+    dt = torch.float32 if out_dtype == NVFP4_OUT_F32 else torch.bfloat16
+    if out is None:
+        out = torch.empty(out_shape, dtype=dt, device=a.device)
+    if workspace is None:
+        workspace = _alloc_ws(nvfp4_linear_workspace_size(op, tokens, din, dout), a.device)
+    ca = ctypes.byref(cfg_a) if cfg_a is not None else None
+    cb = ctypes.byref(cfg_b) if cfg_b is not None else None
+    st = fn(_ptr(a), _ptr(b), tokens, din, dout, ca, cb, out_dtype, _ptr(out), _ptr(workspace), workspace.numel(),
+            _stream(stream))
+    _check(st, fn.__name__)
+    return out
+
+
+def nvfp4_linear_fprop(x, w, cfg_x=None, cfg_w=None, out_dtype=NVFP4_OUT_BF16, y=None, workspace=None,
+                       stream=None):
+    """Y [T, dout] = Q(X) Q(W)^T for X [T, din], W [dout, din] (BF16)."""
+    T, din = x.shape
+    dout = w.shape[0]
+    return _linear(lib().nvfp4_linear_fprop, NVFP4_LINEAR_FPROP, x, w, T, din, dout, cfg_x, cfg_w, out_dtype, y,
+                   (T, dout), workspace, stream)
+
+
+def nvfp4_linear_dgrad(dy, w, cfg_dy=None, cfg_w=None, out_dtype=NVFP4_OUT_BF16, dx=None, workspace=None,
+                       stream=None):
+    """dX [T, din] = Q(dY) Q(W^T)^T for dY [T, dout], W [dout, din]."""
+    T, dout = dy.shape
+    din = w.shape[1]
+    return _linear(lib().nvfp4_linear_dgrad, NVFP4_LINEAR_DGRAD, dy, w, T, din, dout, cfg_dy, cfg_w, out_dtype,
+                   dx, (T, din), workspace, stream)
+
+
+def nvfp4_linear_wgrad(dy, x, cfg_dy=None, cfg_x=None, out_dtype=NVFP4_OUT_BF16, dw=None, workspace=None,
+                       stream=None):
+    """dW [dout, din] = Q(dY^T) Q(X^T)^T for dY [T, dout], X [T, din]."""
+    T, dout = dy.shape
+    din = x.shape[1]
+    return _linear(lib().nvfp4_linear_wgrad, NVFP4_LINEAR_WGRAD, dy, x, T, din, dout, cfg_dy, cfg_x, out_dtype,
+                   dw, (dout, din), workspace, stream)
+
+
+NVFP4_DEFAULT_RHT_SEED = 0x5EEDC0DE0F4
+
+
+def nvfp4_debug_gemm_skip_load(enable=True):
+    """Failure-detection test hook (see include/nvfp4.h)."""
+    lib().nvfp4_debug_gemm_skip_load(1 if enable else 0)
+
+
+def nvfp4_check_device_status(workspace, stream=None):
+    """Synchronise, read and clear the workspace's device status word."""
+    return lib().nvfp4_check_device_status(_ptr(workspace), _stream(stream))

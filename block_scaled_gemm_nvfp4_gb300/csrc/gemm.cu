@@ -1,0 +1,455 @@
+// Block-scaled NVFP4 GEMM on sm_103a tensor cores (tcgen05, kind::mxf4nvf4).
+//
+//   D[m, n] = sA * sB * sum_k (eA[m,k] * scaleA[m,k/16]) * (eB[n,k] * scaleB[n,k/16])
+//
+// NVFP4 operands with FP32 accumulation ("NVIDIA acelera o pre-treinamento de
+// LLM: NVFP4 no Blackwell...", section "Como o treinamento mixed-precision
+// funciona com NVFP4"); both operands K-major (D = A * B^T).
+//
+// Structure: a persistent kernel, one CTA per SM, 128 x 256 output tiles.
+//   warp 0     TMA producer: packed E2M1 codes by tiled TMA (128-byte
+//              swizzle) and the block scales by bulk copies, into a 4-stage
+//              shared-memory ring guarded by mbarriers;
+//   warp 1     allocates TMEM, copies each stage's block scales into TMEM
+//              (tcgen05.cp) and issues the block-scaled MMAs (K = 64 each,
+//              four per 256-wide K stage) into a 128 x 256 FP32 TMEM
+//              accumulator; tcgen05.commit frees ring stages and signals
+//              the epilogue;
+//   warps 2-9  epilogue, two warps per TMEM lane quarter, each owning 128 of
+//              the 256 columns: TMEM -> registers (tcgen05.ld), times sA * sB,
+//              BF16 (RNE) or FP32, stored to global memory.  In BF16 mode a
+//              warp converts its whole half-row block into registers first so
+//              that the accumulator is released before the stores are issued.
+// Every mbarrier wait is bounded; on a timeout the CTA records
+// NVFP4_ERR_TIMEOUT in the status word, drains its in-flight copies and MMAs,
+// frees TMEM and exits.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <cstdint>
+#include <mutex>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace nvfp4 {
+namespace {
+
+constexpr int BM = 128;
+constexpr int BN = 256;
+constexpr int BK = 256;                       // elements of K per stage
+constexpr int kRowBytes = BK / 2;             // 128 bytes of packed codes per row per stage
+constexpr int kStages = 4;
+constexpr int kABytes = BM * kRowBytes;       // 16 KB
+constexpr int kBBytes = BN * kRowBytes;       // 32 KB
+constexpr int kSfAtomBytes = 512;             // 128 rows x 4 scales
+constexpr int kSfaBytes = 4 * kSfAtomBytes;   // one row atom x 4 K atoms
+constexpr int kSfbBytes = 8 * kSfAtomBytes;   // two row atoms x 4 K atoms
+constexpr int kStageBytes = kABytes + kBBytes + kSfaBytes + kSfbBytes;
+constexpr int kThreads = 320;
+constexpr int kEpiWarps = 8;
+constexpr int kEpiCols = BN / 2;            // columns per epilogue warp
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kAccCol = 0;
+constexpr uint32_t kSfaCol = 256;             // + stage * 16 + kk * 4
+constexpr uint32_t kSfbCol = 320;             // + stage * 32 + kk * 8 + row_atom * 4
+constexpr int kGroupM = 16;                   // tile raster: groups of 16 row blocks
+constexpr int kSmemBytes = kStages * kStageBytes + 1024 /*barriers*/ + 1024 /*alignment*/;
+
+static_assert(kStageBytes % 1024 == 0, "stages must keep 1024-byte alignment for 128B swizzle");
+
+// Instruction descriptor for kind::mxf4nvf4: dense, A and B E2M1 (format 1),
+// both K-major, N >> 3 at bit 17, UE4M3 scales (bit 23 = 0), M >> 4 at bit 24,
+// scale-factor ids 0.
+constexpr uint32_t kIdesc = (1u << 7) | (1u << 10) | ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
+
+struct GParams {
+  int64_t M, N, K;
+  int num_kb;        // K stages
+  int tiles_m, tiles_n, num_tiles;
+  int64_t sf_katoms; // 64-wide K atoms per row block in the scale layout
+  int64_t a_row_atoms, b_row_atoms;
+  const uint8_t* a_sf;
+  const uint8_t* b_sf;
+  const float* a_scale;
+  const float* b_scale;
+  void* d;
+  int64_t ldd;
+  int vec_store;
+  int skip_first_load;  // test hook: CTA 0 never loads its first stage
+  uint32_t* status;
+};
+
+struct __align__(8) SmemCtl {
+  uint64_t full[kStages];
+  uint64_t empty[kStages];
+  uint64_t acc_full;
+  uint64_t acc_empty;
+  uint64_t drain;
+  uint32_t tmem_base;
+  int abort;
+};
+
+__device__ __forceinline__ void tile_coords(const GParams& p, int tile, int& m_blk, int& n_blk) {
+  const int per_group = kGroupM * p.tiles_n;
+  const int group = tile / per_group;
+  const int first_m = group * kGroupM;
+  const int gm = min(p.tiles_m - first_m, kGroupM);
+  const int local = tile - group * per_group;
+  m_blk = first_m + local % gm;
+  n_blk = local / gm;
+}
+
+__device__ __forceinline__ int kk_count_for(const GParams& p, int kb) {
+  const int64_t rem = p.K - static_cast<int64_t>(kb) * BK;
+  return static_cast<int>(min(static_cast<int64_t>(4), (rem + 63) / 64));
+}
+
+__device__ __forceinline__ void fail(SmemCtl* ctl, const GParams& p, uint32_t where) {
+  ptx::set_status(p.status, kDevTimeout | (where << 8));
+  *reinterpret_cast<volatile int*>(&ctl->abort) = 1;
+}
+
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+  const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&v);
+}
+
+template <bool OUT_F32>
+__global__ void __launch_bounds__(kThreads, 1)
+    gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
+                const GParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  SmemCtl* ctl = reinterpret_cast<SmemCtl*>(smem + kStages * kStageBytes);
+  volatile int* abort_flag = &ctl->abort;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      ptx::mbar_init(&ctl->full[s], 1);
+      ptx::mbar_init(&ctl->empty[s], 1);
+    }
+    ptx::mbar_init(&ctl->acc_full, 1);
+    ptx::mbar_init(&ctl->acc_empty, kEpiWarps);
+    ptx::mbar_init(&ctl->drain, 1);
+    ctl->abort = 0;
+    ptx::fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    ptx::prefetch_tensormap(&tmap_a);
+    ptx::prefetch_tensormap(&tmap_b);
+  }
+  if (warp == 1) {
+    ptx::tmem_alloc(&ctl->tmem_base, kTmemCols);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = ctl->tmem_base;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      uint32_t issued_mask = 0, issued_parity = 0;
+      int stage = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < p.num_tiles && ok; tile += gridDim.x) {
+        int m_blk, n_blk;
+        tile_coords(p, tile, m_blk, n_blk);
+        const int64_t n_rows_left = p.N - static_cast<int64_t>(n_blk) * BN;
+        const int nb_atoms = static_cast<int>(min(static_cast<int64_t>(2), (n_rows_left + 127) / 128));
+        for (int kb = 0; kb < p.num_kb; ++kb) {
+          if (!ptx::mbar_wait(&ctl->empty[stage], phase ^ 1u, abort_flag)) {
+            fail(ctl, p, 1);
+            ok = false;
+            break;
+          }
+          const int kk = kk_count_for(p, kb);
+          const uint32_t sf_bytes = static_cast<uint32_t>(kk * kSfAtomBytes);
+          uint8_t* st = smem + stage * kStageBytes;
+          if (p.skip_first_load && blockIdx.x == 0 && tile == static_cast<int>(blockIdx.x) && kb == 0) {
+            // Failure-detection test hook: this stage is never filled, so the
+            // MMA warp's bounded wait runs out and the CTA reports a timeout.
+            if (++stage == kStages) {
+              stage = 0;
+              phase ^= 1u;
+            }
+            continue;
+          }
+          ptx::mbar_arrive_expect_tx(&ctl->full[stage],
+                                     static_cast<uint32_t>(kABytes + kBBytes) + sf_bytes * (1 + nb_atoms));
+          ptx::tma_load_2d(st, &tmap_a, &ctl->full[stage], kb * kRowBytes, m_blk * BM);
+          ptx::tma_load_2d(st + kABytes, &tmap_b, &ctl->full[stage], kb * kRowBytes, n_blk * BN);
+          const uint8_t* sfa = p.a_sf + (static_cast<int64_t>(m_blk) * p.sf_katoms + kb * 4) * kSfAtomBytes;
+          ptx::bulk_load(st + kABytes + kBBytes, sfa, sf_bytes, &ctl->full[stage]);
+          for (int rb = 0; rb < nb_atoms; ++rb) {
+            const uint8_t* sfb =
+                p.b_sf + (static_cast<int64_t>(n_blk * 2 + rb) * p.sf_katoms + kb * 4) * kSfAtomBytes;
+            ptx::bulk_load(st + kABytes + kBBytes + kSfaBytes + rb * 4 * kSfAtomBytes, sfb, sf_bytes,
+                           &ctl->full[stage]);
+          }
+          issued_mask |= 1u << stage;
+          issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
+          if (++stage == kStages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      // Drain: every stage this thread loaded must have landed before exit.
+      for (int s = 0; s < kStages; ++s) {
+        if (issued_mask & (1u << s)) {
+          volatile int never = 0;
+          if (!ptx::mbar_wait(&ctl->full[s], (issued_parity >> s) & 1u, &never)) fail(ctl, p, 2);
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ----------------------------------------------------------------- MMA
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0, acc_phase = 0;
+      bool ok = true, issued = false;
+      for (int tile = blockIdx.x; tile < p.num_tiles && ok; tile += gridDim.x) {
+        int m_blk, n_blk;
+        tile_coords(p, tile, m_blk, n_blk);
+        const int64_t n_rows_left = p.N - static_cast<int64_t>(n_blk) * BN;
+        const int nb_atoms = static_cast<int>(min(static_cast<int64_t>(2), (n_rows_left + 127) / 128));
+        if (!ptx::mbar_wait(&ctl->acc_empty, acc_phase ^ 1u, abort_flag)) {
+          fail(ctl, p, 3);
+          break;
+        }
+        ptx::tc_fence_after();
+        for (int kb = 0; kb < p.num_kb; ++kb) {
+          if (!ptx::mbar_wait(&ctl->full[stage], phase, abort_flag)) {
+            fail(ctl, p, 4);
+            ok = false;
+            break;
+          }
+          ptx::tc_fence_after();
+          const int kk_n = kk_count_for(p, kb);
+          uint8_t* st = smem + stage * kStageBytes;
+          const uint32_t a_addr = ptx::smem_u32(st);
+          const uint32_t b_addr = ptx::smem_u32(st + kABytes);
+          const uint32_t sfa_addr = ptx::smem_u32(st + kABytes + kBBytes);
+          const uint32_t sfb_addr = sfa_addr + kSfaBytes;
+          for (int kk = 0; kk < kk_n; ++kk) {
+            const uint32_t sfa_t = tmem + kSfaCol + stage * 16 + kk * 4;
+            ptx::tc_cp_32x128b_warpx4(sfa_t, ptx::smem_desc(sfa_addr + kk * kSfAtomBytes, 16, 128, ptx::kSwizzleNone));
+            for (int rb = 0; rb < nb_atoms; ++rb) {
+              const uint32_t sfb_t = tmem + kSfbCol + stage * 32 + kk * 8 + rb * 4;
+              ptx::tc_cp_32x128b_warpx4(
+                  sfb_t, ptx::smem_desc(sfb_addr + rb * 4 * kSfAtomBytes + kk * kSfAtomBytes, 16, 128,
+                                        ptx::kSwizzleNone));
+            }
+          }
+          for (int kk = 0; kk < kk_n; ++kk) {
+            const uint64_t adesc = ptx::smem_desc(a_addr + kk * 32, 16, 1024, ptx::kSwizzle128B);
+            const uint64_t bdesc = ptx::smem_desc(b_addr + kk * 32, 16, 1024, ptx::kSwizzle128B);
+            ptx::tc_mma_nvf4(tmem + kAccCol, adesc, bdesc, kIdesc, tmem + kSfaCol + stage * 16 + kk * 4,
+                             tmem + kSfbCol + stage * 32 + kk * 8, (kb | kk) != 0 ? 1u : 0u);
+          }
+          ptx::tc_commit(&ctl->empty[stage]);
+          issued = true;
+          if (++stage == kStages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        ptx::tc_commit(&ctl->acc_full);
+        acc_phase ^= 1u;
+      }
+      if (issued) {
+        // Wait for every MMA and scale copy issued above before TMEM is freed.
+        ptx::tc_commit(&ctl->drain);
+        volatile int never = 0;
+        if (!ptx::mbar_wait(&ctl->drain, 0, &never)) fail(ctl, p, 5);
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int q = warp & 3;                 // TMEM lane quarter this warp may access
+    const int half = (warp - 2) >> 2;       // which 128 columns of the tile
+    const int row_in_tile = q * 32 + lane;
+    const float alpha = __fmul_rn(*p.a_scale, *p.b_scale);
+    uint32_t acc_phase = 0;
+    for (int tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x) {
+      int m_blk, n_blk;
+      tile_coords(p, tile, m_blk, n_blk);
+      // One lane waits and the result is broadcast, so the warp stays
+      // converged for the .sync.aligned TMEM loads below.
+      uint32_t ok = 1;
+      if (lane == 0) ok = ptx::mbar_wait(&ctl->acc_full, acc_phase, abort_flag) ? 1u : 0u;
+      ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
+      if (!ok) {
+        if (lane == 0) fail(ctl, p, 6);
+        break;
+      }
+      ptx::tc_fence_after();
+      const int64_t row = static_cast<int64_t>(m_blk) * BM + row_in_tile;
+      const int64_t col0 = static_cast<int64_t>(n_blk) * BN + half * kEpiCols;
+      const uint32_t taddr = tmem + (static_cast<uint32_t>(q * 32) << 16) + kAccCol + half * kEpiCols;
+      if (!OUT_F32) {
+        uint32_t packed[kEpiCols / 2];
+#pragma unroll
+        for (int c = 0; c < kEpiCols / 32; ++c) {
+          uint32_t r[32];
+          ptx::tmem_ld_32x32b_x32(taddr + c * 32, r);
+          ptx::tmem_ld_wait();
+#pragma unroll
+          for (int j = 0; j < 16; ++j)
+            packed[c * 16 + j] = pack_bf16(__fmul_rn(alpha, __uint_as_float(r[2 * j])),
+                                           __fmul_rn(alpha, __uint_as_float(r[2 * j + 1])));
+        }
+        ptx::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(&ctl->acc_empty);
+        if (row < p.M) {
+          __nv_bfloat16* drow = static_cast<__nv_bfloat16*>(p.d) + row * p.ldd;
+#pragma unroll
+          for (int c8 = 0; c8 < kEpiCols / 8; ++c8) {
+            const int64_t col = col0 + c8 * 8;
+            if (p.vec_store && col + 8 <= p.N) {
+              *reinterpret_cast<uint4*>(drow + col) =
+                  make_uint4(packed[c8 * 4], packed[c8 * 4 + 1], packed[c8 * 4 + 2], packed[c8 * 4 + 3]);
+            } else {
+#pragma unroll
+              for (int j = 0; j < 8; ++j) {
+                if (col + j < p.N) {
+                  const uint32_t w = packed[c8 * 4 + j / 2];
+                  const uint16_t h = static_cast<uint16_t>((j & 1) ? (w >> 16) : (w & 0xFFFFu));
+                  reinterpret_cast<uint16_t*>(drow)[col + j] = h;
+                }
+              }
+            }
+          }
+        }
+      } else {
+        float* drow = static_cast<float*>(p.d) + row * p.ldd;
+#pragma unroll 1
+        for (int c = 0; c < kEpiCols / 32; ++c) {
+          uint32_t r[32];
+          ptx::tmem_ld_32x32b_x32(taddr + c * 32, r);
+          ptx::tmem_ld_wait();
+          if (row < p.M) {
+#pragma unroll
+            for (int j4 = 0; j4 < 8; ++j4) {
+              const int64_t col = col0 + c * 32 + j4 * 4;
+              const float4 v = make_float4(__fmul_rn(alpha, __uint_as_float(r[4 * j4])),
+                                           __fmul_rn(alpha, __uint_as_float(r[4 * j4 + 1])),
+                                           __fmul_rn(alpha, __uint_as_float(r[4 * j4 + 2])),
+                                           __fmul_rn(alpha, __uint_as_float(r[4 * j4 + 3])));
+              if (p.vec_store && col + 4 <= p.N) {
+                *reinterpret_cast<float4*>(drow + col) = v;
+              } else {
+                if (col < p.N) drow[col] = v.x;
+                if (col + 1 < p.N) drow[col + 1] = v.y;
+                if (col + 2 < p.N) drow[col + 2] = v.z;
+                if (col + 3 < p.N) drow[col + 3] = v.w;
+              }
+            }
+          }
+        }
+        ptx::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(&ctl->acc_empty);
+      }
+      acc_phase ^= 1u;
+    }
+  }
+
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  });
+  return fn;
+}
+
+// Tensor map over packed codes [rows, K/2] bytes, box = 128 bytes x box_rows,
+// 128-byte swizzle, out-of-range elements read as zero.
+bool make_codes_map(CUtensorMap* map, const uint8_t* codes, int64_t rows, int64_t K, uint32_t box_rows) {
+  auto encode = get_encode();
+  if (!encode) return false;
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(K / 2), static_cast<cuuint64_t>(rows)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(K / 2)};
+  const cuuint32_t box[2] = {static_cast<cuuint32_t>(kRowBytes), box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(codes), dims, strides, box,
+                            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+template <bool OUT_F32>
+cudaError_t launch_typed(const CUtensorMap& ma, const CUtensorMap& mb, const GParams& p, cudaStream_t stream) {
+  static bool configured = false;
+  if (!configured) {
+    cudaError_t e = cudaFuncSetAttribute(gemm_kernel<OUT_F32>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    if (e != cudaSuccess) return e;
+    configured = true;
+  }
+  const int grid = std::min(p.num_tiles, device_sm_count());
+  gemm_kernel<OUT_F32><<<grid, kThreads, kSmemBytes, stream>>>(ma, mb, p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_gemm(const GemmArgs& a, cudaStream_t stream) {
+  if (a.M == 0 || a.N == 0) return cudaSuccess;
+  if (a.K == 0) {
+    const size_t esz = a.out_f32 ? 4 : 2;
+    return cudaMemset2DAsync(a.d, a.ldd * esz, 0, a.N * esz, a.M, stream);
+  }
+  CUtensorMap ma, mb;
+  if (!make_codes_map(&ma, a.a_codes, a.M, a.K, BM) || !make_codes_map(&mb, a.b_codes, a.N, a.K, BN))
+    return cudaErrorInvalidValue;
+  GParams p{};
+  p.M = a.M;
+  p.N = a.N;
+  p.K = a.K;
+  p.num_kb = static_cast<int>((a.K + BK - 1) / BK);
+  p.tiles_m = static_cast<int>((a.M + BM - 1) / BM);
+  p.tiles_n = static_cast<int>((a.N + BN - 1) / BN);
+  p.num_tiles = p.tiles_m * p.tiles_n;
+  p.sf_katoms = (a.K / 16 + 3) / 4;
+  p.a_row_atoms = (a.M + 127) / 128;
+  p.b_row_atoms = (a.N + 127) / 128;
+  p.a_sf = a.a_sf;
+  p.b_sf = a.b_sf;
+  p.a_scale = a.a_scale;
+  p.b_scale = a.b_scale;
+  p.d = a.d;
+  p.ldd = a.ldd;
+  p.status = a.status;
+  p.skip_first_load = a.skip_first_load;
+  const size_t esz = a.out_f32 ? 4 : 2;
+  p.vec_store = (reinterpret_cast<uintptr_t>(a.d) % 16 == 0) && ((a.ldd * esz) % 16 == 0);
+  return a.out_f32 ? launch_typed<true>(ma, mb, p, stream) : launch_typed<false>(ma, mb, p, stream);
+}
+
+}  // namespace nvfp4

@@ -1,0 +1,66 @@
+// Internal launcher interface between the C ABI (api.cu) and the kernels.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cstddef>
+#include <cstdint>
+
+#include "../../include/nvfp4.h"
+
+namespace nvfp4 {
+
+// Every workspace starts with a 256-byte header; its first 32-bit word is the
+// device status word.  The quantiser's scratch follows the header.
+constexpr size_t kWsHeaderBytes = 256;
+// Partial amax slots (one per CTA of the amax pass).
+constexpr int kMaxAmaxPartials = 4096;
+constexpr size_t kQuantScratchBytes = kMaxAmaxPartials * sizeof(uint32_t);
+
+struct QuantArgs {
+  const uint16_t* x;   // BF16 input
+  int64_t rows, cols, ldx;
+  int64_t qr, qk;      // quantised operand shape
+  int block2d, sr, rht, transpose, sf_mma;
+  uint64_t rht_seed, sr_seed, sr_offset;
+  uint8_t* codes;
+  uint8_t* sf;
+  float* tensor_scale;
+  uint32_t* status;    // device status word
+  uint32_t* partials;  // kMaxAmaxPartials slots
+};
+
+cudaError_t launch_quantize(const QuantArgs& a, cudaStream_t stream);
+
+struct DequantArgs {
+  const uint8_t* codes;
+  const uint8_t* sf;
+  const float* tensor_scale;
+  int64_t rows, k;
+  int sf_mma;
+  int out_f32;
+  void* out;
+  int64_t ldo;
+};
+
+cudaError_t launch_dequantize(const DequantArgs& a, cudaStream_t stream);
+
+struct GemmArgs {
+  const uint8_t* a_codes;
+  const uint8_t* a_sf;
+  const float* a_scale;
+  const uint8_t* b_codes;
+  const uint8_t* b_sf;
+  const float* b_scale;
+  int64_t M, N, K;
+  int out_f32;
+  void* d;
+  int64_t ldd;
+  uint32_t* status;
+  int skip_first_load;  // failure-detection test hook (see nvfp4_debug_gemm_skip_load)
+};
+
+cudaError_t launch_gemm(const GemmArgs& a, cudaStream_t stream);
+
+int device_sm_count();
+
+}  // namespace nvfp4

@@ -1,0 +1,219 @@
+/*
+ * libnvfp4 -- NVFP4 quantisation and block-scaled FP4 GEMM for GB300 (sm_103a).
+ *
+ * What the library computes (sources are the pages' titles and sections):
+ *
+ *  - NVFP4 is a 4-bit floating-point format with a sparse grid, used for the
+ *    weights and activations that enter GEMMs while accumulators stay in
+ *    FP32 ("NVIDIA acelera o pre-treinamento de LLM: NVFP4 no Blackwell em
+ *    conjunto com JAX e MaxText", sections "Por que cada porcento e
+ *    importante" and "Como o treinamento mixed-precision funciona com NVFP4").
+ *    Values are brought into the grid's range by custom scaling (same page).
+ *  - Element codes are E2M1 on {0, +-0.5, +-1, +-1.5, +-2, +-3, +-4, +-6};
+ *    every run of 16 elements along K has an E4M3 block scale (1x16 blocks),
+ *    or every 16x16 tile shares one (16x16 blocks); the tensor has one FP32
+ *    decode scale s = amax / (6 * 448).
+ *  - Hadamard mixing before quantisation and stochastic rounding come from
+ *    "Full-Stack FP4: Stable LLM Pretraining with Quantized Projections,
+ *    Optimizers, and Attention", section 2.2.  Here: a 16-point random
+ *    Hadamard transform 1/4 * H16 * diag(sigma) on each run of 16 along K,
+ *    sigma drawn from a seeded Philox4x32-10 word, and stochastic rounding
+ *    from a counter-based Philox4x32-10 stream.
+ *  - The GEMM computes D = A * B^T on NVFP4 operands, both stored K-major,
+ *    with FP32 accumulation and the two tensor scales applied in the
+ *    epilogue; the NVFP4 GEMM speed-up on Blackwell Ultra is the subject of
+ *    "NVFP4 Treina com Precisao de 16 Bits e a Velocidade de 4 Bits para
+ *    Pre-treinamento em Grande Escala", TL;DR.
+ *
+ * Every rounding decision is a fixed sequence of IEEE FP32 operations, so the
+ * quantised codes, block scales and stochastic-rounding draws are a
+ * deterministic function of (input, configuration, seeds):
+ *    s      = amax / 2688           (one FP32 division; 1 if that is zero)
+ *    t      = (bamax / 6) / s        (two FP32 divisions)
+ *    scale  = E4M3(t)                (round to nearest even, saturate at 448)
+ *    v      = x / (scale * s)        (one FP32 multiply, one FP32 division)
+ *    code   = E2M1(v)                (round to nearest even, or stochastic)
+ * A zero block scale encodes its whole run as code 0.  A negative v that
+ * rounds to zero is encoded 0x8.  Packing: element 2j of a row is the low
+ * nibble of byte j, element 2j+1 the high nibble.
+ *
+ * Conventions for every call:
+ *  - Ownership: the caller owns every buffer (device memory unless stated).
+ *    The library never allocates device memory.
+ *  - Execution: calls enqueue kernels on `stream` and return at once.
+ *  - Errors: argument errors are returned before anything is launched.
+ *    A launch failure returns NVFP4_ERR_CUDA.  Errors found on the device
+ *    (non-finite input, a wait that ran out) are recorded in the status word
+ *    at the start of the call's workspace; nvfp4_check_device_status reads
+ *    and clears it.  Workspaces must be zero-filled once before first use.
+ *  - Concurrency: calls that may run at the same time need separate
+ *    workspaces.
+ */
+#ifndef NVFP4_H
+#define NVFP4_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* nvfp4_stream_t; /* same type as cudaStream_t */
+
+typedef enum nvfp4_status {
+  NVFP4_OK = 0,
+  NVFP4_ERR_INVALID_ARG = 1,       /* null pointer, bad enum, bad stride       */
+  NVFP4_ERR_UNSUPPORTED_SHAPE = 2, /* a shape rule below is broken             */
+  NVFP4_ERR_WORKSPACE = 3,         /* workspace missing or too small           */
+  NVFP4_ERR_CUDA = 4,              /* a CUDA call failed                       */
+  NVFP4_ERR_TIMEOUT = 5,           /* a device-side wait ran out (device word) */
+  NVFP4_ERR_NONFINITE = 6          /* input holds inf or NaN (device word)     */
+} nvfp4_status;
+
+typedef enum { NVFP4_BLOCK_1x16 = 0, NVFP4_BLOCK_16x16 = 1 } nvfp4_block;
+typedef enum { NVFP4_ROUND_RNE = 0, NVFP4_ROUND_SR = 1 } nvfp4_rounding;
+/* Block-scale storage.  ROWMAJOR: byte (r, kb) at r * (K/16) + kb.
+ * MMA: the tensor-core layout the GEMM reads -- atoms of 128 rows x 4 scales
+ * (512 bytes), ordered by row block then K block; inside an atom scale
+ * (r, j) is at byte (r % 32) * 16 + (r / 32) * 4 + j.  Rows are padded to a
+ * multiple of 128 and scale columns to a multiple of 4; padding holds 0. */
+typedef enum { NVFP4_SF_ROWMAJOR = 0, NVFP4_SF_MMA = 1 } nvfp4_sf_layout;
+typedef enum { NVFP4_OUT_BF16 = 0, NVFP4_OUT_F32 = 1 } nvfp4_out_dtype;
+
+/* Quantiser configuration.  All fields are 32- or 64-bit for a stable ABI. */
+typedef struct nvfp4_quant_cfg {
+  int32_t block;      /* nvfp4_block                                          */
+  int32_t rounding;   /* nvfp4_rounding                                       */
+  int32_t rht;        /* 1: 16-point random Hadamard transform along K        */
+  int32_t sf_layout;  /* nvfp4_sf_layout of the block scales written          */
+  int32_t transpose;  /* 1: quantise x^T, i.e. blocks run down the rows of x  */
+  int32_t reserved;   /* must be 0                                            */
+  uint64_t rht_seed;  /* sigma_j = -1 iff bit j of Philox(key=rht_seed, ctr=0) word 0 */
+  uint64_t sr_seed;   /* Philox key for stochastic rounding                   */
+  uint64_t sr_offset; /* Philox counter words 2..3 for stochastic rounding    */
+} nvfp4_quant_cfg;
+
+/* A quantised operand Q [rows, k], K-major (device pointers). */
+typedef struct nvfp4_tensor {
+  const void* codes;          /* rows * k / 2 bytes, row stride k / 2       */
+  const void* sf;             /* block scales in `sf_layout`                */
+  const float* tensor_scale;  /* one FP32 decode scale (device memory)      */
+  int64_t rows;
+  int64_t k;
+  int32_t sf_layout;          /* nvfp4_sf_layout                            */
+  int32_t reserved;           /* must be 0                                  */
+} nvfp4_tensor;
+
+const char* nvfp4_status_string(nvfp4_status status);
+/* Library version as major * 10000 + minor * 100 + patch. */
+int32_t nvfp4_version(void);
+
+/* Sizes of the quantiser's outputs for Q [qr, qk]: codes qr * qk / 2 bytes;
+ * block scales qr * qk / 16 bytes (ROWMAJOR) or the padded MMA size. */
+size_t nvfp4_codes_bytes(int64_t qr, int64_t qk);
+size_t nvfp4_sf_bytes(int64_t qr, int64_t qk, int32_t sf_layout);
+
+/*
+ * nvfp4_quantize: BF16 x [rows, cols] (row stride ldx elements, ldx >= cols,
+ * device memory) -> Q = x (or x^T when cfg->transpose), qr x qk with
+ * qr = rows, qk = cols (transposed: qr = cols, qk = rows).
+ * Outputs: codes [qr, qk/2] bytes; sf in cfg->sf_layout; tensor_scale[0] = s.
+ * Two passes over x: the tensor amax (after the transform, if any), then the
+ * per-block encode.  Shape rules: qk % 16 == 0; 16x16 blocks also need
+ * qr % 16 == 0; ldx % 8 == 0 and x 16-byte aligned.
+ * Non-finite input: the device status word is set to NVFP4_ERR_NONFINITE,
+ * tensor_scale[0] is set to NaN and codes/sf are left unspecified.
+ * Workspace: nvfp4_quantize_workspace_size bytes, device memory.
+ * Sources: the encode steps listed at the top of this header.
+ */
+nvfp4_status nvfp4_quantize_workspace_size(int64_t rows, int64_t cols, const nvfp4_quant_cfg* cfg,
+                                           size_t* bytes);
+nvfp4_status nvfp4_quantize(const void* x, int64_t rows, int64_t cols, int64_t ldx,
+                            const nvfp4_quant_cfg* cfg, void* codes, void* sf, float* tensor_scale,
+                            void* workspace, size_t workspace_bytes, nvfp4_stream_t stream);
+
+/*
+ * nvfp4_dequantize: Q -> out [rows, k] with row stride ldo elements, as
+ * e2m1(code) * e4m3(scale) * s computed in FP32 (exact product, one rounding
+ * on the final multiply); BF16 output is that FP32 value rounded to nearest
+ * even.  Any sf layout.  Needs no workspace.
+ */
+nvfp4_status nvfp4_dequantize(const nvfp4_tensor* q, int32_t out_dtype, void* out, int64_t ldo,
+                              nvfp4_stream_t stream);
+
+/*
+ * nvfp4_gemm: D [M, N] = sA * sB * sum_k (eA * scaleA)(eB * scaleB), i.e.
+ * D = A * B^T for A [M, K] and B [N, K] (M = A->rows, N = B->rows,
+ * K = A->k = B->k), FP32 accumulation on the tensor cores (tcgen05
+ * block-scaled MMA), FP32 epilogue multiply by sA * sB, then BF16 (round to
+ * nearest even) or FP32 store, row stride ldd elements.
+ * Shape rules: K % 32 == 0; both operands' scales in NVFP4_SF_MMA layout;
+ * codes 16-byte aligned; ldd >= N.  M, N are arbitrary (ragged tiles are
+ * handled).  Workspace: nvfp4_gemm_workspace_size bytes (status word).
+ * Source: "Como o treinamento mixed-precision funciona com NVFP4" (NVFP4
+ * operands, FP32 accumulators) on the JAX/MaxText page.
+ */
+nvfp4_status nvfp4_gemm_workspace_size(int64_t M, int64_t N, int64_t K, size_t* bytes);
+nvfp4_status nvfp4_gemm(const nvfp4_tensor* a, const nvfp4_tensor* b, int32_t out_dtype, void* d,
+                        int64_t ldd, void* workspace, size_t workspace_bytes, nvfp4_stream_t stream);
+
+/*
+ * The linear layer Y = X W^T with X [T, din], W [dout, din], Y [T, dout]
+ * (all BF16, row-major, densely packed), and its two backward GEMMs:
+ *   fprop:  Y  = Q(X) Q(W)^T           X: 1x16 along din, W: 16x16 along din
+ *   dgrad:  dX = Q(dY) Q(W^T)^T        dY: 1x16 along dout, W^T: 16x16 along dout
+ *   wgrad:  dW = Q(dY^T) Q(X^T)^T      dY^T, X^T: 1x16 along T, RHT + SR
+ * Each wrapper quantises its two operands into its workspace, in the
+ * orientation its GEMM needs, then runs nvfp4_gemm.  cfg_* may be NULL for
+ * the defaults above (seeds: rht_seed NVFP4_DEFAULT_RHT_SEED for every
+ * operand, sr_seed 5 for dY^T and 6 for X^T in wgrad, sr_offset 0); a given
+ * cfg is used as is except that the wrapper sets `transpose` (by role) and
+ * `sf_layout` (MMA).  In wgrad both operands must share rht_seed for the
+ * transform to cancel in the product.
+ * Shape rules: din % 32 == 0, dout % 32 == 0, T % 32 == 0 (wgrad) and
+ * T % 16 == 0 otherwise.  Output dtype per out_dtype.
+ * Source: NVFP4 on weights and activations in GEMMs ("Como o treinamento
+ * mixed-precision funciona com NVFP4", JAX/MaxText page).
+ */
+#define NVFP4_DEFAULT_RHT_SEED 0x5EEDC0DE0F4ull
+typedef enum { NVFP4_LINEAR_FPROP = 0, NVFP4_LINEAR_DGRAD = 1, NVFP4_LINEAR_WGRAD = 2 } nvfp4_linear_op;
+nvfp4_status nvfp4_linear_workspace_size(int32_t op, int64_t tokens, int64_t din, int64_t dout,
+                                         size_t* bytes);
+nvfp4_status nvfp4_linear_fprop(const void* x, const void* w, int64_t tokens, int64_t din, int64_t dout,
+                                const nvfp4_quant_cfg* cfg_x, const nvfp4_quant_cfg* cfg_w,
+                                int32_t out_dtype, void* y, void* workspace, size_t workspace_bytes,
+                                nvfp4_stream_t stream);
+nvfp4_status nvfp4_linear_dgrad(const void* dy, const void* w, int64_t tokens, int64_t din, int64_t dout,
+                                const nvfp4_quant_cfg* cfg_dy, const nvfp4_quant_cfg* cfg_w,
+                                int32_t out_dtype, void* dx, void* workspace, size_t workspace_bytes,
+                                nvfp4_stream_t stream);
+nvfp4_status nvfp4_linear_wgrad(const void* dy, const void* x, int64_t tokens, int64_t din, int64_t dout,
+                                const nvfp4_quant_cfg* cfg_dy, const nvfp4_quant_cfg* cfg_x,
+                                int32_t out_dtype, void* dw, void* workspace, size_t workspace_bytes,
+                                nvfp4_stream_t stream);
+
+/*
+ * Synchronises `stream`, reads the status word of `workspace` (any workspace
+ * used by the calls above), clears it and returns it: NVFP4_OK,
+ * NVFP4_ERR_TIMEOUT or NVFP4_ERR_NONFINITE (or NVFP4_ERR_CUDA if the stream
+ * reports an error).
+ */
+nvfp4_status nvfp4_check_device_status(const void* workspace, nvfp4_stream_t stream);
+
+/*
+ * Failure-detection test hook.  With enable != 0, the next nvfp4_gemm
+ * launch (including one made by a linear wrapper) leaves the first
+ * shared-memory stage of CTA 0 unfilled: that CTA's bounded wait runs out
+ * after about one second, it records NVFP4_ERR_TIMEOUT in the workspace
+ * status word, drains its in-flight copies, frees its tensor memory and
+ * exits; the rest of the grid completes and the CUDA context stays usable.
+ * The output of that launch is unspecified.  One-shot: the flag clears
+ * itself when the launch takes it.  Nothing faults, traps or hangs.
+ */
+void nvfp4_debug_gemm_skip_load(int32_t enable);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* NVFP4_H */

@@ -61,6 +61,8 @@ def _lib():
         lib.oracle_rht16.argtypes = [P, P]
         lib.oracle_quantize.restype = ctypes.c_int
         lib.oracle_quantize.argtypes = [P, I64, I64, I64, ctypes.POINTER(_Cfg), P, P, P]
+        lib.oracle_quantize_rows.restype = ctypes.c_int
+        lib.oracle_quantize_rows.argtypes = [P, I64, I64, I64, ctypes.POINTER(_Cfg), I64, I64, P, P, P]
         lib.oracle_amax.restype = ctypes.c_int
         lib.oracle_amax.argtypes = [P, I64, I64, I64, ctypes.POINTER(_Cfg), P]
         lib.oracle_sf_mma_offset.restype = I64
@@ -154,6 +156,24 @@ def quantize(x_u16, cfg=None):
     sf = np.zeros((qr, max(qk // 16, 0)), dtype=np.uint8)
     ts = np.zeros(1, dtype=np.float32)
     st = _lib().oracle_quantize(_ptr(x), rows, cols, ld, ctypes.byref(c), _ptr(codes), _ptr(sf), _ptr(ts))
+    if st != OK:
+        raise OracleError(st)
+    return codes, sf, ts[0]
+
+
+def quantize_rows(x_u16, cfg, row_begin, row_end):
+    """Encode only rows [row_begin, row_end) of Q; the tensor scale is that
+    of the whole operand."""
+    x = np.ascontiguousarray(x_u16)
+    rows, cols = x.shape
+    c = _cfg(cfg)
+    qr, qk = (cols, rows) if c.transpose else (rows, cols)
+    n = row_end - row_begin
+    codes = np.zeros((n, qk // 2), dtype=np.uint8)
+    sf = np.zeros((n, qk // 16), dtype=np.uint8)
+    ts = np.zeros(1, dtype=np.float32)
+    st = _lib().oracle_quantize_rows(_ptr(x), rows, cols, cols, ctypes.byref(c), int(row_begin), int(row_end),
+                                     _ptr(codes), _ptr(sf), _ptr(ts))
     if st != OK:
         raise OracleError(st)
     return codes, sf, ts[0]

@@ -235,13 +235,19 @@ int oracle_amax(const uint16_t* x, int64_t rows, int64_t cols, int64_t ld,
   return ORACLE_OK;
 }
 
-int oracle_quantize(const uint16_t* x, int64_t rows, int64_t cols, int64_t ld,
-                    const oracle_cfg* cfg, uint8_t* codes, uint8_t* sf, float* tensor_scale) {
+/* Encode rows [row_begin, row_end) of Q; the tensor scale always comes from
+ * the amax of the whole operand.  codes / sf hold only the encoded rows. */
+int oracle_quantize_rows(const uint16_t* x, int64_t rows, int64_t cols, int64_t ld, const oracle_cfg* cfg,
+                         int64_t row_begin, int64_t row_end, uint8_t* codes, uint8_t* sf, float* tensor_scale) {
   int st = check_args(rows, cols, ld, cfg);
   if (st != ORACLE_OK) return st;
   int64_t R = 0, K = 0;
   float* q = logical_operand(x, rows, cols, ld, cfg, &R, &K);
   if (!q) return ORACLE_ERR_INVALID_ARG;
+  if (row_begin < 0 || row_end > R || row_begin > row_end) {
+    free(q);
+    return ORACLE_ERR_INVALID_ARG;
+  }
   int64_t KB = K / 16;
 
   /* Step 1: tensor amax, taken after the transform (reading). */
@@ -258,8 +264,9 @@ int oracle_quantize(const uint16_t* x, int64_t rows, int64_t cols, int64_t ld,
   if (s_dec == 0.0f) s_dec = 1.0f;
   *tensor_scale = s_dec;
 
-  memset(codes, 0, (size_t)(R * (K / 2)));
-  for (int64_t i = 0; i < R; ++i) {
+  memset(codes, 0, (size_t)((row_end - row_begin) * (K / 2)));
+  for (int64_t i = row_begin; i < row_end; ++i) {
+    int64_t oi = i - row_begin;
     for (int64_t b = 0; b < KB; ++b) {
       /* Step 3: block amax over the 1x16 run, or over the whole 16x16 tile
        * the run belongs to (its scale is then repeated on the tile's 16 rows). */
@@ -275,7 +282,7 @@ int oracle_quantize(const uint16_t* x, int64_t rows, int64_t cols, int64_t ld,
        * E4M3 round-to-nearest-even with saturation. */
       float t = (bamax / 6.0f) / s_dec;
       uint8_t sfb = oracle_e4m3_encode(t);
-      sf[i * KB + b] = sfb;
+      sf[oi * KB + b] = sfb;
       /* Step 5: elements v = x / (scale * s), one FP32 multiply then one FP32
        * division, rounded onto the E2M1 grid.  A zero block scale encodes the
        * whole run as code 0. */
@@ -299,12 +306,20 @@ int oracle_quantize(const uint16_t* x, int64_t rows, int64_t cols, int64_t ld,
           }
         }
         /* Packing: element 2j in the low nibble of byte j, 2j+1 in the high. */
-        codes[i * (K / 2) + k / 2] |= (uint8_t)(code << (4 * (k & 1)));
+        codes[oi * (K / 2) + k / 2] |= (uint8_t)(code << (4 * (k & 1)));
       }
     }
   }
   free(q);
   return ORACLE_OK;
+}
+
+int oracle_quantize(const uint16_t* x, int64_t rows, int64_t cols, int64_t ld,
+                    const oracle_cfg* cfg, uint8_t* codes, uint8_t* sf, float* tensor_scale) {
+  int st = check_args(rows, cols, ld, cfg);
+  if (st != ORACLE_OK) return st;
+  int64_t R = cfg->transpose ? cols : rows;
+  return oracle_quantize_rows(x, rows, cols, ld, cfg, 0, R, codes, sf, tensor_scale);
 }
 
 /* ------------------------------------------------------------------------- */

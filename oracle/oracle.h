@@ -77,6 +77,11 @@ void oracle_rht16(float v[16], const float sigma[16]);
 int oracle_quantize(const uint16_t* x, int64_t rows, int64_t cols, int64_t ld,
                     const oracle_cfg* cfg, uint8_t* codes, uint8_t* sf, float* tensor_scale);
 
+/* Same, encoding only rows [row_begin, row_end) of Q (the tensor scale is
+ * still that of the whole operand); codes / sf receive just those rows. */
+int oracle_quantize_rows(const uint16_t* x, int64_t rows, int64_t cols, int64_t ld, const oracle_cfg* cfg,
+                         int64_t row_begin, int64_t row_end, uint8_t* codes, uint8_t* sf, float* tensor_scale);
+
 /* Amax of the (optionally transformed) operand, as the quantiser sees it. */
 int oracle_amax(const uint16_t* x, int64_t rows, int64_t cols, int64_t ld,
                 const oracle_cfg* cfg, float* amax);

@@ -1,0 +1,121 @@
+"""The C ABI boundary without a GPU: the library loads, exports every symbol
+that include/nvfp4.h declares, and rejects bad arguments before launching
+anything."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import block_scaled_gemm_nvfp4_gb300 as nv
+from block_scaled_gemm_nvfp4_gb300 import _build
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "nvfp4.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    _build.build()
+    return nv.lib()
+
+
+def _declared():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(nvfp4_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_exports_every_declared_symbol(lib):
+    names = _declared()
+    assert len(names) >= 14
+    assert sorted(nv.EXPORTS) == names
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_status_strings(lib):
+    for s in range(7):
+        assert nv.nvfp4_status_string(s)
+    assert nv.nvfp4_version() >= 100
+
+
+def test_sizes(lib):
+    assert nv.nvfp4_codes_bytes(4, 32) == 64
+    assert nv.nvfp4_sf_bytes(4, 32, nv.NVFP4_SF_ROWMAJOR) == 8
+    assert nv.nvfp4_sf_bytes(4, 32, nv.NVFP4_SF_MMA) == 512
+    assert nv.nvfp4_sf_bytes(129, 320, nv.NVFP4_SF_MMA) == 2 * 5 * 512
+
+
+def _q(lib, x=8192, rows=64, cols=64, ldx=64, cfg=None, codes=8192, sf=8192, scale=8192, ws=8192, wsb=1 << 20):
+    c = cfg if cfg is not None else nv.quant_cfg()
+    P = ctypes.c_void_p
+    return lib.nvfp4_quantize(P(x), rows, cols, ldx, ctypes.byref(c), P(codes), P(sf), P(scale), P(ws), wsb,
+                              P(0))
+
+
+def test_quantize_validation(lib):
+    # fake, aligned, never dereferenced addresses: every case fails before launch
+    assert _q(lib, cfg=nv.quant_cfg(block=7)) == nv.NVFP4_ERR_INVALID_ARG
+    assert _q(lib, cfg=nv.quant_cfg(rounding=3)) == nv.NVFP4_ERR_INVALID_ARG
+    assert _q(lib, cfg=nv.quant_cfg(sf_layout=9)) == nv.NVFP4_ERR_INVALID_ARG
+    bad = nv.quant_cfg()
+    bad.reserved = 1
+    assert _q(lib, cfg=bad) == nv.NVFP4_ERR_INVALID_ARG
+    assert _q(lib, cols=40, ldx=40) == nv.NVFP4_ERR_UNSUPPORTED_SHAPE
+    assert _q(lib, rows=24, cfg=nv.quant_cfg(block=1)) == nv.NVFP4_ERR_UNSUPPORTED_SHAPE
+    assert _q(lib, rows=40, cfg=nv.quant_cfg(transpose=1)) == nv.NVFP4_ERR_UNSUPPORTED_SHAPE
+    assert _q(lib, ldx=32) == nv.NVFP4_ERR_INVALID_ARG
+    assert _q(lib, x=8194) == nv.NVFP4_ERR_INVALID_ARG
+    assert _q(lib, ldx=68) == nv.NVFP4_ERR_INVALID_ARG
+    assert _q(lib, x=0) == nv.NVFP4_ERR_INVALID_ARG
+    assert _q(lib, scale=0) == nv.NVFP4_ERR_INVALID_ARG
+    assert _q(lib, ws=0) == nv.NVFP4_ERR_WORKSPACE
+    assert _q(lib, wsb=100) == nv.NVFP4_ERR_WORKSPACE
+    assert lib.nvfp4_quantize(ctypes.c_void_p(8192), 64, 64, 64, None, ctypes.c_void_p(8192),
+                              ctypes.c_void_p(8192), ctypes.c_void_p(8192), ctypes.c_void_p(8192), 1 << 20,
+                              ctypes.c_void_p(0)) == nv.NVFP4_ERR_INVALID_ARG
+    n = ctypes.c_size_t(0)
+    assert lib.nvfp4_quantize_workspace_size(64, 64, ctypes.byref(nv.quant_cfg()), ctypes.byref(n)) == 0
+    assert n.value >= 256
+
+
+def _t(codes=8192, sf=8192, scale=8192, rows=64, k=64, layout=nv.NVFP4_SF_MMA):
+    return nv._Tensor(codes, sf, scale, rows, k, layout, 0)
+
+
+def test_gemm_validation(lib):
+    P = ctypes.c_void_p
+
+    def g(a, b, dt=0, d=8192, ldd=64, ws=8192, wsb=4096):
+        return lib.nvfp4_gemm(ctypes.byref(a), ctypes.byref(b), dt, P(d), ldd, P(ws), wsb, P(0))
+
+    assert g(_t(k=48), _t(k=48)) == nv.NVFP4_ERR_UNSUPPORTED_SHAPE      # K % 32
+    assert g(_t(k=64), _t(k=96)) == nv.NVFP4_ERR_INVALID_ARG            # K mismatch
+    assert g(_t(layout=0), _t()) == nv.NVFP4_ERR_UNSUPPORTED_SHAPE      # scales not in MMA layout
+    assert g(_t(), _t(), dt=5) == nv.NVFP4_ERR_INVALID_ARG
+    assert g(_t(), _t(), d=0) == nv.NVFP4_ERR_INVALID_ARG
+    assert g(_t(), _t(rows=100), ldd=64) == nv.NVFP4_ERR_INVALID_ARG    # ldd < N
+    assert g(_t(codes=8200), _t()) == nv.NVFP4_ERR_INVALID_ARG          # codes not 16-byte aligned
+    assert g(_t(), _t(), ws=0) == nv.NVFP4_ERR_WORKSPACE
+    assert g(_t(), _t(), wsb=16) == nv.NVFP4_ERR_WORKSPACE
+    assert g(_t(scale=0), _t()) == nv.NVFP4_ERR_INVALID_ARG
+    n = ctypes.c_size_t(0)
+    assert lib.nvfp4_gemm_workspace_size(128, 128, 80, ctypes.byref(n)) == nv.NVFP4_ERR_UNSUPPORTED_SHAPE
+    assert lib.nvfp4_gemm_workspace_size(128, 128, 128, ctypes.byref(n)) == 0 and n.value >= 4
+
+
+def test_linear_validation(lib):
+    P = ctypes.c_void_p
+    n = ctypes.c_size_t(0)
+    assert lib.nvfp4_linear_workspace_size(9, 64, 64, 64, ctypes.byref(n)) == nv.NVFP4_ERR_INVALID_ARG
+    assert lib.nvfp4_linear_workspace_size(0, 64, 48, 64, ctypes.byref(n)) == nv.NVFP4_ERR_UNSUPPORTED_SHAPE
+    assert lib.nvfp4_linear_workspace_size(2, 48, 64, 64, ctypes.byref(n)) == nv.NVFP4_ERR_UNSUPPORTED_SHAPE
+    assert lib.nvfp4_linear_workspace_size(2, 64, 64, 64, ctypes.byref(n)) == 0
+    need = n.value
+    args = (P(8192), P(8192), 64, 64, 64, None, None, 0, P(8192))
+    assert lib.nvfp4_linear_wgrad(*args, P(8192), need - 1, P(0)) == nv.NVFP4_ERR_WORKSPACE
+    assert lib.nvfp4_linear_fprop(P(0), P(8192), 64, 64, 64, None, None, 0, P(8192), P(8192), 1 << 24,
+                                  P(0)) == nv.NVFP4_ERR_INVALID_ARG
+    assert lib.nvfp4_linear_dgrad(P(8192), P(8192), 64, 64, 64, None, None, 3, P(8192), P(8192), 1 << 24,
+                                  P(0)) == nv.NVFP4_ERR_INVALID_ARG
+    assert lib.nvfp4_check_device_status(P(0), P(0)) == nv.NVFP4_ERR_INVALID_ARG
