@@ -106,8 +106,10 @@ nvfp4_status quantize_into(const void* x, int64_t rows, int64_t cols, int64_t ld
 }
 
 nvfp4_status check_tensor(const nvfp4_tensor* t) {
-  if (!t || !t->codes || !t->sf || !t->tensor_scale) return NVFP4_ERR_INVALID_ARG;
+  if (!t || !t->tensor_scale) return NVFP4_ERR_INVALID_ARG;
   if (t->rows < 0 || t->k < 0 || t->reserved != 0) return NVFP4_ERR_INVALID_ARG;
+  // an empty operand may come with null code / scale pointers
+  if ((t->rows > 0 && t->k > 0) && (!t->codes || !t->sf)) return NVFP4_ERR_INVALID_ARG;
   if (t->sf_layout != NVFP4_SF_ROWMAJOR && t->sf_layout != NVFP4_SF_MMA) return NVFP4_ERR_INVALID_ARG;
   if (t->k % 16 != 0) return NVFP4_ERR_UNSUPPORTED_SHAPE;
   return NVFP4_OK;
@@ -254,9 +256,11 @@ nvfp4_status nvfp4_gemm(const nvfp4_tensor* a, const nvfp4_tensor* b, int32_t ou
   if (a->sf_layout != NVFP4_SF_MMA || b->sf_layout != NVFP4_SF_MMA) return NVFP4_ERR_UNSUPPORTED_SHAPE;
   if (a->rows > (int64_t(1) << 31) || b->rows > (int64_t(1) << 31) || a->k > (int64_t(1) << 31))
     return NVFP4_ERR_UNSUPPORTED_SHAPE;
+  if (a->rows == 0 || b->rows == 0) return NVFP4_OK;  // empty output: nothing to compute
   if (!d || ldd < b->rows) return NVFP4_ERR_INVALID_ARG;
   if (!aligned16(a->codes) || !aligned16(b->codes) || !aligned16(a->sf) || !aligned16(b->sf))
     return NVFP4_ERR_INVALID_ARG;
+
   if (!workspace) return NVFP4_ERR_WORKSPACE;
   if (workspace_bytes < kWsHeaderBytes) return NVFP4_ERR_WORKSPACE;
   return gemm_into(a, b, out_dtype, d, ldd, static_cast<uint32_t*>(workspace),
