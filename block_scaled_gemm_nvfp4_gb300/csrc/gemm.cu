@@ -10,11 +10,14 @@
 //   warp 0     TMA producer: packed E2M1 codes by tiled TMA (128-byte
 //              swizzle) and the block scales by bulk copies, into a 4-stage
 //              shared-memory ring guarded by mbarriers;
-//   warp 1     allocates TMEM, copies each stage's block scales into TMEM
-//              (tcgen05.cp) and issues the block-scaled MMAs (K = 64 each,
+//   warp 1     allocates TMEM and issues the block-scaled MMAs (K = 64 each,
 //              four per 256-wide K stage) into a 128 x 256 FP32 TMEM
 //              accumulator; tcgen05.commit frees ring stages and signals
 //              the epilogue;
+//   warps 2-5  stage each ring stage's block scales from shared memory into
+//              TMEM with tcgen05.st (one warp per TMEM lane quarter), which
+//              keeps the scale traffic off the tensor pipe (a tcgen05.cp per
+//              64-wide K step and 128 rows would serialise with the MMAs);
 //   warps 2-9  epilogue, two warps per TMEM lane quarter, each owning 128 of
 //              the 256 columns: TMEM -> registers (tcgen05.ld), times sA * sB,
 //              BF16 (RNE) or FP32, stored to global memory.  In BF16 mode a
@@ -51,6 +54,7 @@ constexpr int kSfbBytes = 8 * kSfAtomBytes;   // two row atoms x 4 K atoms
 constexpr int kStageBytes = kABytes + kBBytes + kSfaBytes + kSfbBytes;
 constexpr int kThreads = 320;
 constexpr int kEpiWarps = 8;
+constexpr int kSfWarps = 4;                  // warps 2-5 stage block scales into TMEM
 constexpr int kEpiCols = BN / 2;            // columns per epilogue warp
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kAccCol = 0;
@@ -89,6 +93,7 @@ struct __align__(8) SmemCtl {
   uint64_t acc_full;
   uint64_t acc_empty;
   uint64_t drain;
+  uint64_t sfready[kStages];
   uint32_t tmem_base;
   int abort;
 };
@@ -118,6 +123,132 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   return *reinterpret_cast<const uint32_t*>(&v);
 }
 
+// Epilogue for one 128 x 128 half of a tile: TMEM -> registers -> global.
+// The warp's lane quarter q gives its 32 rows.  Returns after releasing the
+// accumulator (one arrival per warp on acc_empty).
+template <bool OUT_F32>
+__device__ __forceinline__ void epilogue_half(const GParams& p, SmemCtl* ctl, uint32_t tmem, int m_blk, int n_blk,
+                                              int q, int half, int lane, float alpha) {
+  const int64_t row = static_cast<int64_t>(m_blk) * BM + q * 32 + lane;
+  const int64_t col0 = static_cast<int64_t>(n_blk) * BN + half * kEpiCols;
+  const uint32_t taddr = tmem + (static_cast<uint32_t>(q * 32) << 16) + kAccCol + half * kEpiCols;
+  if (!OUT_F32) {
+    uint32_t packed[kEpiCols / 2];
+#pragma unroll
+    for (int c = 0; c < kEpiCols / 32; ++c) {
+      uint32_t r[32];
+      ptx::tmem_ld_32x32b_x32(taddr + c * 32, r);
+      ptx::tmem_ld_wait();
+#pragma unroll
+      for (int j = 0; j < 16; ++j)
+        packed[c * 16 + j] = pack_bf16(__fmul_rn(alpha, __uint_as_float(r[2 * j])),
+                                       __fmul_rn(alpha, __uint_as_float(r[2 * j + 1])));
+    }
+    ptx::tc_fence_before();
+    __syncwarp();
+    if (lane == 0) ptx::mbar_arrive(&ctl->acc_empty);
+    if (row < p.M) {
+      __nv_bfloat16* drow = static_cast<__nv_bfloat16*>(p.d) + row * p.ldd;
+#pragma unroll
+      for (int c8 = 0; c8 < kEpiCols / 8; ++c8) {
+        const int64_t col = col0 + c8 * 8;
+        if (p.vec_store && col + 8 <= p.N) {
+          *reinterpret_cast<uint4*>(drow + col) =
+              make_uint4(packed[c8 * 4], packed[c8 * 4 + 1], packed[c8 * 4 + 2], packed[c8 * 4 + 3]);
+        } else {
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            if (col + j < p.N) {
+              const uint32_t w = packed[c8 * 4 + j / 2];
+              const uint16_t h = static_cast<uint16_t>((j & 1) ? (w >> 16) : (w & 0xFFFFu));
+              reinterpret_cast<uint16_t*>(drow)[col + j] = h;
+            }
+          }
+        }
+      }
+    }
+  } else {
+    float* drow = static_cast<float*>(p.d) + row * p.ldd;
+#pragma unroll 1
+    for (int c = 0; c < kEpiCols / 32; ++c) {
+      uint32_t r[32];
+      ptx::tmem_ld_32x32b_x32(taddr + c * 32, r);
+      ptx::tmem_ld_wait();
+      if (row < p.M) {
+#pragma unroll
+        for (int j4 = 0; j4 < 8; ++j4) {
+          const int64_t col = col0 + c * 32 + j4 * 4;
+          const float4 v = make_float4(__fmul_rn(alpha, __uint_as_float(r[4 * j4])),
+                                       __fmul_rn(alpha, __uint_as_float(r[4 * j4 + 1])),
+                                       __fmul_rn(alpha, __uint_as_float(r[4 * j4 + 2])),
+                                       __fmul_rn(alpha, __uint_as_float(r[4 * j4 + 3])));
+          if (p.vec_store && col + 4 <= p.N) {
+            *reinterpret_cast<float4*>(drow + col) = v;
+          } else {
+            if (col < p.N) drow[col] = v.x;
+            if (col + 1 < p.N) drow[col + 1] = v.y;
+            if (col + 2 < p.N) drow[col + 2] = v.z;
+            if (col + 3 < p.N) drow[col + 3] = v.w;
+          }
+        }
+      }
+    }
+    ptx::tc_fence_before();
+    __syncwarp();
+    if (lane == 0) ptx::mbar_arrive(&ctl->acc_empty);
+  }
+}
+
+// Warp-uniform bounded wait: lane 0 polls, the result is broadcast.
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag, int lane) {
+  uint32_t ok = 1;
+  if (lane == 0) ok = ptx::mbar_wait(bar, parity, abort_flag) ? 1u : 0u;
+  return __shfl_sync(0xFFFFFFFFu, ok, 0) != 0;
+}
+
+// Scale staging for one ring stage.  Layout the block-scaled MMA reads
+// (scale_vec::4X, M = 128): for a 128-row operand block and one K = 64 step,
+// TMEM lane 32 q + l, column base + j holds the four scales of row l + 32 j;
+// every lane quarter q holds the whole block, because the quarter that
+// computes output rows 32 q .. 32 q + 31 reads the B scales of all N rows
+// from its own lanes (and the A scales of its own rows from column base + q).
+// That is exactly one 16-byte row of a 512-byte scale atom per lane, so each
+// staging warp (lane quarter q) copies atom row `lane` into its own lanes.
+// Columns: A at kSfaCol + 16 s + 4 kk, B row block rb at kSfbCol + 32 s +
+// 8 kk + 4 rb (a 256-row B tile is read as columns base .. base + 7).
+__device__ __forceinline__ void stage_scales(const uint8_t* st, uint32_t tmem, int s, int q, int lane) {
+  const uint8_t* sfa = st + kABytes + kBBytes;
+  const uint8_t* sfb = sfa + kSfaBytes;
+  const uint32_t lane_base = tmem + (static_cast<uint32_t>(q * 32) << 16);
+  uint32_t va[16];
+#pragma unroll
+  for (int kk = 0; kk < 4; ++kk) {
+    const uint4 v = *reinterpret_cast<const uint4*>(sfa + kk * kSfAtomBytes + lane * 16);
+    va[4 * kk] = v.x;
+    va[4 * kk + 1] = v.y;
+    va[4 * kk + 2] = v.z;
+    va[4 * kk + 3] = v.w;
+  }
+  ptx::tmem_st_32x32b_x16(lane_base + kSfaCol + s * 16, va);
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    uint32_t vb[16];
+#pragma unroll
+    for (int k2 = 0; k2 < 2; ++k2) {
+      const int kk = 2 * h + k2;
+#pragma unroll
+      for (int rb = 0; rb < 2; ++rb) {
+        const uint4 v = *reinterpret_cast<const uint4*>(sfb + rb * 4 * kSfAtomBytes + kk * kSfAtomBytes + lane * 16);
+        vb[8 * k2 + 4 * rb] = v.x;
+        vb[8 * k2 + 4 * rb + 1] = v.y;
+        vb[8 * k2 + 4 * rb + 2] = v.z;
+        vb[8 * k2 + 4 * rb + 3] = v.w;
+      }
+    }
+    ptx::tmem_st_32x32b_x16(lane_base + kSfbCol + s * 32 + h * 16, vb);
+  }
+}
+
 template <bool OUT_F32>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
@@ -134,6 +265,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int s = 0; s < kStages; ++s) {
       ptx::mbar_init(&ctl->full[s], 1);
       ptx::mbar_init(&ctl->empty[s], 1);
+      ptx::mbar_init(&ctl->sfready[s], kSfWarps);
     }
     ptx::mbar_init(&ctl->acc_full, 1);
     ptx::mbar_init(&ctl->acc_empty, kEpiWarps);
@@ -177,7 +309,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           uint8_t* st = smem + stage * kStageBytes;
           if (p.skip_first_load && blockIdx.x == 0 && tile == static_cast<int>(blockIdx.x) && kb == 0) {
             // Failure-detection test hook: this stage is never filled, so the
-            // MMA warp's bounded wait runs out and the CTA reports a timeout.
+            // bounded waits on it run out and the CTA reports a timeout.
             if (++stage == kStages) {
               stage = 0;
               phase ^= 1u;
@@ -219,17 +351,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t phase = 0, acc_phase = 0;
       bool ok = true, issued = false;
       for (int tile = blockIdx.x; tile < p.num_tiles && ok; tile += gridDim.x) {
-        int m_blk, n_blk;
-        tile_coords(p, tile, m_blk, n_blk);
-        const int64_t n_rows_left = p.N - static_cast<int64_t>(n_blk) * BN;
-        const int nb_atoms = static_cast<int>(min(static_cast<int64_t>(2), (n_rows_left + 127) / 128));
         if (!ptx::mbar_wait(&ctl->acc_empty, acc_phase ^ 1u, abort_flag)) {
           fail(ctl, p, 3);
           break;
         }
         ptx::tc_fence_after();
         for (int kb = 0; kb < p.num_kb; ++kb) {
-          if (!ptx::mbar_wait(&ctl->full[stage], phase, abort_flag)) {
+          // The scale warps arrive once the stage's operands have landed and
+          // its scales are in TMEM.
+          if (!ptx::mbar_wait(&ctl->sfready[stage], phase, abort_flag)) {
             fail(ctl, p, 4);
             ok = false;
             break;
@@ -239,18 +369,6 @@ __global__ void __launch_bounds__(kThreads, 1)
           uint8_t* st = smem + stage * kStageBytes;
           const uint32_t a_addr = ptx::smem_u32(st);
           const uint32_t b_addr = ptx::smem_u32(st + kABytes);
-          const uint32_t sfa_addr = ptx::smem_u32(st + kABytes + kBBytes);
-          const uint32_t sfb_addr = sfa_addr + kSfaBytes;
-          for (int kk = 0; kk < kk_n; ++kk) {
-            const uint32_t sfa_t = tmem + kSfaCol + stage * 16 + kk * 4;
-            ptx::tc_cp_32x128b_warpx4(sfa_t, ptx::smem_desc(sfa_addr + kk * kSfAtomBytes, 16, 128, ptx::kSwizzleNone));
-            for (int rb = 0; rb < nb_atoms; ++rb) {
-              const uint32_t sfb_t = tmem + kSfbCol + stage * 32 + kk * 8 + rb * 4;
-              ptx::tc_cp_32x128b_warpx4(
-                  sfb_t, ptx::smem_desc(sfb_addr + rb * 4 * kSfAtomBytes + kk * kSfAtomBytes, 16, 128,
-                                        ptx::kSwizzleNone));
-            }
-          }
           for (int kk = 0; kk < kk_n; ++kk) {
             const uint64_t adesc = ptx::smem_desc(a_addr + kk * 32, 16, 1024, ptx::kSwizzle128B);
             const uint64_t bdesc = ptx::smem_desc(b_addr + kk * 32, 16, 1024, ptx::kSwizzle128B);
@@ -269,100 +387,50 @@ __global__ void __launch_bounds__(kThreads, 1)
         acc_phase ^= 1u;
       }
       if (issued) {
-        // Wait for every MMA and scale copy issued above before TMEM is freed.
+        // Wait for every MMA issued above before TMEM is freed.
         ptx::tc_commit(&ctl->drain);
         volatile int never = 0;
         if (!ptx::mbar_wait(&ctl->drain, 0, &never)) fail(ctl, p, 5);
       }
     }
   } else {
-    // ------------------------------------------------------------ epilogue
-    const int q = warp & 3;                 // TMEM lane quarter this warp may access
-    const int half = (warp - 2) >> 2;       // which 128 columns of the tile
-    const int row_in_tile = q * 32 + lane;
+    // ----------------------------------------- scale staging and epilogue
+    const int q = warp & 3;               // TMEM lane quarter this warp may access
+    const int half = (warp - 2) >> 2;     // which 128 columns of the tile it stores
+    const bool stager = half == 0;        // warps 2-5 also stage the block scales
     const float alpha = __fmul_rn(*p.a_scale, *p.b_scale);
-    uint32_t acc_phase = 0;
-    for (int tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x) {
+    int stage = 0;
+    uint32_t phase = 0, acc_phase = 0;
+    bool ok = true;
+    for (int tile = blockIdx.x; tile < p.num_tiles && ok; tile += gridDim.x) {
       int m_blk, n_blk;
       tile_coords(p, tile, m_blk, n_blk);
-      // One lane waits and the result is broadcast, so the warp stays
-      // converged for the .sync.aligned TMEM loads below.
-      uint32_t ok = 1;
-      if (lane == 0) ok = ptx::mbar_wait(&ctl->acc_full, acc_phase, abort_flag) ? 1u : 0u;
-      ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
-      if (!ok) {
+      if (stager) {
+        for (int kb = 0; kb < p.num_kb; ++kb) {
+          if (!warp_wait(&ctl->full[stage], phase, abort_flag, lane)) {
+            if (lane == 0) fail(ctl, p, 7);
+            ok = false;
+            break;
+          }
+          ptx::tc_fence_after();
+          stage_scales(smem + stage * kStageBytes, tmem, stage, q, lane);
+          ptx::tmem_st_wait();
+          ptx::tc_fence_before();
+          __syncwarp();
+          if (lane == 0) ptx::mbar_arrive(&ctl->sfready[stage]);
+          if (++stage == kStages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+      }
+      if (!warp_wait(&ctl->acc_full, acc_phase, abort_flag, lane)) {
         if (lane == 0) fail(ctl, p, 6);
         break;
       }
       ptx::tc_fence_after();
-      const int64_t row = static_cast<int64_t>(m_blk) * BM + row_in_tile;
-      const int64_t col0 = static_cast<int64_t>(n_blk) * BN + half * kEpiCols;
-      const uint32_t taddr = tmem + (static_cast<uint32_t>(q * 32) << 16) + kAccCol + half * kEpiCols;
-      if (!OUT_F32) {
-        uint32_t packed[kEpiCols / 2];
-#pragma unroll
-        for (int c = 0; c < kEpiCols / 32; ++c) {
-          uint32_t r[32];
-          ptx::tmem_ld_32x32b_x32(taddr + c * 32, r);
-          ptx::tmem_ld_wait();
-#pragma unroll
-          for (int j = 0; j < 16; ++j)
-            packed[c * 16 + j] = pack_bf16(__fmul_rn(alpha, __uint_as_float(r[2 * j])),
-                                           __fmul_rn(alpha, __uint_as_float(r[2 * j + 1])));
-        }
-        ptx::tc_fence_before();
-        __syncwarp();
-        if (lane == 0) ptx::mbar_arrive(&ctl->acc_empty);
-        if (row < p.M) {
-          __nv_bfloat16* drow = static_cast<__nv_bfloat16*>(p.d) + row * p.ldd;
-#pragma unroll
-          for (int c8 = 0; c8 < kEpiCols / 8; ++c8) {
-            const int64_t col = col0 + c8 * 8;
-            if (p.vec_store && col + 8 <= p.N) {
-              *reinterpret_cast<uint4*>(drow + col) =
-                  make_uint4(packed[c8 * 4], packed[c8 * 4 + 1], packed[c8 * 4 + 2], packed[c8 * 4 + 3]);
-            } else {
-#pragma unroll
-              for (int j = 0; j < 8; ++j) {
-                if (col + j < p.N) {
-                  const uint32_t w = packed[c8 * 4 + j / 2];
-                  const uint16_t h = static_cast<uint16_t>((j & 1) ? (w >> 16) : (w & 0xFFFFu));
-                  reinterpret_cast<uint16_t*>(drow)[col + j] = h;
-                }
-              }
-            }
-          }
-        }
-      } else {
-        float* drow = static_cast<float*>(p.d) + row * p.ldd;
-#pragma unroll 1
-        for (int c = 0; c < kEpiCols / 32; ++c) {
-          uint32_t r[32];
-          ptx::tmem_ld_32x32b_x32(taddr + c * 32, r);
-          ptx::tmem_ld_wait();
-          if (row < p.M) {
-#pragma unroll
-            for (int j4 = 0; j4 < 8; ++j4) {
-              const int64_t col = col0 + c * 32 + j4 * 4;
-              const float4 v = make_float4(__fmul_rn(alpha, __uint_as_float(r[4 * j4])),
-                                           __fmul_rn(alpha, __uint_as_float(r[4 * j4 + 1])),
-                                           __fmul_rn(alpha, __uint_as_float(r[4 * j4 + 2])),
-                                           __fmul_rn(alpha, __uint_as_float(r[4 * j4 + 3])));
-              if (p.vec_store && col + 4 <= p.N) {
-                *reinterpret_cast<float4*>(drow + col) = v;
-              } else {
-                if (col < p.N) drow[col] = v.x;
-                if (col + 1 < p.N) drow[col + 1] = v.y;
-                if (col + 2 < p.N) drow[col + 2] = v.z;
-                if (col + 3 < p.N) drow[col + 3] = v.w;
-              }
-            }
-          }
-        }
-        ptx::tc_fence_before();
-        __syncwarp();
-        if (lane == 0) ptx::mbar_arrive(&ctl->acc_empty);
-      }
+      epilogue_half<OUT_F32>(p, ctl, tmem, m_blk, n_blk, q, half, lane, alpha);
       acc_phase ^= 1u;
     }
   }
