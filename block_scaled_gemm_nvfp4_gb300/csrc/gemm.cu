@@ -14,10 +14,11 @@
 //              four per 256-wide K stage) into a 128 x 256 FP32 TMEM
 //              accumulator; tcgen05.commit frees ring stages and signals
 //              the epilogue;
-//   warps 2-5  stage each ring stage's block scales from shared memory into
+//   warps 10-13 stage each ring stage's block scales from shared memory into
 //              TMEM with tcgen05.st (one warp per TMEM lane quarter), which
 //              keeps the scale traffic off the tensor pipe (a tcgen05.cp per
 //              64-wide K step and 128 rows would serialise with the MMAs);
+//              the scales travel on their own barrier, ahead of the codes;
 //   warps 2-9  epilogue, two warps per TMEM lane quarter, each owning 128 of
 //              the 256 columns: TMEM -> registers (tcgen05.ld), times sA * sB,
 //              BF16 (RNE) or FP32, stored to global memory.  In BF16 mode a
@@ -52,9 +53,10 @@ constexpr int kSfAtomBytes = 512;             // 128 rows x 4 scales
 constexpr int kSfaBytes = 4 * kSfAtomBytes;   // one row atom x 4 K atoms
 constexpr int kSfbBytes = 8 * kSfAtomBytes;   // two row atoms x 4 K atoms
 constexpr int kStageBytes = kABytes + kBBytes + kSfaBytes + kSfbBytes;
-constexpr int kThreads = 320;
+constexpr int kThreads = 448;  // 14 warps: producer, MMA, 8 epilogue, 4 scale staging
 constexpr int kEpiWarps = 8;
-constexpr int kSfWarps = 4;                  // warps 2-5 stage block scales into TMEM
+constexpr int kSfWarps = 4;                  // warps 10-13 stage block scales into TMEM
+constexpr int kFirstSfWarp = 10;
 constexpr int kEpiCols = BN / 2;            // columns per epilogue warp
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kAccCol = 0;
@@ -88,7 +90,8 @@ struct GParams {
 };
 
 struct __align__(8) SmemCtl {
-  uint64_t full[kStages];
+  uint64_t full[kStages];      // codes of A and B landed
+  uint64_t sf_full[kStages];   // block scales of A and B landed
   uint64_t empty[kStages];
   uint64_t acc_full;
   uint64_t acc_empty;
@@ -264,6 +267,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       ptx::mbar_init(&ctl->full[s], 1);
+      ptx::mbar_init(&ctl->sf_full[s], 1);
       ptx::mbar_init(&ctl->empty[s], 1);
       ptx::mbar_init(&ctl->sfready[s], kSfWarps);
     }
@@ -316,18 +320,20 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             continue;
           }
-          ptx::mbar_arrive_expect_tx(&ctl->full[stage],
-                                     static_cast<uint32_t>(kABytes + kBBytes) + sf_bytes * (1 + nb_atoms));
-          ptx::tma_load_2d(st, &tmap_a, &ctl->full[stage], kb * kRowBytes, m_blk * BM);
-          ptx::tma_load_2d(st + kABytes, &tmap_b, &ctl->full[stage], kb * kRowBytes, n_blk * BN);
+          // Scales first, on their own barrier: the staging warps can move
+          // them into TMEM while the larger code tiles are still in flight.
+          ptx::mbar_arrive_expect_tx(&ctl->sf_full[stage], sf_bytes * (1 + nb_atoms));
           const uint8_t* sfa = p.a_sf + (static_cast<int64_t>(m_blk) * p.sf_katoms + kb * 4) * kSfAtomBytes;
-          ptx::bulk_load(st + kABytes + kBBytes, sfa, sf_bytes, &ctl->full[stage]);
+          ptx::bulk_load(st + kABytes + kBBytes, sfa, sf_bytes, &ctl->sf_full[stage]);
           for (int rb = 0; rb < nb_atoms; ++rb) {
             const uint8_t* sfb =
                 p.b_sf + (static_cast<int64_t>(n_blk * 2 + rb) * p.sf_katoms + kb * 4) * kSfAtomBytes;
             ptx::bulk_load(st + kABytes + kBBytes + kSfaBytes + rb * 4 * kSfAtomBytes, sfb, sf_bytes,
-                           &ctl->full[stage]);
+                           &ctl->sf_full[stage]);
           }
+          ptx::mbar_arrive_expect_tx(&ctl->full[stage], static_cast<uint32_t>(kABytes + kBBytes));
+          ptx::tma_load_2d(st, &tmap_a, &ctl->full[stage], kb * kRowBytes, m_blk * BM);
+          ptx::tma_load_2d(st + kABytes, &tmap_b, &ctl->full[stage], kb * kRowBytes, n_blk * BN);
           issued_mask |= 1u << stage;
           issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
           if (++stage == kStages) {
@@ -341,6 +347,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (issued_mask & (1u << s)) {
           volatile int never = 0;
           if (!ptx::mbar_wait(&ctl->full[s], (issued_parity >> s) & 1u, &never)) fail(ctl, p, 2);
+          if (!ptx::mbar_wait(&ctl->sf_full[s], (issued_parity >> s) & 1u, &never)) fail(ctl, p, 2);
         }
       }
     }
@@ -357,9 +364,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         ptx::tc_fence_after();
         for (int kb = 0; kb < p.num_kb; ++kb) {
-          // The scale warps arrive once the stage's operands have landed and
-          // its scales are in TMEM.
-          if (!ptx::mbar_wait(&ctl->sfready[stage], phase, abort_flag)) {
+          // The stage's scales are in TMEM and its code tiles have landed.
+          if (!ptx::mbar_wait(&ctl->sfready[stage], phase, abort_flag) ||
+              !ptx::mbar_wait(&ctl->full[stage], phase, abort_flag)) {
             fail(ctl, p, 4);
             ok = false;
             break;
@@ -393,38 +400,40 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!ptx::mbar_wait(&ctl->drain, 0, &never)) fail(ctl, p, 5);
       }
     }
-  } else {
-    // ----------------------------------------- scale staging and epilogue
-    const int q = warp & 3;               // TMEM lane quarter this warp may access
-    const int half = (warp - 2) >> 2;     // which 128 columns of the tile it stores
-    const bool stager = half == 0;        // warps 2-5 also stage the block scales
-    const float alpha = __fmul_rn(*p.a_scale, *p.b_scale);
+  } else if (warp >= kFirstSfWarp) {
+    // ------------------------------------------------------ scale staging
+    const int q = warp & 3;  // TMEM lane quarter this warp may access
     int stage = 0;
-    uint32_t phase = 0, acc_phase = 0;
+    uint32_t phase = 0;
     bool ok = true;
     for (int tile = blockIdx.x; tile < p.num_tiles && ok; tile += gridDim.x) {
+      for (int kb = 0; kb < p.num_kb; ++kb) {
+        if (!warp_wait(&ctl->sf_full[stage], phase, abort_flag, lane)) {
+          if (lane == 0) fail(ctl, p, 7);
+          ok = false;
+          break;
+        }
+        ptx::tc_fence_after();
+        stage_scales(smem + stage * kStageBytes, tmem, stage, q, lane);
+        ptx::tmem_st_wait();
+        ptx::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(&ctl->sfready[stage]);
+        if (++stage == kStages) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int q = warp & 3;              // TMEM lane quarter this warp may access
+    const int half = (warp - 2) >> 2;    // which 128 columns of the tile it stores
+    const float alpha = __fmul_rn(*p.a_scale, *p.b_scale);
+    uint32_t acc_phase = 0;
+    for (int tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x) {
       int m_blk, n_blk;
       tile_coords(p, tile, m_blk, n_blk);
-      if (stager) {
-        for (int kb = 0; kb < p.num_kb; ++kb) {
-          if (!warp_wait(&ctl->full[stage], phase, abort_flag, lane)) {
-            if (lane == 0) fail(ctl, p, 7);
-            ok = false;
-            break;
-          }
-          ptx::tc_fence_after();
-          stage_scales(smem + stage * kStageBytes, tmem, stage, q, lane);
-          ptx::tmem_st_wait();
-          ptx::tc_fence_before();
-          __syncwarp();
-          if (lane == 0) ptx::mbar_arrive(&ctl->sfready[stage]);
-          if (++stage == kStages) {
-            stage = 0;
-            phase ^= 1u;
-          }
-        }
-        if (!ok) break;
-      }
       if (!warp_wait(&ctl->acc_full, acc_phase, abort_flag, lane)) {
         if (lane == 0) fail(ctl, p, 6);
         break;
