@@ -6,24 +6,28 @@
 // LLM: NVFP4 no Blackwell...", section "Como o treinamento mixed-precision
 // funciona com NVFP4"); both operands K-major (D = A * B^T).
 //
-// Structure: a persistent kernel, one CTA per SM, 128 x 256 output tiles.
-//   warp 0     TMA producer: packed E2M1 codes by tiled TMA (128-byte
-//              swizzle) and the block scales by bulk copies, into a 4-stage
-//              shared-memory ring guarded by mbarriers;
-//   warp 1     allocates TMEM and issues the block-scaled MMAs (K = 64 each,
-//              four per 256-wide K stage) into a 128 x 256 FP32 TMEM
-//              accumulator; tcgen05.commit frees ring stages and signals
-//              the epilogue;
-//   warps 10-13 stage each ring stage's block scales from shared memory into
-//              TMEM with tcgen05.st (one warp per TMEM lane quarter), which
-//              keeps the scale traffic off the tensor pipe (a tcgen05.cp per
-//              64-wide K step and 128 rows would serialise with the MMAs);
-//              the scales travel on their own barrier, ahead of the codes;
+// Persistent, warp-specialised kernel, one CTA per SM, two modes:
+//   pair mode (M > 128): a cluster of two CTAs computes a 256 x 256 tile with
+//     cta_group::2 MMAs.  Each CTA holds 128 rows of A and 128 rows of B per
+//     ring stage (38 KB, five stages); the leader CTA issues the MMAs, which
+//     read both CTAs' shared memory and write each CTA's 128 x 256 FP32
+//     accumulator in its own TMEM.  Per SM this halves the B bytes written
+//     by TMA and read by the tensor core, which matters because the kernel is
+//     bound by shared-memory bandwidth (TMA writes + MMA operand reads);
+//   single mode (M <= 128): one CTA per 128 x 256 tile, cta_group::1, four
+//     54 KB stages.
+// Warp roles (14 warps):
+//   warp 0     TMA producer: packed E2M1 codes by tiled TMA (128-byte swizzle),
+//              block scales by bulk copies on their own barrier;
+//   warp 1     TMEM allocation; in the leader (or single) CTA the MMA issuer;
 //   warps 2-9  epilogue, two warps per TMEM lane quarter, each owning 128 of
 //              the 256 columns: TMEM -> registers (tcgen05.ld), times sA * sB,
-//              BF16 (RNE) or FP32, stored to global memory.  In BF16 mode a
-//              warp converts its whole half-row block into registers first so
-//              that the accumulator is released before the stores are issued.
+//              BF16 (RNE) or FP32, stored to global memory.  In BF16 mode the
+//              accumulator is released before the stores are issued;
+//   warps 10-13 stage each ring stage's block scales from shared memory into
+//              TMEM with tcgen05.st (one warp per lane quarter).  This keeps
+//              the scale traffic off the tensor pipe, where a tcgen05.cp per
+//              64-wide K step and 128 rows serialises with the MMAs.
 // Every mbarrier wait is bounded; on a timeout the CTA records
 // NVFP4_ERR_TIMEOUT in the status word, drains its in-flight copies and MMAs,
 // frees TMEM and exits.
@@ -42,42 +46,50 @@
 namespace nvfp4 {
 namespace {
 
-constexpr int BM = 128;
-constexpr int BN = 256;
+constexpr int BM = 128;                       // accumulator rows per CTA
+constexpr int BN = 256;                       // accumulator columns
 constexpr int BK = 256;                       // elements of K per stage
 constexpr int kRowBytes = BK / 2;             // 128 bytes of packed codes per row per stage
-constexpr int kStages = 4;
 constexpr int kABytes = BM * kRowBytes;       // 16 KB
-constexpr int kBBytes = BN * kRowBytes;       // 32 KB
 constexpr int kSfAtomBytes = 512;             // 128 rows x 4 scales
 constexpr int kSfaBytes = 4 * kSfAtomBytes;   // one row atom x 4 K atoms
 constexpr int kSfbBytes = 8 * kSfAtomBytes;   // two row atoms x 4 K atoms
-constexpr int kStageBytes = kABytes + kBBytes + kSfaBytes + kSfbBytes;
-constexpr int kThreads = 448;  // 14 warps: producer, MMA, 8 epilogue, 4 scale staging
+constexpr int kThreads = 448;                 // 14 warps
 constexpr int kEpiWarps = 8;
-constexpr int kSfWarps = 4;                  // warps 10-13 stage block scales into TMEM
+constexpr int kSfWarps = 4;
 constexpr int kFirstSfWarp = 10;
-constexpr int kEpiCols = BN / 2;            // columns per epilogue warp
+constexpr int kEpiCols = BN / 2;              // columns per epilogue warp
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kAccCol = 0;
 constexpr uint32_t kSfaCol = 256;             // + stage * 16 + kk * 4
-constexpr uint32_t kSfbCol = 320;             // + stage * 32 + kk * 8 + row_atom * 4
-constexpr int kGroupM = 16;                   // tile raster: groups of 16 row blocks
-constexpr int kSmemBytes = kStages * kStageBytes + 1024 /*barriers*/ + 1024 /*alignment*/;
+constexpr int kGroup = 16;                    // tile raster group (row or column blocks)
 
-static_assert(kStageBytes % 1024 == 0, "stages must keep 1024-byte alignment for 128B swizzle");
-
-// Instruction descriptor for kind::mxf4nvf4: dense, A and B E2M1 (format 1),
-// both K-major, N >> 3 at bit 17, UE4M3 scales (bit 23 = 0), M >> 4 at bit 24,
-// scale-factor ids 0.
-constexpr uint32_t kIdesc = (1u << 7) | (1u << 10) | ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
+// Per-mode layout.  PAIR: B rows per CTA 128, five stages; single: 256, four.
+template <bool PAIR>
+struct Layout {
+  static constexpr int kBRows = PAIR ? BN / 2 : BN;
+  static constexpr int kBBytes = kBRows * kRowBytes;
+  static constexpr int kStages = PAIR ? 5 : 4;
+  static constexpr int kStageBytes = kABytes + kBBytes + kSfaBytes + kSfbBytes;
+  static constexpr int kSmemBytes = kStages * kStageBytes + 1024 /*barriers*/ + 1024 /*alignment*/;
+  static constexpr uint32_t kSfbCol = kSfaCol + 16 * kStages;  // + stage * 32 + kk * 8 + row_atom * 4
+  // Instruction descriptor for kind::mxf4nvf4: dense, A and B E2M1 (format 1),
+  // both K-major, N >> 3 at bit 17, UE4M3 scales (bit 23 = 0), M >> 4 at bit
+  // 24 (M = 256 across the pair in PAIR mode), scale-factor ids 0.
+  static constexpr uint32_t kIdesc =
+      (1u << 7) | (1u << 10) | ((uint32_t)(BN >> 3) << 17) | ((uint32_t)((PAIR ? 2 * BM : BM) >> 4) << 24);
+  static_assert(kStageBytes % 1024 == 0, "stages must keep 1024-byte alignment for 128B swizzle");
+  static_assert(kSmemBytes <= 232448, "shared memory budget");
+  static_assert(kSfbCol + 32 * kStages <= kTmemCols, "TMEM budget");
+};
 
 struct GParams {
   int64_t M, N, K;
   int num_kb;        // K stages
   int tiles_m, tiles_n, num_tiles;
+  int tiles_mp;      // row-block pairs (pair mode)
+  int num_units;     // tiles, or tile pairs in pair mode
   int64_t sf_katoms; // 64-wide K atoms per row block in the scale layout
-  int64_t a_row_atoms, b_row_atoms;
   const uint8_t* a_sf;
   const uint8_t* b_sf;
   const float* a_scale;
@@ -85,30 +97,53 @@ struct GParams {
   void* d;
   int64_t ldd;
   int vec_store;
+  int group_n;          // raster groups column blocks instead of row blocks
   int skip_first_load;  // test hook: CTA 0 never loads its first stage
   uint32_t* status;
 };
 
+template <int STAGES>
 struct __align__(8) SmemCtl {
-  uint64_t full[kStages];      // codes of A and B landed
-  uint64_t sf_full[kStages];   // block scales of A and B landed
-  uint64_t empty[kStages];
+  uint64_t full[STAGES];      // codes landed (pair mode: both CTAs' codes, leader's copy)
+  uint64_t sf_full[STAGES];   // this CTA's block scales landed
+  uint64_t empty[STAGES];     // stage consumed by the MMAs
+  uint64_t sfready[STAGES];   // scales in TMEM (pair mode: both CTAs', leader's copy)
   uint64_t acc_full;
-  uint64_t acc_empty;
+  uint64_t acc_empty;         // accumulator drained (pair mode: both CTAs', leader's copy)
   uint64_t drain;
-  uint64_t sfready[kStages];
   uint32_t tmem_base;
   int abort;
 };
 
-__device__ __forceinline__ void tile_coords(const GParams& p, int tile, int& m_blk, int& n_blk) {
-  const int per_group = kGroupM * p.tiles_n;
+// Tile raster: tiles are taken in groups of kGroup row blocks (sweeping every
+// column block) or kGroup column blocks (sweeping every row block), whichever
+// re-reads fewer operand bytes from DRAM; inside a group the fast index runs
+// over the group so concurrent CTAs share operand panels in L2.
+__device__ __forceinline__ void tile_coords(const GParams& p, int tile, int tiles_m, int& m_blk, int& n_blk) {
+  const int slow_tiles = p.group_n ? tiles_m : p.tiles_n;
+  const int fast_tiles = p.group_n ? p.tiles_n : tiles_m;
+  const int per_group = kGroup * slow_tiles;
   const int group = tile / per_group;
-  const int first_m = group * kGroupM;
-  const int gm = min(p.tiles_m - first_m, kGroupM);
+  const int first = group * kGroup;
+  const int g = min(fast_tiles - first, kGroup);
   const int local = tile - group * per_group;
-  m_blk = first_m + local % gm;
-  n_blk = local / gm;
+  const int fast = first + local % g;
+  const int slow = local / g;
+  m_blk = p.group_n ? slow : fast;
+  n_blk = p.group_n ? fast : slow;
+}
+
+// A work unit is one tile, or in pair mode one 256-row tile computed by the
+// two CTAs of a cluster (row blocks 2i and 2i+1); `rank` picks this CTA's half.
+template <bool PAIR>
+__device__ __forceinline__ void unit_coords(const GParams& p, int unit, uint32_t rank, int& m_blk, int& n_blk) {
+  if (!PAIR) {
+    tile_coords(p, unit, p.tiles_m, m_blk, n_blk);
+  } else {
+    int mp;
+    tile_coords(p, unit, p.tiles_mp, mp, n_blk);
+    m_blk = 2 * mp + static_cast<int>(rank);
+  }
 }
 
 __device__ __forceinline__ int kk_count_for(const GParams& p, int kb) {
@@ -116,9 +151,9 @@ __device__ __forceinline__ int kk_count_for(const GParams& p, int kb) {
   return static_cast<int>(min(static_cast<int64_t>(4), (rem + 63) / 64));
 }
 
-__device__ __forceinline__ void fail(SmemCtl* ctl, const GParams& p, uint32_t where) {
+__device__ __forceinline__ void fail(int* abort, const GParams& p, uint32_t where) {
   ptx::set_status(p.status, kDevTimeout | (where << 8));
-  *reinterpret_cast<volatile int*>(&ctl->abort) = 1;
+  *reinterpret_cast<volatile int*>(abort) = 1;
 }
 
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
@@ -126,12 +161,31 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   return *reinterpret_cast<const uint32_t*>(&v);
 }
 
+// Warp-uniform bounded wait: lane 0 polls, the result is broadcast.
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag, int lane) {
+  uint32_t ok = 1;
+  if (lane == 0) ok = ptx::mbar_wait(bar, parity, abort_flag) ? 1u : 0u;
+  return __shfl_sync(0xFFFFFFFFu, ok, 0) != 0;
+}
+
+// Arrive on the leader CTA's copy of a barrier: a local arrive in the
+// leader (or single) CTA, a relaxed remote arrive from the follower.  Callers
+// have completed the TMEM accesses being signalled (tcgen05.wait::st or
+// wait::ld, then tcgen05.fence::before_thread_sync).
+template <bool PAIR>
+__device__ __forceinline__ void arrive_leader(uint64_t* bar, uint32_t rank) {
+  if (PAIR && rank != 0)
+    ptx::mbar_arrive_cluster_relaxed(ptx::mapa_shared(ptx::smem_u32(bar), 0));
+  else
+    ptx::mbar_arrive(bar);
+}
+
 // Epilogue for one 128 x 128 half of a tile: TMEM -> registers -> global.
-// The warp's lane quarter q gives its 32 rows.  Returns after releasing the
-// accumulator (one arrival per warp on acc_empty).
-template <bool OUT_F32>
-__device__ __forceinline__ void epilogue_half(const GParams& p, SmemCtl* ctl, uint32_t tmem, int m_blk, int n_blk,
-                                              int q, int half, int lane, float alpha) {
+// The warp's lane quarter q gives its 32 rows.  Releases the accumulator (one
+// arrival per warp on the leader's acc_empty) as soon as it has been read.
+template <bool OUT_F32, bool PAIR>
+__device__ __forceinline__ void epilogue_half(const GParams& p, uint64_t* acc_empty, uint32_t tmem, int m_blk,
+                                              int n_blk, int q, int half, int lane, float alpha, uint32_t rank) {
   const int64_t row = static_cast<int64_t>(m_blk) * BM + q * 32 + lane;
   const int64_t col0 = static_cast<int64_t>(n_blk) * BN + half * kEpiCols;
   const uint32_t taddr = tmem + (static_cast<uint32_t>(q * 32) << 16) + kAccCol + half * kEpiCols;
@@ -149,15 +203,15 @@ __device__ __forceinline__ void epilogue_half(const GParams& p, SmemCtl* ctl, ui
     }
     ptx::tc_fence_before();
     __syncwarp();
-    if (lane == 0) ptx::mbar_arrive(&ctl->acc_empty);
+    if (lane == 0) arrive_leader<PAIR>(acc_empty, rank);
     if (row < p.M) {
       __nv_bfloat16* drow = static_cast<__nv_bfloat16*>(p.d) + row * p.ldd;
 #pragma unroll
       for (int c8 = 0; c8 < kEpiCols / 8; ++c8) {
         const int64_t col = col0 + c8 * 8;
         if (p.vec_store && col + 8 <= p.N) {
-          *reinterpret_cast<uint4*>(drow + col) =
-              make_uint4(packed[c8 * 4], packed[c8 * 4 + 1], packed[c8 * 4 + 2], packed[c8 * 4 + 3]);
+          __stcs(reinterpret_cast<uint4*>(drow + col),
+                 make_uint4(packed[c8 * 4], packed[c8 * 4 + 1], packed[c8 * 4 + 2], packed[c8 * 4 + 3]));
         } else {
 #pragma unroll
           for (int j = 0; j < 8; ++j) {
@@ -186,7 +240,7 @@ __device__ __forceinline__ void epilogue_half(const GParams& p, SmemCtl* ctl, ui
                                        __fmul_rn(alpha, __uint_as_float(r[4 * j4 + 2])),
                                        __fmul_rn(alpha, __uint_as_float(r[4 * j4 + 3])));
           if (p.vec_store && col + 4 <= p.N) {
-            *reinterpret_cast<float4*>(drow + col) = v;
+            __stcs(reinterpret_cast<float4*>(drow + col), v);
           } else {
             if (col < p.N) drow[col] = v.x;
             if (col + 1 < p.N) drow[col + 1] = v.y;
@@ -198,29 +252,24 @@ __device__ __forceinline__ void epilogue_half(const GParams& p, SmemCtl* ctl, ui
     }
     ptx::tc_fence_before();
     __syncwarp();
-    if (lane == 0) ptx::mbar_arrive(&ctl->acc_empty);
+    if (lane == 0) arrive_leader<PAIR>(acc_empty, rank);
   }
 }
 
-// Warp-uniform bounded wait: lane 0 polls, the result is broadcast.
-__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag, int lane) {
-  uint32_t ok = 1;
-  if (lane == 0) ok = ptx::mbar_wait(bar, parity, abort_flag) ? 1u : 0u;
-  return __shfl_sync(0xFFFFFFFFu, ok, 0) != 0;
-}
-
 // Scale staging for one ring stage.  Layout the block-scaled MMA reads
-// (scale_vec::4X, M = 128): for a 128-row operand block and one K = 64 step,
-// TMEM lane 32 q + l, column base + j holds the four scales of row l + 32 j;
-// every lane quarter q holds the whole block, because the quarter that
-// computes output rows 32 q .. 32 q + 31 reads the B scales of all N rows
-// from its own lanes (and the A scales of its own rows from column base + q).
-// That is exactly one 16-byte row of a 512-byte scale atom per lane, so each
-// staging warp (lane quarter q) copies atom row `lane` into its own lanes.
-// Columns: A at kSfaCol + 16 s + 4 kk, B row block rb at kSfbCol + 32 s +
-// 8 kk + 4 rb (a 256-row B tile is read as columns base .. base + 7).
+// (scale_vec::4X): for a 128-row operand block and one K = 64 step, TMEM lane
+// 32 q + l, column base + j holds the four scales of row l + 32 j; every lane
+// quarter q holds the whole block, because the quarter that computes output
+// rows 32 q .. 32 q + 31 reads the B scales of all N rows from its own lanes
+// (and the A scales of its own rows from column base + q).  That is one
+// 16-byte row of a 512-byte scale atom per lane, so each staging warp (lane
+// quarter q) copies atom row `lane` into its own lanes.  Columns: A at
+// kSfaCol + 16 s + 4 kk, B row block rb at kSfbCol + 32 s + 8 kk + 4 rb (a
+// 256-row B operand is read as columns base .. base + 7).
+template <bool PAIR>
 __device__ __forceinline__ void stage_scales(const uint8_t* st, uint32_t tmem, int s, int q, int lane) {
-  const uint8_t* sfa = st + kABytes + kBBytes;
+  using L = Layout<PAIR>;
+  const uint8_t* sfa = st + kABytes + L::kBBytes;
   const uint8_t* sfb = sfa + kSfaBytes;
   const uint32_t lane_base = tmem + (static_cast<uint32_t>(q * 32) << 16);
   uint32_t va[16];
@@ -248,31 +297,37 @@ __device__ __forceinline__ void stage_scales(const uint8_t* st, uint32_t tmem, i
         vb[8 * k2 + 4 * rb + 3] = v.w;
       }
     }
-    ptx::tmem_st_32x32b_x16(lane_base + kSfbCol + s * 32 + h * 16, vb);
+    ptx::tmem_st_32x32b_x16(lane_base + L::kSfbCol + s * 32 + h * 16, vb);
   }
 }
 
-template <bool OUT_F32>
+template <bool OUT_F32, bool PAIR>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
                 const GParams p) {
+  using L = Layout<PAIR>;
+  constexpr int S = L::kStages;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  SmemCtl* ctl = reinterpret_cast<SmemCtl*>(smem + kStages * kStageBytes);
+  SmemCtl<S>* ctl = reinterpret_cast<SmemCtl<S>*>(smem + S * L::kStageBytes);
   volatile int* abort_flag = &ctl->abort;
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  const uint32_t rank = PAIR ? ptx::cluster_ctarank() : 0u;
+  const bool leader = rank == 0;
+  const int unit0 = PAIR ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
+  const int ustep = PAIR ? static_cast<int>(gridDim.x >> 1) : static_cast<int>(gridDim.x);
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kStages; ++s) {
+    for (int s = 0; s < S; ++s) {
       ptx::mbar_init(&ctl->full[s], 1);
       ptx::mbar_init(&ctl->sf_full[s], 1);
       ptx::mbar_init(&ctl->empty[s], 1);
-      ptx::mbar_init(&ctl->sfready[s], kSfWarps);
+      ptx::mbar_init(&ctl->sfready[s], PAIR ? 2 * kSfWarps : kSfWarps);
     }
     ptx::mbar_init(&ctl->acc_full, 1);
-    ptx::mbar_init(&ctl->acc_empty, kEpiWarps);
+    ptx::mbar_init(&ctl->acc_empty, PAIR ? 2 * kEpiWarps : kEpiWarps);
     ptx::mbar_init(&ctl->drain, 1);
     ctl->abort = 0;
     ptx::fence_mbar_init();
@@ -282,11 +337,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     ptx::prefetch_tensormap(&tmap_b);
   }
   if (warp == 1) {
-    ptx::tmem_alloc(&ctl->tmem_base, kTmemCols);
-    ptx::tmem_relinquish();
+    // pair mode: one warp of each CTA of the pair allocates collectively
+    if (PAIR) {
+      ptx::tmem_alloc_pair(&ctl->tmem_base, kTmemCols);
+      ptx::tmem_relinquish_pair();
+    } else {
+      ptx::tmem_alloc(&ctl->tmem_base, kTmemCols);
+      ptx::tmem_relinquish();
+    }
   }
   ptx::tc_fence_before();
   __syncthreads();
+  // the peer's barriers must be initialised before anything reaches them
+  if (PAIR) ptx::cluster_sync();
   ptx::tc_fence_after();
   const uint32_t tmem = ctl->tmem_base;
 
@@ -294,27 +357,29 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       uint32_t issued_mask = 0, issued_parity = 0;
+      const uint64_t l2_keep = ptx::policy_evict_last();
+      const uint32_t full_leader0 = PAIR ? ptx::mapa_shared(ptx::smem_u32(&ctl->full[0]), 0) : 0u;
       int stage = 0;
       uint32_t phase = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; tile < p.num_tiles && ok; tile += gridDim.x) {
+      for (int unit = unit0; unit < p.num_units && ok; unit += ustep) {
         int m_blk, n_blk;
-        tile_coords(p, tile, m_blk, n_blk);
+        unit_coords<PAIR>(p, unit, rank, m_blk, n_blk);
         const int64_t n_rows_left = p.N - static_cast<int64_t>(n_blk) * BN;
         const int nb_atoms = static_cast<int>(min(static_cast<int64_t>(2), (n_rows_left + 127) / 128));
         for (int kb = 0; kb < p.num_kb; ++kb) {
           if (!ptx::mbar_wait(&ctl->empty[stage], phase ^ 1u, abort_flag)) {
-            fail(ctl, p, 1);
+            fail(&ctl->abort, p, 1);
             ok = false;
             break;
           }
           const int kk = kk_count_for(p, kb);
           const uint32_t sf_bytes = static_cast<uint32_t>(kk * kSfAtomBytes);
-          uint8_t* st = smem + stage * kStageBytes;
-          if (p.skip_first_load && blockIdx.x == 0 && tile == static_cast<int>(blockIdx.x) && kb == 0) {
+          uint8_t* st = smem + stage * L::kStageBytes;
+          if (p.skip_first_load && blockIdx.x == 0 && unit == unit0 && kb == 0) {
             // Failure-detection test hook: this stage is never filled, so the
             // bounded waits on it run out and the CTA reports a timeout.
-            if (++stage == kStages) {
+            if (++stage == S) {
               stage = 0;
               phase ^= 1u;
             }
@@ -322,82 +387,116 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           // Scales first, on their own barrier: the staging warps can move
           // them into TMEM while the larger code tiles are still in flight.
-          ptx::mbar_arrive_expect_tx(&ctl->sf_full[stage], sf_bytes * (1 + nb_atoms));
+          // (A row block past the end -- the odd last half of a pair -- has
+          // no scales to load; its rows are never stored.)
+          const bool a_valid = m_blk < p.tiles_m;
+          ptx::mbar_arrive_expect_tx(&ctl->sf_full[stage], sf_bytes * ((a_valid ? 1 : 0) + nb_atoms));
           const uint8_t* sfa = p.a_sf + (static_cast<int64_t>(m_blk) * p.sf_katoms + kb * 4) * kSfAtomBytes;
-          ptx::bulk_load(st + kABytes + kBBytes, sfa, sf_bytes, &ctl->sf_full[stage]);
+          if (a_valid) ptx::bulk_load(st + kABytes + L::kBBytes, sfa, sf_bytes, &ctl->sf_full[stage]);
           for (int rb = 0; rb < nb_atoms; ++rb) {
             const uint8_t* sfb =
                 p.b_sf + (static_cast<int64_t>(n_blk * 2 + rb) * p.sf_katoms + kb * 4) * kSfAtomBytes;
-            ptx::bulk_load(st + kABytes + kBBytes + kSfaBytes + rb * 4 * kSfAtomBytes, sfb, sf_bytes,
+            ptx::bulk_load(st + kABytes + L::kBBytes + kSfaBytes + rb * 4 * kSfAtomBytes, sfb, sf_bytes,
                            &ctl->sf_full[stage]);
           }
-          ptx::mbar_arrive_expect_tx(&ctl->full[stage], static_cast<uint32_t>(kABytes + kBBytes));
-          ptx::tma_load_2d(st, &tmap_a, &ctl->full[stage], kb * kRowBytes, m_blk * BM);
-          ptx::tma_load_2d(st + kABytes, &tmap_b, &ctl->full[stage], kb * kRowBytes, n_blk * BN);
+          if (PAIR) {
+            // both CTAs' code tiles complete on the leader's barrier
+            const uint32_t bar = full_leader0 + static_cast<uint32_t>(stage * sizeof(uint64_t));
+            if (leader) ptx::mbar_arrive_expect_tx(&ctl->full[stage], 2u * (kABytes + L::kBBytes));
+            ptx::tma_load_2d_pair(st, &tmap_a, bar, kb * kRowBytes, m_blk * BM);
+            ptx::tma_load_2d_pair(st + kABytes, &tmap_b, bar, kb * kRowBytes,
+                                  n_blk * BN + static_cast<int>(rank) * L::kBRows);
+          } else {
+            ptx::mbar_arrive_expect_tx(&ctl->full[stage], static_cast<uint32_t>(kABytes + L::kBBytes));
+            ptx::tma_load_2d_hint(st, &tmap_a, &ctl->full[stage], kb * kRowBytes, m_blk * BM, l2_keep);
+            ptx::tma_load_2d_hint(st + kABytes, &tmap_b, &ctl->full[stage], kb * kRowBytes, n_blk * BN, l2_keep);
+          }
           issued_mask |= 1u << stage;
           issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
-          if (++stage == kStages) {
+          if (++stage == S) {
             stage = 0;
             phase ^= 1u;
           }
         }
       }
-      // Drain: every stage this thread loaded must have landed before exit.
-      for (int s = 0; s < kStages; ++s) {
+      // Drain: every copy this thread issued must have landed before exit.
+      // (Pair mode: the code tiles complete on the leader's barrier, which
+      // the leader drains; the final cluster barrier keeps the follower
+      // alive until then.  The stage-free barrier of each CTA also takes the
+      // leader's last multicast commits.)
+      for (int s = 0; s < S; ++s) {
         if (issued_mask & (1u << s)) {
           volatile int never = 0;
-          if (!ptx::mbar_wait(&ctl->full[s], (issued_parity >> s) & 1u, &never)) fail(ctl, p, 2);
-          if (!ptx::mbar_wait(&ctl->sf_full[s], (issued_parity >> s) & 1u, &never)) fail(ctl, p, 2);
+          const uint32_t par = (issued_parity >> s) & 1u;
+          if (!ptx::mbar_wait(&ctl->sf_full[s], par, &never)) fail(&ctl->abort, p, 2);
+          if ((!PAIR || leader) && !ptx::mbar_wait(&ctl->full[s], par, &never)) fail(&ctl->abort, p, 2);
+          if (PAIR && ok && !ptx::mbar_wait(&ctl->empty[s], par, abort_flag)) fail(&ctl->abort, p, 2);
         }
       }
     }
   } else if (warp == 1) {
     // ----------------------------------------------------------------- MMA
-    if (lane == 0) {
+    if (lane == 0 && leader) {
       int stage = 0;
       uint32_t phase = 0, acc_phase = 0;
       bool ok = true, issued = false;
-      for (int tile = blockIdx.x; tile < p.num_tiles && ok; tile += gridDim.x) {
+      for (int unit = unit0; unit < p.num_units && ok; unit += ustep) {
         if (!ptx::mbar_wait(&ctl->acc_empty, acc_phase ^ 1u, abort_flag)) {
-          fail(ctl, p, 3);
+          fail(&ctl->abort, p, 3);
           break;
         }
         ptx::tc_fence_after();
         for (int kb = 0; kb < p.num_kb; ++kb) {
-          // The stage's scales are in TMEM and its code tiles have landed.
+          // The stage's scales are in TMEM and its code tiles have landed
+          // (in pair mode: in both CTAs).  CTA-scope waits suffice: the
+          // peer's arrivals follow completed TMEM writes, and the code tiles
+          // are TMA (async-proxy) writes read by the tensor core.
           if (!ptx::mbar_wait(&ctl->sfready[stage], phase, abort_flag) ||
               !ptx::mbar_wait(&ctl->full[stage], phase, abort_flag)) {
-            fail(ctl, p, 4);
+            fail(&ctl->abort, p, 4);
             ok = false;
             break;
           }
           ptx::tc_fence_after();
           const int kk_n = kk_count_for(p, kb);
-          uint8_t* st = smem + stage * kStageBytes;
+          uint8_t* st = smem + stage * L::kStageBytes;
           const uint32_t a_addr = ptx::smem_u32(st);
           const uint32_t b_addr = ptx::smem_u32(st + kABytes);
           for (int kk = 0; kk < kk_n; ++kk) {
             const uint64_t adesc = ptx::smem_desc(a_addr + kk * 32, 16, 1024, ptx::kSwizzle128B);
             const uint64_t bdesc = ptx::smem_desc(b_addr + kk * 32, 16, 1024, ptx::kSwizzle128B);
-            ptx::tc_mma_nvf4(tmem + kAccCol, adesc, bdesc, kIdesc, tmem + kSfaCol + stage * 16 + kk * 4,
-                             tmem + kSfbCol + stage * 32 + kk * 8, (kb | kk) != 0 ? 1u : 0u);
+            const uint32_t sfa_t = tmem + kSfaCol + stage * 16 + kk * 4;
+            const uint32_t sfb_t = tmem + L::kSfbCol + stage * 32 + kk * 8;
+            if (PAIR)
+              ptx::tc_mma_nvf4_pair(tmem + kAccCol, adesc, bdesc, L::kIdesc, sfa_t, sfb_t, (kb | kk) != 0 ? 1u : 0u);
+            else
+              ptx::tc_mma_nvf4(tmem + kAccCol, adesc, bdesc, L::kIdesc, sfa_t, sfb_t, (kb | kk) != 0 ? 1u : 0u);
           }
-          ptx::tc_commit(&ctl->empty[stage]);
+          if (PAIR)
+            ptx::tc_commit_pair_multicast(&ctl->empty[stage], static_cast<uint16_t>(0x3));
+          else
+            ptx::tc_commit(&ctl->empty[stage]);
           issued = true;
-          if (++stage == kStages) {
+          if (++stage == S) {
             stage = 0;
             phase ^= 1u;
           }
         }
         if (!ok) break;
-        ptx::tc_commit(&ctl->acc_full);
+        if (PAIR)
+          ptx::tc_commit_pair_multicast(&ctl->acc_full, static_cast<uint16_t>(0x3));
+        else
+          ptx::tc_commit(&ctl->acc_full);
         acc_phase ^= 1u;
       }
       if (issued) {
         // Wait for every MMA issued above before TMEM is freed.
-        ptx::tc_commit(&ctl->drain);
+        if (PAIR)
+          ptx::tc_commit_pair(&ctl->drain);
+        else
+          ptx::tc_commit(&ctl->drain);
         volatile int never = 0;
-        if (!ptx::mbar_wait(&ctl->drain, 0, &never)) fail(ctl, p, 5);
+        if (!ptx::mbar_wait(&ctl->drain, 0, &never)) fail(&ctl->abort, p, 5);
       }
     }
   } else if (warp >= kFirstSfWarp) {
@@ -406,20 +505,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     int stage = 0;
     uint32_t phase = 0;
     bool ok = true;
-    for (int tile = blockIdx.x; tile < p.num_tiles && ok; tile += gridDim.x) {
+    for (int unit = unit0; unit < p.num_units && ok; unit += ustep) {
       for (int kb = 0; kb < p.num_kb; ++kb) {
         if (!warp_wait(&ctl->sf_full[stage], phase, abort_flag, lane)) {
-          if (lane == 0) fail(ctl, p, 7);
+          if (lane == 0) fail(&ctl->abort, p, 7);
           ok = false;
           break;
         }
         ptx::tc_fence_after();
-        stage_scales(smem + stage * kStageBytes, tmem, stage, q, lane);
+        stage_scales<PAIR>(smem + stage * L::kStageBytes, tmem, stage, q, lane);
         ptx::tmem_st_wait();
         ptx::tc_fence_before();
         __syncwarp();
-        if (lane == 0) ptx::mbar_arrive(&ctl->sfready[stage]);
-        if (++stage == kStages) {
+        if (lane == 0) arrive_leader<PAIR>(&ctl->sfready[stage], rank);
+        if (++stage == S) {
           stage = 0;
           phase ^= 1u;
         }
@@ -431,24 +530,30 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int half = (warp - 2) >> 2;    // which 128 columns of the tile it stores
     const float alpha = __fmul_rn(*p.a_scale, *p.b_scale);
     uint32_t acc_phase = 0;
-    for (int tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x) {
+    for (int unit = unit0; unit < p.num_units; unit += ustep) {
       int m_blk, n_blk;
-      tile_coords(p, tile, m_blk, n_blk);
+      unit_coords<PAIR>(p, unit, rank, m_blk, n_blk);
       if (!warp_wait(&ctl->acc_full, acc_phase, abort_flag, lane)) {
-        if (lane == 0) fail(ctl, p, 6);
+        if (lane == 0) fail(&ctl->abort, p, 6);
         break;
       }
       ptx::tc_fence_after();
-      epilogue_half<OUT_F32>(p, ctl, tmem, m_blk, n_blk, q, half, lane, alpha);
+      epilogue_half<OUT_F32, PAIR>(p, &ctl->acc_empty, tmem, m_blk, n_blk, q, half, lane, alpha, rank);
       acc_phase ^= 1u;
     }
   }
 
   ptx::tc_fence_before();
   __syncthreads();
+  // neither CTA of a pair leaves (or frees TMEM) while the other may still
+  // write into it
+  if (PAIR) ptx::cluster_sync();
   if (warp == 1) {
     ptx::tc_fence_after();
-    ptx::tmem_dealloc(tmem, kTmemCols);
+    if (PAIR)
+      ptx::tmem_dealloc_pair(tmem, kTmemCols);
+    else
+      ptx::tmem_dealloc(tmem, kTmemCols);
   }
 }
 
@@ -481,17 +586,55 @@ bool make_codes_map(CUtensorMap* map, const uint8_t* codes, int64_t rows, int64_
   return r == CUDA_SUCCESS;
 }
 
-template <bool OUT_F32>
-cudaError_t launch_typed(const CUtensorMap& ma, const CUtensorMap& mb, const GParams& p, cudaStream_t stream) {
+cudaLaunchAttribute pair_cluster_attr() {
+  cudaLaunchAttribute attr{};
+  attr.id = cudaLaunchAttributeClusterDimension;
+  attr.val.clusterDim.x = 2;
+  attr.val.clusterDim.y = 1;
+  attr.val.clusterDim.z = 1;
+  return attr;
+}
+
+template <bool OUT_F32, bool PAIR>
+cudaError_t launch_typed(const CUtensorMap& ma, const CUtensorMap& mb, GParams p, cudaStream_t stream) {
+  using L = Layout<PAIR>;
   static bool configured = false;
+  static int max_clusters = 0;
+  auto kernel = gemm_kernel<OUT_F32, PAIR>;
   if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(gemm_kernel<OUT_F32>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmemBytes);
     if (e != cudaSuccess) return e;
+    if (PAIR) {
+      cudaLaunchConfig_t cfg{};
+      cudaLaunchAttribute attr = pair_cluster_attr();
+      cfg.gridDim = dim3(2 * device_sm_count());
+      cfg.blockDim = dim3(kThreads);
+      cfg.dynamicSmemBytes = L::kSmemBytes;
+      cfg.attrs = &attr;
+      cfg.numAttrs = 1;
+      e = cudaOccupancyMaxActiveClusters(&max_clusters, kernel, &cfg);
+      if (e != cudaSuccess) return e;
+      if (max_clusters < 1) return cudaErrorInvalidConfiguration;
+    }
     configured = true;
   }
-  const int grid = std::min(p.num_tiles, device_sm_count());
-  gemm_kernel<OUT_F32><<<grid, kThreads, kSmemBytes, stream>>>(ma, mb, p);
-  return cudaGetLastError();
+  if (!PAIR) {
+    p.num_units = p.num_tiles;
+    const int grid = std::min(p.num_tiles, device_sm_count());
+    kernel<<<grid, kThreads, L::kSmemBytes, stream>>>(ma, mb, p);
+    return cudaGetLastError();
+  }
+  p.num_units = p.tiles_mp * p.tiles_n;
+  const int clusters = std::min(p.num_units, max_clusters);
+  cudaLaunchConfig_t cfg{};
+  cudaLaunchAttribute attr = pair_cluster_attr();
+  cfg.gridDim = dim3(2 * clusters);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = L::kSmemBytes;
+  cfg.stream = stream;
+  cfg.attrs = &attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, ma, mb, p);
 }
 
 }  // namespace
@@ -502,8 +645,11 @@ cudaError_t launch_gemm(const GemmArgs& a, cudaStream_t stream) {
     const size_t esz = a.out_f32 ? 4 : 2;
     return cudaMemset2DAsync(a.d, a.ldd * esz, 0, a.N * esz, a.M, stream);
   }
+  // Pair mode needs at least two row blocks.
+  const bool pair = (a.M + BM - 1) / BM >= 2;
   CUtensorMap ma, mb;
-  if (!make_codes_map(&ma, a.a_codes, a.M, a.K, BM) || !make_codes_map(&mb, a.b_codes, a.N, a.K, BN))
+  if (!make_codes_map(&ma, a.a_codes, a.M, a.K, BM) ||
+      !make_codes_map(&mb, a.b_codes, a.N, a.K, pair ? Layout<true>::kBRows : Layout<false>::kBRows))
     return cudaErrorInvalidValue;
   GParams p{};
   p.M = a.M;
@@ -513,9 +659,8 @@ cudaError_t launch_gemm(const GemmArgs& a, cudaStream_t stream) {
   p.tiles_m = static_cast<int>((a.M + BM - 1) / BM);
   p.tiles_n = static_cast<int>((a.N + BN - 1) / BN);
   p.num_tiles = p.tiles_m * p.tiles_n;
+  p.tiles_mp = (p.tiles_m + 1) / 2;
   p.sf_katoms = (a.K / 16 + 3) / 4;
-  p.a_row_atoms = (a.M + 127) / 128;
-  p.b_row_atoms = (a.N + 127) / 128;
   p.a_sf = a.a_sf;
   p.b_sf = a.b_sf;
   p.a_scale = a.a_scale;
@@ -524,9 +669,19 @@ cudaError_t launch_gemm(const GemmArgs& a, cudaStream_t stream) {
   p.ldd = a.ldd;
   p.status = a.status;
   p.skip_first_load = a.skip_first_load;
+  {
+    // DRAM operand traffic of the two rasters: the operand swept per group
+    // is read once per group.
+    const double a_bytes = static_cast<double>(a.M) * a.K * 0.5625, b_bytes = static_cast<double>(a.N) * a.K * 0.5625;
+    const int m_units = pair ? p.tiles_mp : p.tiles_m;
+    const double by_m = a_bytes + b_bytes * ((m_units + kGroup - 1) / kGroup);
+    const double by_n = b_bytes + a_bytes * ((p.tiles_n + kGroup - 1) / kGroup);
+    p.group_n = by_n < by_m ? 1 : 0;
+  }
   const size_t esz = a.out_f32 ? 4 : 2;
   p.vec_store = (reinterpret_cast<uintptr_t>(a.d) % 16 == 0) && ((a.ldd * esz) % 16 == 0);
-  return a.out_f32 ? launch_typed<true>(ma, mb, p, stream) : launch_typed<false>(ma, mb, p, stream);
+  if (pair) return a.out_f32 ? launch_typed<true, true>(ma, mb, p, stream) : launch_typed<false, true>(ma, mb, p, stream);
+  return a.out_f32 ? launch_typed<true, false>(ma, mb, p, stream) : launch_typed<false, false>(ma, mb, p, stream);
 }
 
 }  // namespace nvfp4
