@@ -32,7 +32,7 @@ NVFP4_LINEAR_FPROP, NVFP4_LINEAR_DGRAD, NVFP4_LINEAR_WGRAD = 0, 1, 2
 # Every exported symbol of include/nvfp4.h.
 EXPORTS = [
     "nvfp4_status_string", "nvfp4_version", "nvfp4_codes_bytes", "nvfp4_sf_bytes",
-    "nvfp4_quantize_workspace_size", "nvfp4_quantize", "nvfp4_dequantize",
+    "nvfp4_quantize_workspace_size", "nvfp4_quantize", "nvfp4_quantize_noalloc", "nvfp4_dequantize",
     "nvfp4_gemm_workspace_size", "nvfp4_gemm", "nvfp4_linear_workspace_size",
     "nvfp4_linear_fprop", "nvfp4_linear_dgrad", "nvfp4_linear_wgrad",
     "nvfp4_check_device_status", "nvfp4_debug_gemm_skip_load",
@@ -115,6 +115,7 @@ def lib():
             "nvfp4_sf_bytes": (SZ, [I64, I64, I32]),
             "nvfp4_quantize_workspace_size": (I32, [I64, I64, PCFG, PSZ]),
             "nvfp4_quantize": (I32, [P, I64, I64, I64, PCFG, P, P, P, P, SZ, P]),
+            "nvfp4_quantize_noalloc": (I32, [P, I64, I64, I64, PCFG, P, P, P, P]),
             "nvfp4_dequantize": (I32, [PT, I32, P, I64, P]),
             "nvfp4_gemm_workspace_size": (I32, [I64, I64, I64, PSZ]),
             "nvfp4_gemm": (I32, [PT, PT, I32, P, I64, P, SZ, P]),
@@ -194,6 +195,18 @@ def nvfp4_quantize(x, cfg, out=None, workspace=None, stream=None):
     st = lib().nvfp4_quantize(_ptr(x), rows, cols, ldx, ctypes.byref(cfg), _ptr(out.codes), _ptr(out.sf),
                               _ptr(out.tensor_scale), _ptr(workspace), workspace.numel(), _stream(stream))
     _check(st, "nvfp4_quantize")
+    return out
+
+
+def nvfp4_quantize_noalloc(x, cfg, out, stream=None):
+    """Scratch-free quantisation (see include/nvfp4.h): `out` is a
+    preallocated NVFP4Tensor; the library allocates nothing."""
+    assert x.dtype == torch.bfloat16 and x.dim() == 2 and x.stride(1) == 1
+    rows, cols = x.shape
+    ldx = x.stride(0) if rows > 1 else cols
+    st = lib().nvfp4_quantize_noalloc(_ptr(x), rows, cols, ldx, ctypes.byref(cfg), _ptr(out.codes), _ptr(out.sf),
+                                      _ptr(out.tensor_scale), _stream(stream))
+    _check(st, "nvfp4_quantize_noalloc")
     return out
 
 

@@ -217,6 +217,41 @@ nvfp4_status nvfp4_quantize(const void* x, int64_t rows, int64_t cols, int64_t l
                        reinterpret_cast<uint32_t*>(ws + kWsHeaderBytes), reinterpret_cast<cudaStream_t>(stream));
 }
 
+nvfp4_status nvfp4_quantize_noalloc(const void* x, int64_t rows, int64_t cols, int64_t ldx,
+                                    const nvfp4_quant_cfg* cfg, void* codes, void* sf, float* tensor_scale,
+                                    nvfp4_stream_t stream) {
+  nvfp4_status s = check_cfg(cfg);
+  if (s != NVFP4_OK) return s;
+  s = check_quant_shape(rows, cols, cfg);
+  if (s != NVFP4_OK) return s;
+  if (rows > 0 && cols > kNoAllocMaxElements / rows) return NVFP4_ERR_UNSUPPORTED_SHAPE;
+  if (!tensor_scale) return NVFP4_ERR_INVALID_ARG;
+  const bool empty = rows == 0 || cols == 0;
+  if (!empty && (!x || !codes || !sf)) return NVFP4_ERR_INVALID_ARG;
+  if (ldx < cols) return NVFP4_ERR_INVALID_ARG;
+  if (!empty && (!aligned16(x) || ldx % 8 != 0)) return NVFP4_ERR_INVALID_ARG;
+  if (!empty && (reinterpret_cast<uintptr_t>(codes) & 7u)) return NVFP4_ERR_INVALID_ARG;
+  QuantArgs a{};
+  a.x = static_cast<const uint16_t*>(x);
+  a.rows = rows;
+  a.cols = cols;
+  a.ldx = ldx;
+  a.qr = cfg->transpose ? cols : rows;
+  a.qk = cfg->transpose ? rows : cols;
+  a.block2d = cfg->block == NVFP4_BLOCK_16x16;
+  a.sr = cfg->rounding == NVFP4_ROUND_SR;
+  a.rht = cfg->rht;
+  a.transpose = cfg->transpose;
+  a.sf_mma = cfg->sf_layout == NVFP4_SF_MMA;
+  a.rht_seed = cfg->rht_seed;
+  a.sr_seed = cfg->sr_seed;
+  a.sr_offset = cfg->sr_offset;
+  a.codes = static_cast<uint8_t*>(codes);
+  a.sf = static_cast<uint8_t*>(sf);
+  a.tensor_scale = tensor_scale;
+  return cuda_status(launch_quantize_noalloc(a, reinterpret_cast<cudaStream_t>(stream)));
+}
+
 nvfp4_status nvfp4_dequantize(const nvfp4_tensor* q, int32_t out_dtype, void* out, int64_t ldo,
                               nvfp4_stream_t stream) {
   nvfp4_status s = check_tensor(q);

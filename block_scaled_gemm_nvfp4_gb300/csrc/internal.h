@@ -30,6 +30,11 @@ struct QuantArgs {
 };
 
 cudaError_t launch_quantize(const QuantArgs& a, cudaStream_t stream);
+// Same launch with the status word and partial-amax scratch taken from a
+// file-scope device array instead of a caller workspace.
+cudaError_t launch_quantize_noalloc(QuantArgs a, cudaStream_t stream);
+// Largest operand (elements) the scratch-free quantiser accepts.
+constexpr int64_t kNoAllocMaxElements = int64_t(1) << 31;
 
 struct DequantArgs {
   const uint8_t* codes;

@@ -29,6 +29,7 @@
 
 #include <algorithm>
 #include <cstdint>
+#include <mutex>
 
 #include "internal.h"
 #include "ptx.cuh"
@@ -383,7 +384,49 @@ cudaError_t dispatch_block(const QParams& p, int b2d, int rht, int sr, cudaStrea
   return b2d ? dispatch_rht<COL, true>(p, rht, sr, s) : dispatch_rht<COL, false>(p, rht, sr, s);
 }
 
+// Scratch for nvfp4_quantize_noalloc: the status word (first 256 bytes) and
+// the partial-amax slots of the amax pass, in one file-scope device array.
+// Every GPU that loads the library holds it until the process exits.  In
+// host code `g_noalloc_scratch` only names the symbol; its device address
+// comes from cudaGetSymbolAddress, once per device.
+constexpr size_t kNoAllocScratchBytes = kWsHeaderBytes + kQuantScratchBytes;
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_noalloc_mutex;
+void* g_noalloc_ptr[kMaxDevices] = {nullptr};
+
 }  // namespace
+
+cudaError_t noalloc_scratch(void** ptr) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+  if (!g_noalloc_ptr[dev]) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess) return e;
+    g_noalloc_ptr[dev] = p;
+  }
+  *ptr = g_noalloc_ptr[dev];
+  return cudaSuccess;
+}
+
+cudaError_t launch_quantize_noalloc(QuantArgs a, cudaStream_t stream) {
+  void* scratch = nullptr;
+  cudaError_t e = noalloc_scratch(&scratch);
+  if (e != cudaSuccess) return e;
+  uint8_t* base = static_cast<uint8_t*>(scratch);
+  // The status word must start at zero; the partial slots are fully written
+  // by the amax pass before the encode pass reads them.
+  e = cudaMemsetAsync(base, 0, sizeof(uint32_t), stream);
+  if (e != cudaSuccess) return e;
+  a.status = reinterpret_cast<uint32_t*>(base);
+  a.partials = reinterpret_cast<uint32_t*>(base + kWsHeaderBytes);
+  return launch_quantize(a, stream);
+}
 
 cudaError_t launch_quantize(const QuantArgs& a, cudaStream_t stream) {
   QParams p{};

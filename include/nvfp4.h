@@ -134,6 +134,32 @@ nvfp4_status nvfp4_quantize(const void* x, int64_t rows, int64_t cols, int64_t l
                             void* workspace, size_t workspace_bytes, nvfp4_stream_t stream);
 
 /*
+ * nvfp4_quantize_noalloc: nvfp4_quantize for callers that cannot allocate
+ * device memory: a host framework or embedding runtime that owns every
+ * device allocation and forbids others (so no workspace can be created for
+ * this call), code running inside another allocator's callbacks, where
+ * allocating would re-enter it, or latency-critical paths that must never
+ * reach an allocator.  It takes no workspace: its status word and
+ * partial-amax scratch live in one file-scope device array of the library
+ * (16.6 KB, held on every GPU that loads the library until the process
+ * exits).  The paper has no counterpart to this entry point; it belongs to
+ * the library interface only.
+ * Same arguments, shape rules and outputs as nvfp4_quantize, with a limit of
+ * rows * cols <= 2^31 elements (NVFP4_ERR_UNSUPPORTED_SHAPE beyond).
+ * Non-finite input is reported only through tensor_scale[0] = NaN.
+ * The first call on a device looks up the array's device address
+ * (cudaGetSymbolAddress) with that device current; make that first call
+ * before any stream capture.  It calls no cudaMalloc, cudaFree or allocating
+ * library routine.  All calls share the one array, which keeps the last
+ * call's contents (the status word is cleared at the start of every call):
+ * calls that overlap on the GPU -- on different streams, or from host
+ * threads without ordering between them -- race and must not be issued.
+ */
+nvfp4_status nvfp4_quantize_noalloc(const void* x, int64_t rows, int64_t cols, int64_t ldx,
+                                    const nvfp4_quant_cfg* cfg, void* codes, void* sf, float* tensor_scale,
+                                    nvfp4_stream_t stream);
+
+/*
  * nvfp4_dequantize: Q -> out [rows, k] with row stride ldo elements, as
  * e2m1(code) * e4m3(scale) * s computed in FP32 (exact product, one rounding
  * on the final multiply); BF16 output is that FP32 value rounded to nearest
