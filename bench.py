@@ -27,7 +27,8 @@ T, HID, FFN = 8192, 5120, 20480
 GEMM_FLOP = 2.0 * T * HID * FFN  # each of fprop, dgrad, wgrad
 STEP_FLOP = 3 * GEMM_FLOP
 FP4_OVER_BF16 = 13.5 / 2.25  # nominal dense FP4 : BF16 tensor ratio on GB300
-QUANT_BYTES_PER_ELT = 2.0 + 0.5 + 1.0 / 16  # read BF16, write codes + block scales
+QUANT_OUT_BYTES_PER_ELT = 0.5 + 1.0 / 16  # codes + block scales of one quantised output
+QUANT_BYTES_PER_ELT = 2.0 + QUANT_OUT_BYTES_PER_ELT  # read BF16, write one output
 WORKLOAD = ("12B-hybrid MLP up-projection fprop+dgrad+wgrad, tokens 8192 (4x2048), hidden 5120, FFN 20480; "
             "X N(0,1), W N(0,0.02), dY N(0,1e-3); W 16x16, X/dY 1x16, wgrad operands RHT+SR")
 
@@ -363,14 +364,90 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+# ----------------------------------------------------------- single kernels
+def run_case(args):
+    """Time one library call on one shape (for sweeps and ncu captures):
+    ``gemm:M,N,K`` (BF16 output), ``quantize:R,C[,mode]`` with mode one of
+    row, col, row16, col16, colsr (transform + stochastic rounding), or
+    ``dual:R,C[,act|weight]`` (row + colsr, or row16 + col16, from one read).
+    Prints a JSON line with the mean time per call over --steps calls."""
+    import torch
+
+    import block_scaled_gemm_nvfp4_gb300 as nv
+    from block_scaled_gemm_nvfp4_gb300 import synthetic as syn
+
+    kind, _, rest = args.case.partition(":")
+    parts = rest.split(",")
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    nv.lib()
+    s = nv.NVFP4_DEFAULT_RHT_SEED
+    modes = {"row": nv.quant_cfg(), "col": nv.quant_cfg(transpose=1), "row16": nv.quant_cfg(block=1),
+             "col16": nv.quant_cfg(block=1, transpose=1),
+             "colsr": nv.quant_cfg(rounding=1, rht=1, transpose=1, rht_seed=s, sr_seed=5)}
+    if kind == "gemm":
+        M, N, K = (int(v) for v in parts[:3])
+        qa = nv.nvfp4_quantize(syn.normal_bf16((M, K), seed=1).to(dev), nv.quant_cfg())
+        qb = nv.nvfp4_quantize(syn.normal_bf16((N, K), seed=2).to(dev), nv.quant_cfg())
+        d = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+        ws = torch.zeros(4096, dtype=torch.uint8, device=dev)
+
+        def call():
+            nv.nvfp4_gemm(qa, qb, nv.NVFP4_OUT_BF16, d=d, workspace=ws)
+        work, unit = 2.0 * M * N * K / 1e12, "TFLOP/s"
+    elif kind == "dual":
+        R, C = int(parts[0]), int(parts[1])
+        pair = {"act": (modes["row"], modes["colsr"]), "weight": (modes["row16"], modes["col16"])}
+        ca, cb = pair[parts[2] if len(parts) > 2 else "act"]
+        x = syn.normal_bf16((R, C), seed=3).to(dev)
+        oa, ob = nv.nvfp4_quantize_dual(x, ca, cb)
+        ws = torch.zeros(nv.nvfp4_quantize_workspace_size(R, C, ca), dtype=torch.uint8, device=dev)
+
+        def call():
+            nv.nvfp4_quantize_dual(x, ca, cb, oa, ob, workspace=ws)
+        work, unit = R * C * (2.0 + 2 * QUANT_OUT_BYTES_PER_ELT) / 1e9, "GB/s"
+    elif kind == "quantize":
+        R, C = int(parts[0]), int(parts[1])
+        cfg = modes[parts[2] if len(parts) > 2 else "row"]
+        x = syn.normal_bf16((R, C), seed=3).to(dev)
+        out = nv.nvfp4_quantize(x, cfg)
+        ws = torch.zeros(nv.nvfp4_quantize_workspace_size(R, C, cfg), dtype=torch.uint8, device=dev)
+
+        def call():
+            nv.nvfp4_quantize(x, cfg, out=out, workspace=ws)
+        work, unit = R * C * QUANT_BYTES_PER_ELT / 1e9, "GB/s"
+    else:
+        raise SystemExit("unknown --case %r" % args.case)
+    for _ in range(args.warmup):
+        call()
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for _ in range(args.steps):
+        call()
+    t1.record(stream)
+    torch.cuda.synchronize()
+    ms = t0.elapsed_time(t1) / args.steps
+    st = nv.nvfp4_check_device_status(ws)
+    if st != nv.NVFP4_OK:
+        raise RuntimeError("device status %s" % nv.nvfp4_status_string(st))
+    print(json.dumps({"case": args.case, "ms": round(ms, 5), "value": round(work / (ms * 1e-3), 1),
+                      "unit": unit, "steps": args.steps, "warmup": args.warmup}), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=10)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--case", default=None,
+                    help="time one call: gemm:M,N,K, quantize:R,C[,mode] or dual:R,C[,act|weight]")
     args = ap.parse_args()
-    if args.impl == "reference":
+    if args.case:
+        run_case(args)
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_ours(args)

@@ -32,7 +32,8 @@ NVFP4_LINEAR_FPROP, NVFP4_LINEAR_DGRAD, NVFP4_LINEAR_WGRAD = 0, 1, 2
 # Every exported symbol of include/nvfp4.h.
 EXPORTS = [
     "nvfp4_status_string", "nvfp4_version", "nvfp4_codes_bytes", "nvfp4_sf_bytes",
-    "nvfp4_quantize_workspace_size", "nvfp4_quantize", "nvfp4_quantize_noalloc", "nvfp4_dequantize",
+    "nvfp4_quantize_workspace_size", "nvfp4_quantize", "nvfp4_quantize_dual", "nvfp4_quantize_noalloc",
+    "nvfp4_dequantize",
     "nvfp4_gemm_workspace_size", "nvfp4_gemm", "nvfp4_linear_workspace_size",
     "nvfp4_linear_fprop", "nvfp4_linear_dgrad", "nvfp4_linear_wgrad",
     "nvfp4_check_device_status", "nvfp4_debug_gemm_skip_load",
@@ -115,6 +116,7 @@ def lib():
             "nvfp4_sf_bytes": (SZ, [I64, I64, I32]),
             "nvfp4_quantize_workspace_size": (I32, [I64, I64, PCFG, PSZ]),
             "nvfp4_quantize": (I32, [P, I64, I64, I64, PCFG, P, P, P, P, SZ, P]),
+            "nvfp4_quantize_dual": (I32, [P, I64, I64, I64, PCFG, P, P, P, PCFG, P, P, P, P, SZ, P]),
             "nvfp4_quantize_noalloc": (I32, [P, I64, I64, I64, PCFG, P, P, P, P]),
             "nvfp4_dequantize": (I32, [PT, I32, P, I64, P]),
             "nvfp4_gemm_workspace_size": (I32, [I64, I64, I64, PSZ]),
@@ -177,18 +179,24 @@ def nvfp4_quantize_workspace_size(rows, cols, cfg):
     return n.value
 
 
+def nvfp4_empty(x, cfg):
+    """Allocate the outputs of quantising x with cfg."""
+    rows, cols = x.shape
+    qr, qk = (cols, rows) if cfg.transpose else (rows, cols)
+    return NVFP4Tensor(
+        codes=torch.empty((qr, qk // 2), dtype=torch.uint8, device=x.device),
+        sf=torch.empty(max(nvfp4_sf_bytes(qr, qk, cfg.sf_layout), 1), dtype=torch.uint8, device=x.device),
+        tensor_scale=torch.empty(1, dtype=torch.float32, device=x.device),
+        rows=qr, k=qk, sf_layout=cfg.sf_layout)
+
+
 def nvfp4_quantize(x, cfg, out=None, workspace=None, stream=None):
     """x: BF16 CUDA tensor [rows, cols] with unit column stride.  Returns an
     NVFP4Tensor (allocated unless `out` is given)."""
     assert x.dtype == torch.bfloat16 and x.dim() == 2 and x.stride(1) == 1
     rows, cols = x.shape
-    qr, qk = (cols, rows) if cfg.transpose else (rows, cols)
     if out is None:
-        out = NVFP4Tensor(
-            codes=torch.empty((qr, qk // 2), dtype=torch.uint8, device=x.device),
-            sf=torch.empty(max(nvfp4_sf_bytes(qr, qk, cfg.sf_layout), 1), dtype=torch.uint8, device=x.device),
-            tensor_scale=torch.empty(1, dtype=torch.float32, device=x.device),
-            rows=qr, k=qk, sf_layout=cfg.sf_layout)
+        out = nvfp4_empty(x, cfg)
     if workspace is None:
         workspace = _alloc_ws(nvfp4_quantize_workspace_size(rows, cols, cfg), x.device)
     ldx = x.stride(0) if rows > 1 else cols
@@ -196,6 +204,26 @@ def nvfp4_quantize(x, cfg, out=None, workspace=None, stream=None):
                               _ptr(out.tensor_scale), _ptr(workspace), workspace.numel(), _stream(stream))
     _check(st, "nvfp4_quantize")
     return out
+
+
+def nvfp4_quantize_dual(x, cfg_a, cfg_b, out_a=None, out_b=None, workspace=None, stream=None):
+    """Two quantised outputs of one BF16 tensor from one read (see
+    include/nvfp4.h).  Returns (out_a, out_b)."""
+    assert x.dtype == torch.bfloat16 and x.dim() == 2 and x.stride(1) == 1
+    rows, cols = x.shape
+    if out_a is None:
+        out_a = nvfp4_empty(x, cfg_a)
+    if out_b is None:
+        out_b = nvfp4_empty(x, cfg_b)
+    if workspace is None:
+        workspace = _alloc_ws(nvfp4_quantize_workspace_size(rows, cols, cfg_a), x.device)
+    ldx = x.stride(0) if rows > 1 else cols
+    st = lib().nvfp4_quantize_dual(_ptr(x), rows, cols, ldx, ctypes.byref(cfg_a), _ptr(out_a.codes),
+                                   _ptr(out_a.sf), _ptr(out_a.tensor_scale), ctypes.byref(cfg_b),
+                                   _ptr(out_b.codes), _ptr(out_b.sf), _ptr(out_b.tensor_scale), _ptr(workspace),
+                                   workspace.numel(), _stream(stream))
+    _check(st, "nvfp4_quantize_dual")
+    return out_a, out_b
 
 
 def nvfp4_quantize_noalloc(x, cfg, out, stream=None):

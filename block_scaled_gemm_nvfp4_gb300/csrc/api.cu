@@ -78,6 +78,22 @@ QuantizedOperand carve_operand(uint8_t*& cursor, int64_t qr, int64_t qk) {
   return o;
 }
 
+QuantOut make_out(const nvfp4_quant_cfg& cfg, void* codes, void* sf, float* scale) {
+  QuantOut o{};
+  o.block2d = cfg.block == NVFP4_BLOCK_16x16;
+  o.sr = cfg.rounding == NVFP4_ROUND_SR;
+  o.rht = cfg.rht;
+  o.transpose = cfg.transpose;
+  o.sf_mma = cfg.sf_layout == NVFP4_SF_MMA;
+  o.rht_seed = cfg.rht_seed;
+  o.sr_seed = cfg.sr_seed;
+  o.sr_offset = cfg.sr_offset;
+  o.codes = static_cast<uint8_t*>(codes);
+  o.sf = static_cast<uint8_t*>(sf);
+  o.tensor_scale = scale;
+  return o;
+}
+
 // Quantise with an explicit status word and scratch (used by the wrappers).
 nvfp4_status quantize_into(const void* x, int64_t rows, int64_t cols, int64_t ldx, const nvfp4_quant_cfg& cfg,
                            void* codes, void* sf, float* scale, uint32_t* status, uint32_t* partials,
@@ -87,22 +103,28 @@ nvfp4_status quantize_into(const void* x, int64_t rows, int64_t cols, int64_t ld
   a.rows = rows;
   a.cols = cols;
   a.ldx = ldx;
-  a.qr = cfg.transpose ? cols : rows;
-  a.qk = cfg.transpose ? rows : cols;
-  a.block2d = cfg.block == NVFP4_BLOCK_16x16;
-  a.sr = cfg.rounding == NVFP4_ROUND_SR;
-  a.rht = cfg.rht;
-  a.transpose = cfg.transpose;
-  a.sf_mma = cfg.sf_layout == NVFP4_SF_MMA;
-  a.rht_seed = cfg.rht_seed;
-  a.sr_seed = cfg.sr_seed;
-  a.sr_offset = cfg.sr_offset;
-  a.codes = static_cast<uint8_t*>(codes);
-  a.sf = static_cast<uint8_t*>(sf);
-  a.tensor_scale = scale;
+  a.n_out = 1;
+  a.out[0] = make_out(cfg, codes, sf, scale);
   a.status = status;
   a.partials = partials;
   return cuda_status(launch_quantize(a, stream));
+}
+
+// Checks shared by the quantiser entry points: the input and one output.
+nvfp4_status check_quant_call(const void* x, int64_t rows, int64_t cols, int64_t ldx, const nvfp4_quant_cfg* cfg,
+                              const void* codes, const void* sf, const float* tensor_scale) {
+  nvfp4_status s = check_cfg(cfg);
+  if (s != NVFP4_OK) return s;
+  s = check_quant_shape(rows, cols, cfg);
+  if (s != NVFP4_OK) return s;
+  if (!tensor_scale) return NVFP4_ERR_INVALID_ARG;
+  const bool empty = rows == 0 || cols == 0;
+  if (!empty && (!x || !codes || !sf)) return NVFP4_ERR_INVALID_ARG;
+  if (ldx < cols) return NVFP4_ERR_INVALID_ARG;
+  if (!empty && (!aligned16(x) || ldx % 8 != 0)) return NVFP4_ERR_INVALID_ARG;
+  if (!empty && (reinterpret_cast<uintptr_t>(codes) & 7u)) return NVFP4_ERR_INVALID_ARG;
+  if (!empty && cfg->sf_layout == NVFP4_SF_MMA && !aligned16(sf)) return NVFP4_ERR_INVALID_ARG;
+  return NVFP4_OK;
 }
 
 nvfp4_status check_tensor(const nvfp4_tensor* t) {
@@ -199,16 +221,8 @@ nvfp4_status nvfp4_quantize_workspace_size(int64_t rows, int64_t cols, const nvf
 nvfp4_status nvfp4_quantize(const void* x, int64_t rows, int64_t cols, int64_t ldx, const nvfp4_quant_cfg* cfg,
                             void* codes, void* sf, float* tensor_scale, void* workspace, size_t workspace_bytes,
                             nvfp4_stream_t stream) {
-  nvfp4_status s = check_cfg(cfg);
+  nvfp4_status s = check_quant_call(x, rows, cols, ldx, cfg, codes, sf, tensor_scale);
   if (s != NVFP4_OK) return s;
-  s = check_quant_shape(rows, cols, cfg);
-  if (s != NVFP4_OK) return s;
-  if (!tensor_scale) return NVFP4_ERR_INVALID_ARG;
-  const bool empty = rows == 0 || cols == 0;
-  if (!empty && (!x || !codes || !sf)) return NVFP4_ERR_INVALID_ARG;
-  if (ldx < cols) return NVFP4_ERR_INVALID_ARG;
-  if (!empty && (!aligned16(x) || ldx % 8 != 0)) return NVFP4_ERR_INVALID_ARG;
-  if (!empty && (reinterpret_cast<uintptr_t>(codes) & 7u)) return NVFP4_ERR_INVALID_ARG;
   if (!workspace) return NVFP4_ERR_WORKSPACE;
   if (workspace_bytes < quant_ws_bytes()) return NVFP4_ERR_WORKSPACE;
   if (reinterpret_cast<uintptr_t>(workspace) & 255u) return NVFP4_ERR_INVALID_ARG;
@@ -217,38 +231,44 @@ nvfp4_status nvfp4_quantize(const void* x, int64_t rows, int64_t cols, int64_t l
                        reinterpret_cast<uint32_t*>(ws + kWsHeaderBytes), reinterpret_cast<cudaStream_t>(stream));
 }
 
-nvfp4_status nvfp4_quantize_noalloc(const void* x, int64_t rows, int64_t cols, int64_t ldx,
-                                    const nvfp4_quant_cfg* cfg, void* codes, void* sf, float* tensor_scale,
-                                    nvfp4_stream_t stream) {
-  nvfp4_status s = check_cfg(cfg);
+nvfp4_status nvfp4_quantize_dual(const void* x, int64_t rows, int64_t cols, int64_t ldx,
+                                 const nvfp4_quant_cfg* cfg_a, void* codes_a, void* sf_a, float* tensor_scale_a,
+                                 const nvfp4_quant_cfg* cfg_b, void* codes_b, void* sf_b, float* tensor_scale_b,
+                                 void* workspace, size_t workspace_bytes, nvfp4_stream_t stream) {
+  nvfp4_status s = check_quant_call(x, rows, cols, ldx, cfg_a, codes_a, sf_a, tensor_scale_a);
   if (s != NVFP4_OK) return s;
-  s = check_quant_shape(rows, cols, cfg);
+  s = check_quant_call(x, rows, cols, ldx, cfg_b, codes_b, sf_b, tensor_scale_b);
   if (s != NVFP4_OK) return s;
-  if (rows > 0 && cols > kNoAllocMaxElements / rows) return NVFP4_ERR_UNSUPPORTED_SHAPE;
-  if (!tensor_scale) return NVFP4_ERR_INVALID_ARG;
-  const bool empty = rows == 0 || cols == 0;
-  if (!empty && (!x || !codes || !sf)) return NVFP4_ERR_INVALID_ARG;
-  if (ldx < cols) return NVFP4_ERR_INVALID_ARG;
-  if (!empty && (!aligned16(x) || ldx % 8 != 0)) return NVFP4_ERR_INVALID_ARG;
-  if (!empty && (reinterpret_cast<uintptr_t>(codes) & 7u)) return NVFP4_ERR_INVALID_ARG;
+  if (!workspace) return NVFP4_ERR_WORKSPACE;
+  if (workspace_bytes < quant_ws_bytes()) return NVFP4_ERR_WORKSPACE;
+  if (reinterpret_cast<uintptr_t>(workspace) & 255u) return NVFP4_ERR_INVALID_ARG;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
   QuantArgs a{};
   a.x = static_cast<const uint16_t*>(x);
   a.rows = rows;
   a.cols = cols;
   a.ldx = ldx;
-  a.qr = cfg->transpose ? cols : rows;
-  a.qk = cfg->transpose ? rows : cols;
-  a.block2d = cfg->block == NVFP4_BLOCK_16x16;
-  a.sr = cfg->rounding == NVFP4_ROUND_SR;
-  a.rht = cfg->rht;
-  a.transpose = cfg->transpose;
-  a.sf_mma = cfg->sf_layout == NVFP4_SF_MMA;
-  a.rht_seed = cfg->rht_seed;
-  a.sr_seed = cfg->sr_seed;
-  a.sr_offset = cfg->sr_offset;
-  a.codes = static_cast<uint8_t*>(codes);
-  a.sf = static_cast<uint8_t*>(sf);
-  a.tensor_scale = tensor_scale;
+  a.n_out = 2;
+  a.out[0] = make_out(*cfg_a, codes_a, sf_a, tensor_scale_a);
+  a.out[1] = make_out(*cfg_b, codes_b, sf_b, tensor_scale_b);
+  a.status = reinterpret_cast<uint32_t*>(ws);
+  a.partials = reinterpret_cast<uint32_t*>(ws + kWsHeaderBytes);
+  return cuda_status(launch_quantize(a, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+nvfp4_status nvfp4_quantize_noalloc(const void* x, int64_t rows, int64_t cols, int64_t ldx,
+                                    const nvfp4_quant_cfg* cfg, void* codes, void* sf, float* tensor_scale,
+                                    nvfp4_stream_t stream) {
+  nvfp4_status s = check_quant_call(x, rows, cols, ldx, cfg, codes, sf, tensor_scale);
+  if (s != NVFP4_OK) return s;
+  if (rows > 0 && cols > kNoAllocMaxElements / rows) return NVFP4_ERR_UNSUPPORTED_SHAPE;
+  QuantArgs a{};
+  a.x = static_cast<const uint16_t*>(x);
+  a.rows = rows;
+  a.cols = cols;
+  a.ldx = ldx;
+  a.n_out = 1;
+  a.out[0] = make_out(*cfg, codes, sf, tensor_scale);
   return cuda_status(launch_quantize_noalloc(a, reinterpret_cast<cudaStream_t>(stream)));
 }
 

@@ -1,6 +1,8 @@
 // Internal launcher interface between the C ABI (api.cu) and the kernels.
 #pragma once
 
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 #include <cstddef>
 #include <cstdint>
@@ -12,19 +14,29 @@ namespace nvfp4 {
 // Every workspace starts with a 256-byte header; its first 32-bit word is the
 // device status word.  The quantiser's scratch follows the header.
 constexpr size_t kWsHeaderBytes = 256;
-// Partial amax slots (one per CTA of the amax pass).
+// Partial amax slots: the amax pass writes one per CTA and per output
+// (at most kMaxQuantOutputs outputs of kPartialsPerOutput slots each).
 constexpr int kMaxAmaxPartials = 4096;
+constexpr int kMaxQuantOutputs = 2;
+constexpr int kPartialsPerOutput = kMaxAmaxPartials / kMaxQuantOutputs;
 constexpr size_t kQuantScratchBytes = kMaxAmaxPartials * sizeof(uint32_t);
 
-struct QuantArgs {
-  const uint16_t* x;   // BF16 input
-  int64_t rows, cols, ldx;
-  int64_t qr, qk;      // quantised operand shape
+// One quantised output of a BF16 tensor: Q = x (transpose 0) or Q = x^T.
+struct QuantOut {
   int block2d, sr, rht, transpose, sf_mma;
   uint64_t rht_seed, sr_seed, sr_offset;
   uint8_t* codes;
   uint8_t* sf;
   float* tensor_scale;
+};
+
+// One read of x [rows, cols] (row-major, leading dimension ldx) produces
+// n_out (1 or 2) quantised outputs.
+struct QuantArgs {
+  const uint16_t* x;   // BF16 input
+  int64_t rows, cols, ldx;
+  int n_out;
+  QuantOut out[kMaxQuantOutputs];
   uint32_t* status;    // device status word
   uint32_t* partials;  // kMaxAmaxPartials slots
 };
@@ -67,5 +79,8 @@ struct GemmArgs {
 cudaError_t launch_gemm(const GemmArgs& a, cudaStream_t stream);
 
 int device_sm_count();
+
+// cuTensorMapEncodeTiled from the driver (null if unavailable).
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder();
 
 }  // namespace nvfp4

@@ -105,6 +105,11 @@ __device__ __forceinline__ uint64_t policy_evict_last() {
   asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
   return pol;
 }
+__device__ __forceinline__ uint64_t policy_evict_first() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
 // 2-D tiled TMA load multicast to every CTA of the cluster in cta_mask: the
 // box lands at the same shared-memory offset in each, and each CTA's mbarrier
 // at the offset of `bar` receives the byte count.

@@ -1,12 +1,21 @@
 // NVFP4 quantisation of BF16 tensors (sm_103a).
 //
-// Two passes over the input, both persistent grid-stride loops over tiles:
-//   pass 0: tensor amax (after the optional random Hadamard transform), one
-//           partial per CTA written to the workspace;
-//   pass 1: every CTA reduces the partials, derives the FP32 tensor scale
-//           s = amax / 2688 and encodes its tiles into E2M1 codes and E4M3
-//           block scales.  Pass 1 walks the tiles in reverse order so that
-//           its first reads hit the part of the input pass 0 left in L2.
+// One call reads x [rows, cols] and writes one or two quantised outputs, each
+// either Q = x (blocks of 16 along a row of x) or Q = x^T (blocks of 16 down a
+// column of x), each with its own block shape, rounding, transform and tensor
+// scale.  A linear layer needs both orientations of X and dY (fprop/dgrad use
+// rows, wgrad uses columns) and of W (fprop, dgrad), so producing both from one
+// read halves the quantiser's input traffic.
+//
+// Two kernels, both persistent loops over 128 x 128 tiles of x that TMA copies
+// into shared memory (two 64-column boxes, 128-byte swizzle, two-stage ring):
+//   pass 0: per-output tensor amax (after the optional random Hadamard
+//           transform, in the output's orientation); one partial per CTA;
+//   pass 1: every CTA reduces the partials, derives s = amax / 2688 and encodes
+//           its tiles.  It walks the tiles in reverse order, so its first
+//           reads hit the part of x that pass 0 left in L2.
+// Out-of-range parts of a tile read as zero, so ragged tiles need no special
+// case and the padding of the tensor-core scale layout comes out as zeros.
 //
 // Format and rounding sequence (per run of 16 along K; the pages' NVFP4
 // elements on a sparse 4-bit grid with custom scaling, "NVIDIA acelera o
@@ -15,17 +24,21 @@
 // "Full-Stack FP4...", section 2.2):
 //   t = (bamax / 6) / s -> E4M3 (RNE, saturating), d = e4m3(t) * s,
 //   v = x / d -> E2M1 by RNE or by stochastic rounding with a Philox4x32-10
-//   word per element.  All FP32 steps are IEEE round-to-nearest operations
-//   (explicit _rn intrinsics; the file is built without FMA contraction).
+//   word per element.  Every FP32 step is an IEEE round-to-nearest operation
+//   (the file is built without FMA contraction).  The element division uses a
+//   correctly rounded reciprocal and one FMA residual correction, which gives
+//   the IEEE quotient wherever it can change a code (see div_fast).
 //
-// Thread layouts (one thread owns whole runs of 16, so the transform and the
-// block maximum stay in registers):
-//   row mode (Q = x):   a warp covers 16 rows x 32 columns; lane -> row
-//                       (lane & 15), run (lane >> 4).  CTA tile 16 x 256.
-//   col mode (Q = x^T): a warp covers 16 rows x 64 columns of x; lane ->
-//                       columns 2*lane, 2*lane + 1 (two runs).  CTA tile
-//                       128 rows x 64 columns of x.
+// Thread layout: one thread owns whole runs of 16, so the transform and the
+// block maximum stay in registers.  Thread t works on position p = t & 127
+// (a tile row for Q = x, a tile column for Q = x^T) and runs j = (t >> 7) +
+// 2i, i = 0..3; a warp's lanes are 32 consecutive positions of one run, so a
+// 16 x 16 block is 16 adjacent lanes and the 128-byte swizzle keeps both read
+// patterns free of bank conflicts.  Results are staged in shared memory and
+// leave in whole 32-byte pieces.
+#include <cuda.h>
 #include <cuda_runtime.h>
+#include <cudaTypedefs.h>
 
 #include <algorithm>
 #include <cstdint>
@@ -38,49 +51,61 @@ namespace nvfp4 {
 namespace {
 
 constexpr int kThreads = 256;
+constexpr int kTile = 128;                      // tile: 128 rows x 128 columns of x
+constexpr int kBoxBytes = kTile * 128;          // one TMA box: 64 BF16 columns x 128 rows
+constexpr int kStageBytes = 2 * kBoxBytes;      // 32 KB
+constexpr int kStages = 2;
+// Per output, a tile's results are staged in shared memory before they go to
+// global memory in whole 32-byte pieces: codes of position p, run j at
+// p * 72 + 8 j (the 72-byte pitch spreads a warp's stores over the banks);
+// scales as the two 128 x 4 atoms of the tensor-core layout.  Two staging
+// buffers per output follow the ring.
+constexpr int kStgPitch = 72;
+constexpr int kStgCodes = kTile * kStgPitch;    // 9216
+constexpr int kStgBytes = kStgCodes + 2 * 512;  // + scales
+constexpr int kStgOffset = kStages * kStageBytes;
+constexpr int kSmemBytes = kStgOffset + 2 * kMaxQuantOutputs * kStgBytes + 1024;  // + slack to align to 1024 B
 
-struct QParams {
-  const uint16_t* x;
-  int64_t rows, cols, ldx;
-  int64_t qr, qk, kb_count;
+struct OutParams {
   uint8_t* codes;
   uint8_t* sf;
   float* tensor_scale;
-  uint32_t* status;
   uint32_t* partials;
+  int64_t qr, qk, code_ld, kb_count, katoms;
   uint64_t rht_seed, sr_seed, sr_offset;
+  int col, block2d, sr, rht, sf_mma, vec16;
+};
+
+struct TileParams {
   int64_t tiles_c, num_tiles;
-  int64_t sf_katoms;
-  int sf_mma;
+  OutParams out[kMaxQuantOutputs];
+  int n_out;
+  int amax_shared;  // two outputs, neither transformed: output 1 reuses output 0's amax
   int num_partials;
+  uint32_t* status;
 };
 
 // Philox4x32-10 (Salmon et al., SC'11): ten rounds, Weyl key schedule.
 __device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint32_t k0, uint32_t k1) {
 #pragma unroll
   for (int i = 0; i < 10; ++i) {
-    const uint32_t lo0 = 0xD2511F53u * c.x, hi0 = __umulhi(0xD2511F53u, c.x);
-    const uint32_t lo1 = 0xCD9E8D57u * c.z, hi1 = __umulhi(0xCD9E8D57u, c.z);
-    c = make_uint4(hi1 ^ c.y ^ k0, lo1, hi0 ^ c.w ^ k1, lo0);
+    const uint64_t p0 = static_cast<uint64_t>(0xD2511F53u) * c.x;
+    const uint64_t p1 = static_cast<uint64_t>(0xCD9E8D57u) * c.z;
+    c = make_uint4(static_cast<uint32_t>(p1 >> 32) ^ c.y ^ k0, static_cast<uint32_t>(p1),
+                   static_cast<uint32_t>(p0 >> 32) ^ c.w ^ k1, static_cast<uint32_t>(p0));
     k0 += 0x9E3779B9u;
     k1 += 0xBB67AE85u;
   }
   return c;
 }
 
-__device__ __forceinline__ int64_t sf_index(const QParams& p, int64_t r, int64_t kb) {
-  if (!p.sf_mma) return r * p.kb_count + kb;
-  const int64_t atom = (r >> 7) * p.sf_katoms + (kb >> 2);
-  const int rr = static_cast<int>(r & 127);
-  return atom * 512 + (rr & 31) * 16 + (rr >> 5) * 4 + static_cast<int>(kb & 3);
-}
-
 __device__ __forceinline__ uint32_t abs_bits(float v) { return __float_as_uint(v) & 0x7FFFFFFFu; }
 
-// x' = 1/4 * H16 * diag(sigma) * x; butterflies of stride 1, 2, 4, 8.
+// x' = 1/4 * H16 * diag(sigma) * x; butterflies of stride 1, 2, 4, 8.  The
+// signs are applied as multiplications by +-1 (exact; zeros keep IEEE signs).
 __device__ __forceinline__ void rht16(float (&v)[16], uint32_t sign_mask) {
 #pragma unroll
-  for (int j = 0; j < 16; ++j) v[j] = __uint_as_float(__float_as_uint(v[j]) ^ (((sign_mask >> j) & 1u) << 31));
+  for (int j = 0; j < 16; ++j) v[j] = __fmul_rn(v[j], ((sign_mask >> j) & 1u) ? -1.0f : 1.0f);
 #pragma unroll
   for (int s = 1; s < 16; s <<= 1) {
 #pragma unroll
@@ -95,6 +120,8 @@ __device__ __forceinline__ void rht16(float (&v)[16], uint32_t sign_mask) {
   for (int j = 0; j < 16; ++j) v[j] = __fmul_rn(v[j], 0.25f);
 }
 
+// Largest |v| of a run as FP32 bits; inf and NaN sort above every finite
+// value, which is how the amax pass detects them.
 __device__ __forceinline__ uint32_t run_absmax_bits(const float (&v)[16]) {
   uint32_t m = 0;
 #pragma unroll
@@ -102,39 +129,81 @@ __device__ __forceinline__ uint32_t run_absmax_bits(const float (&v)[16]) {
   return m;
 }
 
-// Stochastic rounding of q onto the E2M1 grid: lo, hi the grid points around
-// |q|, f = (|q| - lo) / (hi - lo), up iff (r >> 8) * 2^-24 < f; |q| >= 6 -> 6.
-__device__ __forceinline__ float sr_round(float q, uint32_t r) {
-  const float mag = fabsf(q);
-  float g;
-  if (mag >= 6.0f) {
-    g = 6.0f;
-  } else {
-    const float step = mag < 2.0f ? 0.5f : (mag < 4.0f ? 1.0f : 2.0f);
-    const float inv = mag < 2.0f ? 2.0f : (mag < 4.0f ? 1.0f : 0.5f);
-    const float lo = __fmul_rn(floorf(__fmul_rn(mag, inv)), step);
-    const float f = __fmul_rn(__fsub_rn(mag, lo), inv);
-    const float u = __fmul_rn(static_cast<float>(r >> 8), 5.9604644775390625e-08f);
-    g = (u < f) ? __fadd_rn(lo, step) : lo;
-  }
-  return copysignf(g, q);
+// Largest |v| of a run of finite values, as FP32 bits (for non-negative
+// floats the order of the values is the order of their bits).
+__device__ __forceinline__ uint32_t run_absmax_finite(const float (&v)[16]) {
+  float m = 0.0f;
+#pragma unroll
+  for (int j = 0; j < 16; ++j) m = fmaxf(m, fabsf(v[j]));
+  return __float_as_uint(m);
 }
 
-// Encode one run of 16 values with block maximum `bamax`; e0 is the linear
-// index of the run's first element in Q (for the Philox counter).
+// x / d for 2^-70 <= d < 2^126, given rd = RN(1/d): q0 = RN(x * rd) is
+// within one ulp of x / d, and one residual correction q0 + RN(x - q0 d) * rd
+// with an exact FMA residual rounds to the IEEE quotient (Markstein's
+// division theorem; P. Markstein, "Computation of elementary functions on
+// the IBM RISC System/6000 processor", IBM J. Res. Dev. 34, 1990), as long
+// as nothing underflows: |x| >= 2^-96 and |q| >= 2^-100.  Outside that range
+// the quotient is below 2^-25, where an RNE code is +-0 whatever its exact
+// value and stochastic rounding only asks whether it is zero (encode_run
+// keeps that answer exact by its choice of path).
+__device__ __forceinline__ float div_fast(float x, float d, float rd) {
+  const float q0 = __fmul_rn(x, rd);
+  // (q0 d - x) is the negated residual; q0 - that * rd keeps the sign of a
+  // zero x: for x = -0 both terms are -0, and the sum of two -0 is -0.
+  return __fmaf_rn(-__fmaf_rn(q0, d, -x), rd, q0);
+}
+
+// Stochastic rounding of q onto the E2M1 grid {0, .5, 1, 1.5, 2, 3, 4, 6}:
+// lo, hi the grid points around |q|, f = (|q| - lo) / (hi - lo), round up iff
+// k * 2^-24 < f with k = r >> 8; |q| >= 6 -> 6.  Branch-free:
+//   |q| in [1, 6): the grid points are the values whose 22 mantissa bits
+//     below the top one are zero and f * 2^24 = 4 * (those bits), so
+//     k < f * 2^24 iff adding 2^22 - 1 - (k >> 2) to the bits carries into
+//     the grid bit;
+//   |q| in [0, 1): lo in {0, 1/2} and f * 2^24 = |q| * 2^25 - lo * 2^25,
+//     exact in FP32, compared with k (< 2^24, exact as a float).
+// Returns the grid value with the sign of q.
+__device__ __forceinline__ float sr_round(float q, uint32_t rnd) {
+  const uint32_t b = abs_bits(q);
+  const uint32_t g_hi = (b + ((~rnd) >> 10)) & 0xFFC00000u;
+  const bool half_up = b >= 0x3F000000u;  // |q| >= 1/2: lo = 1/2
+  const float y = __fmaf_rn(__uint_as_float(b), 33554432.0f, half_up ? -16777216.0f : 0.0f);
+  const bool up = __uint2float_rn(rnd >> 8) < y;
+  const uint32_t g_lo = (half_up ? 0x3F000000u : 0u) + (up ? (half_up ? 0x00800000u : 0x3F000000u) : 0u);
+  uint32_t g = b >= 0x3F800000u ? g_hi : g_lo;
+  g = b >= 0x40C00000u ? 0x40C00000u : g;
+  return __uint_as_float(g | (__float_as_uint(q) & 0x80000000u));
+}
+
+// Encode one run of 16 values (already transformed) with block maximum
+// `bamax_bits`; e0 is the linear index of the run's first element in Q, the
+// Philox counter of element e being e >> 2 (word e & 3).
 template <bool SR>
-__device__ __forceinline__ uint2 encode_run(const float (&v)[16], float bamax, float s_dec, uint64_t e0,
-                                            const QParams& p, uint32_t& sfb) {
-  const float t = __fdiv_rn(__fdiv_rn(bamax, 6.0f), s_dec);
+__device__ __forceinline__ uint2 encode_run(const float (&v)[16], uint32_t bamax_bits, float s_dec, uint64_t e0,
+                                            const OutParams& o, uint32_t& sfb) {
+  const float t = __fdiv_rn(__fdiv_rn(__uint_as_float(bamax_bits), 6.0f), s_dec);
   sfb = ptx::cvt_e4m3(t);
   if (sfb == 0) return make_uint2(0u, 0u);
   const float d = __fmul_rn(ptx::e4m3_to_float(sfb), s_dec);
   float q[16];
+  // Fast division where it is exact for every code (see div_fast): d in
+  // [2^-70, 2^126) for RNE.  Stochastic rounding also needs the zero-ness of
+  // quotients below 2^-25: every nonzero input (a BF16 value, or a transform
+  // of BF16 values) is at least 2^-135 in magnitude, so for d < 2^14 every
+  // such quotient and its fast approximation are nonzero.
+  const bool fast = d >= 0x1p-70f && d < (SR ? 0x1p14f : 0x1p126f);
+  if (fast) {
+    const float rd = __frcp_rn(d);
 #pragma unroll
-  for (int j = 0; j < 16; ++j) q[j] = __fdiv_rn(v[j], d);
+    for (int j = 0; j < 16; ++j) q[j] = div_fast(v[j], d, rd);
+  } else {
+#pragma unroll
+    for (int j = 0; j < 16; ++j) q[j] = __fdiv_rn(v[j], d);
+  }
   if (SR) {
-    const uint32_t k0 = static_cast<uint32_t>(p.sr_seed), k1 = static_cast<uint32_t>(p.sr_seed >> 32);
-    const uint32_t o0 = static_cast<uint32_t>(p.sr_offset), o1 = static_cast<uint32_t>(p.sr_offset >> 32);
+    const uint32_t k0 = static_cast<uint32_t>(o.sr_seed), k1 = static_cast<uint32_t>(o.sr_seed >> 32);
+    const uint32_t o0 = static_cast<uint32_t>(o.sr_offset), o1 = static_cast<uint32_t>(o.sr_offset >> 32);
     const uint64_t c = e0 >> 2;
 #pragma unroll
     for (int g = 0; g < 4; ++g) {
@@ -162,108 +231,113 @@ __device__ __forceinline__ void unpack8(const uint4& w, float* v) {
   v[7] = __uint_as_float(w.w & 0xFFFF0000u);
 }
 
-template <int PASS>
-__device__ __forceinline__ uint4 load16(const uint4* ptr) {
-  // The amax pass leaves the input in L2 for the encode pass; the encode
-  // pass is the last reader.
-  return PASS == 0 ? __ldg(ptr) : __ldcs(ptr);
-}
-template <int PASS>
-__device__ __forceinline__ uint32_t load4(const uint32_t* ptr) {
-  return PASS == 0 ? __ldg(ptr) : __ldcs(ptr);
-}
-template <int PASS>
-__device__ __forceinline__ uint32_t load2(const uint16_t* ptr) {
-  return PASS == 0 ? static_cast<uint32_t>(__ldg(ptr)) : static_cast<uint32_t>(__ldcs(ptr));
-}
-
-// ------------------------------------------------------------ row mode tile
-template <bool BLOCK2D, bool RHT, bool SR, int PASS>
-__device__ __forceinline__ void row_tile(const QParams& p, int64_t tile, uint32_t rht_mask, float s_dec,
-                                         uint32_t& tmax) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int64_t tr = tile / p.tiles_c, tc = tile - tr * p.tiles_c;
-  const int64_t row = tr * 16 + (lane & 15);
-  const int64_t kb = tc * 16 + warp * 2 + (lane >> 4);
-  const bool valid = row < p.qr && kb < p.kb_count;
-  float v[16];
-  if (valid) {
-    const uint4* src = reinterpret_cast<const uint4*>(p.x + row * p.ldx + kb * 16);
-    const uint4 a = load16<PASS>(src);
-    const uint4 b = load16<PASS>(src + 1);
+// ----------------------------------------------------------- tile loaders
+// Stage layout: box h (tile columns 64h .. 64h + 63) at h * 16 KB; tile row r
+// at r * 128 bytes within the box; its 16-byte chunk c at ((c ^ (r & 7)) * 16).
+//
+// Run j (0..7) of position p (0..127): for Q = x, tile columns 16j .. 16j+15
+// of tile row p; for Q = x^T, tile rows 16j .. 16j+15 of tile column p.
+template <bool COL>
+__device__ __forceinline__ void load_run(const uint8_t* stage, int p, int j, float (&v)[16]) {
+  if (!COL) {
+    const uint8_t* rowp = stage + (j >> 2) * kBoxBytes + p * 128;
+    const int c = 2 * (j & 3), sw = p & 7;
+    const uint4 a = *reinterpret_cast<const uint4*>(rowp + ((c ^ sw) << 4));
+    const uint4 b = *reinterpret_cast<const uint4*>(rowp + (((c + 1) ^ sw) << 4));
     unpack8(a, v);
     unpack8(b, v + 8);
   } else {
+    const uint8_t* colp = stage + (p >> 6) * kBoxBytes + j * 16 * 128 + (p & 7) * 2;
+    const int c = (p & 63) >> 3;
 #pragma unroll
-    for (int j = 0; j < 16; ++j) v[j] = 0.0f;
+    for (int i = 0; i < 16; ++i) {
+      const uint32_t h = *reinterpret_cast<const uint16_t*>(colp + i * 128 + ((c ^ (i & 7)) << 4));
+      v[i] = __uint_as_float(h << 16);
+    }
   }
-  if (RHT) rht16(v, rht_mask);
-  uint32_t m = run_absmax_bits(v);
-  if (PASS == 0) {
-    tmax = max(tmax, m);
-    return;
-  }
-  if (BLOCK2D) {
-#pragma unroll
-    for (int o = 1; o < 16; o <<= 1) m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
-  }
-  if (!valid) return;
-  uint32_t sfb;
-  const uint2 c = encode_run<SR>(v, __uint_as_float(m), s_dec, static_cast<uint64_t>(row * p.qk + kb * 16), p, sfb);
-  *reinterpret_cast<uint2*>(p.codes + row * (p.qk / 2) + kb * 8) = c;
-  p.sf[sf_index(p, row, kb)] = static_cast<uint8_t>(sfb);
 }
 
-// ------------------------------------------------------------ col mode tile
-template <bool BLOCK2D, bool RHT, bool SR, int PASS>
-__device__ __forceinline__ void col_tile(const QParams& p, int64_t tile, uint32_t rht_mask, float s_dec,
-                                         uint32_t& tmax) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int64_t tr = tile / p.tiles_c, tc = tile - tr * p.tiles_c;
-  const int64_t kb = tr * 8 + warp;           // rows 16 kb .. 16 kb + 15 of x
-  const int64_t c0 = tc * 64 + 2 * lane;      // columns c0, c0 + 1 of x = rows of Q
-  const bool kvalid = kb < p.kb_count;
-  const bool v0ok = kvalid && c0 < p.cols;
-  const bool v1ok = kvalid && c0 + 1 < p.cols;
-  float v0[16], v1[16];
+// ------------------------------------------------------------ amax pass
+template <bool COL>
+__device__ __forceinline__ uint32_t amax_tile(const uint8_t* stage, bool rht, uint32_t rht_mask) {
+  const int p = threadIdx.x & 127, j0 = threadIdx.x >> 7;
+  uint32_t m = 0;
 #pragma unroll
-  for (int j = 0; j < 16; ++j) {
-    uint32_t w = 0;
-    const uint16_t* src = p.x + (kb * 16 + j) * p.ldx + c0;
-    if (v1ok)
-      w = load4<PASS>(reinterpret_cast<const uint32_t*>(src));
-    else if (v0ok)
-      w = load2<PASS>(src);
-    v0[j] = __uint_as_float(w << 16);
-    v1[j] = __uint_as_float(w & 0xFFFF0000u);
+  for (int i = 0; i < 4; ++i) {
+    float v[16];
+    load_run<COL>(stage, p, j0 + 2 * i, v);
+    if (rht) rht16(v, rht_mask);
+    m = max(m, run_absmax_bits(v));
   }
-  if (RHT) {
-    rht16(v0, rht_mask);
-    rht16(v1, rht_mask);
-  }
-  uint32_t m0 = run_absmax_bits(v0), m1 = run_absmax_bits(v1);
-  if (PASS == 0) {
-    tmax = max(tmax, max(m0, m1));
-    return;
-  }
-  if (BLOCK2D) {
-    // a 16x16 tile is 16 columns of x = 8 lanes x 2 columns
-    m0 = max(m0, m1);
+  return m;
+}
+
+// ------------------------------------------------------------ encode pass
+__device__ __forceinline__ int stg_sf_offset(int p, int j) {
+  return kStgCodes + (j >> 2) * 512 + (p & 31) * 16 + (p >> 5) * 4 + (j & 3);
+}
+
+template <bool COL, bool SR>
+__device__ __forceinline__ void encode_tile(const uint8_t* stage, uint8_t* stg, const OutParams& o, float s_dec,
+                                            uint32_t rht_mask, int64_t tr, int64_t tc) {
+  const int p = threadIdx.x & 127, j0 = threadIdx.x >> 7;
+  const int64_t qrow = (COL ? tc : tr) * kTile + p;
+  const int64_t kb0 = (COL ? tr : tc) * 8;
+  // two runs per iteration for instruction-level parallelism, one on the
+  // longer stochastic-rounding path
+#pragma unroll(SR ? 1 : 2)
+  for (int i = 0; i < 4; ++i) {
+    const int j = j0 + 2 * i;
+    float v[16];
+    load_run<COL>(stage, p, j, v);
+    if (o.rht) rht16(v, rht_mask);
+    uint32_t m = run_absmax_finite(v);  // the amax pass has ruled out inf and NaN
+    if (o.block2d) {
 #pragma unroll
-    for (int o = 1; o < 8; o <<= 1) m0 = max(m0, __shfl_xor_sync(0xFFFFFFFFu, m0, o));
-    m1 = m0;
+      for (int x = 1; x < 16; x <<= 1) m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, x));
+    }
+    uint32_t sfb;
+    const uint2 c = encode_run<SR>(v, m, s_dec, static_cast<uint64_t>(qrow * o.qk + (kb0 + j) * 16), o, sfb);
+    *reinterpret_cast<uint2*>(stg + p * kStgPitch + 8 * j) = c;
+    stg[stg_sf_offset(p, j)] = static_cast<uint8_t>(sfb);
   }
-  uint32_t sfb;
-  if (v0ok) {
-    const uint2 c = encode_run<SR>(v0, __uint_as_float(m0), s_dec, static_cast<uint64_t>(c0 * p.qk + kb * 16), p, sfb);
-    *reinterpret_cast<uint2*>(p.codes + c0 * (p.qk / 2) + kb * 8) = c;
-    p.sf[sf_index(p, c0, kb)] = static_cast<uint8_t>(sfb);
+}
+
+// Staged tile -> global memory.  Thread t copies the codes of runs 4 (t & 1)
+// .. + 3 of position t >> 1; the first 64 threads copy the two scale atoms.
+// Rows of Q past qr and blocks past kb_count are not written, except that the
+// tensor-core scale layout receives its zero padding.
+__device__ __forceinline__ void copy_out(const uint8_t* stg, const OutParams& o, int64_t qrow0, int64_t kb0) {
+  const int t = threadIdx.x;
+  const int p = t >> 1, half = t & 1;
+  const int64_t qrow = qrow0 + p;
+  const int64_t kb = kb0 + 4 * half;
+  if (qrow < o.qr && kb < o.kb_count) {
+    const uint8_t* src = stg + p * kStgPitch + 32 * half;
+    uint2 w[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) w[i] = *reinterpret_cast<const uint2*>(src + 8 * i);
+    uint8_t* dst = o.codes + qrow * o.code_ld + kb * 8;
+    if (o.vec16 && kb + 4 <= o.kb_count) {
+      *reinterpret_cast<uint4*>(dst) = make_uint4(w[0].x, w[0].y, w[1].x, w[1].y);
+      *reinterpret_cast<uint4*>(dst + 16) = make_uint4(w[2].x, w[2].y, w[3].x, w[3].y);
+    } else {
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+        if (kb + i < o.kb_count) *reinterpret_cast<uint2*>(dst + 8 * i) = w[i];
+    }
   }
-  if (v1ok) {
-    const uint2 c =
-        encode_run<SR>(v1, __uint_as_float(m1), s_dec, static_cast<uint64_t>((c0 + 1) * p.qk + kb * 16), p, sfb);
-    *reinterpret_cast<uint2*>(p.codes + (c0 + 1) * (p.qk / 2) + kb * 8) = c;
-    p.sf[sf_index(p, c0 + 1, kb)] = static_cast<uint8_t>(sfb);
+  if (o.sf_mma) {
+    if (t < 64) {
+      const int64_t katom = (kb0 >> 2) + (t >> 5);
+      if (katom < o.katoms)
+        *reinterpret_cast<uint4*>(o.sf + ((qrow0 >> 7) * o.katoms + katom) * 512 + (t & 31) * 16) =
+            *reinterpret_cast<const uint4*>(stg + kStgCodes + t * 16);
+    }
+  } else if (qrow < o.qr) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      if (kb + i < o.kb_count) o.sf[qrow * o.kb_count + kb + i] = stg[stg_sf_offset(p, 4 * half + i)];
   }
 }
 
@@ -280,108 +354,179 @@ __device__ __forceinline__ uint32_t block_max(uint32_t v, uint32_t* red) {
   return v;
 }
 
-template <bool COL, bool BLOCK2D, bool RHT, bool SR, int PASS>
-__global__ void __launch_bounds__(kThreads) quant_kernel(const QParams p) {
+template <int PASS>
+__global__ void __launch_bounds__(kThreads, 2) quant_tiles(const __grid_constant__ CUtensorMap xmap,
+                                                           const TileParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ __align__(8) uint64_t full[kStages];
   __shared__ uint32_t red[kThreads / 32];
-  uint32_t rht_mask = 0;
-  if (RHT) {
-    const uint4 w = philox4x32_10(make_uint4(0u, 0u, 0u, 0u), static_cast<uint32_t>(p.rht_seed),
-                                  static_cast<uint32_t>(p.rht_seed >> 32));
-    rht_mask = w.x & 0xFFFFu;
+  __shared__ int abort_flag;
+  uint8_t* ring = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int tid = threadIdx.x;
+
+  uint32_t rht_mask[kMaxQuantOutputs] = {0u, 0u};
+  float s_dec[kMaxQuantOutputs] = {1.0f, 1.0f};
+  bool live[kMaxQuantOutputs] = {true, true};
+#pragma unroll
+  for (int o = 0; o < kMaxQuantOutputs; ++o) {
+    if (o < p.n_out && p.out[o].rht) {
+      const uint64_t seed = p.out[o].rht_seed;
+      const uint4 w = philox4x32_10(make_uint4(0u, 0u, 0u, 0u), static_cast<uint32_t>(seed),
+                                    static_cast<uint32_t>(seed >> 32));
+      rht_mask[o] = w.x & 0xFFFFu;
+    }
   }
-  float s_dec = 1.0f;
   if (PASS == 1) {
-    uint32_t m = 0;
-    for (int i = threadIdx.x; i < p.num_partials; i += kThreads) m = max(m, p.partials[i]);
-    m = block_max(m, red);
-    if (m >= 0x7F800000u) {  // inf or NaN somewhere in the input
-      if (blockIdx.x == 0 && threadIdx.x == 0) {
-        ptx::set_status(p.status, kDevNonFinite);
-        *p.tensor_scale = __uint_as_float(0x7FC00000u);
+#pragma unroll
+    for (int o = 0; o < kMaxQuantOutputs; ++o) {
+      if (o >= p.n_out) break;
+      const uint32_t* part = p.out[(o == 1 && p.amax_shared) ? 0 : o].partials;
+      uint32_t m = 0;
+      for (int i = tid; i < p.num_partials; i += kThreads) m = max(m, part[i]);
+      m = block_max(m, red);
+      if (m >= 0x7F800000u) {  // inf or NaN somewhere in the input
+        live[o] = false;
+        if (blockIdx.x == 0 && tid == 0) {
+          ptx::set_status(p.status, kDevNonFinite);
+          *p.out[o].tensor_scale = __uint_as_float(0x7FC00000u);
+        }
+      } else {
+        float s = __fdiv_rn(__uint_as_float(m), 2688.0f);
+        if (s == 0.0f) s = 1.0f;
+        s_dec[o] = s;
+        if (blockIdx.x == 0 && tid == 0) *p.out[o].tensor_scale = s;
       }
-      return;
     }
-    s_dec = __fdiv_rn(__uint_as_float(m), 2688.0f);
-    if (s_dec == 0.0f) s_dec = 1.0f;
-    if (blockIdx.x == 0 && threadIdx.x == 0) *p.tensor_scale = s_dec;
   }
-  uint32_t tmax = 0;
-  for (int64_t it = blockIdx.x; it < p.num_tiles; it += gridDim.x) {
-    const int64_t tile = PASS == 1 ? p.num_tiles - 1 - it : it;
-    if (COL)
-      col_tile<BLOCK2D, RHT, SR, PASS>(p, tile, rht_mask, s_dec, tmax);
-    else
-      row_tile<BLOCK2D, RHT, SR, PASS>(p, tile, rht_mask, s_dec, tmax);
-  }
-  if (PASS == 0) {
-    tmax = block_max(tmax, red);
-    if (threadIdx.x == 0) p.partials[blockIdx.x] = tmax;
-  }
-}
 
-// Zero the padding of the tensor-core scale layout: rows [qr, pad_r) and
-// scale columns [kb_count, pad_kb).
-__global__ void sf_pad_kernel(uint8_t* sf, int64_t qr, int64_t kb_count, int64_t pad_r, int64_t pad_kb,
-                              int64_t katoms) {
-  const int64_t n_rows_pad = (pad_r - qr) * pad_kb;
-  const int64_t n_cols_pad = qr * (pad_kb - kb_count);
-  const int64_t total = n_rows_pad + n_cols_pad;
-  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total;
-       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-    int64_t r, kb;
-    if (i < n_rows_pad) {
-      r = qr + i / pad_kb;
-      kb = i % pad_kb;
+  if (tid == 0) {
+    for (int s = 0; s < kStages; ++s) ptx::mbar_init(&full[s], 1);
+    abort_flag = 0;
+    ptx::fence_mbar_init();
+  }
+  __syncthreads();
+
+  const int64_t G = gridDim.x;
+  const int64_t n_my = blockIdx.x < p.num_tiles ? (p.num_tiles - 1 - blockIdx.x) / G + 1 : 0;
+  auto tile_of = [&](int64_t i) {
+    const int64_t it = blockIdx.x + i * G;
+    return PASS == 1 ? p.num_tiles - 1 - it : it;
+  };
+  auto issue = [&](int64_t i) {
+    const int s = static_cast<int>(i % kStages);
+    const int64_t tile = tile_of(i);
+    const int32_t x0 = static_cast<int32_t>((tile % p.tiles_c) * kTile);
+    const int32_t y0 = static_cast<int32_t>((tile / p.tiles_c) * kTile);
+    uint8_t* dst = ring + s * kStageBytes;
+    ptx::mbar_arrive_expect_tx(&full[s], kStageBytes);
+    if (PASS == 1) {
+      const uint64_t pol = ptx::policy_evict_first();
+      ptx::tma_load_2d_hint(dst, &xmap, &full[s], x0, y0, pol);
+      ptx::tma_load_2d_hint(dst + kBoxBytes, &xmap, &full[s], x0 + 64, y0, pol);
     } else {
-      const int64_t j = i - n_rows_pad;
-      const int64_t w = pad_kb - kb_count;
-      r = j / w;
-      kb = kb_count + j % w;
+      ptx::tma_load_2d(dst, &xmap, &full[s], x0, y0);
+      ptx::tma_load_2d(dst + kBoxBytes, &xmap, &full[s], x0 + 64, y0);
     }
-    const int64_t atom = (r >> 7) * katoms + (kb >> 2);
-    const int rr = static_cast<int>(r & 127);
-    sf[atom * 512 + (rr & 31) * 16 + (rr >> 5) * 4 + static_cast<int>(kb & 3)] = 0;
+  };
+  if (tid == 0 && n_my > 0) {
+    ptx::prefetch_tensormap(&xmap);
+    for (int64_t i = 0; i < kStages && i < n_my; ++i) issue(i);
+  }
+
+  uint32_t tmax[kMaxQuantOutputs] = {0u, 0u};
+  for (int64_t i = 0; i < n_my; ++i) {
+    const int s = static_cast<int>(i % kStages);
+    const uint32_t parity = static_cast<uint32_t>((i / kStages) & 1);
+    const bool ok = ptx::mbar_wait(&full[s], parity, &abort_flag);
+    if (__syncthreads_or(!ok)) {
+      if (tid == 0) ptx::set_status(p.status, kDevTimeout);
+      break;
+    }
+    const uint8_t* stage = ring + s * kStageBytes;
+    const int64_t tile = tile_of(i);
+    const int64_t tr = tile / p.tiles_c, tc = tile - tr * p.tiles_c;
+    uint8_t* stg = ring + kStgOffset + static_cast<int>(i & 1) * (kMaxQuantOutputs * kStgBytes);
+#pragma unroll
+    for (int o = 0; o < kMaxQuantOutputs; ++o) {
+      if (o >= p.n_out) break;
+      const OutParams& op = p.out[o];
+      if (PASS == 0) {
+        if (o == 1 && p.amax_shared) break;
+        // without the transform the orientation does not change the amax
+        tmax[o] = max(tmax[o], (op.rht && op.col) ? amax_tile<true>(stage, true, rht_mask[o])
+                                                   : amax_tile<false>(stage, op.rht != 0, rht_mask[o]));
+      } else if (live[o]) {
+        uint8_t* so = stg + o * kStgBytes;
+        if (op.col) {
+          if (op.sr)
+            encode_tile<true, true>(stage, so, op, s_dec[o], rht_mask[o], tr, tc);
+          else
+            encode_tile<true, false>(stage, so, op, s_dec[o], rht_mask[o], tr, tc);
+        } else {
+          if (op.sr)
+            encode_tile<false, true>(stage, so, op, s_dec[o], rht_mask[o], tr, tc);
+          else
+            encode_tile<false, false>(stage, so, op, s_dec[o], rht_mask[o], tr, tc);
+        }
+      }
+    }
+    // Every thread is done with this stage and, in pass 1, with its staged
+    // results.  The staging buffers alternate between tiles, so the copy-out
+    // below overlaps the next tile's encode without another barrier.
+    __syncthreads();
+    if (tid == 0 && i + kStages < n_my) issue(i + kStages);
+    if (PASS == 1) {
+#pragma unroll
+      for (int o = 0; o < kMaxQuantOutputs; ++o) {
+        if (o >= p.n_out) break;
+        if (!live[o]) continue;
+        const OutParams& op = p.out[o];
+        copy_out(stg + o * kStgBytes, op, (op.col ? tc : tr) * kTile, (op.col ? tr : tc) * 8);
+      }
+    }
+  }
+
+  if (PASS == 0) {
+#pragma unroll
+    for (int o = 0; o < kMaxQuantOutputs; ++o) {
+      if (o >= p.n_out || (o == 1 && p.amax_shared)) break;
+      const uint32_t m = block_max(tmax[o], red);
+      if (tid == 0) p.out[o].partials[blockIdx.x] = m;
+    }
   }
 }
 
-template <bool COL, bool BLOCK2D, bool RHT, bool SR, int PASS>
-int grid_for(int64_t num_tiles) {
-  static int per_sm = -1;
-  if (per_sm < 0) {
+template <int PASS>
+int tiles_per_sm(cudaError_t* err) {
+  static int per_sm[64] = {0};
+  int dev = 0;
+  *err = cudaGetDevice(&dev);
+  if (*err != cudaSuccess) return 0;
+  int& cached = per_sm[(dev >= 0 && dev < 64) ? dev : 0];
+  if (cached == 0) {
+    *err = cudaFuncSetAttribute(quant_tiles<PASS>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    if (*err != cudaSuccess) return 0;
     int b = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, quant_kernel<COL, BLOCK2D, RHT, SR, PASS>, kThreads, 0) !=
-            cudaSuccess ||
-        b < 1)
-      b = 1;
-    per_sm = b;
+    *err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, quant_tiles<PASS>, kThreads, kSmemBytes);
+    if (*err != cudaSuccess) return 0;
+    cached = std::max(b, 1);
   }
-  int64_t g = static_cast<int64_t>(per_sm) * device_sm_count();
-  g = std::min<int64_t>(g, kMaxAmaxPartials);
-  g = std::min<int64_t>(g, std::max<int64_t>(num_tiles, 1));
-  return static_cast<int>(std::max<int64_t>(g, 1));
+  return cached;
 }
 
-template <bool COL, bool BLOCK2D, bool RHT, bool SR>
-cudaError_t run_passes(QParams p, cudaStream_t stream) {
-  const int g0 = grid_for<COL, false, RHT, false, 0>(p.num_tiles);
-  p.num_partials = g0;
-  quant_kernel<COL, false, RHT, false, 0><<<g0, kThreads, 0, stream>>>(p);
-  const int g1 = grid_for<COL, BLOCK2D, RHT, SR, 1>(p.num_tiles);
-  quant_kernel<COL, BLOCK2D, RHT, SR, 1><<<g1, kThreads, 0, stream>>>(p);
-  return cudaGetLastError();
-}
-
-template <bool COL, bool BLOCK2D, bool RHT>
-cudaError_t dispatch_sr(const QParams& p, int sr, cudaStream_t s) {
-  return sr ? run_passes<COL, BLOCK2D, RHT, true>(p, s) : run_passes<COL, BLOCK2D, RHT, false>(p, s);
-}
-template <bool COL, bool BLOCK2D>
-cudaError_t dispatch_rht(const QParams& p, int rht, int sr, cudaStream_t s) {
-  return rht ? dispatch_sr<COL, BLOCK2D, true>(p, sr, s) : dispatch_sr<COL, BLOCK2D, false>(p, sr, s);
-}
-template <bool COL>
-cudaError_t dispatch_block(const QParams& p, int b2d, int rht, int sr, cudaStream_t s) {
-  return b2d ? dispatch_rht<COL, true>(p, rht, sr, s) : dispatch_rht<COL, false>(p, rht, sr, s);
+// Tensor map over x [rows, cols] BF16: box 64 columns x 128 rows, 128-byte
+// swizzle, out-of-range elements read as zero.
+bool make_x_map(CUtensorMap* map, const uint16_t* x, int64_t rows, int64_t cols, int64_t ldx) {
+  auto encode = tensor_map_encoder();
+  if (!encode) return false;
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(ldx) * 2};
+  const cuuint32_t box[2] = {64, static_cast<cuuint32_t>(kTile)};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, const_cast<uint16_t*>(x), dims, strides, box,
+                            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
 }
 
 // Scratch for nvfp4_quantize_noalloc: the status word (first 256 bytes) and
@@ -429,48 +574,54 @@ cudaError_t launch_quantize_noalloc(QuantArgs a, cudaStream_t stream) {
 }
 
 cudaError_t launch_quantize(const QuantArgs& a, cudaStream_t stream) {
-  QParams p{};
-  p.x = a.x;
-  p.rows = a.rows;
-  p.cols = a.cols;
-  p.ldx = a.ldx;
-  p.qr = a.qr;
-  p.qk = a.qk;
-  p.kb_count = a.qk / 16;
-  p.codes = a.codes;
-  p.sf = a.sf;
-  p.tensor_scale = a.tensor_scale;
+  if (a.n_out < 1 || a.n_out > kMaxQuantOutputs) return cudaErrorInvalidValue;
+  TileParams p{};
+  const int64_t tiles_r = (a.rows + kTile - 1) / kTile;
+  p.tiles_c = (a.cols + kTile - 1) / kTile;
+  p.num_tiles = (a.rows > 0 && a.cols > 0) ? tiles_r * p.tiles_c : 0;
+  p.n_out = a.n_out;
   p.status = a.status;
-  p.partials = a.partials;
-  p.rht_seed = a.rht_seed;
-  p.sr_seed = a.sr_seed;
-  p.sr_offset = a.sr_offset;
-  p.sf_mma = a.sf_mma;
-  p.sf_katoms = (p.kb_count + 3) / 4;
-  int64_t tiles_r;
-  if (!a.transpose) {
-    tiles_r = (p.qr + 15) / 16;
-    p.tiles_c = (p.kb_count + 15) / 16;
-  } else {
-    tiles_r = (p.kb_count + 7) / 8;
-    p.tiles_c = (p.qr + 63) / 64;
+  for (int o = 0; o < a.n_out; ++o) {
+    const QuantOut& q = a.out[o];
+    OutParams& op = p.out[o];
+    op.codes = q.codes;
+    op.sf = q.sf;
+    op.tensor_scale = q.tensor_scale;
+    op.partials = a.partials + o * kPartialsPerOutput;
+    op.qr = q.transpose ? a.cols : a.rows;
+    op.qk = q.transpose ? a.rows : a.cols;
+    op.code_ld = op.qk / 2;
+    op.kb_count = op.qk / 16;
+    op.katoms = (op.kb_count + 3) / 4;
+    op.rht_seed = q.rht_seed;
+    op.sr_seed = q.sr_seed;
+    op.sr_offset = q.sr_offset;
+    op.col = q.transpose;
+    op.block2d = q.block2d;
+    op.sr = q.sr;
+    op.rht = q.rht;
+    op.sf_mma = q.sf_mma;
+    op.vec16 = (reinterpret_cast<uintptr_t>(q.codes) % 16 == 0) && (op.code_ld % 16 == 0);
   }
-  p.num_tiles = tiles_r * p.tiles_c;
-  cudaError_t err = a.transpose ? dispatch_block<true>(p, a.block2d, a.rht, a.sr, stream)
-                                : dispatch_block<false>(p, a.block2d, a.rht, a.sr, stream);
+  p.amax_shared = a.n_out == 2 && !a.out[0].rht && !a.out[1].rht;
+
+  CUtensorMap xmap{};
+  if (p.num_tiles > 0 && !make_x_map(&xmap, a.x, a.rows, a.cols, a.ldx)) return cudaErrorInvalidValue;
+  cudaError_t err = cudaSuccess;
+  const int b0 = tiles_per_sm<0>(&err);
   if (err != cudaSuccess) return err;
-  if (a.sf_mma) {
-    const int64_t pad_r = (p.qr + 127) / 128 * 128;
-    const int64_t pad_kb = p.sf_katoms * 4;
-    const int64_t total = (pad_r - p.qr) * pad_kb + p.qr * (pad_kb - p.kb_count);
-    if (total > 0) {
-      const int64_t blocks = std::min<int64_t>((total + 255) / 256, 4 * device_sm_count());
-      sf_pad_kernel<<<static_cast<int>(blocks), 256, 0, stream>>>(p.sf, p.qr, p.kb_count, pad_r, pad_kb,
-                                                                  p.sf_katoms);
-      err = cudaGetLastError();
-    }
-  }
-  return err;
+  const int b1 = tiles_per_sm<1>(&err);
+  if (err != cudaSuccess) return err;
+  // Both passes use one grid: pass 1 reduces one partial per CTA of pass 0.
+  int64_t g = static_cast<int64_t>(std::min(b0, b1)) * device_sm_count();
+  g = std::min<int64_t>(g, kPartialsPerOutput);
+  g = std::max<int64_t>(std::min<int64_t>(g, p.num_tiles), 1);
+  p.num_partials = static_cast<int>(g);
+  quant_tiles<0><<<static_cast<int>(g), kThreads, kSmemBytes, stream>>>(xmap, p);
+  err = cudaGetLastError();
+  if (err != cudaSuccess) return err;
+  quant_tiles<1><<<static_cast<int>(g), kThreads, kSmemBytes, stream>>>(xmap, p);
+  return cudaGetLastError();
 }
 
 }  // namespace nvfp4

@@ -121,7 +121,8 @@ size_t nvfp4_sf_bytes(int64_t qr, int64_t qk, int32_t sf_layout);
  * Outputs: codes [qr, qk/2] bytes; sf in cfg->sf_layout; tensor_scale[0] = s.
  * Two passes over x: the tensor amax (after the transform, if any), then the
  * per-block encode.  Shape rules: qk % 16 == 0; 16x16 blocks also need
- * qr % 16 == 0; ldx % 8 == 0 and x 16-byte aligned.
+ * qr % 16 == 0; ldx % 8 == 0 and x 16-byte aligned; codes 8-byte aligned;
+ * MMA-layout sf 16-byte aligned.
  * Non-finite input: the device status word is set to NVFP4_ERR_NONFINITE,
  * tensor_scale[0] is set to NaN and codes/sf are left unspecified.
  * Workspace: nvfp4_quantize_workspace_size bytes, device memory.
@@ -132,6 +133,27 @@ nvfp4_status nvfp4_quantize_workspace_size(int64_t rows, int64_t cols, const nvf
 nvfp4_status nvfp4_quantize(const void* x, int64_t rows, int64_t cols, int64_t ldx,
                             const nvfp4_quant_cfg* cfg, void* codes, void* sf, float* tensor_scale,
                             void* workspace, size_t workspace_bytes, nvfp4_stream_t stream);
+
+/*
+ * nvfp4_quantize_dual: two quantised outputs from one read of x, each with
+ * its own configuration (orientation, block shape, rounding, transform,
+ * seeds, scale layout) and its own tensor scale.  A training step needs X and
+ * dY both along rows (fprop, dgrad) and along columns (wgrad), and W both ways
+ * (fprop, dgrad); this call reads the BF16 tensor twice (amax pass, encode
+ * pass) instead of four times.  Output A is bit-identical to nvfp4_quantize
+ * with cfg_a, output B to nvfp4_quantize with cfg_b.
+ * Arguments and rules as nvfp4_quantize for each output; the two outputs
+ * must not overlap.  Workspace: nvfp4_quantize_workspace_size bytes (the same
+ * size serves both outputs).  Source: the encode steps at the top of this
+ * header; quantising every GEMM operand along its own K is the pages' NVFP4
+ * training recipe ("NVIDIA acelera o pre-treinamento de LLM: NVFP4 no
+ * Blackwell...", section "Como o treinamento mixed-precision funciona com
+ * NVFP4").
+ */
+nvfp4_status nvfp4_quantize_dual(const void* x, int64_t rows, int64_t cols, int64_t ldx,
+                                 const nvfp4_quant_cfg* cfg_a, void* codes_a, void* sf_a, float* tensor_scale_a,
+                                 const nvfp4_quant_cfg* cfg_b, void* codes_b, void* sf_b, float* tensor_scale_b,
+                                 void* workspace, size_t workspace_bytes, nvfp4_stream_t stream);
 
 /*
  * nvfp4_quantize_noalloc: nvfp4_quantize for callers that cannot allocate
