@@ -2,9 +2,9 @@
 
 One step = one pass of the whole hot path over the 12B-hybrid-shaped MLP
 up-projection (tokens 8192 = 4 x 2048, hidden 5120, FFN 20480): quantise
-X, W, dY in the orientation each GEMM needs (1x16 activations/gradients,
-16x16 weights, transform + stochastic rounding on the wgrad operands), then
-the three block-scaled FP4 GEMMs with BF16 outputs.  Inputs are synthetic
+each of X, W, dY once into both orientations the GEMMs need (1x16
+activations/gradients, 16x16 weights, transform + stochastic rounding on the
+wgrad operands), then the three block-scaled FP4 GEMMs with BF16 outputs.  Inputs are synthetic
 BF16 tensors resident in HBM (629 MB per step, larger than L2).
 
 Prints one JSON line.  `--impl reference` times the CPU oracle (the plain C
@@ -29,8 +29,26 @@ STEP_FLOP = 3 * GEMM_FLOP
 FP4_OVER_BF16 = 13.5 / 2.25  # nominal dense FP4 : BF16 tensor ratio on GB300
 QUANT_OUT_BYTES_PER_ELT = 0.5 + 1.0 / 16  # codes + block scales of one quantised output
 QUANT_BYTES_PER_ELT = 2.0 + QUANT_OUT_BYTES_PER_ELT  # read BF16, write one output
+# one dual quantise per tensor and step: read BF16 once, write two quantised outputs
+QUANT_STEP_BYTES = (T * HID + FFN * HID + T * FFN) * (2.0 + 2 * QUANT_OUT_BYTES_PER_ELT)
 WORKLOAD = ("12B-hybrid MLP up-projection fprop+dgrad+wgrad, tokens 8192 (4x2048), hidden 5120, FFN 20480; "
             "X N(0,1), W N(0,0.02), dY N(0,1e-3); W 16x16, X/dY 1x16, wgrad operands RHT+SR")
+
+
+# DRAM bytes per GEMM launch (dram__bytes_read.sum + dram__bytes_write.sum from
+# one ncu capture of each of the step's three GEMM shapes, averaged like the
+# achieved rate), keyed by the SHA-256 prefix of the GEMM kernel's sources: a
+# changed kernel reports null until it is measured again.
+GEMM_TRAFFIC = {"58a7385b026e57d6": 420285099}
+
+
+def _gemm_traffic():
+    import hashlib
+    h = hashlib.sha256()
+    for f in ("gemm.cu", "ptx.cuh"):
+        with open(os.path.join(ROOT, "block_scaled_gemm_nvfp4_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return GEMM_TRAFFIC.get(h.hexdigest()[:16])
 
 
 def _config():
@@ -133,52 +151,13 @@ def run_ours(args):
     x_c, w_c, dy_c = syn.config2()
     x, w, dy = x_c.to(dev), w_c.to(dev), dy_c.to(dev)
 
-    s = nv.NVFP4_DEFAULT_RHT_SEED
-    roles = {
-        # (source, cfg) for the A and B operands of each GEMM
-        "fprop": ((x, nv.quant_cfg(block=0)), (w, nv.quant_cfg(block=1))),
-        "dgrad": ((dy, nv.quant_cfg(block=0)), (w, nv.quant_cfg(block=1, transpose=1))),
-        "wgrad": ((dy, nv.quant_cfg(rounding=1, rht=1, transpose=1, rht_seed=s, sr_seed=5)),
-                  (x, nv.quant_cfg(rounding=1, rht=1, transpose=1, rht_seed=s, sr_seed=6))),
-    }
-    outs = {"fprop": torch.empty((T, FFN), dtype=torch.bfloat16, device=dev),
-            "dgrad": torch.empty((T, HID), dtype=torch.bfloat16, device=dev),
-            "wgrad": torch.empty((FFN, HID), dtype=torch.bfloat16, device=dev)}
-    # preallocated quantised operands and workspaces (the library never allocates)
-    qbufs, wss = {}, {}
-    for op, pair in roles.items():
-        qbufs[op] = []
-        for src, cfg in pair:
-            r, c = src.shape
-            qr, qk = (c, r) if cfg.transpose else (r, c)
-            qbufs[op].append(nv.NVFP4Tensor(
-                codes=torch.empty((qr, qk // 2), dtype=torch.uint8, device=dev),
-                sf=torch.empty(nv.nvfp4_sf_bytes(qr, qk, nv.NVFP4_SF_MMA), dtype=torch.uint8, device=dev),
-                tensor_scale=torch.empty(1, dtype=torch.float32, device=dev), rows=qr, k=qk,
-                sf_layout=nv.NVFP4_SF_MMA))
-        wss[op] = torch.zeros(nv.nvfp4_quantize_workspace_size(T, FFN, roles[op][0][1]) + (1 << 16),
-                              dtype=torch.uint8, device=dev)
-
+    plan = _step_plan(nv, torch, x, w, dy, dev)
     stream = torch.cuda.current_stream()
     gemm_events = []
     quant_events = []
 
     def step(record):
-        for op, pair in roles.items():
-            if record:
-                q0 = torch.cuda.Event(enable_timing=True)
-                q0.record(stream)
-            for (src, cfg), qb in zip(pair, qbufs[op]):
-                nv.nvfp4_quantize(src, cfg, out=qb, workspace=wss[op])
-            if record:
-                g0 = torch.cuda.Event(enable_timing=True)
-                g1 = torch.cuda.Event(enable_timing=True)
-                g0.record(stream)
-            nv.nvfp4_gemm(qbufs[op][0], qbufs[op][1], out_dtype=nv.NVFP4_OUT_BF16, d=outs[op], workspace=wss[op])
-            if record:
-                g1.record(stream)
-                quant_events.append((q0, g0))
-                gemm_events.append((g0, g1))
+        _run_step(nv, plan, stream, quant_events if record else None, gemm_events if record else None)
 
     for _ in range(args.warmup):
         step(False)
@@ -199,10 +178,9 @@ def run_ours(args):
         if pg:
             pg.barrier()
     ms_total = t0.elapsed_time(t1)
-    for op in roles:
-        st = nv.nvfp4_check_device_status(wss[op])
-        if st != nv.NVFP4_OK:
-            raise RuntimeError("device status %s after %s" % (nv.nvfp4_status_string(st), op))
+    st = nv.nvfp4_check_device_status(plan["ws"])
+    if st != nv.NVFP4_OK:
+        raise RuntimeError("device status %s" % nv.nvfp4_status_string(st))
     if pg:
         t = torch.tensor([ms_total], device=dev)
         pg.all_reduce(t, op=pg.ReduceOp.MAX)
@@ -210,19 +188,16 @@ def run_ours(args):
     ms_step = ms_total / args.steps
     value = world * STEP_FLOP / (ms_step * 1e-3) / 1e12
 
-    gemm_ms = statistics.mean(a.elapsed_time(b) for a, b in gemm_events)
-    quant_ms = statistics.mean(a.elapsed_time(b) for a, b in quant_events)  # two quantises per GEMM
+    gemm_ms = statistics.mean(a.elapsed_time(b) for a, b in gemm_events)  # per GEMM
+    quant_ms = sum(a.elapsed_time(b) for a, b in quant_events) / args.steps  # three dual quantises per step
     peaks, src = _peaks()
     peak_fp4 = peaks["bf16_tflops"] * FP4_OVER_BF16
     achieved = GEMM_FLOP / (gemm_ms * 1e-3) / 1e12
-    # quantised elements per GEMM pass: fprop X + W, dgrad dY + W, wgrad dY + X (same total each pass on average)
-    q_elts = {"fprop": T * HID + FFN * HID, "dgrad": T * FFN + FFN * HID, "wgrad": T * FFN + T * HID}
-    q_bytes = statistics.mean(q_elts.values()) * QUANT_BYTES_PER_ELT
-    quant_gbs = q_bytes / (quant_ms * 1e-3) / 1e9
+    quant_gbs = QUANT_STEP_BYTES / (quant_ms * 1e-3) / 1e9
     clock = clocks.summary()
 
-    # launches per step: each quantise = amax + encode kernels, each GEMM = 1
-    launches_per_step = 3 * (2 * 2 + 1)
+    # launches per step: three dual quantises (amax + encode kernels) and three GEMMs
+    launches_per_step = 3 * 2 + 3
 
     e2e = run_e2e(args, nv, torch, x_c, w_c, dy_c, dev, world, pg)
 
@@ -233,13 +208,14 @@ def run_ours(args):
         "data": "synthetic", "config": _config(),
         "roofline": {"bound": "tensor", "kernel": "nvfp4_gemm (tcgen05 mxf4nvf4)", "achieved": round(achieved, 1),
                      "peak": round(peak_fp4, 1), "unit": "TFLOP/s", "frac": round(achieved / peak_fp4, 4),
-                     "traffic": None,
+                     "traffic": _gemm_traffic(),
                      "peak_source": "%s bf16 %.1f TFLOP/s x nominal FP4/BF16 ratio %.1f" % (
                          src, peaks["bf16_tflops"], FP4_OVER_BF16),
                      "gemm_ms": round(gemm_ms, 4)},
         "quantize": {"bound": "hbm", "achieved": round(quant_gbs, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                     "frac": round(quant_gbs / peaks["hbm_gbs"], 4), "ms_per_gemm_pass": round(quant_ms, 4),
-                     "bytes_model": "2.5625 B/element (read BF16, write codes + scales)"},
+                     "frac": round(quant_gbs / peaks["hbm_gbs"], 4), "ms_per_step": round(quant_ms, 4),
+                     "bytes_model": "per tensor (X, W, dY): read BF16 once + two outputs of codes and scales "
+                                    "= 2 + 2 x 0.5625 B/element"},
         "clocks": clock,
         "gpu_launches": launches_per_step * args.steps,
         "e2e": e2e,
@@ -252,38 +228,86 @@ def run_ours(args):
         pg.destroy_process_group()
 
 
+def _step_plan(nv, torch, x, w, dy, dev):
+    """Preallocated quantised operands, outputs and one workspace for the
+    training step of the linear layer (the library never allocates)."""
+    s = nv.NVFP4_DEFAULT_RHT_SEED
+    cfg = {
+        "x": nv.quant_cfg(block=0),  # fprop A: X [T, hidden] along hidden
+        "xt": nv.quant_cfg(rounding=1, rht=1, transpose=1, rht_seed=s, sr_seed=6),  # wgrad B: X^T along T
+        "w": nv.quant_cfg(block=1),  # fprop B: W [ffn, hidden] along hidden
+        "wt": nv.quant_cfg(block=1, transpose=1),  # dgrad B: W^T along ffn
+        "dy": nv.quant_cfg(block=0),  # dgrad A: dY [T, ffn] along ffn
+        "dyt": nv.quant_cfg(rounding=1, rht=1, transpose=1, rht_seed=s, sr_seed=5),  # wgrad A: dY^T along T
+    }
+    src = {"x": x, "xt": x, "w": w, "wt": w, "dy": dy, "dyt": dy}
+    q = {k: nv.nvfp4_empty(src[k], cfg[k]) for k in cfg}
+    out = {"y": torch.empty((T, FFN), dtype=torch.bfloat16, device=dev),
+           "dx": torch.empty((T, HID), dtype=torch.bfloat16, device=dev),
+           "dw": torch.empty((FFN, HID), dtype=torch.bfloat16, device=dev)}
+    ws = torch.zeros(nv.nvfp4_quantize_workspace_size(T, FFN, cfg["x"]) + (1 << 16), dtype=torch.uint8,
+                     device=dev)
+    return {"cfg": cfg, "q": q, "out": out, "ws": ws, "src": {"x": x, "w": w, "dy": dy}}
+
+
+def _run_step(nv, plan, stream, quant_events=None, gemm_events=None):
+    """fprop, dgrad, wgrad of Y = X W^T: each BF16 tensor is quantised once
+    into both orientations the GEMMs need, then the three GEMMs run."""
+    import torch
+
+    c, q, o, ws, src = plan["cfg"], plan["q"], plan["out"], plan["ws"], plan["src"]
+    rec = quant_events is not None
+
+    def ev():
+        if not rec:
+            return None
+        e = torch.cuda.Event(enable_timing=True)
+        e.record(stream)
+        return e
+
+    e0 = ev()
+    nv.nvfp4_quantize_dual(src["x"], c["x"], c["xt"], q["x"], q["xt"], workspace=ws)
+    nv.nvfp4_quantize_dual(src["w"], c["w"], c["wt"], q["w"], q["wt"], workspace=ws)
+    e1 = ev()
+    nv.nvfp4_gemm(q["x"], q["w"], nv.NVFP4_OUT_BF16, d=o["y"], workspace=ws)
+    e2 = ev()
+    nv.nvfp4_quantize_dual(src["dy"], c["dy"], c["dyt"], q["dy"], q["dyt"], workspace=ws)
+    e3 = ev()
+    nv.nvfp4_gemm(q["dy"], q["wt"], nv.NVFP4_OUT_BF16, d=o["dx"], workspace=ws)
+    e4 = ev()
+    nv.nvfp4_gemm(q["dyt"], q["xt"], nv.NVFP4_OUT_BF16, d=o["dw"], workspace=ws)
+    e5 = ev()
+    if rec:
+        quant_events += [(e0, e1), (e2, e3)]
+        gemm_events += [(e1, e2), (e3, e4), (e4, e5)]
+
+
 def run_e2e(args, nv, torch, x_c, w_c, dy_c, dev, world, pg):
-    """The same step through the linear wrappers with pinned host buffers:
-    host->device copies of X, W, dY and device->host copies of Y, dX, dW are
-    inside the timed region."""
+    """The same step through the public API with pinned host buffers: the
+    host->device copies of X, W, dY and the device->host copies of Y, dX, dW
+    are inside the timed region."""
     xh, wh, dyh = x_c.pin_memory(), w_c.pin_memory(), dy_c.pin_memory()
     yh = torch.empty((T, FFN), dtype=torch.bfloat16).pin_memory()
     dxh = torch.empty((T, HID), dtype=torch.bfloat16).pin_memory()
     dwh = torch.empty((FFN, HID), dtype=torch.bfloat16).pin_memory()
     xd, wd, dyd = torch.empty_like(x_c, device=dev), torch.empty_like(w_c, device=dev), torch.empty_like(dy_c, device=dev)
-    yd = torch.empty((T, FFN), dtype=torch.bfloat16, device=dev)
-    dxd = torch.empty((T, HID), dtype=torch.bfloat16, device=dev)
-    dwd = torch.empty((FFN, HID), dtype=torch.bfloat16, device=dev)
-    ws = {op: torch.zeros(nv.nvfp4_linear_workspace_size(i, T, HID, FFN), dtype=torch.uint8, device=dev)
-          for i, op in enumerate(("fprop", "dgrad", "wgrad"))}
+    plan = _step_plan(nv, torch, xd, wd, dyd, dev)
+    stream = torch.cuda.current_stream()
 
     def step():
         xd.copy_(xh, non_blocking=True)
         wd.copy_(wh, non_blocking=True)
         dyd.copy_(dyh, non_blocking=True)
-        nv.nvfp4_linear_fprop(xd, wd, y=yd, workspace=ws["fprop"])
-        nv.nvfp4_linear_dgrad(dyd, wd, dx=dxd, workspace=ws["dgrad"])
-        nv.nvfp4_linear_wgrad(dyd, xd, dw=dwd, workspace=ws["wgrad"])
-        yh.copy_(yd, non_blocking=True)
-        dxh.copy_(dxd, non_blocking=True)
-        dwh.copy_(dwd, non_blocking=True)
+        _run_step(nv, plan, stream)
+        yh.copy_(plan["out"]["y"], non_blocking=True)
+        dxh.copy_(plan["out"]["dx"], non_blocking=True)
+        dwh.copy_(plan["out"]["dw"], non_blocking=True)
 
     for _ in range(max(1, args.warmup)):
         step()
     torch.cuda.synchronize()
     if pg:
         pg.barrier()
-    stream = torch.cuda.current_stream()
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
     n = max(1, min(args.steps, 5))
@@ -298,11 +322,14 @@ def run_e2e(args, nv, torch, x_c, w_c, dy_c, dev, world, pg):
         pg.all_reduce(t, op=pg.ReduceOp.MAX)
         ms = t.item()
     ms /= n
+    st = nv.nvfp4_check_device_status(plan["ws"])
+    if st != nv.NVFP4_OK:
+        raise RuntimeError("device status %s (end-to-end run)" % nv.nvfp4_status_string(st))
     h2d = (T * HID + FFN * HID + T * FFN) * 2
     d2h = (T * FFN + T * HID + FFN * HID) * 2
     return {"value": round(world * STEP_FLOP / (ms * 1e-3) / 1e12, 3), "unit": "TFLOP/s",
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(ms, 4),
-            "api": "nvfp4_linear_{fprop,dgrad,wgrad} with pinned host buffers"}
+            "api": "nvfp4_quantize_dual + nvfp4_gemm with pinned host buffers"}
 
 
 # ------------------------------------------------------------- CPU oracle
