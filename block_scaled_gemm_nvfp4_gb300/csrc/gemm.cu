@@ -9,25 +9,31 @@
 // Persistent, warp-specialised kernel, one CTA per SM, two modes:
 //   pair mode (M > 128): a cluster of two CTAs computes a 256 x 256 tile with
 //     cta_group::2 MMAs.  Each CTA holds 128 rows of A and 128 rows of B per
-//     ring stage (38 KB, five stages); the leader CTA issues the MMAs, which
+//     code stage (32 KB, five stages); the leader CTA issues the MMAs, which
 //     read both CTAs' shared memory and write each CTA's 128 x 256 FP32
-//     accumulator in its own TMEM.  Per SM this halves the B bytes written
-//     by TMA and read by the tensor core, which matters because the kernel is
-//     bound by shared-memory bandwidth (TMA writes + MMA operand reads);
+//     accumulator in its own TMEM;
 //   single mode (M <= 128): one CTA per 128 x 256 tile, cta_group::1, four
-//     54 KB stages.
-// Warp roles (14 warps):
-//   warp 0     TMA producer: packed E2M1 codes by tiled TMA (128-byte swizzle),
-//              block scales by bulk copies on their own barrier;
+//     48 KB code stages.
+// Codes and block scales travel in separate rings.  The scale ring (eight or
+// four 6 KB stages) runs ahead of the code ring, and the scales move into
+// TMEM slots (five k-blocks) that are freed by their own MMA commit, so the
+// scale copy, the staging into TMEM and the pair's cross-CTA arrivals are
+// hidden behind earlier k-blocks instead of lengthening each stage's round
+// trip (measured on GB300: with scales in the code stage the k-block period
+// was about 1.8x that of the same pipeline without scales).
+// Warp roles (15 warps):
+//   warp 0     TMA producer for the packed E2M1 codes (tiled TMA, 128-byte
+//              swizzle);
 //   warp 1     TMEM allocation; in the leader (or single) CTA the MMA issuer;
 //   warps 2-9  epilogue, two warps per TMEM lane quarter, each owning 128 of
 //              the 256 columns: TMEM -> registers (tcgen05.ld), times sA * sB,
 //              BF16 (RNE) or FP32, stored to global memory.  In BF16 mode the
 //              accumulator is released before the stores are issued;
-//   warps 10-13 stage each ring stage's block scales from shared memory into
-//              TMEM with tcgen05.st (one warp per lane quarter).  This keeps
+//   warps 10-13 stage each k-block's block scales from the scale ring into a
+//              TMEM slot with tcgen05.st (one warp per lane quarter), keeping
 //              the scale traffic off the tensor pipe, where a tcgen05.cp per
-//              64-wide K step and 128 rows serialises with the MMAs.
+//              64-wide K step and 128 rows serialises with the MMAs;
+//   warp 14    bulk-copy producer for the block scales.
 // Every mbarrier wait is bounded; on a timeout the CTA records
 // NVFP4_ERR_TIMEOUT in the status word, drains its in-flight copies and MMAs,
 // frees TMEM and exits.
@@ -69,33 +75,45 @@ constexpr int kABytes = BM * kRowBytes;       // 16 KB
 constexpr int kSfAtomBytes = 512;             // 128 rows x 4 scales
 constexpr int kSfaBytes = 4 * kSfAtomBytes;   // one row atom x 4 K atoms
 constexpr int kSfbBytes = 8 * kSfAtomBytes;   // two row atoms x 4 K atoms
-constexpr int kThreads = 448;                 // 14 warps
+constexpr int kThreads = 480;                 // 15 warps
 constexpr int kEpiWarps = 8;
 constexpr int kSfWarps = 4;
 constexpr int kFirstSfWarp = 10;
+constexpr int kSfProducerWarp = 14;
 constexpr int kEpiCols = BN / 2;              // columns per epilogue warp
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kAccCol = 0;
-constexpr uint32_t kSfaCol = 256;             // + stage * 16 + kk * 4
+constexpr uint32_t kSfaCol = 256;             // + slot * 16 + kk * 4
+constexpr int kTmemSlots = 5;                 // TMEM scale slots (one k-block each)
+constexpr uint32_t kSfbCol = kSfaCol + 16 * kTmemSlots;  // + slot * 32 + kk * 8 + row_atom * 4
+constexpr int kSfStageBytes = kSfaBytes + kSfbBytes;     // 6 KB of block scales per k-block
 constexpr int kGroup = 16;                    // tile raster group (row or column blocks)
+static_assert(kSfbCol + 32 * kTmemSlots <= kTmemCols, "TMEM budget");
 
-// Per-mode layout.  PAIR: B rows per CTA 128, five stages; single: 256, four.
+// Per-mode layout.  Codes and block scales travel in separate rings: a code
+// stage holds one k-block of A and B codes; the scale ring is deeper, so the
+// small scale copies are issued several k-blocks ahead and their latency
+// (copy, staging into TMEM, the pair's arrivals) stays off the MMA's path.
+//   PAIR: B rows per CTA 128, five 32 KB code stages, eight scale stages;
+//   single: B rows 256, four 48 KB code stages, four scale stages.
 template <bool PAIR>
 struct Layout {
   static constexpr int kBRows = PAIR ? BN / 2 : BN;
   static constexpr int kBBytes = kBRows * kRowBytes;
   static constexpr int kStages = PAIR ? 5 : 4;
-  static constexpr int kStageBytes = kABytes + kBBytes + kSfaBytes + kSfbBytes;
-  static constexpr int kSmemBytes = kStages * kStageBytes + 1024 /*barriers*/ + 1024 /*alignment*/;
-  static constexpr uint32_t kSfbCol = kSfaCol + 16 * kStages;  // + stage * 32 + kk * 8 + row_atom * 4
+  static constexpr int kSfStages = PAIR ? 8 : 4;
+  static constexpr int kStageBytes = kABytes + kBBytes;
+  static constexpr int kSfRing = kStages * kStageBytes;  // offset of the scale ring
+  static constexpr int kSmemBytes =
+      kSfRing + kSfStages * kSfStageBytes + 1024 /*barriers*/ + 1024 /*alignment*/;
   // Instruction descriptor for kind::mxf4nvf4: dense, A and B E2M1 (format 1),
   // both K-major, N >> 3 at bit 17, UE4M3 scales (bit 23 = 0), M >> 4 at bit
   // 24 (M = 256 across the pair in PAIR mode), scale-factor ids 0.
   static constexpr uint32_t kIdesc =
       (1u << 7) | (1u << 10) | ((uint32_t)(BN >> 3) << 17) | ((uint32_t)((PAIR ? 2 * BM : BM) >> 4) << 24);
   static_assert(kStageBytes % 1024 == 0, "stages must keep 1024-byte alignment for 128B swizzle");
+  static_assert(kSfStageBytes % 16 == 0, "bulk copies need 16-byte alignment");
   static_assert(kSmemBytes <= 232448, "shared memory budget");
-  static_assert(kSfbCol + 32 * kStages <= kTmemCols, "TMEM budget");
 };
 
 struct GParams {
@@ -117,14 +135,16 @@ struct GParams {
   uint32_t* status;
 };
 
-template <int STAGES>
+template <int STAGES, int SF_STAGES>
 struct __align__(8) SmemCtl {
-  uint64_t full[STAGES];      // codes landed (pair mode: both CTAs' codes, leader's copy)
-  uint64_t sf_full[STAGES];   // this CTA's block scales landed
-  uint64_t empty[STAGES];     // stage consumed by the MMAs
-  uint64_t sfready[STAGES];   // scales in TMEM (pair mode: both CTAs', leader's copy)
+  uint64_t full[STAGES];          // codes landed (pair mode: both CTAs' codes, leader's copy)
+  uint64_t empty[STAGES];         // code stage consumed by the MMAs
+  uint64_t sf_full[SF_STAGES];    // this CTA's block scales landed in the scale ring
+  uint64_t sf_empty[SF_STAGES];   // scale ring stage copied into TMEM
+  uint64_t sfready[kTmemSlots];   // scales in TMEM (pair mode: both CTAs', leader's copy)
+  uint64_t tfree[kTmemSlots];     // TMEM scale slot no longer read by MMAs
   uint64_t acc_full;
-  uint64_t acc_empty;         // accumulator drained (pair mode: both CTAs', leader's copy)
+  uint64_t acc_empty;             // accumulator drained (pair mode: both CTAs', leader's copy)
   uint64_t drain;
   uint32_t tmem_base;
   int abort;
@@ -271,20 +291,17 @@ __device__ __forceinline__ void epilogue_half(const GParams& p, uint64_t* acc_em
   }
 }
 
-// Scale staging for one ring stage.  Layout the block-scaled MMA reads
+// Scale staging for one k-block.  Layout the block-scaled MMA reads
 // (scale_vec::4X): for a 128-row operand block and one K = 64 step, TMEM lane
 // 32 q + l, column base + j holds the four scales of row l + 32 j; every lane
 // quarter q holds the whole block, because the quarter that computes output
 // rows 32 q .. 32 q + 31 reads the B scales of all N rows from its own lanes
 // (and the A scales of its own rows from column base + q).  That is one
 // 16-byte row of a 512-byte scale atom per lane, so each staging warp (lane
-// quarter q) copies atom row `lane` into its own lanes.  Columns: A at
-// kSfaCol + 16 s + 4 kk, B row block rb at kSfbCol + 32 s + 8 kk + 4 rb (a
-// 256-row B operand is read as columns base .. base + 7).
-template <bool PAIR>
-__device__ __forceinline__ void stage_scales(const uint8_t* st, uint32_t tmem, int s, int q, int lane) {
-  using L = Layout<PAIR>;
-  const uint8_t* sfa = st + kABytes + L::kBBytes;
+// quarter q) copies atom row `lane` into its own lanes.  Columns of TMEM
+// slot t: A at kSfaCol + 16 t + 4 kk, B row block rb at kSfbCol + 32 t + 8 kk
+// + 4 rb (a 256-row B operand is read as columns base .. base + 7).
+__device__ __forceinline__ void stage_scales(const uint8_t* sfa, uint32_t tmem, int slot, int q, int lane) {
   const uint8_t* sfb = sfa + kSfaBytes;
   const uint32_t lane_base = tmem + (static_cast<uint32_t>(q * 32) << 16);
   uint32_t va[16];
@@ -296,7 +313,7 @@ __device__ __forceinline__ void stage_scales(const uint8_t* st, uint32_t tmem, i
     va[4 * kk + 2] = v.z;
     va[4 * kk + 3] = v.w;
   }
-  ptx::tmem_st_32x32b_x16(lane_base + kSfaCol + s * 16, va);
+  ptx::tmem_st_32x32b_x16(lane_base + kSfaCol + slot * 16, va);
 #pragma unroll
   for (int h = 0; h < 2; ++h) {
     uint32_t vb[16];
@@ -312,7 +329,7 @@ __device__ __forceinline__ void stage_scales(const uint8_t* st, uint32_t tmem, i
         vb[8 * k2 + 4 * rb + 3] = v.w;
       }
     }
-    ptx::tmem_st_32x32b_x16(lane_base + L::kSfbCol + s * 32 + h * 16, vb);
+    ptx::tmem_st_32x32b_x16(lane_base + kSfbCol + slot * 32 + h * 16, vb);
   }
 }
 
@@ -322,9 +339,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const GParams p) {
   using L = Layout<PAIR>;
   constexpr int S = L::kStages;
+  constexpr int SS = L::kSfStages;
+  constexpr int T = kTmemSlots;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  SmemCtl<S>* ctl = reinterpret_cast<SmemCtl<S>*>(smem + S * L::kStageBytes);
+  uint8_t* sf_ring = smem + L::kSfRing;
+  SmemCtl<S, SS>* ctl = reinterpret_cast<SmemCtl<S, SS>*>(sf_ring + SS * kSfStageBytes);
   volatile int* abort_flag = &ctl->abort;
 
   const int warp = threadIdx.x >> 5;
@@ -337,9 +357,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
       ptx::mbar_init(&ctl->full[s], 1);
-      ptx::mbar_init(&ctl->sf_full[s], 1);
       ptx::mbar_init(&ctl->empty[s], 1);
-      ptx::mbar_init(&ctl->sfready[s], PAIR ? 2 * kSfWarps : kSfWarps);
+    }
+    for (int s = 0; s < SS; ++s) {
+      ptx::mbar_init(&ctl->sf_full[s], 1);
+      ptx::mbar_init(&ctl->sf_empty[s], kSfWarps);
+    }
+    for (int t = 0; t < T; ++t) {
+      ptx::mbar_init(&ctl->sfready[t], PAIR ? 2 * kSfWarps : kSfWarps);
+      ptx::mbar_init(&ctl->tfree[t], 1);
     }
     ptx::mbar_init(&ctl->acc_full, 1);
     ptx::mbar_init(&ctl->acc_empty, PAIR ? 2 * kEpiWarps : kEpiWarps);
@@ -369,7 +395,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = ctl->tmem_base;
 
   if (warp == 0) {
-    // ------------------------------------------------------------ producer
+    // ------------------------------------------------------ code producer
     if (lane == 0) {
       uint32_t issued_mask = 0, issued_parity = 0;
       const uint64_t l2_keep = ptx::policy_evict_last();
@@ -380,16 +406,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int unit = unit0; unit < p.num_units && ok; unit += ustep) {
         int m_blk, n_blk;
         unit_coords<PAIR>(p, unit, rank, m_blk, n_blk);
-        const int64_t n_rows_left = p.N - static_cast<int64_t>(n_blk) * BN;
-        const int nb_atoms = static_cast<int>(min(static_cast<int64_t>(2), (n_rows_left + 127) / 128));
         for (int kb = 0; kb < p.num_kb; ++kb) {
           if (!ptx::mbar_wait(&ctl->empty[stage], phase ^ 1u, abort_flag)) {
             fail(&ctl->abort, p, 1);
             ok = false;
             break;
           }
-          const int kk = kk_count_for(p, kb);
-          const uint32_t sf_bytes = static_cast<uint32_t>(kk * kSfAtomBytes);
           uint8_t* st = smem + stage * L::kStageBytes;
           if (p.skip_first_load && blockIdx.x == 0 && unit == unit0 && kb == 0) {
             // Failure-detection test hook: this stage is never filled, so the
@@ -399,20 +421,6 @@ __global__ void __launch_bounds__(kThreads, 1)
               phase ^= 1u;
             }
             continue;
-          }
-          // Scales first, on their own barrier: the staging warps can move
-          // them into TMEM while the larger code tiles are still in flight.
-          // (A row block past the end -- the odd last half of a pair -- has
-          // no scales to load; its rows are never stored.)
-          const bool a_valid = m_blk < p.tiles_m;
-          ptx::mbar_arrive_expect_tx(&ctl->sf_full[stage], sf_bytes * ((a_valid ? 1 : 0) + nb_atoms));
-          const uint8_t* sfa = p.a_sf + (static_cast<int64_t>(m_blk) * p.sf_katoms + kb * 4) * kSfAtomBytes;
-          if (a_valid) ptx::bulk_load(st + kABytes + L::kBBytes, sfa, sf_bytes, &ctl->sf_full[stage]);
-          for (int rb = 0; rb < nb_atoms; ++rb) {
-            const uint8_t* sfb =
-                p.b_sf + (static_cast<int64_t>(n_blk * 2 + rb) * p.sf_katoms + kb * 4) * kSfAtomBytes;
-            ptx::bulk_load(st + kABytes + L::kBBytes + kSfaBytes + rb * 4 * kSfAtomBytes, sfb, sf_bytes,
-                           &ctl->sf_full[stage]);
           }
           if (PAIR) {
             // both CTAs' code tiles complete on the leader's barrier
@@ -443,18 +451,67 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (issued_mask & (1u << s)) {
           volatile int never = 0;
           const uint32_t par = (issued_parity >> s) & 1u;
-          if (!ptx::mbar_wait(&ctl->sf_full[s], par, &never)) fail(&ctl->abort, p, 2);
           if ((!PAIR || leader) && !ptx::mbar_wait(&ctl->full[s], par, &never)) fail(&ctl->abort, p, 2);
           if (PAIR && ok && !ptx::mbar_wait(&ctl->empty[s], par, abort_flag)) fail(&ctl->abort, p, 2);
+        }
+      }
+    }
+  } else if (warp == kSfProducerWarp) {
+    // ----------------------------------------------------- scale producer
+    if (lane == 0) {
+      uint32_t issued_mask = 0, issued_parity = 0;
+      int stage = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      for (int unit = unit0; unit < p.num_units && ok; unit += ustep) {
+        int m_blk, n_blk;
+        unit_coords<PAIR>(p, unit, rank, m_blk, n_blk);
+        const int64_t n_rows_left = p.N - static_cast<int64_t>(n_blk) * BN;
+        const int nb_atoms = static_cast<int>(min(static_cast<int64_t>(2), (n_rows_left + 127) / 128));
+        // (a row block past the end -- the odd last half of a pair -- has no
+        // scales to load; its rows are never stored)
+        const bool a_valid = m_blk < p.tiles_m;
+        for (int kb = 0; kb < p.num_kb; ++kb) {
+          if (!ptx::mbar_wait(&ctl->sf_empty[stage], phase ^ 1u, abort_flag)) {
+            fail(&ctl->abort, p, 9);
+            ok = false;
+            break;
+          }
+          const uint32_t sf_bytes = static_cast<uint32_t>(kk_count_for(p, kb) * kSfAtomBytes);
+          uint8_t* st = sf_ring + stage * kSfStageBytes;
+          ptx::mbar_arrive_expect_tx(&ctl->sf_full[stage], sf_bytes * ((a_valid ? 1 : 0) + nb_atoms));
+          if (a_valid)
+            ptx::bulk_load(st, p.a_sf + (static_cast<int64_t>(m_blk) * p.sf_katoms + kb * 4) * kSfAtomBytes, sf_bytes,
+                           &ctl->sf_full[stage]);
+          for (int rb = 0; rb < nb_atoms; ++rb)
+            ptx::bulk_load(st + kSfaBytes + rb * 4 * kSfAtomBytes,
+                           p.b_sf + (static_cast<int64_t>(n_blk * 2 + rb) * p.sf_katoms + kb * 4) * kSfAtomBytes,
+                           sf_bytes, &ctl->sf_full[stage]);
+          issued_mask |= 1u << stage;
+          issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
+          if (++stage == SS) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      for (int s = 0; s < SS; ++s) {
+        if (issued_mask & (1u << s)) {
+          volatile int never = 0;
+          if (!ptx::mbar_wait(&ctl->sf_full[s], (issued_parity >> s) & 1u, &never)) fail(&ctl->abort, p, 10);
         }
       }
     }
   } else if (warp == 1) {
     // ----------------------------------------------------------------- MMA
     if (lane == 0 && leader) {
-      int stage = 0;
-      uint32_t phase = 0, acc_phase = 0;
+      int stage = 0, slot = 0;
+      uint32_t phase = 0, tphase = 0, acc_phase = 0;
       bool ok = true, issued = false;
+      // descriptors of stage 0; other stages and K steps are plain offsets
+      // of the 14-bit start-address field (shared-memory addresses < 256 KB)
+      const uint64_t a_desc0 = ptx::smem_desc(ptx::smem_u32(smem), 16, 1024, ptx::kSwizzle128B);
+      const uint64_t b_desc0 = ptx::smem_desc(ptx::smem_u32(smem + kABytes), 16, 1024, ptx::kSwizzle128B);
       for (int unit = unit0; unit < p.num_units && ok; unit += ustep) {
         if (!ptx::mbar_wait(&ctl->acc_empty, acc_phase ^ 1u, abort_flag)) {
           fail(&ctl->abort, p, 3);
@@ -462,39 +519,51 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         ptx::tc_fence_after();
         for (int kb = 0; kb < p.num_kb; ++kb) {
-          // The stage's scales are in TMEM and its code tiles have landed
-          // (in pair mode: in both CTAs).  CTA-scope waits suffice: the
-          // peer's arrivals follow completed TMEM writes, and the code tiles
-          // are TMA (async-proxy) writes read by the tensor core.
-          if (!ptx::mbar_wait(&ctl->sfready[stage], phase, abort_flag) ||
-              !ptx::mbar_wait(&ctl->full[stage], phase, abort_flag)) {
+          // The k-block's code tiles have landed (pair mode: in both CTAs)
+          // and its scales are in TMEM (both CTAs').  CTA-scope waits
+          // suffice: the peer's arrivals follow completed TMEM writes, and the
+          // code tiles are TMA (async-proxy) writes read by the tensor core.
+          if (!ptx::mbar_wait(&ctl->full[stage], phase, abort_flag) ||
+              !ptx::mbar_wait(&ctl->sfready[slot], tphase, abort_flag)) {
             fail(&ctl->abort, p, 4);
             ok = false;
             break;
           }
           ptx::tc_fence_after();
           const int kk_n = kk_count_for(p, kb);
-          uint8_t* st = smem + stage * L::kStageBytes;
-          const uint32_t a_addr = ptx::smem_u32(st);
-          const uint32_t b_addr = ptx::smem_u32(st + kABytes);
-          for (int kk = 0; kk < kk_n; ++kk) {
-            const uint64_t adesc = ptx::smem_desc(a_addr + kk * 32, 16, 1024, ptx::kSwizzle128B);
-            const uint64_t bdesc = ptx::smem_desc(b_addr + kk * 32, 16, 1024, ptx::kSwizzle128B);
-            const uint32_t sfa_t = tmem + kSfaCol + stage * 16 + kk * 4;
-            const uint32_t sfb_t = tmem + L::kSfbCol + stage * 32 + kk * 8;
-            if (PAIR)
-              ptx::tc_mma_nvf4_pair(tmem + kAccCol, adesc, bdesc, L::kIdesc, sfa_t, sfb_t, (kb | kk) != 0 ? 1u : 0u);
-            else
-              ptx::tc_mma_nvf4(tmem + kAccCol, adesc, bdesc, L::kIdesc, sfa_t, sfb_t, (kb | kk) != 0 ? 1u : 0u);
+          const uint32_t st_off = static_cast<uint32_t>(stage * L::kStageBytes);
+          const uint64_t adesc0 = a_desc0 + (st_off >> 4);
+          const uint64_t bdesc0 = b_desc0 + (st_off >> 4);
+          const uint32_t sfa_t0 = tmem + kSfaCol + slot * 16;
+          const uint32_t sfb_t0 = tmem + kSfbCol + slot * 32;
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) {
+            if (kk < kk_n) {
+              // +32 bytes along K inside the swizzled 128-byte rows
+              const uint64_t adesc = adesc0 + 2 * kk, bdesc = bdesc0 + 2 * kk;
+              const uint32_t acc = (kb | kk) != 0 ? 1u : 0u;
+              if (PAIR)
+                ptx::tc_mma_nvf4_pair(tmem + kAccCol, adesc, bdesc, L::kIdesc, sfa_t0 + kk * 4, sfb_t0 + kk * 8, acc);
+              else
+                ptx::tc_mma_nvf4(tmem + kAccCol, adesc, bdesc, L::kIdesc, sfa_t0 + kk * 4, sfb_t0 + kk * 8, acc);
+            }
           }
-          if (PAIR)
+          // free the code stage and the TMEM scale slot once these MMAs are done
+          if (PAIR) {
             ptx::tc_commit_pair_multicast(&ctl->empty[stage], static_cast<uint16_t>(0x3));
-          else
+            ptx::tc_commit_pair_multicast(&ctl->tfree[slot], static_cast<uint16_t>(0x3));
+          } else {
             ptx::tc_commit(&ctl->empty[stage]);
+            ptx::tc_commit(&ctl->tfree[slot]);
+          }
           issued = true;
           if (++stage == S) {
             stage = 0;
             phase ^= 1u;
+          }
+          if (++slot == T) {
+            slot = 0;
+            tphase ^= 1u;
           }
         }
         if (!ok) break;
@@ -517,25 +586,48 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp >= kFirstSfWarp) {
     // ------------------------------------------------------ scale staging
     const int q = warp & 3;  // TMEM lane quarter this warp may access
-    int stage = 0;
-    uint32_t phase = 0;
+    int stage = 0, slot = 0;
+    uint32_t phase = 0, tphase = 0;
+    uint32_t used_mask = 0, used_parity = 0;
     bool ok = true;
     for (int unit = unit0; unit < p.num_units && ok; unit += ustep) {
       for (int kb = 0; kb < p.num_kb; ++kb) {
-        if (!warp_wait(&ctl->sf_full[stage], phase, abort_flag, lane)) {
+        // the scales are in the ring, and the MMAs that last read this TMEM
+        // slot have completed
+        if (!warp_wait(&ctl->sf_full[stage], phase, abort_flag, lane) ||
+            !warp_wait(&ctl->tfree[slot], tphase ^ 1u, abort_flag, lane)) {
           if (lane == 0) fail(&ctl->abort, p, 7);
           ok = false;
           break;
         }
         ptx::tc_fence_after();
-        stage_scales<PAIR>(smem + stage * L::kStageBytes, tmem, stage, q, lane);
+        stage_scales(sf_ring + stage * kSfStageBytes, tmem, slot, q, lane);
         ptx::tmem_st_wait();
         ptx::tc_fence_before();
         __syncwarp();
-        if (lane == 0) arrive_leader<PAIR>(&ctl->sfready[stage], rank);
-        if (++stage == S) {
+        if (lane == 0) {
+          ptx::mbar_arrive(&ctl->sf_empty[stage]);
+          arrive_leader<PAIR>(&ctl->sfready[slot], rank);
+        }
+        used_mask |= 1u << slot;
+        used_parity = (used_parity & ~(1u << slot)) | (tphase << slot);
+        if (++stage == SS) {
           stage = 0;
           phase ^= 1u;
+        }
+        if (++slot == T) {
+          slot = 0;
+          tphase ^= 1u;
+        }
+      }
+    }
+    // The slot-free commits are multicast to both CTAs of a pair: wait for
+    // the last one of every slot used before this CTA may exit.
+    if (PAIR && ok && warp == kFirstSfWarp) {
+      for (int t = 0; t < T; ++t) {
+        if ((used_mask >> t) & 1u) {
+          if (!warp_wait(&ctl->tfree[t], (used_parity >> t) & 1u, abort_flag, lane) && lane == 0)
+            fail(&ctl->abort, p, 11);
         }
       }
     }
