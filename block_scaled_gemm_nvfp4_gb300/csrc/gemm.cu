@@ -15,12 +15,15 @@
 //   single mode (M <= 128): one CTA per 128 x 256 tile, cta_group::1, four
 //     48 KB code stages.
 // Codes and block scales travel in separate rings.  The scale ring (eight or
-// four 6 KB stages) runs ahead of the code ring, and the scales move into
-// TMEM slots (five k-blocks) that are freed by their own MMA commit, so the
-// scale copy, the staging into TMEM and the pair's cross-CTA arrivals are
-// hidden behind earlier k-blocks instead of lengthening each stage's round
-// trip (measured on GB300: with scales in the code stage the k-block period
-// was about 1.8x that of the same pipeline without scales).
+// four 6 KB stages) runs ahead of the code ring; the staging warps move each
+// k-block's scales into the TMEM slot of its code stage as soon as the stage's
+// previous MMAs are done, and arrive on the stage's own barrier, so the scale
+// copies and the staging are hidden behind earlier k-blocks.  The MMA issuer
+// then waits on one barrier and commits once per k-block: the tensor pipe
+// leaves one thread issuing four MMAs per k-block little time to spare, and
+// every extra barrier hop on its path (a separate scale-ready barrier with the
+// peer CTA's remote arrivals cost about a quarter of the throughput) shows up
+// directly in the k-block period (measured on GB300 with traces and variants).
 // Warp roles (15 warps):
 //   warp 0     TMA producer for the packed E2M1 codes (tiled TMA, 128-byte
 //              swizzle);
@@ -84,11 +87,11 @@ constexpr int kEpiCols = BN / 2;              // columns per epilogue warp
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kAccCol = 0;
 constexpr uint32_t kSfaCol = 256;             // + slot * 16 + kk * 4
-constexpr int kTmemSlots = 5;                 // TMEM scale slots (one k-block each)
-constexpr uint32_t kSfbCol = kSfaCol + 16 * kTmemSlots;  // + slot * 32 + kk * 8 + row_atom * 4
+constexpr int kMaxStages = 5;                 // code stages = TMEM scale slots (one k-block each)
+constexpr uint32_t kSfbCol = kSfaCol + 16 * kMaxStages;  // + stage * 32 + kk * 8 + row_atom * 4
 constexpr int kSfStageBytes = kSfaBytes + kSfbBytes;     // 6 KB of block scales per k-block
 constexpr int kGroup = 16;                    // tile raster group (row or column blocks)
-static_assert(kSfbCol + 32 * kTmemSlots <= kTmemCols, "TMEM budget");
+static_assert(kSfbCol + 32 * kMaxStages <= kTmemCols, "TMEM budget");
 
 // Per-mode layout.  Codes and block scales travel in separate rings: a code
 // stage holds one k-block of A and B codes; the scale ring is deeper, so the
@@ -102,6 +105,7 @@ struct Layout {
   static constexpr int kBBytes = kBRows * kRowBytes;
   static constexpr int kStages = PAIR ? 5 : 4;
   static constexpr int kSfStages = PAIR ? 8 : 4;
+  static_assert(kStages <= kMaxStages, "one TMEM scale slot per code stage");
   static constexpr int kStageBytes = kABytes + kBBytes;
   static constexpr int kSfRing = kStages * kStageBytes;  // offset of the scale ring
   static constexpr int kSmemBytes =
@@ -137,12 +141,11 @@ struct GParams {
 
 template <int STAGES, int SF_STAGES>
 struct __align__(8) SmemCtl {
-  uint64_t full[STAGES];          // codes landed (pair mode: both CTAs' codes, leader's copy)
-  uint64_t empty[STAGES];         // code stage consumed by the MMAs
+  uint64_t full[STAGES];          // k-block ready: codes landed and scales in TMEM (pair mode:
+                                  // both CTAs', leader's copy)
+  uint64_t empty[STAGES];         // code stage and its TMEM scale slot no longer read by MMAs
   uint64_t sf_full[SF_STAGES];    // this CTA's block scales landed in the scale ring
   uint64_t sf_empty[SF_STAGES];   // scale ring stage copied into TMEM
-  uint64_t sfready[kTmemSlots];   // scales in TMEM (pair mode: both CTAs', leader's copy)
-  uint64_t tfree[kTmemSlots];     // TMEM scale slot no longer read by MMAs
   uint64_t acc_full;
   uint64_t acc_empty;             // accumulator drained (pair mode: both CTAs', leader's copy)
   uint64_t drain;
@@ -340,7 +343,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   using L = Layout<PAIR>;
   constexpr int S = L::kStages;
   constexpr int SS = L::kSfStages;
-  constexpr int T = kTmemSlots;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sf_ring = smem + L::kSfRing;
@@ -356,16 +358,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
-      ptx::mbar_init(&ctl->full[s], 1);
+      // the code producer's arrival (with the tiles' byte count) and one
+      // arrival per scale-staging warp of each CTA
+      ptx::mbar_init(&ctl->full[s], 1 + (PAIR ? 2 : 1) * kSfWarps);
       ptx::mbar_init(&ctl->empty[s], 1);
     }
     for (int s = 0; s < SS; ++s) {
       ptx::mbar_init(&ctl->sf_full[s], 1);
       ptx::mbar_init(&ctl->sf_empty[s], kSfWarps);
-    }
-    for (int t = 0; t < T; ++t) {
-      ptx::mbar_init(&ctl->sfready[t], PAIR ? 2 * kSfWarps : kSfWarps);
-      ptx::mbar_init(&ctl->tfree[t], 1);
     }
     ptx::mbar_init(&ctl->acc_full, 1);
     ptx::mbar_init(&ctl->acc_empty, PAIR ? 2 * kEpiWarps : kEpiWarps);
@@ -505,8 +505,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 1) {
     // ----------------------------------------------------------------- MMA
     if (lane == 0 && leader) {
-      int stage = 0, slot = 0;
-      uint32_t phase = 0, tphase = 0, acc_phase = 0;
+      int stage = 0;
+      uint32_t phase = 0, acc_phase = 0;
       bool ok = true, issued = false;
       // descriptors of stage 0; other stages and K steps are plain offsets
       // of the 14-bit start-address field (shared-memory addresses < 256 KB)
@@ -519,12 +519,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         ptx::tc_fence_after();
         for (int kb = 0; kb < p.num_kb; ++kb) {
-          // The k-block's code tiles have landed (pair mode: in both CTAs)
-          // and its scales are in TMEM (both CTAs').  CTA-scope waits
-          // suffice: the peer's arrivals follow completed TMEM writes, and the
-          // code tiles are TMA (async-proxy) writes read by the tensor core.
-          if (!ptx::mbar_wait(&ctl->full[stage], phase, abort_flag) ||
-              !ptx::mbar_wait(&ctl->sfready[slot], tphase, abort_flag)) {
+          // One wait per k-block: the stage's barrier completes when its code
+          // tiles have landed (pair mode: both CTAs') and every staging warp
+          // (both CTAs') has put its scales into the stage's TMEM slot.
+          // CTA-scope waits suffice: the peer's arrivals follow completed
+          // TMEM writes, and the code tiles are TMA (async-proxy) writes read
+          // by the tensor core.
+          if (!ptx::mbar_wait(&ctl->full[stage], phase, abort_flag)) {
             fail(&ctl->abort, p, 4);
             ok = false;
             break;
@@ -534,8 +535,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t st_off = static_cast<uint32_t>(stage * L::kStageBytes);
           const uint64_t adesc0 = a_desc0 + (st_off >> 4);
           const uint64_t bdesc0 = b_desc0 + (st_off >> 4);
-          const uint32_t sfa_t0 = tmem + kSfaCol + slot * 16;
-          const uint32_t sfb_t0 = tmem + kSfbCol + slot * 32;
+          const uint32_t sfa_t0 = tmem + kSfaCol + stage * 16;
+          const uint32_t sfb_t0 = tmem + kSfbCol + stage * 32;
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk) {
             if (kk < kk_n) {
@@ -548,22 +549,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ptx::tc_mma_nvf4(tmem + kAccCol, adesc, bdesc, L::kIdesc, sfa_t0 + kk * 4, sfb_t0 + kk * 8, acc);
             }
           }
-          // free the code stage and the TMEM scale slot once these MMAs are done
-          if (PAIR) {
+          // one commit frees the code stage and its TMEM scale slot
+          if (PAIR)
             ptx::tc_commit_pair_multicast(&ctl->empty[stage], static_cast<uint16_t>(0x3));
-            ptx::tc_commit_pair_multicast(&ctl->tfree[slot], static_cast<uint16_t>(0x3));
-          } else {
+          else
             ptx::tc_commit(&ctl->empty[stage]);
-            ptx::tc_commit(&ctl->tfree[slot]);
-          }
           issued = true;
           if (++stage == S) {
             stage = 0;
             phase ^= 1u;
-          }
-          if (++slot == T) {
-            slot = 0;
-            tphase ^= 1u;
           }
         }
         if (!ok) break;
@@ -586,48 +580,41 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp >= kFirstSfWarp) {
     // ------------------------------------------------------ scale staging
     const int q = warp & 3;  // TMEM lane quarter this warp may access
-    int stage = 0, slot = 0;
-    uint32_t phase = 0, tphase = 0;
-    uint32_t used_mask = 0, used_parity = 0;
+    int sstage = 0, slot = 0;
+    uint32_t sphase = 0, tphase = 0;
     bool ok = true;
+    const uint32_t full_leader0 = PAIR ? ptx::mapa_shared(ptx::smem_u32(&ctl->full[0]), 0) : 0u;
     for (int unit = unit0; unit < p.num_units && ok; unit += ustep) {
       for (int kb = 0; kb < p.num_kb; ++kb) {
-        // the scales are in the ring, and the MMAs that last read this TMEM
-        // slot have completed
-        if (!warp_wait(&ctl->sf_full[stage], phase, abort_flag, lane) ||
-            !warp_wait(&ctl->tfree[slot], tphase ^ 1u, abort_flag, lane)) {
+        // The scales are in the ring, and the MMAs that last read this TMEM
+        // slot (the k-block one ring lap earlier, in the same code stage)
+        // have completed.
+        if (!warp_wait(&ctl->sf_full[sstage], sphase, abort_flag, lane) ||
+            !warp_wait(&ctl->empty[slot], tphase ^ 1u, abort_flag, lane)) {
           if (lane == 0) fail(&ctl->abort, p, 7);
           ok = false;
           break;
         }
         ptx::tc_fence_after();
-        stage_scales(sf_ring + stage * kSfStageBytes, tmem, slot, q, lane);
+        stage_scales(sf_ring + sstage * kSfStageBytes, tmem, slot, q, lane);
         ptx::tmem_st_wait();
         ptx::tc_fence_before();
         __syncwarp();
         if (lane == 0) {
-          ptx::mbar_arrive(&ctl->sf_empty[stage]);
-          arrive_leader<PAIR>(&ctl->sfready[slot], rank);
+          ptx::mbar_arrive(&ctl->sf_empty[sstage]);
+          // the stage's ready barrier lives in the leader (or single) CTA
+          if (PAIR && !leader)
+            ptx::mbar_arrive_cluster_relaxed(full_leader0 + static_cast<uint32_t>(slot * sizeof(uint64_t)));
+          else
+            ptx::mbar_arrive(&ctl->full[slot]);
         }
-        used_mask |= 1u << slot;
-        used_parity = (used_parity & ~(1u << slot)) | (tphase << slot);
-        if (++stage == SS) {
-          stage = 0;
-          phase ^= 1u;
+        if (++sstage == SS) {
+          sstage = 0;
+          sphase ^= 1u;
         }
-        if (++slot == T) {
+        if (++slot == S) {
           slot = 0;
           tphase ^= 1u;
-        }
-      }
-    }
-    // The slot-free commits are multicast to both CTAs of a pair: wait for
-    // the last one of every slot used before this CTA may exit.
-    if (PAIR && ok && warp == kFirstSfWarp) {
-      for (int t = 0; t < T; ++t) {
-        if ((used_mask >> t) & 1u) {
-          if (!warp_wait(&ctl->tfree[t], (used_parity >> t) & 1u, abort_flag, lane) && lane == 0)
-            fail(&ctl->abort, p, 11);
         }
       }
     }
