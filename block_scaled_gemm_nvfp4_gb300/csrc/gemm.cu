@@ -12,13 +12,14 @@
 //     code stage (32 KB, five stages); the leader CTA issues the MMAs, which
 //     read both CTAs' shared memory and write each CTA's 128 x 256 FP32
 //     accumulator in its own TMEM;
-//   single mode (M <= 128): one CTA per 128 x 256 tile, cta_group::1, four
+//   single mode (M <= 128): one CTA per 128 x 256 tile, cta_group::1, three
 //     48 KB code stages.
-// Codes and block scales travel in separate rings.  The scale ring (eight or
-// four 6 KB stages) runs ahead of the code ring; the staging warps move each
-// k-block's scales into the TMEM slot of its code stage as soon as the stage's
-// previous MMAs are done, and arrive on the stage's own barrier, so the scale
-// copies and the staging are hidden behind earlier k-blocks.  The MMA issuer
+// Codes and block scales travel in separate rings.  A scale stage holds four
+// k-blocks (three 8 KB copies) and runs ahead of the code ring; the staging
+// warps move each k-block's scales into the TMEM slot of its code stage as
+// soon as the stage's previous MMAs are done, two k-blocks at a time, and
+// arrive on the stage's own barrier, so the scale copies and the staging are
+// hidden behind earlier k-blocks.  The MMA issuer
 // then waits on one barrier and commits once per k-block: the tensor pipe
 // leaves one thread issuing four MMAs per k-block little time to spare, and
 // every extra barrier hop on its path (a separate scale-ready barrier with the
@@ -89,22 +90,25 @@ constexpr uint32_t kAccCol = 0;
 constexpr uint32_t kSfaCol = 256;             // + slot * 16 + kk * 4
 constexpr int kMaxStages = 5;                 // code stages = TMEM scale slots (one k-block each)
 constexpr uint32_t kSfbCol = kSfaCol + 16 * kMaxStages;  // + stage * 32 + kk * 8 + row_atom * 4
-constexpr int kSfStageBytes = kSfaBytes + kSfbBytes;     // 6 KB of block scales per k-block
+constexpr int kSfGroup = 4;                   // k-blocks per scale stage
+constexpr int kSfaGroupBytes = kSfGroup * kSfaBytes;     // 8 KB: 16 K atoms of one A row block
+constexpr int kSfStageBytes = 3 * kSfaGroupBytes;        // A + two B row blocks: 24 KB
 constexpr int kGroup = 16;                    // tile raster group (row or column blocks)
 static_assert(kSfbCol + 32 * kMaxStages <= kTmemCols, "TMEM budget");
 
 // Per-mode layout.  Codes and block scales travel in separate rings: a code
-// stage holds one k-block of A and B codes; the scale ring is deeper, so the
-// small scale copies are issued several k-blocks ahead and their latency
-// (copy, staging into TMEM, the pair's arrivals) stays off the MMA's path.
-//   PAIR: B rows per CTA 128, five 32 KB code stages, eight scale stages;
-//   single: B rows 256, four 48 KB code stages, four scale stages.
+// stage holds one k-block of A and B codes (and owns one TMEM scale slot); a
+// scale stage holds four k-blocks of scales, so the small scale copies are
+// issued ahead of the codes and their latency stays off the MMA's path.
+//   PAIR: B rows per CTA 128, five 32 KB code stages;
+//   single: B rows 256, three 48 KB code stages;
+// both with two 24 KB scale stages.
 template <bool PAIR>
 struct Layout {
   static constexpr int kBRows = PAIR ? BN / 2 : BN;
   static constexpr int kBBytes = kBRows * kRowBytes;
-  static constexpr int kStages = PAIR ? 5 : 4;
-  static constexpr int kSfStages = PAIR ? 8 : 4;
+  static constexpr int kStages = PAIR ? 5 : 3;
+  static constexpr int kSfStages = 2;
   static_assert(kStages <= kMaxStages, "one TMEM scale slot per code stage");
   static constexpr int kStageBytes = kABytes + kBBytes;
   static constexpr int kSfRing = kStages * kStageBytes;  // offset of the scale ring
@@ -304,8 +308,8 @@ __device__ __forceinline__ void epilogue_half(const GParams& p, uint64_t* acc_em
 // quarter q) copies atom row `lane` into its own lanes.  Columns of TMEM
 // slot t: A at kSfaCol + 16 t + 4 kk, B row block rb at kSfbCol + 32 t + 8 kk
 // + 4 rb (a 256-row B operand is read as columns base .. base + 7).
-__device__ __forceinline__ void stage_scales(const uint8_t* sfa, uint32_t tmem, int slot, int q, int lane) {
-  const uint8_t* sfb = sfa + kSfaBytes;
+__device__ __forceinline__ void stage_scales(const uint8_t* sfa, const uint8_t* sfb, int sfb_rb_stride,
+                                             uint32_t tmem, int slot, int q, int lane) {
   const uint32_t lane_base = tmem + (static_cast<uint32_t>(q * 32) << 16);
   uint32_t va[16];
 #pragma unroll
@@ -317,23 +321,19 @@ __device__ __forceinline__ void stage_scales(const uint8_t* sfa, uint32_t tmem, 
     va[4 * kk + 3] = v.w;
   }
   ptx::tmem_st_32x32b_x16(lane_base + kSfaCol + slot * 16, va);
+  uint32_t vb[32];
 #pragma unroll
-  for (int h = 0; h < 2; ++h) {
-    uint32_t vb[16];
+  for (int kk = 0; kk < 4; ++kk) {
 #pragma unroll
-    for (int k2 = 0; k2 < 2; ++k2) {
-      const int kk = 2 * h + k2;
-#pragma unroll
-      for (int rb = 0; rb < 2; ++rb) {
-        const uint4 v = *reinterpret_cast<const uint4*>(sfb + rb * 4 * kSfAtomBytes + kk * kSfAtomBytes + lane * 16);
-        vb[8 * k2 + 4 * rb] = v.x;
-        vb[8 * k2 + 4 * rb + 1] = v.y;
-        vb[8 * k2 + 4 * rb + 2] = v.z;
-        vb[8 * k2 + 4 * rb + 3] = v.w;
-      }
+    for (int rb = 0; rb < 2; ++rb) {
+      const uint4 v = *reinterpret_cast<const uint4*>(sfb + rb * sfb_rb_stride + kk * kSfAtomBytes + lane * 16);
+      vb[8 * kk + 4 * rb] = v.x;
+      vb[8 * kk + 4 * rb + 1] = v.y;
+      vb[8 * kk + 4 * rb + 2] = v.z;
+      vb[8 * kk + 4 * rb + 3] = v.w;
     }
-    ptx::tmem_st_32x32b_x16(lane_base + kSfbCol + slot * 32 + h * 16, vb);
   }
+  ptx::tmem_st_32x32b_x32(lane_base + kSfbCol + slot * 32, vb);
 }
 
 template <bool OUT_F32, bool PAIR>
@@ -471,22 +471,25 @@ __global__ void __launch_bounds__(kThreads, 1)
         // (a row block past the end -- the odd last half of a pair -- has no
         // scales to load; its rows are never stored)
         const bool a_valid = m_blk < p.tiles_m;
-        for (int kb = 0; kb < p.num_kb; ++kb) {
+        for (int kb0 = 0; kb0 < p.num_kb; kb0 += kSfGroup) {
           if (!ptx::mbar_wait(&ctl->sf_empty[stage], phase ^ 1u, abort_flag)) {
             fail(&ctl->abort, p, 9);
             ok = false;
             break;
           }
-          const uint32_t sf_bytes = static_cast<uint32_t>(kk_count_for(p, kb) * kSfAtomBytes);
+          // the 64-wide K atoms of k-blocks kb0 .. kb0 + 3, contiguous per row block
+          const int64_t atom0 = static_cast<int64_t>(kb0) * 4;
+          const uint32_t bytes =
+              static_cast<uint32_t>(min(static_cast<int64_t>(4 * kSfGroup), p.sf_katoms - atom0) * kSfAtomBytes);
           uint8_t* st = sf_ring + stage * kSfStageBytes;
-          ptx::mbar_arrive_expect_tx(&ctl->sf_full[stage], sf_bytes * ((a_valid ? 1 : 0) + nb_atoms));
+          ptx::mbar_arrive_expect_tx(&ctl->sf_full[stage], bytes * ((a_valid ? 1 : 0) + nb_atoms));
           if (a_valid)
-            ptx::bulk_load(st, p.a_sf + (static_cast<int64_t>(m_blk) * p.sf_katoms + kb * 4) * kSfAtomBytes, sf_bytes,
+            ptx::bulk_load(st, p.a_sf + (static_cast<int64_t>(m_blk) * p.sf_katoms + atom0) * kSfAtomBytes, bytes,
                            &ctl->sf_full[stage]);
           for (int rb = 0; rb < nb_atoms; ++rb)
-            ptx::bulk_load(st + kSfaBytes + rb * 4 * kSfAtomBytes,
-                           p.b_sf + (static_cast<int64_t>(n_blk * 2 + rb) * p.sf_katoms + kb * 4) * kSfAtomBytes,
-                           sf_bytes, &ctl->sf_full[stage]);
+            ptx::bulk_load(st + (1 + rb) * kSfaGroupBytes,
+                           p.b_sf + (static_cast<int64_t>(n_blk * 2 + rb) * p.sf_katoms + atom0) * kSfAtomBytes, bytes,
+                           &ctl->sf_full[stage]);
           issued_mask |= 1u << stage;
           issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
           if (++stage == SS) {
@@ -579,42 +582,62 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp >= kFirstSfWarp) {
     // ------------------------------------------------------ scale staging
+    // Two k-blocks per iteration: their stores share one wait::st and the
+    // arrivals go out together, which halves this warp's fixed per-k-block
+    // cost (barrier waits, arrivals, a remote one in the follower); staging
+    // had become the slowest stage of the pipeline.
     const int q = warp & 3;  // TMEM lane quarter this warp may access
     int sstage = 0, slot = 0;
     uint32_t sphase = 0, tphase = 0;
     bool ok = true;
     const uint32_t full_leader0 = PAIR ? ptx::mapa_shared(ptx::smem_u32(&ctl->full[0]), 0) : 0u;
+    auto arrive_full = [&](int s_) {
+      // the stage's ready barrier lives in the leader (or single) CTA
+      if (PAIR && !leader)
+        ptx::mbar_arrive_cluster_relaxed(full_leader0 + static_cast<uint32_t>(s_ * sizeof(uint64_t)));
+      else
+        ptx::mbar_arrive(&ctl->full[s_]);
+    };
     for (int unit = unit0; unit < p.num_units && ok; unit += ustep) {
-      for (int kb = 0; kb < p.num_kb; ++kb) {
-        // The scales are in the ring, and the MMAs that last read this TMEM
-        // slot (the k-block one ring lap earlier, in the same code stage)
-        // have completed.
-        if (!warp_wait(&ctl->sf_full[sstage], sphase, abort_flag, lane) ||
-            !warp_wait(&ctl->empty[slot], tphase ^ 1u, abort_flag, lane)) {
+      for (int kb = 0; kb < p.num_kb; kb += 2) {
+        const int n2 = min(2, p.num_kb - kb);
+        const int slot1 = slot + 1 == S ? 0 : slot + 1;
+        const uint32_t tphase1 = slot + 1 == S ? tphase ^ 1u : tphase;
+        // The scales are in the ring (one wait per scale stage), and the MMAs
+        // that last read these TMEM slots (one ring lap earlier, in the same
+        // code stages) have completed.
+        if ((kb % kSfGroup == 0 && !warp_wait(&ctl->sf_full[sstage], sphase, abort_flag, lane)) ||
+            !warp_wait(&ctl->empty[slot], tphase ^ 1u, abort_flag, lane) ||
+            (n2 == 2 && !warp_wait(&ctl->empty[slot1], tphase1 ^ 1u, abort_flag, lane))) {
           if (lane == 0) fail(&ctl->abort, p, 7);
           ok = false;
           break;
         }
         ptx::tc_fence_after();
-        stage_scales(sf_ring + sstage * kSfStageBytes, tmem, slot, q, lane);
+        const uint8_t* st = sf_ring + sstage * kSfStageBytes;
+        const int j = kb % kSfGroup;
+        stage_scales(st + j * kSfaBytes, st + kSfaGroupBytes + j * kSfaBytes, kSfaGroupBytes, tmem, slot, q, lane);
+        if (n2 == 2)
+          stage_scales(st + (j + 1) * kSfaBytes, st + kSfaGroupBytes + (j + 1) * kSfaBytes, kSfaGroupBytes, tmem,
+                       slot1, q, lane);
         ptx::tmem_st_wait();
         ptx::tc_fence_before();
         __syncwarp();
+        const bool group_done = j + n2 >= kSfGroup || kb + n2 >= p.num_kb;
         if (lane == 0) {
-          ptx::mbar_arrive(&ctl->sf_empty[sstage]);
-          // the stage's ready barrier lives in the leader (or single) CTA
-          if (PAIR && !leader)
-            ptx::mbar_arrive_cluster_relaxed(full_leader0 + static_cast<uint32_t>(slot * sizeof(uint64_t)));
-          else
-            ptx::mbar_arrive(&ctl->full[slot]);
+          if (group_done) ptx::mbar_arrive(&ctl->sf_empty[sstage]);
+          arrive_full(slot);
+          if (n2 == 2) arrive_full(slot1);
         }
-        if (++sstage == SS) {
+        if (group_done && ++sstage == SS) {
           sstage = 0;
           sphase ^= 1u;
         }
-        if (++slot == S) {
-          slot = 0;
-          tphase ^= 1u;
+        for (int i = 0; i < n2; ++i) {
+          if (++slot == S) {
+            slot = 0;
+            tphase ^= 1u;
+          }
         }
       }
     }
