@@ -73,6 +73,9 @@ struct OutParams {
   uint32_t* partials;
   int64_t qr, qk, code_ld, kb_count, katoms;
   uint64_t rht_seed, sr_seed, sr_offset;
+  // Philox key schedule of sr_seed, one pair per round (parameter space, so
+  // the round XORs read them as constant operands)
+  uint32_t sr_rk0[10], sr_rk1[10];
   int col, block2d, sr, rht, sf_mma, vec16;
 };
 
@@ -95,6 +98,18 @@ __device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint32_t k0, uint32_t k1
                    static_cast<uint32_t>(p0 >> 32) ^ c.w ^ k1, static_cast<uint32_t>(p0));
     k0 += 0x9E3779B9u;
     k1 += 0xBB67AE85u;
+  }
+  return c;
+}
+
+// The same rounds with the key schedule precomputed.
+__device__ __forceinline__ uint4 philox4x32_10_rk(uint4 c, const uint32_t (&rk0)[10], const uint32_t (&rk1)[10]) {
+#pragma unroll
+  for (int i = 0; i < 10; ++i) {
+    const uint64_t p0 = static_cast<uint64_t>(0xD2511F53u) * c.x;
+    const uint64_t p1 = static_cast<uint64_t>(0xCD9E8D57u) * c.z;
+    c = make_uint4(static_cast<uint32_t>(p1 >> 32) ^ c.y ^ rk0[i], static_cast<uint32_t>(p1),
+                   static_cast<uint32_t>(p0 >> 32) ^ c.w ^ rk1[i], static_cast<uint32_t>(p0));
   }
   return c;
 }
@@ -202,14 +217,14 @@ __device__ __forceinline__ uint2 encode_run(const float (&v)[16], uint32_t bamax
     for (int j = 0; j < 16; ++j) q[j] = __fdiv_rn(v[j], d);
   }
   if (SR) {
-    const uint32_t k0 = static_cast<uint32_t>(o.sr_seed), k1 = static_cast<uint32_t>(o.sr_seed >> 32);
     const uint32_t o0 = static_cast<uint32_t>(o.sr_offset), o1 = static_cast<uint32_t>(o.sr_offset >> 32);
     const uint64_t c = e0 >> 2;
 #pragma unroll
     for (int g = 0; g < 4; ++g) {
       const uint64_t cg = c + g;
-      const uint4 w = philox4x32_10(make_uint4(static_cast<uint32_t>(cg), static_cast<uint32_t>(cg >> 32), o0, o1),
-                                    k0, k1);
+      const uint4 w =
+          philox4x32_10_rk(make_uint4(static_cast<uint32_t>(cg), static_cast<uint32_t>(cg >> 32), o0, o1), o.sr_rk0,
+                           o.sr_rk1);
       q[4 * g + 0] = sr_round(q[4 * g + 0], w.x);
       q[4 * g + 1] = sr_round(q[4 * g + 1], w.y);
       q[4 * g + 2] = sr_round(q[4 * g + 2], w.z);
@@ -596,6 +611,16 @@ cudaError_t launch_quantize(const QuantArgs& a, cudaStream_t stream) {
     op.rht_seed = q.rht_seed;
     op.sr_seed = q.sr_seed;
     op.sr_offset = q.sr_offset;
+    {
+      // Weyl key schedule of Philox4x32-10 (Salmon et al., SC'11)
+      uint32_t k0 = static_cast<uint32_t>(q.sr_seed), k1 = static_cast<uint32_t>(q.sr_seed >> 32);
+      for (int i = 0; i < 10; ++i) {
+        op.sr_rk0[i] = k0;
+        op.sr_rk1[i] = k1;
+        k0 += 0x9E3779B9u;
+        k1 += 0xBB67AE85u;
+      }
+    }
     op.col = q.transpose;
     op.block2d = q.block2d;
     op.sr = q.sr;
