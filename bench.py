@@ -123,6 +123,23 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
+def _max_over_ranks(ms, pg, dev):
+    """The slowest rank's time (every rank gets it); ms itself when alone."""
+    if pg is None:
+        return ms
+    import torch
+
+    t = torch.tensor([ms], dtype=torch.float64, device=dev)
+    pg.all_reduce(t, op=pg.ReduceOp.MAX)
+    return t.item()
+
+
+def _tflops(world, ms_per_step):
+    """Whole-job throughput: every rank runs one step of the workload (weak
+    scaling, independent replicas), timed by the slowest rank."""
+    return world * STEP_FLOP / (ms_per_step * 1e-3) / 1e12
+
+
 def _dist():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -181,12 +198,9 @@ def run_ours(args):
     st = nv.nvfp4_check_device_status(plan["ws"])
     if st != nv.NVFP4_OK:
         raise RuntimeError("device status %s" % nv.nvfp4_status_string(st))
-    if pg:
-        t = torch.tensor([ms_total], device=dev)
-        pg.all_reduce(t, op=pg.ReduceOp.MAX)
-        ms_total = t.item()
+    ms_total = _max_over_ranks(ms_total, pg, dev)
     ms_step = ms_total / args.steps
-    value = world * STEP_FLOP / (ms_step * 1e-3) / 1e12
+    value = _tflops(world, ms_step)
 
     gemm_ms = statistics.mean(a.elapsed_time(b) for a, b in gemm_events)  # per GEMM
     quant_ms = sum(a.elapsed_time(b) for a, b in quant_events) / args.steps  # three dual quantises per step
@@ -352,10 +366,7 @@ def run_e2e(args, nv, torch, x_c, w_c, dy_c, dev, world, pg):
     t1.record(s_out)
     torch.cuda.synchronize()
     ms = t0.elapsed_time(t1)
-    if pg:
-        t = torch.tensor([ms], device=dev)
-        pg.all_reduce(t, op=pg.ReduceOp.MAX)
-        ms = t.item()
+    ms = _max_over_ranks(ms, pg, dev)
     ms /= n
     for sl in slots:
         st = nv.nvfp4_check_device_status(sl["plan"]["ws"])
@@ -363,7 +374,7 @@ def run_e2e(args, nv, torch, x_c, w_c, dy_c, dev, world, pg):
             raise RuntimeError("device status %s (end-to-end run)" % nv.nvfp4_status_string(st))
     h2d = (T * HID + FFN * HID + T * FFN) * 2
     d2h = (T * FFN + T * HID + FFN * HID) * 2
-    return {"value": round(world * STEP_FLOP / (ms * 1e-3) / 1e12, 3), "unit": "TFLOP/s",
+    return {"value": round(_tflops(world, ms), 3), "unit": "TFLOP/s",
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(ms, 4),
             "api": "nvfp4_quantize_dual + nvfp4_gemm with pinned host buffers; copy-in, compute and copy-out "
                    "streams overlap neighbouring steps"}
