@@ -63,6 +63,8 @@ def _lib():
         lib.oracle_quantize.argtypes = [P, I64, I64, I64, ctypes.POINTER(_Cfg), P, P, P]
         lib.oracle_quantize_rows.restype = ctypes.c_int
         lib.oracle_quantize_rows.argtypes = [P, I64, I64, I64, ctypes.POINTER(_Cfg), I64, I64, P, P, P]
+        lib.oracle_quantize_given_amax.restype = ctypes.c_int
+        lib.oracle_quantize_given_amax.argtypes = [P, I64, I64, I64, ctypes.POINTER(_Cfg), ctypes.c_float, P, P, P]
         lib.oracle_amax.restype = ctypes.c_int
         lib.oracle_amax.argtypes = [P, I64, I64, I64, ctypes.POINTER(_Cfg), P]
         lib.oracle_sf_mma_offset.restype = I64
@@ -174,6 +176,24 @@ def quantize_rows(x_u16, cfg, row_begin, row_end):
     ts = np.zeros(1, dtype=np.float32)
     st = _lib().oracle_quantize_rows(_ptr(x), rows, cols, cols, ctypes.byref(c), int(row_begin), int(row_end),
                                      _ptr(codes), _ptr(sf), _ptr(ts))
+    if st != OK:
+        raise OracleError(st)
+    return codes, sf, ts[0]
+
+
+def quantize_given_amax(x_u16, cfg, amax_value):
+    """Delayed scaling: quantise with the tensor scale amax_value / 2688
+    instead of the operand's own amax.  Returns (codes, sf, tensor_scale)."""
+    x = np.ascontiguousarray(x_u16)
+    assert x.dtype == np.uint16 and x.ndim == 2
+    rows, cols = x.shape
+    c = _cfg(cfg)
+    qr, qk = (cols, rows) if c.transpose else (rows, cols)
+    codes = np.zeros((qr, max(qk // 2, 0)), dtype=np.uint8)
+    sf = np.zeros((qr, max(qk // 16, 0)), dtype=np.uint8)
+    ts = np.zeros(1, dtype=np.float32)
+    st = _lib().oracle_quantize_given_amax(_ptr(x), rows, cols, cols, ctypes.byref(c), float(amax_value),
+                                           _ptr(codes), _ptr(sf), _ptr(ts))
     if st != OK:
         raise OracleError(st)
     return codes, sf, ts[0]

@@ -235,35 +235,11 @@ int oracle_amax(const uint16_t* x, int64_t rows, int64_t cols, int64_t ld,
   return ORACLE_OK;
 }
 
-/* Encode rows [row_begin, row_end) of Q; the tensor scale always comes from
- * the amax of the whole operand.  codes / sf hold only the encoded rows. */
-int oracle_quantize_rows(const uint16_t* x, int64_t rows, int64_t cols, int64_t ld, const oracle_cfg* cfg,
-                         int64_t row_begin, int64_t row_end, uint8_t* codes, uint8_t* sf, float* tensor_scale) {
-  int st = check_args(rows, cols, ld, cfg);
-  if (st != ORACLE_OK) return st;
-  int64_t R = 0, K = 0;
-  float* q = logical_operand(x, rows, cols, ld, cfg, &R, &K);
-  if (!q) return ORACLE_ERR_INVALID_ARG;
-  if (row_begin < 0 || row_end > R || row_begin > row_end) {
-    free(q);
-    return ORACLE_ERR_INVALID_ARG;
-  }
+/* Steps 3-5 for rows [row_begin, row_end) of the materialised operand q
+ * [R, K] under the FP32 tensor scale s_dec.  codes / sf hold only those rows. */
+static void encode_rows(const float* q, int64_t K, const oracle_cfg* cfg, float s_dec, int64_t row_begin,
+                        int64_t row_end, uint8_t* codes, uint8_t* sf) {
   int64_t KB = K / 16;
-
-  /* Step 1: tensor amax, taken after the transform (reading). */
-  float amax = amax_of(q, R * K);
-  if (!isfinite(amax)) {
-    free(q);
-    return ORACLE_ERR_NONFINITE;
-  }
-  /* Step 2: FP32 tensor (decode) scale s = amax / (6 * 448): the largest
-   * block can then reach both the largest E4M3 scale and the largest E2M1
-   * element (reading).  A zero scale (all-zero or subnormal-tiny tensor)
-   * is replaced by 1, which makes every block scale and every code zero. */
-  float s_dec = amax / 2688.0f;
-  if (s_dec == 0.0f) s_dec = 1.0f;
-  *tensor_scale = s_dec;
-
   memset(codes, 0, (size_t)((row_end - row_begin) * (K / 2)));
   for (int64_t i = row_begin; i < row_end; ++i) {
     int64_t oi = i - row_begin;
@@ -310,6 +286,67 @@ int oracle_quantize_rows(const uint16_t* x, int64_t rows, int64_t cols, int64_t 
       }
     }
   }
+}
+
+/* Step 2: FP32 tensor (decode) scale s = amax / (6 * 448): the largest block
+ * can then reach both the largest E4M3 scale and the largest E2M1 element
+ * (reading).  A zero scale (all-zero or subnormal-tiny tensor) is replaced by
+ * 1, which makes every block scale and every code zero. */
+static float tensor_scale_of(float amax) {
+  float s_dec = amax / 2688.0f;
+  if (s_dec == 0.0f) s_dec = 1.0f;
+  return s_dec;
+}
+
+/* Encode rows [row_begin, row_end) of Q; the tensor scale always comes from
+ * the amax of the whole operand.  codes / sf hold only the encoded rows. */
+int oracle_quantize_rows(const uint16_t* x, int64_t rows, int64_t cols, int64_t ld, const oracle_cfg* cfg,
+                         int64_t row_begin, int64_t row_end, uint8_t* codes, uint8_t* sf, float* tensor_scale) {
+  int st = check_args(rows, cols, ld, cfg);
+  if (st != ORACLE_OK) return st;
+  int64_t R = 0, K = 0;
+  float* q = logical_operand(x, rows, cols, ld, cfg, &R, &K);
+  if (!q) return ORACLE_ERR_INVALID_ARG;
+  if (row_begin < 0 || row_end > R || row_begin > row_end) {
+    free(q);
+    return ORACLE_ERR_INVALID_ARG;
+  }
+  /* Step 1: tensor amax, taken after the transform (reading). */
+  float amax = amax_of(q, R * K);
+  if (!isfinite(amax)) {
+    free(q);
+    return ORACLE_ERR_NONFINITE;
+  }
+  float s_dec = tensor_scale_of(amax);
+  *tensor_scale = s_dec;
+  encode_rows(q, K, cfg, s_dec, row_begin, row_end, codes, sf);
+  free(q);
+  return ORACLE_OK;
+}
+
+/* Delayed scaling: step 1 is replaced by an amax the caller supplies (for
+ * instance the one measured on the previous step), so the operand is not
+ * scanned before it is encoded.  The supplied amax must be finite and >= 0;
+ * so must every element (ORACLE_ERR_NONFINITE otherwise).  Elements above the
+ * supplied amax saturate: their block scale stops at 448 and their codes at
+ * +-6, both by the rounding rules of steps 4 and 5 (reading: the format pages
+ * fix no scaling policy; this keeps every other step unchanged). */
+int oracle_quantize_given_amax(const uint16_t* x, int64_t rows, int64_t cols, int64_t ld,
+                               const oracle_cfg* cfg, float amax, uint8_t* codes, uint8_t* sf,
+                               float* tensor_scale) {
+  int st = check_args(rows, cols, ld, cfg);
+  if (st != ORACLE_OK) return st;
+  if (!(amax >= 0.0f) || isinf(amax)) return ORACLE_ERR_NONFINITE;
+  int64_t R = 0, K = 0;
+  float* q = logical_operand(x, rows, cols, ld, cfg, &R, &K);
+  if (!q) return ORACLE_ERR_INVALID_ARG;
+  if (!isfinite(amax_of(q, R * K))) {
+    free(q);
+    return ORACLE_ERR_NONFINITE;
+  }
+  float s_dec = tensor_scale_of(fabsf(amax));
+  *tensor_scale = s_dec;
+  encode_rows(q, K, cfg, s_dec, 0, R, codes, sf);
   free(q);
   return ORACLE_OK;
 }

@@ -82,6 +82,13 @@ int oracle_quantize(const uint16_t* x, int64_t rows, int64_t cols, int64_t ld,
 int oracle_quantize_rows(const uint16_t* x, int64_t rows, int64_t cols, int64_t ld, const oracle_cfg* cfg,
                          int64_t row_begin, int64_t row_end, uint8_t* codes, uint8_t* sf, float* tensor_scale);
 
+/* Delayed scaling: as oracle_quantize, but the tensor scale is amax / 2688
+ * for a caller-supplied amax instead of the operand's own (elements above it
+ * saturate).  The operand must be finite. */
+int oracle_quantize_given_amax(const uint16_t* x, int64_t rows, int64_t cols, int64_t ld,
+                               const oracle_cfg* cfg, float amax, uint8_t* codes, uint8_t* sf,
+                               float* tensor_scale);
+
 /* Amax of the (optionally transformed) operand, as the quantiser sees it. */
 int oracle_amax(const uint16_t* x, int64_t rows, int64_t cols, int64_t ld,
                 const oracle_cfg* cfg, float* amax);
