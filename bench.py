@@ -444,7 +444,10 @@ def run_case(args):
     """Time one library call on one shape (for sweeps and ncu captures):
     ``gemm:M,N,K`` (BF16 output), ``quantize:R,C[,mode]`` with mode one of
     row, col, row16, col16, colsr (transform + stochastic rounding), or
-    ``dual:R,C[,act|weight]`` (row + colsr, or row16 + col16, from one read).
+    ``dual:R,C[,act|weight]`` (row + colsr, or row16 + col16, from one read),
+    ``given:R,C[,mode]`` (one-pass quantiser with a supplied amax) or
+    ``gemmq:M,N,K[,nod]`` (GEMM whose epilogue also quantises D along N under
+    a supplied amax; ``nod``: D itself is not stored).
     Prints a JSON line with the mean time per call over --steps calls."""
     import torch
 
@@ -470,6 +473,30 @@ def run_case(args):
         def call():
             nv.nvfp4_gemm(qa, qb, nv.NVFP4_OUT_BF16, d=d, workspace=ws)
         work, unit = 2.0 * M * N * K / 1e12, "TFLOP/s"
+    elif kind == "gemmq":
+        M, N, K = (int(v) for v in parts[:3])
+        store_d = not (len(parts) > 3 and parts[3] == "nod")
+        qa = nv.nvfp4_quantize(syn.normal_bf16((M, K), seed=1).to(dev), nv.quant_cfg())
+        qb = nv.nvfp4_quantize(syn.normal_bf16((N, K), seed=2).to(dev), nv.quant_cfg())
+        amax_in = torch.full((1,), 40.0, dtype=torch.float32, device=dev)
+        amax_out = torch.zeros(1, dtype=torch.float32, device=dev)
+        d, q = nv.nvfp4_gemm_quantize(qa, qb, amax_in, store_d=store_d, amax_out=amax_out)
+        ws = torch.zeros(4096, dtype=torch.uint8, device=dev)
+
+        def call():
+            nv.nvfp4_gemm_quantize(qa, qb, amax_in, d=d, store_d=store_d, amax_out=amax_out, out=q, workspace=ws)
+        work, unit = 2.0 * M * N * K / 1e12, "TFLOP/s"
+    elif kind == "given":
+        R, C = int(parts[0]), int(parts[1])
+        cfg = modes[parts[2] if len(parts) > 2 else "row"]
+        x = syn.normal_bf16((R, C), seed=3).to(dev)
+        amax_in = x.abs().max().float().reshape(1)
+        out = nv.nvfp4_quantize_given_amax(x, cfg, amax_in)
+        ws = torch.zeros(nv.nvfp4_quantize_workspace_size(R, C, cfg), dtype=torch.uint8, device=dev)
+
+        def call():
+            nv.nvfp4_quantize_given_amax(x, cfg, amax_in, out=out, workspace=ws)
+        work, unit = R * C * QUANT_BYTES_PER_ELT / 1e9, "GB/s"
     elif kind == "dual":
         R, C = int(parts[0]), int(parts[1])
         pair = {"act": (modes["row"], modes["colsr"]), "weight": (modes["row16"], modes["col16"])}

@@ -32,9 +32,9 @@ NVFP4_LINEAR_FPROP, NVFP4_LINEAR_DGRAD, NVFP4_LINEAR_WGRAD = 0, 1, 2
 # Every exported symbol of include/nvfp4.h.
 EXPORTS = [
     "nvfp4_status_string", "nvfp4_version", "nvfp4_codes_bytes", "nvfp4_sf_bytes",
-    "nvfp4_quantize_workspace_size", "nvfp4_quantize", "nvfp4_quantize_dual", "nvfp4_quantize_noalloc",
-    "nvfp4_dequantize",
-    "nvfp4_gemm_workspace_size", "nvfp4_gemm", "nvfp4_linear_workspace_size",
+    "nvfp4_quantize_workspace_size", "nvfp4_quantize", "nvfp4_quantize_dual", "nvfp4_quantize_given_amax",
+    "nvfp4_quantize_noalloc", "nvfp4_dequantize",
+    "nvfp4_gemm_workspace_size", "nvfp4_gemm", "nvfp4_gemm_quantize", "nvfp4_linear_workspace_size",
     "nvfp4_linear_fprop", "nvfp4_linear_dgrad", "nvfp4_linear_wgrad",
     "nvfp4_check_device_status", "nvfp4_debug_gemm_skip_load",
 ]
@@ -80,6 +80,19 @@ class _Tensor(ctypes.Structure):
     ]
 
 
+class _QuantOut(ctypes.Structure):
+    """nvfp4_quant_out."""
+    _fields_ = [
+        ("amax_in", ctypes.c_void_p),
+        ("amax_out", ctypes.c_void_p),
+        ("codes", ctypes.c_void_p),
+        ("sf", ctypes.c_void_p),
+        ("tensor_scale", ctypes.c_void_p),
+        ("sf_layout", ctypes.c_int32),
+        ("reserved", ctypes.c_int32),
+    ]
+
+
 @dataclass
 class NVFP4Tensor:
     """A quantised operand Q [rows, k] held in torch device buffers."""
@@ -117,10 +130,12 @@ def lib():
             "nvfp4_quantize_workspace_size": (I32, [I64, I64, PCFG, PSZ]),
             "nvfp4_quantize": (I32, [P, I64, I64, I64, PCFG, P, P, P, P, SZ, P]),
             "nvfp4_quantize_dual": (I32, [P, I64, I64, I64, PCFG, P, P, P, PCFG, P, P, P, P, SZ, P]),
+            "nvfp4_quantize_given_amax": (I32, [P, I64, I64, I64, PCFG, P, P, P, P, P, SZ, P]),
             "nvfp4_quantize_noalloc": (I32, [P, I64, I64, I64, PCFG, P, P, P, P]),
             "nvfp4_dequantize": (I32, [PT, I32, P, I64, P]),
             "nvfp4_gemm_workspace_size": (I32, [I64, I64, I64, PSZ]),
             "nvfp4_gemm": (I32, [PT, PT, I32, P, I64, P, SZ, P]),
+            "nvfp4_gemm_quantize": (I32, [PT, PT, P, I64, ctypes.POINTER(_QuantOut), P, SZ, P]),
             "nvfp4_linear_workspace_size": (I32, [I32, I64, I64, I64, PSZ]),
             "nvfp4_linear_fprop": (I32, [P, P, I64, I64, I64, PCFG, PCFG, I32, P, P, SZ, P]),
             "nvfp4_linear_dgrad": (I32, [P, P, I64, I64, I64, PCFG, PCFG, I32, P, P, SZ, P]),
@@ -226,6 +241,24 @@ def nvfp4_quantize_dual(x, cfg_a, cfg_b, out_a=None, out_b=None, workspace=None,
     return out_a, out_b
 
 
+def nvfp4_quantize_given_amax(x, cfg, amax, out=None, workspace=None, stream=None):
+    """Delayed scaling (see include/nvfp4.h): quantise x with the tensor
+    scale amax[0] / 2688, amax a float32 CUDA tensor; one read of x."""
+    assert x.dtype == torch.bfloat16 and x.dim() == 2 and x.stride(1) == 1
+    assert amax.dtype == torch.float32 and amax.is_cuda
+    rows, cols = x.shape
+    if out is None:
+        out = nvfp4_empty(x, cfg)
+    if workspace is None:
+        workspace = _alloc_ws(nvfp4_quantize_workspace_size(rows, cols, cfg), x.device)
+    ldx = x.stride(0) if rows > 1 else cols
+    st = lib().nvfp4_quantize_given_amax(_ptr(x), rows, cols, ldx, ctypes.byref(cfg), _ptr(amax), _ptr(out.codes),
+                                         _ptr(out.sf), _ptr(out.tensor_scale), _ptr(workspace), workspace.numel(),
+                                         _stream(stream))
+    _check(st, "nvfp4_quantize_given_amax")
+    return out
+
+
 def nvfp4_quantize_noalloc(x, cfg, out, stream=None):
     """Scratch-free quantisation (see include/nvfp4.h): `out` is a
     preallocated NVFP4Tensor; the library allocates nothing."""
@@ -268,6 +301,33 @@ def nvfp4_gemm(a, b, out_dtype=NVFP4_OUT_BF16, d=None, workspace=None, stream=No
                           workspace.numel(), _stream(stream))
     _check(st, "nvfp4_gemm")
     return d
+
+
+def nvfp4_gemm_quantize(a, b, amax_in, sf_layout=NVFP4_SF_MMA, d=None, store_d=True, amax_out=None, out=None,
+                        workspace=None, stream=None):
+    """D [a.rows, b.rows] = A * B^T (BF16) and its NVFP4 quantisation along N
+    (1x16, round to nearest even) under the tensor scale amax_in[0] / 2688,
+    from the GEMM's epilogue (see include/nvfp4.h).  amax_out, if given,
+    receives max |D|.  Returns (d or None, NVFP4Tensor)."""
+    M, N = a.rows, b.rows
+    dev = a.codes.device
+    if d is None and store_d:
+        d = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+    if out is None:
+        out = NVFP4Tensor(codes=torch.empty((M, N // 2), dtype=torch.uint8, device=dev),
+                          sf=torch.empty(max(nvfp4_sf_bytes(M, N, sf_layout), 1), dtype=torch.uint8, device=dev),
+                          tensor_scale=torch.empty(1, dtype=torch.float32, device=dev),
+                          rows=M, k=N, sf_layout=sf_layout)
+    if workspace is None:
+        workspace = _alloc_ws(nvfp4_gemm_workspace_size(M, N, a.k), dev)
+    ta, tb = a._c(), b._c()
+    q = _QuantOut(amax_in.data_ptr(), amax_out.data_ptr() if amax_out is not None else None, out.codes.data_ptr(),
+                  out.sf.data_ptr(), out.tensor_scale.data_ptr(), out.sf_layout, 0)
+    ldd = d.stride(0) if d is not None and d.shape[0] > 1 else N
+    st = lib().nvfp4_gemm_quantize(ctypes.byref(ta), ctypes.byref(tb), _ptr(d), ldd, ctypes.byref(q),
+                                   _ptr(workspace), workspace.numel(), _stream(stream))
+    _check(st, "nvfp4_gemm_quantize")
+    return d, out
 
 
 def nvfp4_linear_workspace_size(op, tokens, din, dout):

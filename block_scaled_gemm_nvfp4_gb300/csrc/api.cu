@@ -256,6 +256,30 @@ nvfp4_status nvfp4_quantize_dual(const void* x, int64_t rows, int64_t cols, int6
   return cuda_status(launch_quantize(a, reinterpret_cast<cudaStream_t>(stream)));
 }
 
+nvfp4_status nvfp4_quantize_given_amax(const void* x, int64_t rows, int64_t cols, int64_t ldx,
+                                       const nvfp4_quant_cfg* cfg, const float* amax, void* codes, void* sf,
+                                       float* tensor_scale, void* workspace, size_t workspace_bytes,
+                                       nvfp4_stream_t stream) {
+  nvfp4_status s = check_quant_call(x, rows, cols, ldx, cfg, codes, sf, tensor_scale);
+  if (s != NVFP4_OK) return s;
+  if (!amax) return NVFP4_ERR_INVALID_ARG;
+  if (!workspace) return NVFP4_ERR_WORKSPACE;
+  if (workspace_bytes < quant_ws_bytes()) return NVFP4_ERR_WORKSPACE;
+  if (reinterpret_cast<uintptr_t>(workspace) & 255u) return NVFP4_ERR_INVALID_ARG;
+  QuantArgs a{};
+  a.x = static_cast<const uint16_t*>(x);
+  a.rows = rows;
+  a.cols = cols;
+  a.ldx = ldx;
+  a.n_out = 1;
+  a.out[0] = make_out(*cfg, codes, sf, tensor_scale);
+  a.out[0].amax_in = amax;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  a.status = reinterpret_cast<uint32_t*>(ws);
+  a.partials = reinterpret_cast<uint32_t*>(ws + kWsHeaderBytes);
+  return cuda_status(launch_quantize(a, reinterpret_cast<cudaStream_t>(stream)));
+}
+
 nvfp4_status nvfp4_quantize_noalloc(const void* x, int64_t rows, int64_t cols, int64_t ldx,
                                     const nvfp4_quant_cfg* cfg, void* codes, void* sf, float* tensor_scale,
                                     nvfp4_stream_t stream) {
@@ -320,6 +344,59 @@ nvfp4_status nvfp4_gemm(const nvfp4_tensor* a, const nvfp4_tensor* b, int32_t ou
   if (workspace_bytes < kWsHeaderBytes) return NVFP4_ERR_WORKSPACE;
   return gemm_into(a, b, out_dtype, d, ldd, static_cast<uint32_t*>(workspace),
                    reinterpret_cast<cudaStream_t>(stream));
+}
+
+nvfp4_status nvfp4_gemm_quantize(const nvfp4_tensor* a, const nvfp4_tensor* b, void* d, int64_t ldd,
+                                 const nvfp4_quant_out* q, void* workspace, size_t workspace_bytes,
+                                 nvfp4_stream_t stream) {
+  nvfp4_status s = check_tensor(a);
+  if (s != NVFP4_OK) return s;
+  s = check_tensor(b);
+  if (s != NVFP4_OK) return s;
+  if (!q || q->reserved != 0 || !q->amax_in || !q->tensor_scale) return NVFP4_ERR_INVALID_ARG;
+  if (q->sf_layout != NVFP4_SF_ROWMAJOR && q->sf_layout != NVFP4_SF_MMA) return NVFP4_ERR_INVALID_ARG;
+  if (a->k != b->k) return NVFP4_ERR_INVALID_ARG;
+  if (a->k % 32 != 0 || a->k == 0) return NVFP4_ERR_UNSUPPORTED_SHAPE;
+  if (a->sf_layout != NVFP4_SF_MMA || b->sf_layout != NVFP4_SF_MMA) return NVFP4_ERR_UNSUPPORTED_SHAPE;
+  if (a->rows > (int64_t(1) << 31) || b->rows > (int64_t(1) << 31) || a->k > (int64_t(1) << 31))
+    return NVFP4_ERR_UNSUPPORTED_SHAPE;
+  if (b->rows % 32 != 0) return NVFP4_ERR_UNSUPPORTED_SHAPE;  // N: whole 16-byte code pieces per 32 columns
+  if (a->rows == 0 || b->rows == 0) return NVFP4_OK;
+  if (d && ldd < b->rows) return NVFP4_ERR_INVALID_ARG;
+  if (!q->codes || !q->sf || !aligned16(q->codes)) return NVFP4_ERR_INVALID_ARG;
+  if (q->sf_layout == NVFP4_SF_MMA && !aligned16(q->sf)) return NVFP4_ERR_INVALID_ARG;
+  if (q->amax_out && (reinterpret_cast<uintptr_t>(q->amax_out) & 3u)) return NVFP4_ERR_INVALID_ARG;
+  if (!aligned16(a->codes) || !aligned16(b->codes) || !aligned16(a->sf) || !aligned16(b->sf))
+    return NVFP4_ERR_INVALID_ARG;
+  if (!workspace) return NVFP4_ERR_WORKSPACE;
+  if (workspace_bytes < kWsHeaderBytes) return NVFP4_ERR_WORKSPACE;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (q->amax_out && cudaMemsetAsync(q->amax_out, 0, sizeof(float), st) != cudaSuccess) return NVFP4_ERR_CUDA;
+  GemmArgs g{};
+  g.a_codes = static_cast<const uint8_t*>(a->codes);
+  g.a_sf = static_cast<const uint8_t*>(a->sf);
+  g.a_scale = a->tensor_scale;
+  g.b_codes = static_cast<const uint8_t*>(b->codes);
+  g.b_sf = static_cast<const uint8_t*>(b->sf);
+  g.b_scale = b->tensor_scale;
+  g.M = a->rows;
+  g.N = b->rows;
+  g.K = a->k;
+  g.out_f32 = 0;
+  g.d = d;
+  g.ldd = d ? ldd : b->rows;
+  g.status = static_cast<uint32_t*>(workspace);
+  g.skip_first_load = g_skip_load_once.exchange(0);
+  g.quant = 1;
+  g.q_codes = static_cast<uint8_t*>(q->codes);
+  g.q_sf = static_cast<uint8_t*>(q->sf);
+  g.q_tensor_scale = q->tensor_scale;
+  g.q_amax_in = q->amax_in;
+  g.q_amax_out = q->amax_out;
+  g.q_sf_mma = q->sf_layout == NVFP4_SF_MMA;
+  const cudaError_t e = launch_gemm(g, st);
+  if (e == cudaErrorInvalidValue) return NVFP4_ERR_INVALID_ARG;
+  return cuda_status(e);
 }
 
 // ------------------------------------------------------------ linear layer

@@ -1,0 +1,68 @@
+// NVFP4 encoding steps shared by the quantiser and the GEMM's quantising
+// epilogue: the E4M3 block scale of a run of 16 and the exact element
+// division that precedes rounding onto the E2M1 grid.
+//
+//   t = (bamax / 6) / s -> E4M3 (round to nearest even, saturating at 448),
+//   d = e4m3(t) * s,  v = x / d (IEEE quotient).
+//
+// Every FP32 step is written as an explicit round-to-nearest intrinsic, so the
+// results do not depend on the translation unit's contraction setting.
+#pragma once
+
+#include <cstdint>
+
+#include "ptx.cuh"
+
+namespace nvfp4 {
+
+// E4M3 block-scale byte of a run whose largest magnitude has FP32 bits
+// `bamax_bits`, under the FP32 tensor scale s_dec.
+__device__ __forceinline__ uint32_t block_scale_byte(uint32_t bamax_bits, float s_dec) {
+  return ptx::cvt_e4m3(__fdiv_rn(__fdiv_rn(__uint_as_float(bamax_bits), 6.0f), s_dec));
+}
+
+// x / d for 2^-70 <= d < 2^126, given rd = RN(1/d): q0 = RN(x * rd) is
+// within one ulp of x / d, and one residual correction q0 + RN(x - q0 d) * rd
+// with an exact FMA residual rounds to the IEEE quotient (Markstein's
+// division theorem; P. Markstein, "Computation of elementary functions on
+// the IBM RISC System/6000 processor", IBM J. Res. Dev. 34, 1990), as long
+// as nothing underflows: |x| >= 2^-96 and |q| >= 2^-100.  Outside that range
+// the quotient is below 2^-25, where an RNE code is +-0 whatever its exact
+// value and stochastic rounding only asks whether it is zero (divide_run
+// keeps that answer exact by its choice of path).
+__device__ __forceinline__ float div_fast(float x, float d, float rd) {
+  const float q0 = __fmul_rn(x, rd);
+  // (q0 d - x) is the negated residual; q0 - that * rd keeps the sign of a
+  // zero x: for x = -0 both terms are -0, and the sum of two -0 is -0.
+  return __fmaf_rn(-__fmaf_rn(q0, d, -x), rd, q0);
+}
+
+// q[j] = v[j] / d wherever the quotient can change a code.  Fast division
+// where it is exact for every code (see div_fast): d in [2^-70, 2^126) for
+// round-to-nearest.  Stochastic rounding (SR) also needs the zero-ness of
+// quotients below 2^-25: every nonzero input (a BF16 value, or a transform of
+// BF16 values) is at least 2^-135 in magnitude, so for d < 2^14 every such
+// quotient and its fast approximation are nonzero.  Elsewhere IEEE division.
+template <bool SR>
+__device__ __forceinline__ void divide_run(const float (&v)[16], float d, float (&q)[16]) {
+  const bool fast = d >= 0x1p-70f && d < (SR ? 0x1p14f : 0x1p126f);
+  if (fast) {
+    const float rd = __frcp_rn(d);
+#pragma unroll
+    for (int j = 0; j < 16; ++j) q[j] = div_fast(v[j], d, rd);
+  } else {
+#pragma unroll
+    for (int j = 0; j < 16; ++j) q[j] = __fdiv_rn(v[j], d);
+  }
+}
+
+// Largest |v| of a run as FP32 bits, with NaN propagated (max.NaN), so that
+// a non-finite run shows as bits >= 0x7F800000.
+__device__ __forceinline__ uint32_t run_absmax_nan(const float (&v)[16]) {
+  float m = 0.0f;
+#pragma unroll
+  for (int j = 0; j < 16; ++j) asm("max.NaN.f32 %0, %0, %1;" : "+f"(m) : "f"(fabsf(v[j])));
+  return __float_as_uint(m);
+}
+
+}  // namespace nvfp4

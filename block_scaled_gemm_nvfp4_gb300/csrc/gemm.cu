@@ -50,6 +50,7 @@
 #include <cstdint>
 #include <mutex>
 
+#include "encode.cuh"
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -141,6 +142,16 @@ struct GParams {
   int group_n;          // raster groups column blocks instead of row blocks
   int skip_first_load;  // test hook: CTA 0 never loads its first stage
   uint32_t* status;
+  // quantising epilogue (QUANT kernels): D's NVFP4 codes and block scales
+  // along N under the tensor scale amax_in / 2688
+  uint8_t* q_codes;
+  uint8_t* q_sf;
+  float* q_tensor_scale;
+  const float* q_amax_in;
+  uint32_t* q_amax_out;  // max |D| as FP32 bits, or null
+  int q_sf_mma;
+  int64_t q_kb_count;    // N / 16
+  int64_t q_katoms;      // 64-wide N atoms of the MMA scale layout
 };
 
 template <int STAGES, int SF_STAGES>
@@ -222,12 +233,76 @@ __device__ __forceinline__ void arrive_leader(uint64_t* bar, uint32_t rank) {
     ptx::mbar_arrive(bar);
 }
 
+// Quantising epilogue for this thread's 128 BF16 outputs of row `row`
+// (columns col0 .. col0 + 127, two per word of `packed`): eight runs of 16
+// along N, each with its E4M3 block scale and E2M1 codes (round to nearest
+// even) under the tensor scale s_dec -- the quantiser's steps applied to the
+// BF16 values D holds, so the result equals quantising the stored D.  Rows
+// past M and blocks past N are not encoded; in the tensor-core scale layout
+// their scale bytes are written as the layout's zero padding.  Returns the
+// largest |value| of the valid runs as FP32 bits (NaN propagated).
+__device__ __forceinline__ uint32_t quantize_half(const GParams& p, const uint32_t (&packed)[kEpiCols / 2],
+                                                  int64_t row, int64_t col0, int q, int lane, float s_dec) {
+  const int64_t kb0 = col0 / 16;  // a multiple of 8
+  const bool row_ok = row < p.M;
+  uint32_t sfw[2] = {0u, 0u};     // block kb0 + j in byte (j & 3) of word j >> 2
+  uint32_t amax_bits = 0;
+  uint8_t* crow = p.q_codes + row * (p.N / 2) + col0 / 2;
+#pragma unroll
+  for (int r2 = 0; r2 < kEpiCols / 32; ++r2) {
+    // two runs, 32 columns: one 16-byte store of codes (N % 32 == 0, so the
+    // pair is either wholly inside N or wholly outside)
+    const bool in = row_ok && kb0 + 2 * r2 < p.q_kb_count;
+    uint32_t c[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int r = 2 * r2 + h;
+      float v[16];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const uint32_t w = packed[r * 8 + j];
+        v[2 * j] = __uint_as_float(w << 16);
+        v[2 * j + 1] = __uint_as_float(w & 0xFFFF0000u);
+      }
+      const uint32_t m = run_absmax_nan(v);
+      const uint32_t sfb = in ? block_scale_byte(m, s_dec) : 0u;
+      if (in) amax_bits = max(amax_bits, m);
+      if (sfb != 0) {
+        divide_run<false>(v, __fmul_rn(ptx::e4m3_to_float(sfb), s_dec), v);  // elementwise, in place
+        c[2 * h] = ptx::cvt_e2m1x8(v[0], v[1], v[2], v[3], v[4], v[5], v[6], v[7]);
+        c[2 * h + 1] = ptx::cvt_e2m1x8(v[8], v[9], v[10], v[11], v[12], v[13], v[14], v[15]);
+      }
+      sfw[r >> 2] |= sfb << (8 * (r & 3));
+    }
+    if (in) __stcs(reinterpret_cast<uint4*>(crow + 16 * r2), make_uint4(c[0], c[1], c[2], c[3]));
+  }
+  if (p.q_sf_mma) {
+    // atoms of 128 rows x 4 blocks: this thread's four blocks of an atom are
+    // the 4-byte word at lane * 16 + q * 4 (row % 32 = lane, row % 128 / 32 = q).
+    // In pair mode with an odd number of row blocks the follower's last tile
+    // lies wholly past M: its row atom does not exist and is not written.
+    const bool atom_row_ok = row / BM < p.tiles_m;
+#pragma unroll
+    for (int a = 0; a < 2; ++a) {
+      const int64_t katom = kb0 / 4 + a;
+      if (atom_row_ok && katom < p.q_katoms)
+        *reinterpret_cast<uint32_t*>(p.q_sf + ((row / BM) * p.q_katoms + katom) * 512 + lane * 16 + q * 4) = sfw[a];
+    }
+  } else if (row_ok) {
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+      if (kb0 + j < p.q_kb_count) p.q_sf[row * p.q_kb_count + kb0 + j] = static_cast<uint8_t>(sfw[j >> 2] >> (8 * (j & 3)));
+  }
+  return amax_bits;
+}
+
 // Epilogue for one 128 x 128 half of a tile: TMEM -> registers -> global.
 // The warp's lane quarter q gives its 32 rows.  Releases the accumulator (one
 // arrival per warp on the leader's acc_empty) as soon as it has been read.
-template <bool OUT_F32, bool PAIR>
+template <bool OUT_F32, bool PAIR, bool QUANT>
 __device__ __forceinline__ void epilogue_half(const GParams& p, uint64_t* acc_empty, uint32_t tmem, int m_blk,
-                                              int n_blk, int q, int half, int lane, float alpha, uint32_t rank) {
+                                              int n_blk, int q, int half, int lane, float alpha, uint32_t rank,
+                                              float s_dec, uint32_t& amax_bits) {
   const int64_t row = static_cast<int64_t>(m_blk) * BM + q * 32 + lane;
   const int64_t col0 = static_cast<int64_t>(n_blk) * BN + half * kEpiCols;
   const uint32_t taddr = tmem + (static_cast<uint32_t>(q * 32) << 16) + kAccCol + half * kEpiCols;
@@ -246,7 +321,7 @@ __device__ __forceinline__ void epilogue_half(const GParams& p, uint64_t* acc_em
     ptx::tc_fence_before();
     __syncwarp();
     if (lane == 0) arrive_leader<PAIR>(acc_empty, rank);
-    if (row < p.M) {
+    if (row < p.M && p.d != nullptr) {  // D is optional for the quantising epilogue
       __nv_bfloat16* drow = static_cast<__nv_bfloat16*>(p.d) + row * p.ldd;
 #pragma unroll
       for (int c8 = 0; c8 < kEpiCols / 8; ++c8) {
@@ -266,6 +341,7 @@ __device__ __forceinline__ void epilogue_half(const GParams& p, uint64_t* acc_em
         }
       }
     }
+    if constexpr (QUANT) amax_bits = max(amax_bits, quantize_half(p, packed, row, col0, q, lane, s_dec));
   } else {
     float* drow = static_cast<float*>(p.d) + row * p.ldd;
 #pragma unroll 1
@@ -336,7 +412,7 @@ __device__ __forceinline__ void stage_scales(const uint8_t* sfa, const uint8_t* 
   ptx::tmem_st_32x32b_x32(lane_base + kSfbCol + slot * 32, vb);
 }
 
-template <bool OUT_F32, bool PAIR>
+template <bool OUT_F32, bool PAIR, bool QUANT>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
                 const GParams p) {
@@ -646,6 +722,27 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int q = warp & 3;              // TMEM lane quarter this warp may access
     const int half = (warp - 2) >> 2;    // which 128 columns of the tile it stores
     const float alpha = __fmul_rn(*p.a_scale, *p.b_scale);
+    // quantising epilogue: tensor scale s = amax_in / 2688 (1 if that is
+    // zero); a negative or non-finite amax_in is reported and nothing is
+    // encoded
+    float s_dec = 1.0f;
+    bool q_live = true;
+    uint32_t amax_bits = 0;
+    if (QUANT) {
+      const float a_in = *p.q_amax_in;
+      const bool first = blockIdx.x == 0 && threadIdx.x == 64;  // warp 2, lane 0
+      if (!(a_in >= 0.0f) || isinf(a_in)) {
+        q_live = false;
+        if (first) {
+          ptx::set_status(p.status, kDevNonFinite);
+          *p.q_tensor_scale = __uint_as_float(0x7FC00000u);
+        }
+      } else {
+        s_dec = __fdiv_rn(fabsf(a_in), 2688.0f);
+        if (s_dec == 0.0f) s_dec = 1.0f;
+        if (first) *p.q_tensor_scale = s_dec;
+      }
+    }
     uint32_t acc_phase = 0;
     for (int unit = unit0; unit < p.num_units; unit += ustep) {
       int m_blk, n_blk;
@@ -655,8 +752,28 @@ __global__ void __launch_bounds__(kThreads, 1)
         break;
       }
       ptx::tc_fence_after();
-      epilogue_half<OUT_F32, PAIR>(p, &ctl->acc_empty, tmem, m_blk, n_blk, q, half, lane, alpha, rank);
+      if constexpr (QUANT) {
+        if (q_live)
+          epilogue_half<OUT_F32, PAIR, true>(p, &ctl->acc_empty, tmem, m_blk, n_blk, q, half, lane, alpha, rank,
+                                             s_dec, amax_bits);
+        else
+          epilogue_half<OUT_F32, PAIR, false>(p, &ctl->acc_empty, tmem, m_blk, n_blk, q, half, lane, alpha, rank,
+                                              s_dec, amax_bits);
+      } else {
+        epilogue_half<OUT_F32, PAIR, false>(p, &ctl->acc_empty, tmem, m_blk, n_blk, q, half, lane, alpha, rank,
+                                            s_dec, amax_bits);
+      }
       acc_phase ^= 1u;
+    }
+    if (QUANT && q_live) {
+      // the lanes of a warp leave the loop above together (warp_wait is
+      // warp-uniform), so the shuffles below see the whole warp
+      if (amax_bits >= 0x7F800000u) ptx::set_status(p.status, kDevNonFinite);  // D overflowed
+      if (p.q_amax_out) {
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) amax_bits = max(amax_bits, __shfl_xor_sync(0xFFFFFFFFu, amax_bits, o));
+        if (lane == 0) atomicMax(p.q_amax_out, amax_bits);
+      }
     }
   }
 
@@ -698,12 +815,12 @@ cudaLaunchAttribute pair_cluster_attr() {
   return attr;
 }
 
-template <bool OUT_F32, bool PAIR>
+template <bool OUT_F32, bool PAIR, bool QUANT>
 cudaError_t launch_typed(const CUtensorMap& ma, const CUtensorMap& mb, GParams p, cudaStream_t stream) {
   using L = Layout<PAIR>;
   static bool configured = false;
   static int max_clusters = 0;
-  auto kernel = gemm_kernel<OUT_F32, PAIR>;
+  auto kernel = gemm_kernel<OUT_F32, PAIR, QUANT>;
   if (!configured) {
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmemBytes);
     if (e != cudaSuccess) return e;
@@ -783,8 +900,22 @@ cudaError_t launch_gemm(const GemmArgs& a, cudaStream_t stream) {
   }
   const size_t esz = a.out_f32 ? 4 : 2;
   p.vec_store = (reinterpret_cast<uintptr_t>(a.d) % 16 == 0) && ((a.ldd * esz) % 16 == 0);
-  if (pair) return a.out_f32 ? launch_typed<true, true>(ma, mb, p, stream) : launch_typed<false, true>(ma, mb, p, stream);
-  return a.out_f32 ? launch_typed<true, false>(ma, mb, p, stream) : launch_typed<false, false>(ma, mb, p, stream);
+  if (a.quant) {
+    // BF16 output only; N % 32 == 0 and 16-byte aligned codes (checked by the caller)
+    if (a.out_f32) return cudaErrorInvalidValue;
+    p.q_codes = a.q_codes;
+    p.q_sf = a.q_sf;
+    p.q_tensor_scale = a.q_tensor_scale;
+    p.q_amax_in = a.q_amax_in;
+    p.q_amax_out = reinterpret_cast<uint32_t*>(a.q_amax_out);
+    p.q_sf_mma = a.q_sf_mma;
+    p.q_kb_count = a.N / 16;
+    p.q_katoms = (p.q_kb_count + 3) / 4;
+    return pair ? launch_typed<false, true, true>(ma, mb, p, stream) : launch_typed<false, false, true>(ma, mb, p, stream);
+  }
+  if (pair)
+    return a.out_f32 ? launch_typed<true, true, false>(ma, mb, p, stream) : launch_typed<false, true, false>(ma, mb, p, stream);
+  return a.out_f32 ? launch_typed<true, false, false>(ma, mb, p, stream) : launch_typed<false, false, false>(ma, mb, p, stream);
 }
 
 }  // namespace nvfp4

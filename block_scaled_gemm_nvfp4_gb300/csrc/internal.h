@@ -28,6 +28,7 @@ struct QuantOut {
   uint8_t* codes;
   uint8_t* sf;
   float* tensor_scale;
+  const float* amax_in;  // device; null: the amax pass scans the operand
 };
 
 // One read of x [rows, cols] (row-major, leading dimension ldx) produces
@@ -74,6 +75,14 @@ struct GemmArgs {
   int64_t ldd;
   uint32_t* status;
   int skip_first_load;  // failure-detection test hook (see nvfp4_debug_gemm_skip_load)
+  // quantising epilogue (nvfp4_gemm_quantize): D's codes and block scales
+  int quant;
+  uint8_t* q_codes;
+  uint8_t* q_sf;
+  float* q_tensor_scale;
+  const float* q_amax_in;
+  float* q_amax_out;
+  int q_sf_mma;
 };
 
 cudaError_t launch_gemm(const GemmArgs& a, cudaStream_t stream);

@@ -44,6 +44,7 @@
 #include <cstdint>
 #include <mutex>
 
+#include "encode.cuh"
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -71,6 +72,7 @@ struct OutParams {
   uint8_t* sf;
   float* tensor_scale;
   uint32_t* partials;
+  const float* amax_in;  // supplied amax (delayed scaling), or null: scan the operand
   int64_t qr, qk, code_ld, kb_count, katoms;
   uint64_t rht_seed, sr_seed, sr_offset;
   // Philox key schedule of sr_seed, one pair per round (parameter space, so
@@ -144,31 +146,6 @@ __device__ __forceinline__ uint32_t run_absmax_bits(const float (&v)[16]) {
   return m;
 }
 
-// Largest |v| of a run of finite values, as FP32 bits (for non-negative
-// floats the order of the values is the order of their bits).
-__device__ __forceinline__ uint32_t run_absmax_finite(const float (&v)[16]) {
-  float m = 0.0f;
-#pragma unroll
-  for (int j = 0; j < 16; ++j) m = fmaxf(m, fabsf(v[j]));
-  return __float_as_uint(m);
-}
-
-// x / d for 2^-70 <= d < 2^126, given rd = RN(1/d): q0 = RN(x * rd) is
-// within one ulp of x / d, and one residual correction q0 + RN(x - q0 d) * rd
-// with an exact FMA residual rounds to the IEEE quotient (Markstein's
-// division theorem; P. Markstein, "Computation of elementary functions on
-// the IBM RISC System/6000 processor", IBM J. Res. Dev. 34, 1990), as long
-// as nothing underflows: |x| >= 2^-96 and |q| >= 2^-100.  Outside that range
-// the quotient is below 2^-25, where an RNE code is +-0 whatever its exact
-// value and stochastic rounding only asks whether it is zero (encode_run
-// keeps that answer exact by its choice of path).
-__device__ __forceinline__ float div_fast(float x, float d, float rd) {
-  const float q0 = __fmul_rn(x, rd);
-  // (q0 d - x) is the negated residual; q0 - that * rd keeps the sign of a
-  // zero x: for x = -0 both terms are -0, and the sum of two -0 is -0.
-  return __fmaf_rn(-__fmaf_rn(q0, d, -x), rd, q0);
-}
-
 // Stochastic rounding of q onto the E2M1 grid {0, .5, 1, 1.5, 2, 3, 4, 6}:
 // lo, hi the grid points around |q|, f = (|q| - lo) / (hi - lo), round up iff
 // k * 2^-24 < f with k = r >> 8; |q| >= 6 -> 6.  Branch-free:
@@ -197,25 +174,10 @@ __device__ __forceinline__ float sr_round(float q, uint32_t rnd) {
 template <bool SR>
 __device__ __forceinline__ uint2 encode_run(const float (&v)[16], uint32_t bamax_bits, float s_dec, uint64_t e0,
                                             const OutParams& o, uint32_t& sfb) {
-  const float t = __fdiv_rn(__fdiv_rn(__uint_as_float(bamax_bits), 6.0f), s_dec);
-  sfb = ptx::cvt_e4m3(t);
+  sfb = block_scale_byte(bamax_bits, s_dec);
   if (sfb == 0) return make_uint2(0u, 0u);
-  const float d = __fmul_rn(ptx::e4m3_to_float(sfb), s_dec);
   float q[16];
-  // Fast division where it is exact for every code (see div_fast): d in
-  // [2^-70, 2^126) for RNE.  Stochastic rounding also needs the zero-ness of
-  // quotients below 2^-25: every nonzero input (a BF16 value, or a transform
-  // of BF16 values) is at least 2^-135 in magnitude, so for d < 2^14 every
-  // such quotient and its fast approximation are nonzero.
-  const bool fast = d >= 0x1p-70f && d < (SR ? 0x1p14f : 0x1p126f);
-  if (fast) {
-    const float rd = __frcp_rn(d);
-#pragma unroll
-    for (int j = 0; j < 16; ++j) q[j] = div_fast(v[j], d, rd);
-  } else {
-#pragma unroll
-    for (int j = 0; j < 16; ++j) q[j] = __fdiv_rn(v[j], d);
-  }
+  divide_run<SR>(v, __fmul_rn(ptx::e4m3_to_float(sfb), s_dec), q);
   if (SR) {
     const uint32_t o0 = static_cast<uint32_t>(o.sr_offset), o1 = static_cast<uint32_t>(o.sr_offset >> 32);
     const uint64_t c = e0 >> 2;
@@ -294,7 +256,7 @@ __device__ __forceinline__ int stg_sf_offset(int p, int j) {
 
 template <bool COL, bool SR>
 __device__ __forceinline__ void encode_tile(const uint8_t* stage, uint8_t* stg, const OutParams& o, float s_dec,
-                                            uint32_t rht_mask, int64_t tr, int64_t tc) {
+                                            uint32_t rht_mask, int64_t tr, int64_t tc, uint32_t* status) {
   const int p = threadIdx.x & 127, j0 = threadIdx.x >> 7;
   const int64_t qrow = (COL ? tc : tr) * kTile + p;
   const int64_t kb0 = (COL ? tr : tc) * 8;
@@ -306,11 +268,15 @@ __device__ __forceinline__ void encode_tile(const uint8_t* stage, uint8_t* stg, 
     float v[16];
     load_run<COL>(stage, p, j, v);
     if (o.rht) rht16(v, rht_mask);
-    uint32_t m = run_absmax_finite(v);  // the amax pass has ruled out inf and NaN
+    // Inf and NaN were ruled out by the amax pass, except under a supplied
+    // amax, where the operand is not scanned first: a non-finite run is
+    // reported here (its codes are unspecified).
+    uint32_t m = run_absmax_nan(v);
     if (o.block2d) {
 #pragma unroll
       for (int x = 1; x < 16; x <<= 1) m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, x));
     }
+    if (m >= 0x7F800000u) ptx::set_status(status, kDevNonFinite);
     uint32_t sfb;
     const uint2 c = encode_run<SR>(v, m, s_dec, static_cast<uint64_t>(qrow * o.qk + (kb0 + j) * 16), o, sfb);
     *reinterpret_cast<uint2*>(stg + p * kStgPitch + 8 * j) = c;
@@ -395,10 +361,17 @@ __global__ void __launch_bounds__(kThreads, 2) quant_tiles(const __grid_constant
 #pragma unroll
     for (int o = 0; o < kMaxQuantOutputs; ++o) {
       if (o >= p.n_out) break;
-      const uint32_t* part = p.out[(o == 1 && p.amax_shared) ? 0 : o].partials;
       uint32_t m = 0;
-      for (int i = tid; i < p.num_partials; i += kThreads) m = max(m, part[i]);
-      m = block_max(m, red);
+      if (p.out[o].amax_in) {
+        // delayed scaling: a finite amax >= 0 from the caller (anything else
+        // is reported like a non-finite operand)
+        const float a = *p.out[o].amax_in;
+        m = (a >= 0.0f) ? __float_as_uint(fabsf(a)) : 0x7FC00000u;
+      } else {
+        const uint32_t* part = p.out[(o == 1 && p.amax_shared) ? 0 : o].partials;
+        for (int i = tid; i < p.num_partials; i += kThreads) m = max(m, part[i]);
+        m = block_max(m, red);
+      }
       if (m >= 0x7F800000u) {  // inf or NaN somewhere in the input
         live[o] = false;
         if (blockIdx.x == 0 && tid == 0) {
@@ -467,6 +440,7 @@ __global__ void __launch_bounds__(kThreads, 2) quant_tiles(const __grid_constant
       const OutParams& op = p.out[o];
       if (PASS == 0) {
         if (o == 1 && p.amax_shared) break;
+        if (op.amax_in) continue;
         // without the transform the orientation does not change the amax
         tmax[o] = max(tmax[o], (op.rht && op.col) ? amax_tile<true>(stage, true, rht_mask[o])
                                                    : amax_tile<false>(stage, op.rht != 0, rht_mask[o]));
@@ -474,14 +448,14 @@ __global__ void __launch_bounds__(kThreads, 2) quant_tiles(const __grid_constant
         uint8_t* so = stg + o * kStgBytes;
         if (op.col) {
           if (op.sr)
-            encode_tile<true, true>(stage, so, op, s_dec[o], rht_mask[o], tr, tc);
+            encode_tile<true, true>(stage, so, op, s_dec[o], rht_mask[o], tr, tc, p.status);
           else
-            encode_tile<true, false>(stage, so, op, s_dec[o], rht_mask[o], tr, tc);
+            encode_tile<true, false>(stage, so, op, s_dec[o], rht_mask[o], tr, tc, p.status);
         } else {
           if (op.sr)
-            encode_tile<false, true>(stage, so, op, s_dec[o], rht_mask[o], tr, tc);
+            encode_tile<false, true>(stage, so, op, s_dec[o], rht_mask[o], tr, tc, p.status);
           else
-            encode_tile<false, false>(stage, so, op, s_dec[o], rht_mask[o], tr, tc);
+            encode_tile<false, false>(stage, so, op, s_dec[o], rht_mask[o], tr, tc, p.status);
         }
       }
     }
@@ -506,7 +480,7 @@ __global__ void __launch_bounds__(kThreads, 2) quant_tiles(const __grid_constant
     for (int o = 0; o < kMaxQuantOutputs; ++o) {
       if (o >= p.n_out || (o == 1 && p.amax_shared)) break;
       const uint32_t m = block_max(tmax[o], red);
-      if (tid == 0) p.out[o].partials[blockIdx.x] = m;
+      if (tid == 0 && !p.out[o].amax_in) p.out[o].partials[blockIdx.x] = m;
     }
   }
 }
@@ -603,6 +577,7 @@ cudaError_t launch_quantize(const QuantArgs& a, cudaStream_t stream) {
     op.sf = q.sf;
     op.tensor_scale = q.tensor_scale;
     op.partials = a.partials + o * kPartialsPerOutput;
+    op.amax_in = q.amax_in;
     op.qr = q.transpose ? a.cols : a.rows;
     op.qk = q.transpose ? a.rows : a.cols;
     op.code_ld = op.qk / 2;
@@ -628,7 +603,9 @@ cudaError_t launch_quantize(const QuantArgs& a, cudaStream_t stream) {
     op.sf_mma = q.sf_mma;
     op.vec16 = (reinterpret_cast<uintptr_t>(q.codes) % 16 == 0) && (op.code_ld % 16 == 0);
   }
-  p.amax_shared = a.n_out == 2 && !a.out[0].rht && !a.out[1].rht;
+  p.amax_shared = a.n_out == 2 && !a.out[0].rht && !a.out[1].rht && !a.out[0].amax_in && !a.out[1].amax_in;
+  bool scan = false;  // the amax pass runs unless every output has a supplied amax
+  for (int o = 0; o < a.n_out; ++o) scan = scan || !a.out[o].amax_in;
 
   CUtensorMap xmap{};
   if (p.num_tiles > 0 && !make_x_map(&xmap, a.x, a.rows, a.cols, a.ldx)) return cudaErrorInvalidValue;
@@ -642,9 +619,11 @@ cudaError_t launch_quantize(const QuantArgs& a, cudaStream_t stream) {
   g = std::min<int64_t>(g, kPartialsPerOutput);
   g = std::max<int64_t>(std::min<int64_t>(g, p.num_tiles), 1);
   p.num_partials = static_cast<int>(g);
-  quant_tiles<0><<<static_cast<int>(g), kThreads, kSmemBytes, stream>>>(xmap, p);
-  err = cudaGetLastError();
-  if (err != cudaSuccess) return err;
+  if (scan) {
+    quant_tiles<0><<<static_cast<int>(g), kThreads, kSmemBytes, stream>>>(xmap, p);
+    err = cudaGetLastError();
+    if (err != cudaSuccess) return err;
+  }
   quant_tiles<1><<<static_cast<int>(g), kThreads, kSmemBytes, stream>>>(xmap, p);
   return cudaGetLastError();
 }

@@ -156,6 +156,29 @@ nvfp4_status nvfp4_quantize_dual(const void* x, int64_t rows, int64_t cols, int6
                                  void* workspace, size_t workspace_bytes, nvfp4_stream_t stream);
 
 /*
+ * nvfp4_quantize_given_amax: nvfp4_quantize under delayed scaling.  The
+ * tensor scale is s = amax[0] / 2688 (1 if that is zero) for an amax the
+ * caller supplies in device memory -- typically the one measured on the
+ * previous step, for instance by nvfp4_gemm_quantize's amax_out -- so x is
+ * read once (one pass) instead of twice.  Elements above amax[0] saturate:
+ * their block scale stops at 448 and their codes at +-6, by the rounding
+ * rules at the top of this header.  Every other step is nvfp4_quantize's, so
+ * with amax[0] equal to the operand's own amax the outputs are identical.
+ * amax[0] must be finite and >= 0: otherwise the device status word is set
+ * to NVFP4_ERR_NONFINITE, tensor_scale[0] to NaN, and codes/sf are not
+ * written.  x must be finite (it is not scanned first): a run holding inf or
+ * NaN sets NVFP4_ERR_NONFINITE and its codes are unspecified.
+ * Arguments, shape rules and workspace otherwise as nvfp4_quantize.
+ * Source: custom scaling of NVFP4 values ("Por que cada porcento e
+ * importante", JAX/MaxText page); the pages fix no scaling policy, and this
+ * is the delayed-scaling reading with every other step unchanged.
+ */
+nvfp4_status nvfp4_quantize_given_amax(const void* x, int64_t rows, int64_t cols, int64_t ldx,
+                                       const nvfp4_quant_cfg* cfg, const float* amax, void* codes, void* sf,
+                                       float* tensor_scale, void* workspace, size_t workspace_bytes,
+                                       nvfp4_stream_t stream);
+
+/*
  * nvfp4_quantize_noalloc: nvfp4_quantize for callers that cannot allocate
  * device memory: a host framework or embedding runtime that owns every
  * device allocation and forbids others (so no workspace can be created for
@@ -205,6 +228,42 @@ nvfp4_status nvfp4_dequantize(const nvfp4_tensor* q, int32_t out_dtype, void* ou
 nvfp4_status nvfp4_gemm_workspace_size(int64_t M, int64_t N, int64_t K, size_t* bytes);
 nvfp4_status nvfp4_gemm(const nvfp4_tensor* a, const nvfp4_tensor* b, int32_t out_dtype, void* d,
                         int64_t ldd, void* workspace, size_t workspace_bytes, nvfp4_stream_t stream);
+
+/* The quantised output of nvfp4_gemm_quantize (device pointers). */
+typedef struct nvfp4_quant_out {
+  const float* amax_in;  /* amax for the tensor scale s = amax_in[0] / 2688    */
+  float* amax_out;       /* NULL, or receives max |D| over the BF16 outputs    */
+  void* codes;           /* [M, N/2] bytes, 16-byte aligned                    */
+  void* sf;              /* block scales in sf_layout (MMA: 16-byte aligned)   */
+  float* tensor_scale;   /* receives s                                         */
+  int32_t sf_layout;     /* nvfp4_sf_layout                                    */
+  int32_t reserved;      /* must be 0                                          */
+} nvfp4_quant_out;
+
+/*
+ * nvfp4_gemm_quantize: nvfp4_gemm with BF16 output whose epilogue also
+ * quantises D for the next layer, straight from the accumulator: 1x16 blocks
+ * along N (the next GEMM's K), round to nearest even, no transform, tensor
+ * scale from q->amax_in (delayed scaling).  The codes, block scales and
+ * tensor scale equal nvfp4_quantize_given_amax of the BF16 D with the same
+ * amax, bit for bit, without D being read back from memory.
+ * d may be NULL: D is then not stored (ldd is ignored).  q->amax_out, if not
+ * NULL, is overwritten with max |D| of the BF16 values, the amax for the next
+ * step's delayed scale.
+ * Shape rules: as nvfp4_gemm, plus N % 32 == 0 and K > 0.  M == 0 or N == 0
+ * launches nothing and writes nothing.
+ * Errors: q->amax_in negative or non-finite -> NVFP4_ERR_NONFINITE in the
+ * status word, tensor_scale NaN, codes/sf not written (D still is).  A D
+ * value that overflows BF16 -> NVFP4_ERR_NONFINITE, codes of its block
+ * unspecified.  Workspace: nvfp4_gemm_workspace_size bytes.
+ * Source: the NVFP4 recipe quantises every GEMM input, activations included
+ * ("Como o treinamento mixed-precision funciona com NVFP4", JAX/MaxText
+ * page); the next layer's input is this GEMM's output, so the epilogue that
+ * already holds it in registers encodes it.
+ */
+nvfp4_status nvfp4_gemm_quantize(const nvfp4_tensor* a, const nvfp4_tensor* b, void* d, int64_t ldd,
+                                 const nvfp4_quant_out* q, void* workspace, size_t workspace_bytes,
+                                 nvfp4_stream_t stream);
 
 /*
  * The linear layer Y = X W^T with X [T, din], W [dout, din], Y [T, dout]
