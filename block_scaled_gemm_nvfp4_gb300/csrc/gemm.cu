@@ -95,6 +95,13 @@ constexpr int kSfGroup = 4;                   // k-blocks per scale stage
 constexpr int kSfaGroupBytes = kSfGroup * kSfaBytes;     // 8 KB: 16 K atoms of one A row block
 constexpr int kSfStageBytes = 3 * kSfaGroupBytes;        // A + two B row blocks: 24 KB
 constexpr int kGroup = 16;                    // tile raster group (row or column blocks)
+// BF16 output leaves through shared memory: each epilogue warp stages a
+// 32-row x 32-column chunk (64-byte rows, 64-byte swizzle) and a TMA store
+// writes it, so global writes are whole 64-byte row segments instead of one
+// 16-byte piece per row per store instruction.
+constexpr int kEpiChunkCols = 32;
+constexpr int kEpiStgBytes = 32 * kEpiChunkCols * 2;       // 2 KB per warp
+constexpr int kEpiStgTotal = kEpiWarps * kEpiStgBytes;     // 16 KB
 static_assert(kSfbCol + 32 * kMaxStages <= kTmemCols, "TMEM budget");
 
 // Per-mode layout.  Codes and block scales travel in separate rings: a code
@@ -113,8 +120,9 @@ struct Layout {
   static_assert(kStages <= kMaxStages, "one TMEM scale slot per code stage");
   static constexpr int kStageBytes = kABytes + kBBytes;
   static constexpr int kSfRing = kStages * kStageBytes;  // offset of the scale ring
-  static constexpr int kSmemBytes =
-      kSfRing + kSfStages * kSfStageBytes + 1024 /*barriers*/ + 1024 /*alignment*/;
+  static constexpr int kEpiStg = kSfRing + kSfStages * kSfStageBytes;  // epilogue staging
+  static constexpr int kCtl = kEpiStg + kEpiStgTotal;                  // barriers
+  static constexpr int kSmemBytes = kCtl + 1024 /*barriers*/ + 1024 /*alignment*/;
   // Instruction descriptor for kind::mxf4nvf4: dense, A and B E2M1 (format 1),
   // both K-major, N >> 3 at bit 17, UE4M3 scales (bit 23 = 0), M >> 4 at bit
   // 24 (M = 256 across the pair in PAIR mode), scale-factor ids 0.
@@ -122,6 +130,7 @@ struct Layout {
       (1u << 7) | (1u << 10) | ((uint32_t)(BN >> 3) << 17) | ((uint32_t)((PAIR ? 2 * BM : BM) >> 4) << 24);
   static_assert(kStageBytes % 1024 == 0, "stages must keep 1024-byte alignment for 128B swizzle");
   static_assert(kSfStageBytes % 16 == 0, "bulk copies need 16-byte alignment");
+  static_assert(kEpiStg % 1024 == 0, "staging buffers keep the 64-byte swizzle's 512-byte alignment");
   static_assert(kSmemBytes <= 232448, "shared memory budget");
 };
 
@@ -139,6 +148,7 @@ struct GParams {
   void* d;
   int64_t ldd;
   int vec_store;
+  int tma_store;        // BF16 D leaves by TMA stores (tensor map tmap_d)
   int group_n;          // raster groups column blocks instead of row blocks
   int skip_first_load;  // test hook: CTA 0 never loads its first stage
   uint32_t* status;
@@ -300,7 +310,8 @@ __device__ __forceinline__ uint32_t quantize_half(const GParams& p, const uint32
 // The warp's lane quarter q gives its 32 rows.  Releases the accumulator (one
 // arrival per warp on the leader's acc_empty) as soon as it has been read.
 template <bool OUT_F32, bool PAIR, bool QUANT>
-__device__ __forceinline__ void epilogue_half(const GParams& p, uint64_t* acc_empty, uint32_t tmem, int m_blk,
+__device__ __forceinline__ void epilogue_half(const GParams& p, const CUtensorMap* tmap_d, uint8_t* stg,
+                                              uint64_t* acc_empty, uint32_t tmem, int m_blk,
                                               int n_blk, int q, int half, int lane, float alpha, uint32_t rank,
                                               float s_dec, uint32_t& amax_bits) {
   const int64_t row = static_cast<int64_t>(m_blk) * BM + q * 32 + lane;
@@ -321,7 +332,35 @@ __device__ __forceinline__ void epilogue_half(const GParams& p, uint64_t* acc_em
     ptx::tc_fence_before();
     __syncwarp();
     if (lane == 0) arrive_leader<PAIR>(acc_empty, rank);
-    if (row < p.M && p.d != nullptr) {  // D is optional for the quantising epilogue
+    if (p.tma_store) {
+      // Chunk c (columns col0 + 32 c ..): lane l writes its row's 64 bytes
+      // into row l of the warp's buffer, 16-byte piece j at slot
+      // j ^ ((l >> 1) & 3) (the 64-byte swizzle the tensor map names, which
+      // also keeps the writes free of bank conflicts); one lane then stores
+      // the box.  Boxes wholly past M or N are skipped; ragged boxes are
+      // clipped by the TMA unit.  The buffer is reused once the previous
+      // store has finished reading it.
+      const int64_t row0 = static_cast<int64_t>(m_blk) * BM + q * 32;
+#pragma unroll
+      for (int c = 0; c < kEpiCols / kEpiChunkCols; ++c) {
+        const int64_t col = col0 + c * kEpiChunkCols;
+        if (row0 >= p.M || col >= p.N) continue;  // warp-uniform
+        if (lane == 0) ptx::bulk_wait_group_read0();
+        __syncwarp();
+        uint8_t* rowp = stg + lane * 64;
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          *reinterpret_cast<uint4*>(rowp + ((j ^ ((lane >> 1) & 3)) << 4)) =
+              make_uint4(packed[c * 16 + 4 * j], packed[c * 16 + 4 * j + 1], packed[c * 16 + 4 * j + 2],
+                         packed[c * 16 + 4 * j + 3]);
+        ptx::fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          ptx::tma_store_2d(tmap_d, stg, static_cast<int32_t>(col), static_cast<int32_t>(row0));
+          ptx::bulk_commit_group();
+        }
+      }
+    } else if (row < p.M && p.d != nullptr) {  // D is optional for the quantising epilogue
       __nv_bfloat16* drow = static_cast<__nv_bfloat16*>(p.d) + row * p.ldd;
 #pragma unroll
       for (int c8 = 0; c8 < kEpiCols / 8; ++c8) {
@@ -415,14 +454,14 @@ __device__ __forceinline__ void stage_scales(const uint8_t* sfa, const uint8_t* 
 template <bool OUT_F32, bool PAIR, bool QUANT>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
-                const GParams p) {
+                const __grid_constant__ CUtensorMap tmap_d, const GParams p) {
   using L = Layout<PAIR>;
   constexpr int S = L::kStages;
   constexpr int SS = L::kSfStages;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sf_ring = smem + L::kSfRing;
-  SmemCtl<S, SS>* ctl = reinterpret_cast<SmemCtl<S, SS>*>(sf_ring + SS * kSfStageBytes);
+  SmemCtl<S, SS>* ctl = reinterpret_cast<SmemCtl<S, SS>*>(smem + L::kCtl);
   volatile int* abort_flag = &ctl->abort;
 
   const int warp = threadIdx.x >> 5;
@@ -452,6 +491,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0 && lane == 0) {
     ptx::prefetch_tensormap(&tmap_a);
     ptx::prefetch_tensormap(&tmap_b);
+    if (p.tma_store) ptx::prefetch_tensormap(&tmap_d);
   }
   if (warp == 1) {
     // pair mode: one warp of each CTA of the pair allocates collectively
@@ -721,6 +761,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;              // TMEM lane quarter this warp may access
     const int half = (warp - 2) >> 2;    // which 128 columns of the tile it stores
+    uint8_t* stg = smem + L::kEpiStg + (warp - 2) * kEpiStgBytes;  // this warp's output staging
     const float alpha = __fmul_rn(*p.a_scale, *p.b_scale);
     // quantising epilogue: tensor scale s = amax_in / 2688 (1 if that is
     // zero); a negative or non-finite amax_in is reported and nothing is
@@ -754,17 +795,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       ptx::tc_fence_after();
       if constexpr (QUANT) {
         if (q_live)
-          epilogue_half<OUT_F32, PAIR, true>(p, &ctl->acc_empty, tmem, m_blk, n_blk, q, half, lane, alpha, rank,
+          epilogue_half<OUT_F32, PAIR, true>(p, &tmap_d, stg, &ctl->acc_empty, tmem, m_blk, n_blk, q, half, lane, alpha, rank,
                                              s_dec, amax_bits);
         else
-          epilogue_half<OUT_F32, PAIR, false>(p, &ctl->acc_empty, tmem, m_blk, n_blk, q, half, lane, alpha, rank,
+          epilogue_half<OUT_F32, PAIR, false>(p, &tmap_d, stg, &ctl->acc_empty, tmem, m_blk, n_blk, q, half, lane, alpha, rank,
                                               s_dec, amax_bits);
       } else {
-        epilogue_half<OUT_F32, PAIR, false>(p, &ctl->acc_empty, tmem, m_blk, n_blk, q, half, lane, alpha, rank,
+        epilogue_half<OUT_F32, PAIR, false>(p, &tmap_d, stg, &ctl->acc_empty, tmem, m_blk, n_blk, q, half, lane, alpha, rank,
                                             s_dec, amax_bits);
       }
       acc_phase ^= 1u;
     }
+    // the staging buffer and the kernel's lifetime must outlast the stores
+    if (p.tma_store && lane == 0) ptx::bulk_wait_group0();
     if (QUANT && q_live) {
       // the lanes of a warp leave the loop above together (warp_wait is
       // warp-uniform), so the shuffles below see the whole warp
@@ -806,6 +849,21 @@ bool make_codes_map(CUtensorMap* map, const uint8_t* codes, int64_t rows, int64_
   return r == CUDA_SUCCESS;
 }
 
+// Tensor map over BF16 D [M, N] (row stride ldd elements) for the staged
+// output: box 32 columns x 32 rows, 64-byte swizzle.
+bool make_d_map(CUtensorMap* map, void* d, int64_t M, int64_t N, int64_t ldd) {
+  auto encode = tensor_map_encoder();
+  if (!encode) return false;
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(M)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(ldd) * 2};
+  const cuuint32_t box[2] = {static_cast<cuuint32_t>(kEpiChunkCols), 32};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, d, dims, strides, box, estr,
+                            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+                            CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 cudaLaunchAttribute pair_cluster_attr() {
   cudaLaunchAttribute attr{};
   attr.id = cudaLaunchAttributeClusterDimension;
@@ -816,7 +874,8 @@ cudaLaunchAttribute pair_cluster_attr() {
 }
 
 template <bool OUT_F32, bool PAIR, bool QUANT>
-cudaError_t launch_typed(const CUtensorMap& ma, const CUtensorMap& mb, GParams p, cudaStream_t stream) {
+cudaError_t launch_typed(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& md, GParams p,
+                         cudaStream_t stream) {
   using L = Layout<PAIR>;
   static bool configured = false;
   static int max_clusters = 0;
@@ -841,7 +900,7 @@ cudaError_t launch_typed(const CUtensorMap& ma, const CUtensorMap& mb, GParams p
   if (!PAIR) {
     p.num_units = p.num_tiles;
     const int grid = std::min(p.num_tiles, device_sm_count());
-    kernel<<<grid, kThreads, L::kSmemBytes, stream>>>(ma, mb, p);
+    kernel<<<grid, kThreads, L::kSmemBytes, stream>>>(ma, mb, md, p);
     return cudaGetLastError();
   }
   p.num_units = p.tiles_mp * p.tiles_n;
@@ -854,7 +913,7 @@ cudaError_t launch_typed(const CUtensorMap& ma, const CUtensorMap& mb, GParams p
   cfg.stream = stream;
   cfg.attrs = &attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kernel, ma, mb, p);
+  return cudaLaunchKernelEx(&cfg, kernel, ma, mb, md, p);
 }
 
 }  // namespace
@@ -900,6 +959,9 @@ cudaError_t launch_gemm(const GemmArgs& a, cudaStream_t stream) {
   }
   const size_t esz = a.out_f32 ? 4 : 2;
   p.vec_store = (reinterpret_cast<uintptr_t>(a.d) % 16 == 0) && ((a.ldd * esz) % 16 == 0);
+  CUtensorMap md{};
+  p.tma_store = !a.out_f32 && a.d != nullptr && p.vec_store;
+  if (p.tma_store && !make_d_map(&md, a.d, a.M, a.N, a.ldd)) return cudaErrorInvalidValue;
   if (a.quant) {
     // BF16 output only; N % 32 == 0 and 16-byte aligned codes (checked by the caller)
     if (a.out_f32) return cudaErrorInvalidValue;
@@ -911,11 +973,11 @@ cudaError_t launch_gemm(const GemmArgs& a, cudaStream_t stream) {
     p.q_sf_mma = a.q_sf_mma;
     p.q_kb_count = a.N / 16;
     p.q_katoms = (p.q_kb_count + 3) / 4;
-    return pair ? launch_typed<false, true, true>(ma, mb, p, stream) : launch_typed<false, false, true>(ma, mb, p, stream);
+    return pair ? launch_typed<false, true, true>(ma, mb, md, p, stream) : launch_typed<false, false, true>(ma, mb, md, p, stream);
   }
   if (pair)
-    return a.out_f32 ? launch_typed<true, true, false>(ma, mb, p, stream) : launch_typed<false, true, false>(ma, mb, p, stream);
-  return a.out_f32 ? launch_typed<true, false, false>(ma, mb, p, stream) : launch_typed<false, false, false>(ma, mb, p, stream);
+    return a.out_f32 ? launch_typed<true, true, false>(ma, mb, md, p, stream) : launch_typed<false, true, false>(ma, mb, md, p, stream);
+  return a.out_f32 ? launch_typed<true, false, false>(ma, mb, md, p, stream) : launch_typed<false, false, false>(ma, mb, md, p, stream);
 }
 
 }  // namespace nvfp4

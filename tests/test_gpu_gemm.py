@@ -76,7 +76,8 @@ def _quantised(x, **mode):
     return q, oracle.quantize(syn.as_u16(x), o)
 
 
-@pytest.mark.parametrize("M,N,K", [(256, 256, 256), (130, 260, 320), (383, 513, 544), (64, 1000, 128)])
+@pytest.mark.parametrize("M,N,K", [(256, 256, 256), (130, 260, 320), (383, 513, 544), (64, 1000, 128),
+                                   (383, 520, 544), (1000, 776, 256)])
 @pytest.mark.parametrize("out", ["f32", "bf16"])
 def test_quantised_operands_vs_oracle(M, N, K, out):
     a = syn.normal_bf16((M, K), seed=M)
@@ -98,6 +99,22 @@ def test_config0_fprop_fp32():
     qw, ow = _quantised(w)
     d = nv.nvfp4_gemm(qx, qw, out_dtype=nv.NVFP4_OUT_F32).cpu().numpy()
     assert rel_err(d, oracle.gemm_f64(ox, ow, 256, 256, 256)) <= 1e-3
+
+
+def test_padded_output_stride_bf16_clipped():
+    # BF16 output through the staged (TMA) store path with a padded row
+    # stride and a D view shorter than its buffer: ragged row and column
+    # boxes must be clipped at M and N, nothing written outside.
+    M, N, K = 200, 200, 256
+    a = syn.normal_bf16((M, K), seed=5)
+    b = syn.normal_bf16((N, K), seed=6)
+    qa, oa = _quantised(a)
+    qb, ob = _quantised(b)
+    big = torch.full((M + 40, 264), 7.0, dtype=torch.bfloat16, device=DEV)
+    nv.nvfp4_gemm(qa, qb, out_dtype=nv.NVFP4_OUT_BF16, d=big[:M, :N])
+    host = big.float().cpu().numpy()
+    assert np.all(host[:, N:] == 7.0) and np.all(host[M:, :] == 7.0)
+    assert bf16_within_one_ulp(host[:M, :N], oracle.gemm_f64(oa, ob, M, N, K))
 
 
 def test_padded_output_stride():
