@@ -79,7 +79,6 @@ constexpr int kRowBytes = BK / 2;             // 128 bytes of packed codes per r
 constexpr int kABytes = BM * kRowBytes;       // 16 KB
 constexpr int kSfAtomBytes = 512;             // 128 rows x 4 scales
 constexpr int kSfaBytes = 4 * kSfAtomBytes;   // one row atom x 4 K atoms
-constexpr int kSfbBytes = 8 * kSfAtomBytes;   // two row atoms x 4 K atoms
 constexpr int kThreads = 480;                 // 15 warps
 constexpr int kEpiWarps = 8;
 constexpr int kSfWarps = 4;
@@ -249,42 +248,62 @@ __device__ __forceinline__ void arrive_leader(uint64_t* bar, uint32_t rank) {
 // even) under the tensor scale s_dec -- the quantiser's steps applied to the
 // BF16 values D holds, so the result equals quantising the stored D.  Rows
 // past M and blocks past N are not encoded; in the tensor-core scale layout
-// their scale bytes are written as the layout's zero padding.  Returns the
-// largest |value| of the valid runs as FP32 bits (NaN propagated).
-__device__ __forceinline__ uint32_t quantize_half(const GParams& p, const uint32_t (&packed)[kEpiCols / 2],
-                                                  int64_t row, int64_t col0, int q, int lane, float s_dec) {
-  const int64_t kb0 = col0 / 16;  // a multiple of 8
-  const bool row_ok = row < p.M;
-  uint32_t sfw[2] = {0u, 0u};     // block kb0 + j in byte (j & 3) of word j >> 2
-  uint32_t amax_bits = 0;
-  uint8_t* crow = p.q_codes + row * (p.N / 2) + col0 / 2;
+// their scale bytes are written as the layout's zero padding.
+struct QuantHalf {
+  uint32_t codes[kEpiCols / 8];  // 16 bytes of codes per 32 columns
+  uint32_t sfw[2];               // block kb0 + j in byte (j & 3) of word j >> 2
+  uint32_t amax_bits;            // largest |value| of the valid runs (FP32 bits, NaN propagated)
+};
+
+// Encode chunk c (columns col0 + 32 c .. + 31: two runs).  N % 32 == 0, so
+// the chunk is either wholly inside N or wholly outside.
+__device__ __forceinline__ void quantize_chunk(const GParams& p, const uint32_t (&packed)[kEpiCols / 2], int c,
+                                               bool row_ok, int64_t kb0, float s_dec, QuantHalf& qh) {
+  const bool in = row_ok && kb0 + 2 * c < p.q_kb_count;
 #pragma unroll
-  for (int r2 = 0; r2 < kEpiCols / 32; ++r2) {
-    // two runs, 32 columns: one 16-byte store of codes (N % 32 == 0, so the
-    // pair is either wholly inside N or wholly outside)
-    const bool in = row_ok && kb0 + 2 * r2 < p.q_kb_count;
-    uint32_t c[4] = {0u, 0u, 0u, 0u};
+  for (int h = 0; h < 2; ++h) {
+    const int r = 2 * c + h;
+    float v[16];
 #pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      const int r = 2 * r2 + h;
-      float v[16];
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const uint32_t w = packed[r * 8 + j];
-        v[2 * j] = __uint_as_float(w << 16);
-        v[2 * j + 1] = __uint_as_float(w & 0xFFFF0000u);
-      }
-      const uint32_t m = run_absmax_nan(v);
-      const uint32_t sfb = in ? block_scale_byte(m, s_dec) : 0u;
-      if (in) amax_bits = max(amax_bits, m);
-      if (sfb != 0) {
-        divide_run<false>(v, __fmul_rn(ptx::e4m3_to_float(sfb), s_dec), v);  // elementwise, in place
-        c[2 * h] = ptx::cvt_e2m1x8(v[0], v[1], v[2], v[3], v[4], v[5], v[6], v[7]);
-        c[2 * h + 1] = ptx::cvt_e2m1x8(v[8], v[9], v[10], v[11], v[12], v[13], v[14], v[15]);
-      }
-      sfw[r >> 2] |= sfb << (8 * (r & 3));
+    for (int j = 0; j < 8; ++j) {
+      const uint32_t w = packed[r * 8 + j];
+      v[2 * j] = __uint_as_float(w << 16);
+      v[2 * j + 1] = __uint_as_float(w & 0xFFFF0000u);
     }
-    if (in) __stcs(reinterpret_cast<uint4*>(crow + 16 * r2), make_uint4(c[0], c[1], c[2], c[3]));
+    const uint32_t m = run_absmax_nan(v);
+    const uint32_t sfb = in ? block_scale_byte(m, s_dec) : 0u;
+    if (in) qh.amax_bits = max(qh.amax_bits, m);
+    qh.codes[2 * r] = 0u;
+    qh.codes[2 * r + 1] = 0u;
+    if (sfb != 0) {
+      divide_run<false>(v, __fmul_rn(ptx::e4m3_to_float(sfb), s_dec), v);  // elementwise, in place
+      qh.codes[2 * r] = ptx::cvt_e2m1x8(v[0], v[1], v[2], v[3], v[4], v[5], v[6], v[7]);
+      qh.codes[2 * r + 1] = ptx::cvt_e2m1x8(v[8], v[9], v[10], v[11], v[12], v[13], v[14], v[15]);
+    }
+    qh.sfw[r >> 2] |= sfb << (8 * (r & 3));
+  }
+}
+
+// Write the encoded half: the warp's codes (32 rows x 64 bytes) leave like D,
+// staged in its buffer (64-byte swizzle) once the previous store has read it,
+// then one TMA store; the block scales go straight to their layout.
+__device__ __forceinline__ void store_quantised(const GParams& p, const CUtensorMap* tmap_q, uint8_t* stg,
+                                                const QuantHalf& qh, int64_t row, int64_t row0, int64_t col0, int q,
+                                                int lane) {
+  const int64_t kb0 = col0 / 16;
+  const bool box = row0 < p.M && col0 < p.N;   // warp-uniform: some of the box is inside D
+  if (lane == 0) ptx::bulk_wait_group_read0();  // a D store may still be reading the buffer
+  __syncwarp();
+  uint8_t* srow = stg + lane * 64;
+#pragma unroll
+  for (int c = 0; c < kEpiCols / 32; ++c)
+    *reinterpret_cast<uint4*>(srow + ((c ^ ((lane >> 1) & 3)) << 4)) =
+        make_uint4(qh.codes[4 * c], qh.codes[4 * c + 1], qh.codes[4 * c + 2], qh.codes[4 * c + 3]);
+  ptx::fence_proxy_async_smem();
+  __syncwarp();
+  if (box && lane == 0) {
+    ptx::tma_store_2d(tmap_q, stg, static_cast<int32_t>(col0 / 2), static_cast<int32_t>(row0));
+    ptx::bulk_commit_group();
   }
   if (p.q_sf_mma) {
     // atoms of 128 rows x 4 blocks: this thread's four blocks of an atom are
@@ -296,21 +315,23 @@ __device__ __forceinline__ uint32_t quantize_half(const GParams& p, const uint32
     for (int a = 0; a < 2; ++a) {
       const int64_t katom = kb0 / 4 + a;
       if (atom_row_ok && katom < p.q_katoms)
-        *reinterpret_cast<uint32_t*>(p.q_sf + ((row / BM) * p.q_katoms + katom) * 512 + lane * 16 + q * 4) = sfw[a];
+        *reinterpret_cast<uint32_t*>(p.q_sf + ((row / BM) * p.q_katoms + katom) * 512 + lane * 16 + q * 4) =
+            qh.sfw[a];
     }
-  } else if (row_ok) {
+  } else if (row < p.M) {
 #pragma unroll
     for (int j = 0; j < 8; ++j)
-      if (kb0 + j < p.q_kb_count) p.q_sf[row * p.q_kb_count + kb0 + j] = static_cast<uint8_t>(sfw[j >> 2] >> (8 * (j & 3)));
+      if (kb0 + j < p.q_kb_count)
+        p.q_sf[row * p.q_kb_count + kb0 + j] = static_cast<uint8_t>(qh.sfw[j >> 2] >> (8 * (j & 3)));
   }
-  return amax_bits;
 }
 
 // Epilogue for one 128 x 128 half of a tile: TMEM -> registers -> global.
 // The warp's lane quarter q gives its 32 rows.  Releases the accumulator (one
 // arrival per warp on the leader's acc_empty) as soon as it has been read.
 template <bool OUT_F32, bool PAIR, bool QUANT>
-__device__ __forceinline__ void epilogue_half(const GParams& p, const CUtensorMap* tmap_d, uint8_t* stg,
+__device__ __forceinline__ void epilogue_half(const GParams& p, const CUtensorMap* tmap_d, const CUtensorMap* tmap_q,
+                                              uint8_t* stg,
                                               uint64_t* acc_empty, uint32_t tmem, int m_blk,
                                               int n_blk, int q, int half, int lane, float alpha, uint32_t rank,
                                               float s_dec, uint32_t& amax_bits) {
@@ -319,6 +340,9 @@ __device__ __forceinline__ void epilogue_half(const GParams& p, const CUtensorMa
   const uint32_t taddr = tmem + (static_cast<uint32_t>(q * 32) << 16) + kAccCol + half * kEpiCols;
   if (!OUT_F32) {
     uint32_t packed[kEpiCols / 2];
+    QuantHalf qh;  // used by the quantising epilogue only
+    qh.sfw[0] = qh.sfw[1] = 0u;
+    qh.amax_bits = 0u;
 #pragma unroll
     for (int c = 0; c < kEpiCols / 32; ++c) {
       uint32_t r[32];
@@ -344,7 +368,10 @@ __device__ __forceinline__ void epilogue_half(const GParams& p, const CUtensorMa
 #pragma unroll
       for (int c = 0; c < kEpiCols / kEpiChunkCols; ++c) {
         const int64_t col = col0 + c * kEpiChunkCols;
-        if (row0 >= p.M || col >= p.N) continue;  // warp-uniform
+        if (row0 >= p.M || col >= p.N) {  // warp-uniform
+          if constexpr (QUANT) quantize_chunk(p, packed, c, row < p.M, col0 / 16, s_dec, qh);
+          continue;
+        }
         if (lane == 0) ptx::bulk_wait_group_read0();
         __syncwarp();
         uint8_t* rowp = stg + lane * 64;
@@ -359,6 +386,8 @@ __device__ __forceinline__ void epilogue_half(const GParams& p, const CUtensorMa
           ptx::tma_store_2d(tmap_d, stg, static_cast<int32_t>(col), static_cast<int32_t>(row0));
           ptx::bulk_commit_group();
         }
+        // encode this chunk while the store reads the buffer
+        if constexpr (QUANT) quantize_chunk(p, packed, c, row < p.M, col0 / 16, s_dec, qh);
       }
     } else if (row < p.M && p.d != nullptr) {  // D is optional for the quantising epilogue
       __nv_bfloat16* drow = static_cast<__nv_bfloat16*>(p.d) + row * p.ldd;
@@ -380,7 +409,14 @@ __device__ __forceinline__ void epilogue_half(const GParams& p, const CUtensorMa
         }
       }
     }
-    if constexpr (QUANT) amax_bits = max(amax_bits, quantize_half(p, packed, row, col0, q, lane, s_dec));
+    if constexpr (QUANT) {
+      if (!p.tma_store) {
+#pragma unroll
+        for (int c = 0; c < kEpiCols / kEpiChunkCols; ++c) quantize_chunk(p, packed, c, row < p.M, col0 / 16, s_dec, qh);
+      }
+      store_quantised(p, tmap_q, stg, qh, row, static_cast<int64_t>(m_blk) * BM + q * 32, col0, q, lane);
+      amax_bits = max(amax_bits, qh.amax_bits);
+    }
   } else {
     float* drow = static_cast<float*>(p.d) + row * p.ldd;
 #pragma unroll 1
@@ -454,7 +490,8 @@ __device__ __forceinline__ void stage_scales(const uint8_t* sfa, const uint8_t* 
 template <bool OUT_F32, bool PAIR, bool QUANT>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
-                const __grid_constant__ CUtensorMap tmap_d, const GParams p) {
+                const __grid_constant__ CUtensorMap tmap_d, const __grid_constant__ CUtensorMap tmap_q,
+                const GParams p) {
   using L = Layout<PAIR>;
   constexpr int S = L::kStages;
   constexpr int SS = L::kSfStages;
@@ -492,6 +529,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     ptx::prefetch_tensormap(&tmap_a);
     ptx::prefetch_tensormap(&tmap_b);
     if (p.tma_store) ptx::prefetch_tensormap(&tmap_d);
+    if (QUANT) ptx::prefetch_tensormap(&tmap_q);
   }
   if (warp == 1) {
     // pair mode: one warp of each CTA of the pair allocates collectively
@@ -795,19 +833,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       ptx::tc_fence_after();
       if constexpr (QUANT) {
         if (q_live)
-          epilogue_half<OUT_F32, PAIR, true>(p, &tmap_d, stg, &ctl->acc_empty, tmem, m_blk, n_blk, q, half, lane, alpha, rank,
+          epilogue_half<OUT_F32, PAIR, true>(p, &tmap_d, &tmap_q, stg, &ctl->acc_empty, tmem, m_blk, n_blk, q, half, lane, alpha, rank,
                                              s_dec, amax_bits);
         else
-          epilogue_half<OUT_F32, PAIR, false>(p, &tmap_d, stg, &ctl->acc_empty, tmem, m_blk, n_blk, q, half, lane, alpha, rank,
+          epilogue_half<OUT_F32, PAIR, false>(p, &tmap_d, &tmap_q, stg, &ctl->acc_empty, tmem, m_blk, n_blk, q, half, lane, alpha, rank,
                                               s_dec, amax_bits);
       } else {
-        epilogue_half<OUT_F32, PAIR, false>(p, &tmap_d, stg, &ctl->acc_empty, tmem, m_blk, n_blk, q, half, lane, alpha, rank,
+        epilogue_half<OUT_F32, PAIR, false>(p, &tmap_d, &tmap_q, stg, &ctl->acc_empty, tmem, m_blk, n_blk, q, half, lane, alpha, rank,
                                             s_dec, amax_bits);
       }
       acc_phase ^= 1u;
     }
     // the staging buffer and the kernel's lifetime must outlast the stores
-    if (p.tma_store && lane == 0) ptx::bulk_wait_group0();
+    if ((p.tma_store || QUANT) && lane == 0) ptx::bulk_wait_group0();
     if (QUANT && q_live) {
       // the lanes of a warp leave the loop above together (warp_wait is
       // warp-uniform), so the shuffles below see the whole warp
@@ -864,6 +902,21 @@ bool make_d_map(CUtensorMap* map, void* d, int64_t M, int64_t N, int64_t ldd) {
   return r == CUDA_SUCCESS;
 }
 
+// Tensor map over the quantised output's codes [M, N/2] bytes: box 64 bytes
+// x 32 rows, 64-byte swizzle.
+bool make_qcodes_map(CUtensorMap* map, uint8_t* codes, int64_t M, int64_t N) {
+  auto encode = tensor_map_encoder();
+  if (!encode) return false;
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(N / 2), static_cast<cuuint64_t>(M)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(N / 2)};
+  const cuuint32_t box[2] = {64, 32};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, codes, dims, strides, box, estr,
+                            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+                            CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 cudaLaunchAttribute pair_cluster_attr() {
   cudaLaunchAttribute attr{};
   attr.id = cudaLaunchAttributeClusterDimension;
@@ -874,8 +927,8 @@ cudaLaunchAttribute pair_cluster_attr() {
 }
 
 template <bool OUT_F32, bool PAIR, bool QUANT>
-cudaError_t launch_typed(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& md, GParams p,
-                         cudaStream_t stream) {
+cudaError_t launch_typed(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& md,
+                         const CUtensorMap& mq, GParams p, cudaStream_t stream) {
   using L = Layout<PAIR>;
   static bool configured = false;
   static int max_clusters = 0;
@@ -900,7 +953,7 @@ cudaError_t launch_typed(const CUtensorMap& ma, const CUtensorMap& mb, const CUt
   if (!PAIR) {
     p.num_units = p.num_tiles;
     const int grid = std::min(p.num_tiles, device_sm_count());
-    kernel<<<grid, kThreads, L::kSmemBytes, stream>>>(ma, mb, md, p);
+    kernel<<<grid, kThreads, L::kSmemBytes, stream>>>(ma, mb, md, mq, p);
     return cudaGetLastError();
   }
   p.num_units = p.tiles_mp * p.tiles_n;
@@ -913,7 +966,7 @@ cudaError_t launch_typed(const CUtensorMap& ma, const CUtensorMap& mb, const CUt
   cfg.stream = stream;
   cfg.attrs = &attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kernel, ma, mb, md, p);
+  return cudaLaunchKernelEx(&cfg, kernel, ma, mb, md, mq, p);
 }
 
 }  // namespace
@@ -959,7 +1012,7 @@ cudaError_t launch_gemm(const GemmArgs& a, cudaStream_t stream) {
   }
   const size_t esz = a.out_f32 ? 4 : 2;
   p.vec_store = (reinterpret_cast<uintptr_t>(a.d) % 16 == 0) && ((a.ldd * esz) % 16 == 0);
-  CUtensorMap md{};
+  CUtensorMap md{}, mq{};
   p.tma_store = !a.out_f32 && a.d != nullptr && p.vec_store;
   if (p.tma_store && !make_d_map(&md, a.d, a.M, a.N, a.ldd)) return cudaErrorInvalidValue;
   if (a.quant) {
@@ -973,11 +1026,12 @@ cudaError_t launch_gemm(const GemmArgs& a, cudaStream_t stream) {
     p.q_sf_mma = a.q_sf_mma;
     p.q_kb_count = a.N / 16;
     p.q_katoms = (p.q_kb_count + 3) / 4;
-    return pair ? launch_typed<false, true, true>(ma, mb, md, p, stream) : launch_typed<false, false, true>(ma, mb, md, p, stream);
+    if (!make_qcodes_map(&mq, a.q_codes, a.M, a.N)) return cudaErrorInvalidValue;
+    return pair ? launch_typed<false, true, true>(ma, mb, md, mq, p, stream) : launch_typed<false, false, true>(ma, mb, md, mq, p, stream);
   }
   if (pair)
-    return a.out_f32 ? launch_typed<true, true, false>(ma, mb, md, p, stream) : launch_typed<false, true, false>(ma, mb, md, p, stream);
-  return a.out_f32 ? launch_typed<true, false, false>(ma, mb, md, p, stream) : launch_typed<false, false, false>(ma, mb, md, p, stream);
+    return a.out_f32 ? launch_typed<true, true, false>(ma, mb, md, mq, p, stream) : launch_typed<false, true, false>(ma, mb, md, mq, p, stream);
+  return a.out_f32 ? launch_typed<true, false, false>(ma, mb, md, mq, p, stream) : launch_typed<false, false, false>(ma, mb, md, mq, p, stream);
 }
 
 }  // namespace nvfp4
