@@ -37,6 +37,25 @@ __device__ __forceinline__ float div_fast(float x, float d, float rd) {
   return __fmaf_rn(-__fmaf_rn(q0, d, -x), rd, q0);
 }
 
+// The same block-scale byte with the two divisions done as residual-corrected
+// divisions by constant reciprocals (RN(1/6) and rs = RN(1/s_dec), rs = 0 when
+// s_dec is outside [2^-70, 2^126)): exact where div_fast is, which the
+// condition bamax >= 2^-93 secures for both steps (then bamax / 6 >= 2^-96);
+// a quotient below 2^-100 is below the smallest E4M3 step whatever its last
+// bits, and one above 2^100 (or an overflow) is clamped there, where E4M3
+// saturates at 448 anyway.  Elsewhere IEEE divisions.
+__device__ __forceinline__ uint32_t block_scale_byte_rcp(uint32_t bamax_bits, float s_dec, float rs) {
+  const float x = __uint_as_float(bamax_bits);
+  float t;
+  if (rs != 0.0f && x >= 0x1p-93f) {
+    t = div_fast(div_fast(x, 6.0f, 0x1.555556p-3f), s_dec, rs);
+    t = (t <= 0x1p100f) ? t : 0x1p100f;
+  } else {
+    t = __fdiv_rn(__fdiv_rn(x, 6.0f), s_dec);
+  }
+  return ptx::cvt_e4m3(t);
+}
+
 // q[j] = v[j] / d wherever the quotient can change a code.  Fast division
 // where it is exact for every code (see div_fast): d in [2^-70, 2^126) for
 // round-to-nearest.  Stochastic rounding (SR) also needs the zero-ness of

@@ -171,13 +171,27 @@ __device__ __forceinline__ float sr_round(float q, uint32_t rnd) {
 // Encode one run of 16 values (already transformed) with block maximum
 // `bamax_bits`; e0 is the linear index of the run's first element in Q, the
 // Philox counter of element e being e >> 2 (word e & 3).
+// Per-output divisor table, built once per CTA: for every nonzero finite
+// scale byte b, d = e4m3(b) * s and rd = RN(1/d) where the fast division is
+// exact for this rounding mode (rd = 0 elsewhere: IEEE division).
+struct DivTable {
+  float2 e[128];
+};
+
 template <bool SR>
-__device__ __forceinline__ uint2 encode_run(const float (&v)[16], uint32_t bamax_bits, float s_dec, uint64_t e0,
-                                            const OutParams& o, uint32_t& sfb) {
-  sfb = block_scale_byte(bamax_bits, s_dec);
+__device__ __forceinline__ uint2 encode_run(const float (&v)[16], uint32_t bamax_bits, float s_dec, float rs,
+                                            const DivTable& dt, uint64_t e0, const OutParams& o, uint32_t& sfb) {
+  sfb = block_scale_byte_rcp(bamax_bits, s_dec, rs);
   if (sfb == 0) return make_uint2(0u, 0u);
+  const float2 dd = dt.e[sfb];
   float q[16];
-  divide_run<SR>(v, __fmul_rn(ptx::e4m3_to_float(sfb), s_dec), q);
+  if (dd.y != 0.0f) {
+#pragma unroll
+    for (int j = 0; j < 16; ++j) q[j] = div_fast(v[j], dd.x, dd.y);
+  } else {
+#pragma unroll
+    for (int j = 0; j < 16; ++j) q[j] = __fdiv_rn(v[j], dd.x);
+  }
   if (SR) {
     const uint32_t o0 = static_cast<uint32_t>(o.sr_offset), o1 = static_cast<uint32_t>(o.sr_offset >> 32);
     const uint64_t c = e0 >> 2;
@@ -256,7 +270,8 @@ __device__ __forceinline__ int stg_sf_offset(int p, int j) {
 
 template <bool COL, bool SR>
 __device__ __forceinline__ void encode_tile(const uint8_t* stage, uint8_t* stg, const OutParams& o, float s_dec,
-                                            uint32_t rht_mask, int64_t tr, int64_t tc, uint32_t* status) {
+                                            float rs, const DivTable& dt, uint32_t rht_mask, int64_t tr,
+                                            int64_t tc, uint32_t* status) {
   const int p = threadIdx.x & 127, j0 = threadIdx.x >> 7;
   const int64_t qrow = (COL ? tc : tr) * kTile + p;
   const int64_t kb0 = (COL ? tr : tc) * 8;
@@ -278,7 +293,8 @@ __device__ __forceinline__ void encode_tile(const uint8_t* stage, uint8_t* stg, 
     }
     if (m >= 0x7F800000u) ptx::set_status(status, kDevNonFinite);
     uint32_t sfb;
-    const uint2 c = encode_run<SR>(v, m, s_dec, static_cast<uint64_t>(qrow * o.qk + (kb0 + j) * 16), o, sfb);
+    const uint2 c =
+        encode_run<SR>(v, m, s_dec, rs, dt, static_cast<uint64_t>(qrow * o.qk + (kb0 + j) * 16), o, sfb);
     *reinterpret_cast<uint2*>(stg + p * kStgPitch + 8 * j) = c;
     stg[stg_sf_offset(p, j)] = static_cast<uint8_t>(sfb);
   }
@@ -342,11 +358,13 @@ __global__ void __launch_bounds__(kThreads, 2) quant_tiles(const __grid_constant
   __shared__ __align__(8) uint64_t full[kStages];
   __shared__ uint32_t red[kThreads / 32];
   __shared__ int abort_flag;
+  __shared__ DivTable dtab[kMaxQuantOutputs];  // encode pass only
   uint8_t* ring = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int tid = threadIdx.x;
 
   uint32_t rht_mask[kMaxQuantOutputs] = {0u, 0u};
   float s_dec[kMaxQuantOutputs] = {1.0f, 1.0f};
+  float rs[kMaxQuantOutputs] = {0.0f, 0.0f};  // RN(1/s_dec) where the fast block-scale division applies
   bool live[kMaxQuantOutputs] = {true, true};
 #pragma unroll
   for (int o = 0; o < kMaxQuantOutputs; ++o) {
@@ -382,7 +400,13 @@ __global__ void __launch_bounds__(kThreads, 2) quant_tiles(const __grid_constant
         float s = __fdiv_rn(__uint_as_float(m), 2688.0f);
         if (s == 0.0f) s = 1.0f;
         s_dec[o] = s;
+        rs[o] = (s >= 0x1p-70f && s < 0x1p126f) ? __frcp_rn(s) : 0.0f;
         if (blockIdx.x == 0 && tid == 0) *p.out[o].tensor_scale = s;
+        if (tid >= 1 && tid < 127) {  // every nonzero finite E4M3 byte
+          const float d = __fmul_rn(ptx::e4m3_to_float(static_cast<uint32_t>(tid)), s);
+          const bool fast = d >= 0x1p-70f && d < (p.out[o].sr ? 0x1p14f : 0x1p126f);
+          dtab[o].e[tid] = make_float2(d, fast ? __frcp_rn(d) : 0.0f);
+        }
       }
     }
   }
@@ -448,14 +472,14 @@ __global__ void __launch_bounds__(kThreads, 2) quant_tiles(const __grid_constant
         uint8_t* so = stg + o * kStgBytes;
         if (op.col) {
           if (op.sr)
-            encode_tile<true, true>(stage, so, op, s_dec[o], rht_mask[o], tr, tc, p.status);
+            encode_tile<true, true>(stage, so, op, s_dec[o], rs[o], dtab[o], rht_mask[o], tr, tc, p.status);
           else
-            encode_tile<true, false>(stage, so, op, s_dec[o], rht_mask[o], tr, tc, p.status);
+            encode_tile<true, false>(stage, so, op, s_dec[o], rs[o], dtab[o], rht_mask[o], tr, tc, p.status);
         } else {
           if (op.sr)
-            encode_tile<false, true>(stage, so, op, s_dec[o], rht_mask[o], tr, tc, p.status);
+            encode_tile<false, true>(stage, so, op, s_dec[o], rs[o], dtab[o], rht_mask[o], tr, tc, p.status);
           else
-            encode_tile<false, false>(stage, so, op, s_dec[o], rht_mask[o], tr, tc, p.status);
+            encode_tile<false, false>(stage, so, op, s_dec[o], rs[o], dtab[o], rht_mask[o], tr, tc, p.status);
         }
       }
     }

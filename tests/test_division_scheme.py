@@ -90,3 +90,90 @@ def test_residual_corrected_division_is_ieee_in_range():
         assert r.returncode == 0, r.stdout + r.stderr
         n = int(r.stdout.split()[1])
         assert n > 10_000_000, r.stdout
+
+
+SRC_SCALE = r"""
+#include <math.h>
+#include <stdint.h>
+#include <stdio.h>
+#include <string.h>
+static uint64_t st = 0xD1B54A32D192ED03ull;
+static uint64_t rnd(void) { st ^= st << 13; st ^= st >> 7; st ^= st << 17; return st; }
+static float u2f(uint32_t u) { float f; memcpy(&f, &u, 4); return f; }
+static uint32_t f2u(float f) { uint32_t u; memcpy(&u, &f, 4); return u; }
+static float div_fast(float x, float d, float rd) {
+  float q0 = x * rd;
+  return fmaf(-fmaf(q0, d, -x), rd, q0);
+}
+/* the block-scale argument as the kernel computes it: t = (bamax / 6) / s by
+   two residual-corrected divisions when bamax >= 2^-93 and s in [2^-70,
+   2^126), clamped at 2^100 (E4M3 saturates far below), else IEEE divisions */
+static float t_fast(float x, float s) {
+  float rs = 1.0f / s;
+  if (s >= 0x1p-70f && s < 0x1p126f && x >= 0x1p-93f) {
+    float d1 = div_fast(x, 6.0f, 0x1.555556p-3f);
+    float t = div_fast(d1, s, rs);
+    return t <= 0x1p100f ? t : 0x1p100f;
+  }
+  float t = (x / 6.0f) / s;  /* the IEEE path; E4M3 saturates above 464 either way */
+  return t <= 0x1p100f ? t : 0x1p100f;
+}
+static float t_ieee(float x, float s) {
+  float t = (x / 6.0f) / s;
+  return t <= 0x1p100f ? t : 0x1p100f;
+}
+/* what decides an E4M3 code: equal values, or both below 2^-11 (code 0) */
+static int same_code_input(float a, float b) {
+  if (f2u(a) == f2u(b)) return 1;
+  return a < 0x1p-11f && b < 0x1p-11f;
+}
+int main(void) {
+  long long n = 0, bad = 0;
+  if (0x1.555556p-3f != 1.0f / 6.0f) { printf("constant\n"); return 1; }
+  /* every positive finite BF16 block maximum against structured and random s */
+  for (int si = 0; si < 40; ++si) {
+    uint32_t sm = si < 8 ? 0x7FFFFF - si : (si < 12 ? (uint32_t)(si - 8) : (uint32_t)(rnd() & 0x7FFFFF));
+    int se = 1 + (int)(rnd() % 253);
+    float s = u2f(sm | ((uint32_t)se << 23));
+    for (uint32_t h = 1; h < 0x7F80; ++h) {
+      float x = u2f(h << 16);
+      ++n;
+      float a = t_fast(x, s), b = t_ieee(x, s);
+      if (!same_code_input(a, b)) { if (bad < 5) printf("x=%a s=%a ieee=%a got=%a\n", x, s, b, a); ++bad; }
+    }
+  }
+  /* random FP32 block maxima (transform outputs) and random s */
+  for (long long it = 0; it < 30000000LL; ++it) {
+    uint64_t r = rnd();
+    float x = u2f((uint32_t)(r & 0x7FFFFFFF));
+    float s = u2f((uint32_t)((rnd() & 0x7FFFFF) | ((1 + rnd() % 253) << 23)));
+    if (!isfinite(x)) continue;
+    ++n;
+    float a = t_fast(x, s), b = t_ieee(x, s);
+    if (!same_code_input(a, b)) { if (bad < 10) printf("x=%a s=%a ieee=%a got=%a\n", x, s, b, a); ++bad; }
+  }
+  printf("checked %lld mismatches %lld\n", n, bad);
+  return bad != 0;
+}
+"""
+
+
+def test_block_scale_divisions_match_ieee():
+    """The block-scale argument t = (bamax / 6) / s, as the quantiser computes
+    it with two residual-corrected divisions (constant reciprocals of 6 and
+    of s) and a clamp at 2^100, equals the IEEE value wherever the E4M3
+    conversion can tell them apart (any value below 2^-11 encodes as 0)."""
+    with tempfile.TemporaryDirectory() as d:
+        c = os.path.join(d, "scale.c")
+        exe = os.path.join(d, "scale")
+        with open(c, "w") as f:
+            f.write(SRC_SCALE)
+        try:
+            subprocess.run(["gcc", "-O2", "-ffp-contract=off", "-fno-fast-math", "-o", exe, c, "-lm"], check=True,
+                           capture_output=True)
+        except (OSError, subprocess.CalledProcessError) as e:
+            pytest.skip("no host C compiler: %s" % e)
+        r = subprocess.run([exe], capture_output=True, text=True, timeout=300)
+        assert r.returncode == 0, r.stdout + r.stderr
+        n = int(r.stdout.split()[1])
+        assert n > 10_000_000, r.stdout
