@@ -343,15 +343,33 @@ __device__ __forceinline__ void epilogue_half(const GParams& p, const CUtensorMa
     QuantHalf qh;  // used by the quantising epilogue only
     qh.sfw[0] = qh.sfw[1] = 0u;
     qh.amax_bits = 0u;
+    // Four 32-column loads in two waits: chunks 2 and 3 are requested while
+    // chunks 0 and 1 are converted, which shortens the accumulator hand-off.
+    static_assert(kEpiCols == 128, "four 32-column chunks");
+    uint32_t r0[32], r1[32];
+    ptx::tmem_ld_32x32b_x32(taddr, r0);
+    ptx::tmem_ld_32x32b_x32(taddr + 32, r1);
+    ptx::tmem_ld_wait();
+    ptx::tmem_ld_regs_ready(r0);
+    ptx::tmem_ld_regs_ready(r1);
 #pragma unroll
-    for (int c = 0; c < kEpiCols / 32; ++c) {
-      uint32_t r[32];
-      ptx::tmem_ld_32x32b_x32(taddr + c * 32, r);
-      ptx::tmem_ld_wait();
+    for (int j = 0; j < 16; ++j)
+      packed[j] = pack_bf16(__fmul_rn(alpha, __uint_as_float(r0[2 * j])), __fmul_rn(alpha, __uint_as_float(r0[2 * j + 1])));
+    ptx::tmem_ld_32x32b_x32(taddr + 64, r0);
 #pragma unroll
-      for (int j = 0; j < 16; ++j)
-        packed[c * 16 + j] = pack_bf16(__fmul_rn(alpha, __uint_as_float(r[2 * j])),
-                                       __fmul_rn(alpha, __uint_as_float(r[2 * j + 1])));
+    for (int j = 0; j < 16; ++j)
+      packed[16 + j] =
+          pack_bf16(__fmul_rn(alpha, __uint_as_float(r1[2 * j])), __fmul_rn(alpha, __uint_as_float(r1[2 * j + 1])));
+    ptx::tmem_ld_32x32b_x32(taddr + 96, r1);
+    ptx::tmem_ld_wait();
+    ptx::tmem_ld_regs_ready(r0);
+    ptx::tmem_ld_regs_ready(r1);
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      packed[32 + j] =
+          pack_bf16(__fmul_rn(alpha, __uint_as_float(r0[2 * j])), __fmul_rn(alpha, __uint_as_float(r0[2 * j + 1])));
+      packed[48 + j] =
+          pack_bf16(__fmul_rn(alpha, __uint_as_float(r1[2 * j])), __fmul_rn(alpha, __uint_as_float(r1[2 * j + 1])));
     }
     ptx::tc_fence_before();
     __syncwarp();
@@ -424,6 +442,7 @@ __device__ __forceinline__ void epilogue_half(const GParams& p, const CUtensorMa
       uint32_t r[32];
       ptx::tmem_ld_32x32b_x32(taddr + c * 32, r);
       ptx::tmem_ld_wait();
+      ptx::tmem_ld_regs_ready(r);
       if (row < p.M) {
 #pragma unroll
         for (int j4 = 0; j4 < 8; ++j4) {
