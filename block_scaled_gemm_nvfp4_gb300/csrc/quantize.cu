@@ -78,6 +78,8 @@ struct OutParams {
   // Philox key schedule of sr_seed, one pair per round (parameter space, so
   // the round XORs read them as constant operands)
   uint32_t sr_rk0[10], sr_rk1[10];
+  // transform signs: sigma_j = -1 as 0x80000000 (the FP32 sign bit), else 0
+  uint32_t rht_sgn[16];
   int col, block2d, sr, rht, sf_mma, vec16;
 };
 
@@ -90,21 +92,8 @@ struct TileParams {
   uint32_t* status;
 };
 
-// Philox4x32-10 (Salmon et al., SC'11): ten rounds, Weyl key schedule.
-__device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint32_t k0, uint32_t k1) {
-#pragma unroll
-  for (int i = 0; i < 10; ++i) {
-    const uint64_t p0 = static_cast<uint64_t>(0xD2511F53u) * c.x;
-    const uint64_t p1 = static_cast<uint64_t>(0xCD9E8D57u) * c.z;
-    c = make_uint4(static_cast<uint32_t>(p1 >> 32) ^ c.y ^ k0, static_cast<uint32_t>(p1),
-                   static_cast<uint32_t>(p0 >> 32) ^ c.w ^ k1, static_cast<uint32_t>(p0));
-    k0 += 0x9E3779B9u;
-    k1 += 0xBB67AE85u;
-  }
-  return c;
-}
-
-// The same rounds with the key schedule precomputed.
+// Philox4x32-10 (Salmon et al., SC'11): ten rounds; the Weyl key schedule is
+// precomputed on the host (sr_rk0 / sr_rk1).
 __device__ __forceinline__ uint4 philox4x32_10_rk(uint4 c, const uint32_t (&rk0)[10], const uint32_t (&rk1)[10]) {
 #pragma unroll
   for (int i = 0; i < 10; ++i) {
@@ -118,11 +107,11 @@ __device__ __forceinline__ uint4 philox4x32_10_rk(uint4 c, const uint32_t (&rk0)
 
 __device__ __forceinline__ uint32_t abs_bits(float v) { return __float_as_uint(v) & 0x7FFFFFFFu; }
 
-// x' = 1/4 * H16 * diag(sigma) * x; butterflies of stride 1, 2, 4, 8.  The
-// signs are applied as multiplications by +-1 (exact; zeros keep IEEE signs).
-__device__ __forceinline__ void rht16(float (&v)[16], uint32_t sign_mask) {
-#pragma unroll
-  for (int j = 0; j < 16; ++j) v[j] = __fmul_rn(v[j], ((sign_mask >> j) & 1u) ? -1.0f : 1.0f);
+// x' = 1/4 * H16 * (diag(sigma) x) for a run whose signs were applied as it
+// was loaded (load_run with SIGNED: flipping the sign bit is the exact product
+// by -1, zeros included); butterflies of stride 1, 2, 4, 8, then the exact
+// scaling by 1/4.
+__device__ __forceinline__ void hadamard16(float (&v)[16]) {
 #pragma unroll
   for (int s = 1; s < 16; s <<= 1) {
 #pragma unroll
@@ -228,8 +217,12 @@ __device__ __forceinline__ void unpack8(const uint4& w, float* v) {
 //
 // Run j (0..7) of position p (0..127): for Q = x, tile columns 16j .. 16j+15
 // of tile row p; for Q = x^T, tile rows 16j .. 16j+15 of tile column p.
-template <bool COL>
-__device__ __forceinline__ void load_run(const uint8_t* stage, int p, int j, float (&v)[16]) {
+// SIGNED: element i also gets the sign bit sgn[i] (0 or 0x80000000) of the
+// transform's sigma, folded into the widening as h * 2^16 + sgn (the low
+// sixteen bits are zero, so the add is an exact sign flip).
+template <bool COL, bool SIGNED = false>
+__device__ __forceinline__ void load_run(const uint8_t* stage, int p, int j, float (&v)[16],
+                                         const uint32_t* sgn = nullptr) {
   if (!COL) {
     const uint8_t* rowp = stage + (j >> 2) * kBoxBytes + p * 128;
     const int c = 2 * (j & 3), sw = p & 7;
@@ -237,27 +230,35 @@ __device__ __forceinline__ void load_run(const uint8_t* stage, int p, int j, flo
     const uint4 b = *reinterpret_cast<const uint4*>(rowp + (((c + 1) ^ sw) << 4));
     unpack8(a, v);
     unpack8(b, v + 8);
+    if (SIGNED) {
+#pragma unroll
+      for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(__float_as_uint(v[i]) ^ sgn[i]);
+    }
   } else {
     const uint8_t* colp = stage + (p >> 6) * kBoxBytes + j * 16 * 128 + (p & 7) * 2;
     const int c = (p & 63) >> 3;
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
       const uint32_t h = *reinterpret_cast<const uint16_t*>(colp + i * 128 + ((c ^ (i & 7)) << 4));
-      v[i] = __uint_as_float(h << 16);
+      v[i] = __uint_as_float(SIGNED ? h * 65536u + sgn[i] : h << 16);
     }
   }
 }
 
 // ------------------------------------------------------------ amax pass
 template <bool COL>
-__device__ __forceinline__ uint32_t amax_tile(const uint8_t* stage, bool rht, uint32_t rht_mask) {
+__device__ __forceinline__ uint32_t amax_tile(const uint8_t* stage, bool rht, const uint32_t* sgn) {
   const int p = threadIdx.x & 127, j0 = threadIdx.x >> 7;
   uint32_t m = 0;
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
     float v[16];
-    load_run<COL>(stage, p, j0 + 2 * i, v);
-    if (rht) rht16(v, rht_mask);
+    if (rht) {
+      load_run<COL, true>(stage, p, j0 + 2 * i, v, sgn);
+      hadamard16(v);
+    } else {
+      load_run<COL>(stage, p, j0 + 2 * i, v);
+    }
     m = max(m, run_absmax_bits(v));
   }
   return m;
@@ -270,7 +271,7 @@ __device__ __forceinline__ int stg_sf_offset(int p, int j) {
 
 template <bool COL, bool SR>
 __device__ __forceinline__ void encode_tile(const uint8_t* stage, uint8_t* stg, const OutParams& o, float s_dec,
-                                            float rs, const DivTable& dt, uint32_t rht_mask, int64_t tr,
+                                            float rs, const DivTable& dt, int64_t tr,
                                             int64_t tc, uint32_t* status) {
   const int p = threadIdx.x & 127, j0 = threadIdx.x >> 7;
   const int64_t qrow = (COL ? tc : tr) * kTile + p;
@@ -281,8 +282,12 @@ __device__ __forceinline__ void encode_tile(const uint8_t* stage, uint8_t* stg, 
   for (int i = 0; i < 4; ++i) {
     const int j = j0 + 2 * i;
     float v[16];
-    load_run<COL>(stage, p, j, v);
-    if (o.rht) rht16(v, rht_mask);
+    if (o.rht) {
+      load_run<COL, true>(stage, p, j, v, o.rht_sgn);
+      hadamard16(v);
+    } else {
+      load_run<COL>(stage, p, j, v);
+    }
     // Inf and NaN were ruled out by the amax pass, except under a supplied
     // amax, where the operand is not scanned first: a non-finite run is
     // reported here (its codes are unspecified).
@@ -362,19 +367,9 @@ __global__ void __launch_bounds__(kThreads, 2) quant_tiles(const __grid_constant
   uint8_t* ring = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int tid = threadIdx.x;
 
-  uint32_t rht_mask[kMaxQuantOutputs] = {0u, 0u};
   float s_dec[kMaxQuantOutputs] = {1.0f, 1.0f};
   float rs[kMaxQuantOutputs] = {0.0f, 0.0f};  // RN(1/s_dec) where the fast block-scale division applies
   bool live[kMaxQuantOutputs] = {true, true};
-#pragma unroll
-  for (int o = 0; o < kMaxQuantOutputs; ++o) {
-    if (o < p.n_out && p.out[o].rht) {
-      const uint64_t seed = p.out[o].rht_seed;
-      const uint4 w = philox4x32_10(make_uint4(0u, 0u, 0u, 0u), static_cast<uint32_t>(seed),
-                                    static_cast<uint32_t>(seed >> 32));
-      rht_mask[o] = w.x & 0xFFFFu;
-    }
-  }
   if (PASS == 1) {
 #pragma unroll
     for (int o = 0; o < kMaxQuantOutputs; ++o) {
@@ -466,20 +461,20 @@ __global__ void __launch_bounds__(kThreads, 2) quant_tiles(const __grid_constant
         if (o == 1 && p.amax_shared) break;
         if (op.amax_in) continue;
         // without the transform the orientation does not change the amax
-        tmax[o] = max(tmax[o], (op.rht && op.col) ? amax_tile<true>(stage, true, rht_mask[o])
-                                                   : amax_tile<false>(stage, op.rht != 0, rht_mask[o]));
+        tmax[o] = max(tmax[o], (op.rht && op.col) ? amax_tile<true>(stage, true, op.rht_sgn)
+                                                   : amax_tile<false>(stage, op.rht != 0, op.rht_sgn));
       } else if (live[o]) {
         uint8_t* so = stg + o * kStgBytes;
         if (op.col) {
           if (op.sr)
-            encode_tile<true, true>(stage, so, op, s_dec[o], rs[o], dtab[o], rht_mask[o], tr, tc, p.status);
+            encode_tile<true, true>(stage, so, op, s_dec[o], rs[o], dtab[o], tr, tc, p.status);
           else
-            encode_tile<true, false>(stage, so, op, s_dec[o], rs[o], dtab[o], rht_mask[o], tr, tc, p.status);
+            encode_tile<true, false>(stage, so, op, s_dec[o], rs[o], dtab[o], tr, tc, p.status);
         } else {
           if (op.sr)
-            encode_tile<false, true>(stage, so, op, s_dec[o], rs[o], dtab[o], rht_mask[o], tr, tc, p.status);
+            encode_tile<false, true>(stage, so, op, s_dec[o], rs[o], dtab[o], tr, tc, p.status);
           else
-            encode_tile<false, false>(stage, so, op, s_dec[o], rs[o], dtab[o], rht_mask[o], tr, tc, p.status);
+            encode_tile<false, false>(stage, so, op, s_dec[o], rs[o], dtab[o], tr, tc, p.status);
         }
       }
     }
@@ -619,6 +614,24 @@ cudaError_t launch_quantize(const QuantArgs& a, cudaStream_t stream) {
         k0 += 0x9E3779B9u;
         k1 += 0xBB67AE85u;
       }
+    }
+    {
+      // sigma_j = -1 iff bit j of word 0 of Philox4x32-10(key = rht_seed,
+      // counter = 0), the same generator the kernels run
+      uint32_t c0 = 0, c1 = 0, c2 = 0, c3 = 0;
+      uint32_t k0 = static_cast<uint32_t>(q.rht_seed), k1 = static_cast<uint32_t>(q.rht_seed >> 32);
+      for (int i = 0; i < 10; ++i) {
+        const uint64_t p0 = static_cast<uint64_t>(0xD2511F53u) * c0;
+        const uint64_t p1 = static_cast<uint64_t>(0xCD9E8D57u) * c2;
+        const uint32_t n0 = static_cast<uint32_t>(p1 >> 32) ^ c1 ^ k0, n2 = static_cast<uint32_t>(p0 >> 32) ^ c3 ^ k1;
+        c1 = static_cast<uint32_t>(p1);
+        c3 = static_cast<uint32_t>(p0);
+        c0 = n0;
+        c2 = n2;
+        k0 += 0x9E3779B9u;
+        k1 += 0xBB67AE85u;
+      }
+      for (int j = 0; j < 16; ++j) op.rht_sgn[j] = (q.rht && ((c0 >> j) & 1u)) ? 0x80000000u : 0u;
     }
     op.col = q.transpose;
     op.block2d = q.block2d;
