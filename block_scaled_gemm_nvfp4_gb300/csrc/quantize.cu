@@ -14,6 +14,8 @@
 //   pass 1: every CTA reduces the partials, derives s = amax / 2688 and encodes
 //           its tiles.  It walks the tiles in reverse order, so its first
 //           reads hit the part of x that pass 0 left in L2.
+// Under delayed scaling (a supplied amax for every output) pass 0 is not
+// launched and pass 1 takes s from that amax: one read of x.
 // Out-of-range parts of a tile read as zero, so ragged tiles need no special
 // case and the padding of the tensor-core scale layout comes out as zeros.
 //
@@ -26,8 +28,11 @@
 //   v = x / d -> E2M1 by RNE or by stochastic rounding with a Philox4x32-10
 //   word per element.  Every FP32 step is an IEEE round-to-nearest operation
 //   (the file is built without FMA contraction).  The element division uses a
-//   correctly rounded reciprocal and one FMA residual correction, which gives
-//   the IEEE quotient wherever it can change a code (see div_fast).
+//   correctly rounded reciprocal (from a per-CTA table indexed by the scale
+//   byte) and one FMA residual correction, which gives the IEEE quotient
+//   wherever it can change a code (div_fast in encode.cuh); the block
+//   scale's two divisions use the same scheme with the constant reciprocals
+//   of 6 and of s (block_scale_byte_rcp).
 //
 // Thread layout: one thread owns whole runs of 16, so the transform and the
 // block maximum stay in registers.  Thread t works on position p = t & 127
