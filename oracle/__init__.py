@@ -80,6 +80,19 @@ def _lib():
         lib.oracle_gemm_f64_sampled.restype = None
         lib.oracle_gemm_f64_sampled.argtypes = [P, P, ctypes.c_float, P, P, ctypes.c_float,
                                                 I64, P, P, I64, P]
+        U64 = ctypes.c_uint64
+        lib.oracle_rht16_inverse.restype = None
+        lib.oracle_rht16_inverse.argtypes = [P, P]
+        lib.oracle_bf16_rne.restype = ctypes.c_uint16
+        lib.oracle_bf16_rne.argtypes = [ctypes.c_float]
+        lib.oracle_qadamw_m_encode.restype = ctypes.c_int
+        lib.oracle_qadamw_m_encode.argtypes = [P, I64, I64, U64, U64, U64, P, P, P]
+        lib.oracle_qadamw_m_decode.restype = None
+        lib.oracle_qadamw_m_decode.argtypes = [P, P, ctypes.c_float, I64, I64, U64, P]
+        lib.oracle_qadamw_v_encode.restype = ctypes.c_int
+        lib.oracle_qadamw_v_encode.argtypes = [P, I64, I64, U64, P, P, P, P]
+        lib.oracle_qadamw_v_decode.restype = None
+        lib.oracle_qadamw_v_decode.argtypes = [P, P, ctypes.c_float, P, I64, I64, U64, P]
         _LIB = lib
     return _LIB
 
@@ -255,4 +268,64 @@ def gemm_f64_sampled(a, b, K, m_idx, n_idx):
     out = np.zeros(mi.shape[0], dtype=np.float64)
     _lib().oracle_gemm_f64_sampled(_ptr(ac), _ptr(asf), float(ascale), _ptr(bc), _ptr(bsf), float(bscale),
                                    int(K), _ptr(mi), _ptr(ni), int(mi.shape[0]), _ptr(out))
+    return out
+
+
+# --- quantised AdamW state codec -------------------------------------------
+def rht16_inverse(v, sigma):
+    out = np.ascontiguousarray(v, dtype=np.float32).copy()
+    s = np.ascontiguousarray(sigma, dtype=np.float32)
+    _lib().oracle_rht16_inverse(_ptr(out), _ptr(s))
+    return out
+
+
+def bf16_rne(f):
+    return _lib().oracle_bf16_rne(float(f))
+
+
+def qadamw_m_encode(m, rht_seed, sr_seed, sr_offset=0):
+    """m: float32 [rows, cols].  Returns (codes, sf row-major, tensor_scale)."""
+    m = np.ascontiguousarray(m, dtype=np.float32)
+    rows, cols = m.shape
+    codes = np.zeros((rows, cols // 2), dtype=np.uint8)
+    sf = np.zeros((rows, cols // 16), dtype=np.uint8)
+    ts = np.zeros(1, dtype=np.float32)
+    st = _lib().oracle_qadamw_m_encode(_ptr(m), rows, cols, int(rht_seed), int(sr_seed), int(sr_offset),
+                                       _ptr(codes), _ptr(sf), _ptr(ts))
+    if st != OK:
+        raise OracleError(st)
+    return codes, sf, ts[0]
+
+
+def qadamw_m_decode(codes, sf, tensor_scale, rows, cols, rht_seed):
+    codes = np.ascontiguousarray(codes, dtype=np.uint8)
+    sf = np.ascontiguousarray(sf, dtype=np.uint8)
+    out = np.zeros((rows, cols), dtype=np.float32)
+    _lib().oracle_qadamw_m_decode(_ptr(codes), _ptr(sf), float(tensor_scale), int(rows), int(cols), int(rht_seed),
+                                  _ptr(out))
+    return out
+
+
+def qadamw_v_encode(v, rht_seed):
+    """v: float32 [rows, cols] >= 0.  Returns (codes, sf row-major,
+    tensor_scale, tile means [rows/16, cols/16] as uint16 BF16 bits)."""
+    v = np.ascontiguousarray(v, dtype=np.float32)
+    rows, cols = v.shape
+    codes = np.zeros((rows, cols // 2), dtype=np.uint8)
+    sf = np.zeros((rows, cols // 16), dtype=np.uint8)
+    ts = np.zeros(1, dtype=np.float32)
+    mu = np.zeros((max(rows // 16, 0), max(cols // 16, 0)), dtype=np.uint16)
+    st = _lib().oracle_qadamw_v_encode(_ptr(v), rows, cols, int(rht_seed), _ptr(codes), _ptr(sf), _ptr(ts), _ptr(mu))
+    if st != OK:
+        raise OracleError(st)
+    return codes, sf, ts[0], mu
+
+
+def qadamw_v_decode(codes, sf, tensor_scale, tile_mean, rows, cols, rht_seed):
+    codes = np.ascontiguousarray(codes, dtype=np.uint8)
+    sf = np.ascontiguousarray(sf, dtype=np.uint8)
+    mu = np.ascontiguousarray(tile_mean, dtype=np.uint16)
+    out = np.zeros((rows, cols), dtype=np.float32)
+    _lib().oracle_qadamw_v_decode(_ptr(codes), _ptr(sf), float(tensor_scale), _ptr(mu), int(rows), int(cols),
+                                  int(rht_seed), _ptr(out))
     return out

@@ -425,3 +425,199 @@ void oracle_gemm_f64_sampled(const uint8_t* a_codes, const uint8_t* a_sf, float 
     out[c] = acc;
   }
 }
+
+/* ------------------------------------------------------------------------- */
+/* Quantised AdamW state codec ("Full-Stack FP4: Stable LLM Pretraining with  */
+/* Quantized Projections, Optimizers, and Attention", section 2.2, Q-AdamW):  */
+/* the first moment is Hadamard-mixed and stored in NVFP4 with stochastic     */
+/* rounding and an adaptive 4/6 block mapping; the second moment is stored as */
+/* sqrt, minus a BF16 tile mean, Hadamard-mixed, in NVFP4; reconstruction     */
+/* inverts each step and squares.                                             */
+/* ------------------------------------------------------------------------- */
+
+/* Inverse of oracle_rht16: x = diag(sigma) * (1/4) * H16 * x' (H16 H16 = 16 I),
+ * the same butterflies, then the exact scaling by 1/4, then the signs. */
+void oracle_rht16_inverse(float v[16], const float sigma[16]) {
+  for (int stride = 1; stride < 16; stride *= 2) {
+    for (int i = 0; i < 16; ++i) {
+      if (i & stride) continue;
+      float a = v[i], b = v[i + stride];
+      v[i] = a + b;
+      v[i + stride] = a - b;
+    }
+  }
+  for (int j = 0; j < 16; ++j) v[j] = v[j] * 0.25f;
+  for (int j = 0; j < 16; ++j) v[j] = v[j] * sigma[j];
+}
+
+/* FP32 -> BF16 bits, round to nearest even (finite input). */
+uint16_t oracle_bf16_rne(float f) {
+  uint32_t u;
+  memcpy(&u, &f, 4);
+  u += 0x7FFFu + ((u >> 16) & 1u);
+  return (uint16_t)(u >> 16);
+}
+
+/* Round-to-nearest squared error of one run under scale byte sfb:
+ * sum over j, in order, of (x_j - e2m1(RNE(x_j / d)) * d)^2 in FP32, d = e4m3(sfb) * s. */
+static float run_rne_error(const float* x, uint8_t sfb, float s_dec) {
+  float err = 0.0f;
+  float d = (float)oracle_e4m3_value(sfb) * s_dec;
+  for (int j = 0; j < 16; ++j) {
+    float deq = 0.0f;
+    if (sfb != 0) deq = (float)oracle_e2m1_value(oracle_e2m1_encode_rne(x[j] / d)) * d;
+    float e = x[j] - deq;
+    err = err + e * e;
+  }
+  return err;
+}
+
+static void sr_code_run(const float* x, uint8_t sfb, float s_dec, uint64_t e0, uint64_t sr_seed, uint64_t sr_offset,
+                        uint8_t* codes_row, int64_t k0) {
+  float d = (float)oracle_e4m3_value(sfb) * s_dec;
+  for (int j = 0; j < 16; ++j) {
+    uint8_t code = 0;
+    if (sfb != 0) {
+      uint64_t e = e0 + (uint64_t)j;
+      uint32_t ctr[4] = {(uint32_t)(e >> 2), (uint32_t)(e >> 34), (uint32_t)sr_offset, (uint32_t)(sr_offset >> 32)};
+      uint32_t key[2] = {(uint32_t)sr_seed, (uint32_t)(sr_seed >> 32)};
+      uint32_t out[4];
+      oracle_philox4x32_10(ctr, key, out);
+      code = oracle_e2m1_encode_sr(x[j] / d, out[e & 3]);
+    }
+    int64_t k = k0 + j;
+    codes_row[k / 2] |= (uint8_t)(code << (4 * (k & 1)));
+  }
+}
+
+/* First moment m [rows, cols] (FP32, row-major, cols % 16 == 0):
+ *  1. x = 1/4 H16 diag(sigma) m on every run of 16 along a row (sigma from rht_seed);
+ *  2. s = amax(x) / 2688 (1 if zero);
+ *  3. per run (reading of "adaptive 4/6"): candidate scale bytes E4M3((bamax/6)/s)
+ *     and E4M3((bamax/4)/s); the one whose round-to-nearest squared error is
+ *     smaller is kept, the 6-mapping on a tie;
+ *  4. codes by stochastic rounding with the Philox stream of the quantiser
+ *     (element index i * cols + k, key sr_seed, counter words 2..3 sr_offset).
+ * Outputs: codes [rows, cols/2], sf [rows, cols/16] row-major, tensor_scale. */
+int oracle_qadamw_m_encode(const float* m, int64_t rows, int64_t cols, uint64_t rht_seed, uint64_t sr_seed,
+                           uint64_t sr_offset, uint8_t* codes, uint8_t* sf, float* tensor_scale) {
+  if (rows < 0 || cols < 0) return ORACLE_ERR_INVALID_ARG;
+  if (cols % 16 != 0) return ORACLE_ERR_UNSUPPORTED_SHAPE;
+  int64_t n = rows * cols, KB = cols / 16;
+  float* x = (float*)malloc((size_t)(n + 1) * sizeof(float));
+  if (!x) return ORACLE_ERR_INVALID_ARG;
+  memcpy(x, m, (size_t)n * sizeof(float));
+  float sigma[16];
+  oracle_rht_signs(rht_seed, sigma);
+  for (int64_t i = 0; i < n; i += 16) oracle_rht16(&x[i], sigma);
+  float amax = amax_of(x, n);
+  if (!isfinite(amax)) {
+    free(x);
+    return ORACLE_ERR_NONFINITE;
+  }
+  float s_dec = tensor_scale_of(amax);
+  *tensor_scale = s_dec;
+  memset(codes, 0, (size_t)(n / 2));
+  for (int64_t i = 0; i < rows; ++i)
+    for (int64_t b = 0; b < KB; ++b) {
+      const float* run = &x[i * cols + b * 16];
+      float bamax = 0.0f;
+      for (int j = 0; j < 16; ++j)
+        if (fabsf(run[j]) > bamax) bamax = fabsf(run[j]);
+      uint8_t sf6 = oracle_e4m3_encode((bamax / 6.0f) / s_dec);
+      uint8_t sf4 = oracle_e4m3_encode((bamax / 4.0f) / s_dec);
+      uint8_t sfb = run_rne_error(run, sf4, s_dec) < run_rne_error(run, sf6, s_dec) ? sf4 : sf6;
+      sf[i * KB + b] = sfb;
+      sr_code_run(run, sfb, s_dec, (uint64_t)(i * cols + b * 16), sr_seed, sr_offset, &codes[i * (cols / 2)], b * 16);
+    }
+  free(x);
+  return ORACLE_OK;
+}
+
+/* m_hat = diag(sigma) 1/4 H16 (e2m1(code) * e4m3(sf) * s) per run, in FP32
+ * (dequantised value: code value times the FP32 product e4m3(sf) * s). */
+void oracle_qadamw_m_decode(const uint8_t* codes, const uint8_t* sf, float tensor_scale, int64_t rows, int64_t cols,
+                            uint64_t rht_seed, float* m_out) {
+  float sigma[16];
+  oracle_rht_signs(rht_seed, sigma);
+  int64_t KB = cols / 16;
+  for (int64_t i = 0; i < rows; ++i)
+    for (int64_t b = 0; b < KB; ++b) {
+      float v[16];
+      float d = (float)oracle_e4m3_value(sf[i * KB + b]) * tensor_scale;
+      for (int j = 0; j < 16; ++j) {
+        int64_t k = b * 16 + j;
+        uint8_t byte = codes[i * (cols / 2) + k / 2];
+        uint8_t code = (k & 1) ? (byte >> 4) : (byte & 15);
+        v[j] = (float)oracle_e2m1_value(code) * d;
+      }
+      oracle_rht16_inverse(v, sigma);
+      memcpy(&m_out[i * cols + b * 16], v, sizeof(v));
+    }
+}
+
+/* Second moment v [rows, cols] (FP32 >= 0, rows and cols multiples of 16):
+ *  1. r = sqrt(v) (IEEE);
+ *  2. per 16x16 tile, mu = BF16_RNE(T * 2^-8) where T sums the tile's row sums
+ *     (each a left-to-right FP32 sum of 16) in row order (reading: "tile" =
+ *     16 x 16, the 2-D block of the format);
+ *  3. residual e = r - mu (FP32);
+ *  4. x = 1/4 H16 diag(sigma) e per run of 16 along a row;
+ *  5. s = amax(x) / 2688, then round-to-nearest NVFP4 with 1x16 blocks
+ *     (E4M3((bamax/6)/s)), as the quantiser's steps 3-5.
+ * Outputs: codes, sf (row-major), tensor_scale, tile means [rows/16, cols/16] as BF16 bits.
+ * A negative or non-finite v is ORACLE_ERR_NONFINITE. */
+int oracle_qadamw_v_encode(const float* v, int64_t rows, int64_t cols, uint64_t rht_seed, uint8_t* codes, uint8_t* sf,
+                           float* tensor_scale, uint16_t* tile_mean) {
+  if (rows < 0 || cols < 0) return ORACLE_ERR_INVALID_ARG;
+  if (cols % 16 != 0 || rows % 16 != 0) return ORACLE_ERR_UNSUPPORTED_SHAPE;
+  int64_t n = rows * cols, KB = cols / 16, TR = rows / 16;
+  for (int64_t i = 0; i < n; ++i)
+    if (!(v[i] >= 0.0f) || isinf(v[i])) return ORACLE_ERR_NONFINITE;
+  float* x = (float*)malloc((size_t)(n + 1) * sizeof(float));
+  if (!x) return ORACLE_ERR_INVALID_ARG;
+  for (int64_t i = 0; i < n; ++i) x[i] = sqrtf(v[i]);
+  for (int64_t tr = 0; tr < TR; ++tr)
+    for (int64_t tc = 0; tc < KB; ++tc) {
+      float total = 0.0f;
+      for (int i = 0; i < 16; ++i) {
+        float row = 0.0f;
+        for (int j = 0; j < 16; ++j) row = row + x[(tr * 16 + i) * cols + tc * 16 + j];
+        total = total + row;
+      }
+      uint16_t mu = oracle_bf16_rne(total * 0.00390625f);
+      tile_mean[tr * KB + tc] = mu;
+      float muf = bf16_to_float(mu);
+      for (int i = 0; i < 16; ++i)
+        for (int j = 0; j < 16; ++j) {
+          float* p = &x[(tr * 16 + i) * cols + tc * 16 + j];
+          *p = *p - muf;
+        }
+    }
+  float sigma[16];
+  oracle_rht_signs(rht_seed, sigma);
+  for (int64_t i = 0; i < n; i += 16) oracle_rht16(&x[i], sigma);
+  float amax = amax_of(x, n);
+  float s_dec = tensor_scale_of(amax);
+  *tensor_scale = s_dec;
+  oracle_cfg cfg;
+  memset(&cfg, 0, sizeof(cfg));
+  encode_rows(x, cols, &cfg, s_dec, 0, rows, codes, sf);
+  free(x);
+  return ORACLE_OK;
+}
+
+/* v_hat = (mu + diag(sigma) 1/4 H16 deq)^2 per element, in FP32. */
+void oracle_qadamw_v_decode(const uint8_t* codes, const uint8_t* sf, float tensor_scale, const uint16_t* tile_mean,
+                            int64_t rows, int64_t cols, uint64_t rht_seed, float* v_out) {
+  float* r = (float*)malloc((size_t)(rows * cols + 1) * sizeof(float));
+  if (!r) return;
+  oracle_qadamw_m_decode(codes, sf, tensor_scale, rows, cols, rht_seed, r);
+  int64_t KB = cols / 16;
+  for (int64_t i = 0; i < rows; ++i)
+    for (int64_t k = 0; k < cols; ++k) {
+      float q = bf16_to_float(tile_mean[(i / 16) * KB + k / 16]) + r[i * cols + k];
+      v_out[i * cols + k] = q * q;
+    }
+  free(r);
+}

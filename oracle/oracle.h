@@ -115,6 +115,18 @@ void oracle_gemm_f64_sampled(const uint8_t* a_codes, const uint8_t* a_sf, float 
                              int64_t K, const int64_t* m_idx, const int64_t* n_idx,
                              int64_t count, double* out);
 
+/* Quantised AdamW state codec (first moment m, second moment v); see oracle.c. */
+void oracle_rht16_inverse(float v[16], const float sigma[16]);
+uint16_t oracle_bf16_rne(float f);
+int oracle_qadamw_m_encode(const float* m, int64_t rows, int64_t cols, uint64_t rht_seed, uint64_t sr_seed,
+                           uint64_t sr_offset, uint8_t* codes, uint8_t* sf, float* tensor_scale);
+void oracle_qadamw_m_decode(const uint8_t* codes, const uint8_t* sf, float tensor_scale, int64_t rows, int64_t cols,
+                            uint64_t rht_seed, float* m_out);
+int oracle_qadamw_v_encode(const float* v, int64_t rows, int64_t cols, uint64_t rht_seed, uint8_t* codes, uint8_t* sf,
+                           float* tensor_scale, uint16_t* tile_mean);
+void oracle_qadamw_v_decode(const uint8_t* codes, const uint8_t* sf, float tensor_scale, const uint16_t* tile_mean,
+                            int64_t rows, int64_t cols, uint64_t rht_seed, float* v_out);
+
 #ifdef __cplusplus
 }
 #endif
