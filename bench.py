@@ -447,7 +447,8 @@ def run_case(args):
     ``dual:R,C[,act|weight]`` (row + colsr, or row16 + col16, from one read),
     ``given:R,C[,mode]`` (one-pass quantiser with a supplied amax) or
     ``gemmq:M,N,K[,nod]`` (GEMM whose epilogue also quantises D along N under
-    a supplied amax; ``nod``: D itself is not stored).
+    a supplied amax; ``nod``: D itself is not stored) or
+    ``qadamw:R,C,m|v|mdec|vdec`` (optimizer-state codec on an FP32 state).
     Prints a JSON line with the mean time per call over --steps calls."""
     import torch
 
@@ -497,6 +498,35 @@ def run_case(args):
         def call():
             nv.nvfp4_quantize_given_amax(x, cfg, amax_in, out=out, workspace=ws)
         work, unit = R * C * QUANT_BYTES_PER_ELT / 1e9, "GB/s"
+    elif kind == "qadamw":
+        # optimizer-state codec: m | v (encode, two passes) or mdec | vdec
+        R, C = int(parts[0]), int(parts[1])
+        what = parts[2] if len(parts) > 2 else "m"
+        g = torch.Generator().manual_seed(7)
+        state = (torch.randn((R, C), generator=g) * 1e-3)
+        if what in ("v", "vdec"):
+            state = state * state
+        state = state.to(dev)
+        ws = torch.zeros(nv.nvfp4_qadamw_workspace_size(), dtype=torch.uint8, device=dev)
+        s = nv.NVFP4_DEFAULT_RHT_SEED
+        if what in ("m", "mdec"):
+            enc = nv.nvfp4_qadamw_m_encode(state, s, 5, workspace=ws)
+        else:
+            enc = nv.nvfp4_qadamw_v_encode(state, s, workspace=ws)
+        packed = QUANT_OUT_BYTES_PER_ELT + (2.0 / 256 if what in ("v", "vdec") else 0.0)
+        if what == "m":
+            def call():
+                nv.nvfp4_qadamw_m_encode(state, s, 5, out=enc, workspace=ws)
+        elif what == "v":
+            def call():
+                nv.nvfp4_qadamw_v_encode(state, s, out=enc, workspace=ws)
+        elif what == "mdec":
+            def call():
+                nv.nvfp4_qadamw_m_decode(enc, s, out=state)
+        else:
+            def call():
+                nv.nvfp4_qadamw_v_decode(enc, s, out=state)
+        work, unit = R * C * (4.0 + packed) / 1e9, "GB/s"
     elif kind == "dual":
         R, C = int(parts[0]), int(parts[1])
         pair = {"act": (modes["row"], modes["colsr"]), "weight": (modes["row16"], modes["col16"])}

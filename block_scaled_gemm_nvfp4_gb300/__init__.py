@@ -37,6 +37,8 @@ EXPORTS = [
     "nvfp4_gemm_workspace_size", "nvfp4_gemm", "nvfp4_gemm_quantize", "nvfp4_linear_workspace_size",
     "nvfp4_linear_fprop", "nvfp4_linear_dgrad", "nvfp4_linear_wgrad",
     "nvfp4_check_device_status", "nvfp4_debug_gemm_skip_load",
+    "nvfp4_qadamw_workspace_size", "nvfp4_qadamw_m_encode", "nvfp4_qadamw_m_decode", "nvfp4_qadamw_v_encode",
+    "nvfp4_qadamw_v_decode",
 ]
 
 
@@ -142,6 +144,12 @@ def lib():
             "nvfp4_linear_wgrad": (I32, [P, P, I64, I64, I64, PCFG, PCFG, I32, P, P, SZ, P]),
             "nvfp4_check_device_status": (I32, [P, P]),
             "nvfp4_debug_gemm_skip_load": (None, [I32]),
+            "nvfp4_qadamw_workspace_size": (I32, [PSZ]),
+            "nvfp4_qadamw_m_encode": (I32, [P, I64, I64, ctypes.c_uint64, ctypes.c_uint64, ctypes.c_uint64, P, P, P, P,
+                                            SZ, P]),
+            "nvfp4_qadamw_m_decode": (I32, [P, P, P, I64, I64, ctypes.c_uint64, P, P]),
+            "nvfp4_qadamw_v_encode": (I32, [P, I64, I64, ctypes.c_uint64, P, P, P, P, P, SZ, P]),
+            "nvfp4_qadamw_v_decode": (I32, [P, P, P, P, I64, I64, ctypes.c_uint64, P, P]),
         }
         for name, (res, args) in sigs.items():
             fn = getattr(L, name)
@@ -389,3 +397,79 @@ def nvfp4_debug_gemm_skip_load(enable=True):
 def nvfp4_check_device_status(workspace, stream=None):
     """Synchronise, read and clear the workspace's device status word."""
     return lib().nvfp4_check_device_status(_ptr(workspace), _stream(stream))
+
+
+# --- quantised AdamW state codec -------------------------------------------
+@dataclass
+class QAdamWState:
+    """An optimizer moment stored in NVFP4 (see include/nvfp4.h)."""
+    codes: torch.Tensor         # uint8 [rows, cols/2]
+    sf: torch.Tensor            # uint8 [rows, cols/16] row-major
+    tensor_scale: torch.Tensor  # float32 [1]
+    tile_mean: torch.Tensor     # uint16 BF16 bits [rows/16, cols/16] (second moment), else empty
+    rows: int
+    cols: int
+
+
+def _qadamw_empty(rows, cols, device, second):
+    return QAdamWState(codes=torch.empty((rows, cols // 2), dtype=torch.uint8, device=device),
+                       sf=torch.empty((rows, cols // 16), dtype=torch.uint8, device=device),
+                       tensor_scale=torch.empty(1, dtype=torch.float32, device=device),
+                       tile_mean=torch.empty((rows // 16, cols // 16) if second else (0,), dtype=torch.int16,
+                                             device=device),
+                       rows=rows, cols=cols)
+
+
+def nvfp4_qadamw_workspace_size():
+    n = ctypes.c_size_t(0)
+    _check(lib().nvfp4_qadamw_workspace_size(ctypes.byref(n)), "nvfp4_qadamw_workspace_size")
+    return n.value
+
+
+def nvfp4_qadamw_m_encode(m, rht_seed, sr_seed, sr_offset=0, out=None, workspace=None, stream=None):
+    """First moment m (float32 CUDA [rows, cols]) -> QAdamWState."""
+    assert m.dtype == torch.float32 and m.dim() == 2 and m.is_contiguous()
+    rows, cols = m.shape
+    if out is None:
+        out = _qadamw_empty(rows, cols, m.device, False)
+    if workspace is None:
+        workspace = _alloc_ws(nvfp4_qadamw_workspace_size(), m.device)
+    st = lib().nvfp4_qadamw_m_encode(_ptr(m), rows, cols, rht_seed, sr_seed, sr_offset, _ptr(out.codes),
+                                     _ptr(out.sf), _ptr(out.tensor_scale), _ptr(workspace), workspace.numel(),
+                                     _stream(stream))
+    _check(st, "nvfp4_qadamw_m_encode")
+    return out
+
+
+def nvfp4_qadamw_m_decode(state, rht_seed, out=None, stream=None):
+    if out is None:
+        out = torch.empty((state.rows, state.cols), dtype=torch.float32, device=state.codes.device)
+    st = lib().nvfp4_qadamw_m_decode(_ptr(state.codes), _ptr(state.sf), _ptr(state.tensor_scale), state.rows,
+                                     state.cols, rht_seed, _ptr(out), _stream(stream))
+    _check(st, "nvfp4_qadamw_m_decode")
+    return out
+
+
+def nvfp4_qadamw_v_encode(v, rht_seed, out=None, workspace=None, stream=None):
+    """Second moment v (float32 CUDA [rows, cols], >= 0) -> QAdamWState."""
+    assert v.dtype == torch.float32 and v.dim() == 2 and v.is_contiguous()
+    rows, cols = v.shape
+    if out is None:
+        out = _qadamw_empty(rows, cols, v.device, True)
+    if workspace is None:
+        workspace = _alloc_ws(nvfp4_qadamw_workspace_size(), v.device)
+    st = lib().nvfp4_qadamw_v_encode(_ptr(v), rows, cols, rht_seed, _ptr(out.codes), _ptr(out.sf),
+                                     _ptr(out.tensor_scale), _ptr(out.tile_mean), _ptr(workspace), workspace.numel(),
+                                     _stream(stream))
+    _check(st, "nvfp4_qadamw_v_encode")
+    return out
+
+
+def nvfp4_qadamw_v_decode(state, rht_seed, out=None, stream=None):
+    if out is None:
+        out = torch.empty((state.rows, state.cols), dtype=torch.float32, device=state.codes.device)
+    st = lib().nvfp4_qadamw_v_decode(_ptr(state.codes), _ptr(state.sf), _ptr(state.tensor_scale),
+                                     _ptr(state.tile_mean), state.rows, state.cols, rht_seed, _ptr(out),
+                                     _stream(stream))
+    _check(st, "nvfp4_qadamw_v_decode")
+    return out

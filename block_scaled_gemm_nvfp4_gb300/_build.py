@@ -23,6 +23,7 @@ UNITS = {
     "quantize.cu": ["-fmad=false"],
     "dequantize.cu": ["-fmad=false"],
     "gemm.cu": [],
+    "qadamw.cu": ["-fmad=false"],
 }
 
 

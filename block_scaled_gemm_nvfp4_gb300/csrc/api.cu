@@ -399,6 +399,122 @@ nvfp4_status nvfp4_gemm_quantize(const nvfp4_tensor* a, const nvfp4_tensor* b, v
   return cuda_status(e);
 }
 
+// ------------------------------------------------------- optimizer states
+static nvfp4_status qadamw_shape(const void* state, int64_t rows, int64_t cols, bool v) {
+  if (rows < 0 || cols < 0) return NVFP4_ERR_INVALID_ARG;
+  if (cols % 16 != 0 || (v && rows % 16 != 0)) return NVFP4_ERR_UNSUPPORTED_SHAPE;
+  if (rows > (int64_t(1) << 31) || cols > (int64_t(1) << 31)) return NVFP4_ERR_UNSUPPORTED_SHAPE;
+  if (rows > 0 && cols > 0 && (!state || !aligned16(state))) return NVFP4_ERR_INVALID_ARG;
+  return NVFP4_OK;
+}
+
+static nvfp4_status qadamw_codes(const void* codes, const void* sf, const void* scale, int64_t rows, int64_t cols) {
+  if (!scale) return NVFP4_ERR_INVALID_ARG;
+  if (rows > 0 && cols > 0 && (!codes || !sf || (reinterpret_cast<uintptr_t>(codes) & 7u))) return NVFP4_ERR_INVALID_ARG;
+  return NVFP4_OK;
+}
+
+static nvfp4_status qadamw_ws(const void* workspace, size_t bytes) {
+  if (!workspace || bytes < kWsHeaderBytes) return NVFP4_ERR_WORKSPACE;
+  if (reinterpret_cast<uintptr_t>(workspace) & 255u) return NVFP4_ERR_INVALID_ARG;
+  return NVFP4_OK;
+}
+
+static nvfp4_status qadamw_run(const QadamwArgs& a, nvfp4_stream_t stream) {
+  const cudaError_t e = launch_qadamw(a, reinterpret_cast<cudaStream_t>(stream));
+  if (e == cudaErrorInvalidValue) return NVFP4_ERR_UNSUPPORTED_SHAPE;
+  return cuda_status(e);
+}
+
+nvfp4_status nvfp4_qadamw_workspace_size(size_t* bytes) {
+  if (!bytes) return NVFP4_ERR_INVALID_ARG;
+  *bytes = kWsHeaderBytes;
+  return NVFP4_OK;
+}
+
+nvfp4_status nvfp4_qadamw_m_encode(const float* m, int64_t rows, int64_t cols, uint64_t rht_seed, uint64_t sr_seed,
+                                   uint64_t sr_offset, void* codes, void* sf, float* tensor_scale, void* workspace,
+                                   size_t workspace_bytes, nvfp4_stream_t stream) {
+  nvfp4_status s = qadamw_shape(m, rows, cols, false);
+  if (s == NVFP4_OK) s = qadamw_codes(codes, sf, tensor_scale, rows, cols);
+  if (s == NVFP4_OK) s = qadamw_ws(workspace, workspace_bytes);
+  if (s != NVFP4_OK) return s;
+  QadamwArgs a{};
+  a.op = QadamwArgs::kMEncode;
+  a.in = m;
+  a.codes = static_cast<uint8_t*>(codes);
+  a.sf = static_cast<uint8_t*>(sf);
+  a.tensor_scale = tensor_scale;
+  a.rows = rows;
+  a.cols = cols;
+  a.rht_seed = rht_seed;
+  a.sr_seed = sr_seed;
+  a.sr_offset = sr_offset;
+  a.workspace = workspace;
+  return qadamw_run(a, stream);
+}
+
+nvfp4_status nvfp4_qadamw_m_decode(const void* codes, const void* sf, const float* tensor_scale, int64_t rows,
+                                   int64_t cols, uint64_t rht_seed, float* m_out, nvfp4_stream_t stream) {
+  nvfp4_status s = qadamw_shape(m_out, rows, cols, false);
+  if (s == NVFP4_OK) s = qadamw_codes(codes, sf, tensor_scale, rows, cols);
+  if (s != NVFP4_OK) return s;
+  QadamwArgs a{};
+  a.op = QadamwArgs::kMDecode;
+  a.out = m_out;
+  a.codes = const_cast<uint8_t*>(static_cast<const uint8_t*>(codes));
+  a.sf = const_cast<uint8_t*>(static_cast<const uint8_t*>(sf));
+  a.tensor_scale_in = tensor_scale;
+  a.rows = rows;
+  a.cols = cols;
+  a.rht_seed = rht_seed;
+  return qadamw_run(a, stream);
+}
+
+nvfp4_status nvfp4_qadamw_v_encode(const float* v, int64_t rows, int64_t cols, uint64_t rht_seed, void* codes,
+                                   void* sf, float* tensor_scale, void* tile_mean, void* workspace,
+                                   size_t workspace_bytes, nvfp4_stream_t stream) {
+  nvfp4_status s = qadamw_shape(v, rows, cols, true);
+  if (s == NVFP4_OK) s = qadamw_codes(codes, sf, tensor_scale, rows, cols);
+  if (s == NVFP4_OK && rows > 0 && cols > 0 && (!tile_mean || (reinterpret_cast<uintptr_t>(tile_mean) & 1u)))
+    s = NVFP4_ERR_INVALID_ARG;
+  if (s == NVFP4_OK) s = qadamw_ws(workspace, workspace_bytes);
+  if (s != NVFP4_OK) return s;
+  QadamwArgs a{};
+  a.op = QadamwArgs::kVEncode;
+  a.in = v;
+  a.codes = static_cast<uint8_t*>(codes);
+  a.sf = static_cast<uint8_t*>(sf);
+  a.tensor_scale = tensor_scale;
+  a.mean = static_cast<uint16_t*>(tile_mean);
+  a.rows = rows;
+  a.cols = cols;
+  a.rht_seed = rht_seed;
+  a.workspace = workspace;
+  return qadamw_run(a, stream);
+}
+
+nvfp4_status nvfp4_qadamw_v_decode(const void* codes, const void* sf, const float* tensor_scale,
+                                   const void* tile_mean, int64_t rows, int64_t cols, uint64_t rht_seed,
+                                   float* v_out, nvfp4_stream_t stream) {
+  nvfp4_status s = qadamw_shape(v_out, rows, cols, true);
+  if (s == NVFP4_OK) s = qadamw_codes(codes, sf, tensor_scale, rows, cols);
+  if (s == NVFP4_OK && rows > 0 && cols > 0 && (!tile_mean || (reinterpret_cast<uintptr_t>(tile_mean) & 1u)))
+    s = NVFP4_ERR_INVALID_ARG;
+  if (s != NVFP4_OK) return s;
+  QadamwArgs a{};
+  a.op = QadamwArgs::kVDecode;
+  a.out = v_out;
+  a.codes = const_cast<uint8_t*>(static_cast<const uint8_t*>(codes));
+  a.sf = const_cast<uint8_t*>(static_cast<const uint8_t*>(sf));
+  a.tensor_scale_in = tensor_scale;
+  a.mean_in = static_cast<const uint16_t*>(tile_mean);
+  a.rows = rows;
+  a.cols = cols;
+  a.rht_seed = rht_seed;
+  return qadamw_run(a, stream);
+}
+
 // ------------------------------------------------------------ linear layer
 // Workspace: [header | quantiser scratch | operand A | operand B].
 static size_t linear_ws(int64_t am, int64_t bn, int64_t k) {

@@ -1,6 +1,7 @@
-// NVFP4 encoding steps shared by the quantiser and the GEMM's quantising
-// epilogue: the E4M3 block scale of a run of 16 and the exact element
-// division that precedes rounding onto the E2M1 grid.
+// NVFP4 encoding steps shared by the quantiser, the GEMM's quantising epilogue
+// and the optimizer-state codec: the E4M3 block scale of a run of 16, the
+// exact element division that precedes rounding onto the E2M1 grid, the
+// Philox4x32-10 stream and the stochastic-rounding decision.
 //
 //   t = (bamax / 6) / s -> E4M3 (round to nearest even, saturating at 448),
 //   d = e4m3(t) * s,  v = x / d (IEEE quotient).
@@ -82,6 +83,43 @@ __device__ __forceinline__ uint32_t run_absmax_nan(const float (&v)[16]) {
 #pragma unroll
   for (int j = 0; j < 16; ++j) asm("max.NaN.f32 %0, %0, %1;" : "+f"(m) : "f"(fabsf(v[j])));
   return __float_as_uint(m);
+}
+
+__device__ __forceinline__ uint32_t abs_bits(float v) { return __float_as_uint(v) & 0x7FFFFFFFu; }
+
+// Philox4x32-10 (Salmon et al., SC'11): ten rounds; the Weyl key schedule is
+// precomputed on the host (sr_rk0 / sr_rk1).
+__device__ __forceinline__ uint4 philox4x32_10_rk(uint4 c, const uint32_t (&rk0)[10], const uint32_t (&rk1)[10]) {
+#pragma unroll
+  for (int i = 0; i < 10; ++i) {
+    const uint64_t p0 = static_cast<uint64_t>(0xD2511F53u) * c.x;
+    const uint64_t p1 = static_cast<uint64_t>(0xCD9E8D57u) * c.z;
+    c = make_uint4(static_cast<uint32_t>(p1 >> 32) ^ c.y ^ rk0[i], static_cast<uint32_t>(p1),
+                   static_cast<uint32_t>(p0 >> 32) ^ c.w ^ rk1[i], static_cast<uint32_t>(p0));
+  }
+  return c;
+}
+
+// Stochastic rounding of q onto the E2M1 grid {0, .5, 1, 1.5, 2, 3, 4, 6}:
+// lo, hi the grid points around |q|, f = (|q| - lo) / (hi - lo), round up iff
+// k * 2^-24 < f with k = r >> 8; |q| >= 6 -> 6.  Branch-free:
+//   |q| in [1, 6): the grid points are the values whose 22 mantissa bits
+//     below the top one are zero and f * 2^24 = 4 * (those bits), so
+//     k < f * 2^24 iff adding 2^22 - 1 - (k >> 2) to the bits carries into
+//     the grid bit;
+//   |q| in [0, 1): lo in {0, 1/2} and f * 2^24 = |q| * 2^25 - lo * 2^25,
+//     exact in FP32, compared with k (< 2^24, exact as a float).
+// Returns the grid value with the sign of q.
+__device__ __forceinline__ float sr_round(float q, uint32_t rnd) {
+  const uint32_t b = abs_bits(q);
+  const uint32_t g_hi = (b + ((~rnd) >> 10)) & 0xFFC00000u;
+  const bool half_up = b >= 0x3F000000u;  // |q| >= 1/2: lo = 1/2
+  const float y = __fmaf_rn(__uint_as_float(b), 33554432.0f, half_up ? -16777216.0f : 0.0f);
+  const bool up = __uint2float_rn(rnd >> 8) < y;
+  const uint32_t g_lo = (half_up ? 0x3F000000u : 0u) + (up ? (half_up ? 0x00800000u : 0x3F000000u) : 0u);
+  uint32_t g = b >= 0x3F800000u ? g_hi : g_lo;
+  g = b >= 0x40C00000u ? 0x40C00000u : g;
+  return __uint_as_float(g | (__float_as_uint(q) & 0x80000000u));
 }
 
 }  // namespace nvfp4

@@ -87,7 +87,55 @@ struct GemmArgs {
 
 cudaError_t launch_gemm(const GemmArgs& a, cudaStream_t stream);
 
+// Quantised AdamW state codec (qadamw.cu).
+struct QadamwArgs {
+  enum Op { kMEncode, kMDecode, kVEncode, kVDecode } op;
+  const float* in;           // m or v (encode)
+  float* out;                // m_hat or v_hat (decode)
+  uint8_t* codes;            // [rows, cols/2]
+  uint8_t* sf;               // [rows, cols/16] row-major
+  float* tensor_scale;       // written by the encoders
+  const float* tensor_scale_in;
+  uint16_t* mean;            // v tile means, BF16 bits (v encode)
+  const uint16_t* mean_in;   // (v decode)
+  int64_t rows, cols;
+  uint64_t rht_seed, sr_seed, sr_offset;
+  void* workspace;           // encoders: status word + amax word
+};
+cudaError_t launch_qadamw(const QadamwArgs& a, cudaStream_t stream);
+
 int device_sm_count();
+
+// Sign words of the 16-point transform: sigma_j = -1 (word 0x80000000, the
+// FP32 sign bit) iff bit j of word 0 of Philox4x32-10(key = seed, counter 0);
+// all zero when `on` is false.  Host code, the same generator the kernels run.
+inline void rht_sign_words(uint64_t seed, bool on, uint32_t out[16]) {
+  uint32_t c0 = 0, c1 = 0, c2 = 0, c3 = 0;
+  uint32_t k0 = static_cast<uint32_t>(seed), k1 = static_cast<uint32_t>(seed >> 32);
+  for (int i = 0; i < 10; ++i) {
+    const uint64_t p0 = static_cast<uint64_t>(0xD2511F53u) * c0;
+    const uint64_t p1 = static_cast<uint64_t>(0xCD9E8D57u) * c2;
+    const uint32_t n0 = static_cast<uint32_t>(p1 >> 32) ^ c1 ^ k0, n2 = static_cast<uint32_t>(p0 >> 32) ^ c3 ^ k1;
+    c1 = static_cast<uint32_t>(p1);
+    c3 = static_cast<uint32_t>(p0);
+    c0 = n0;
+    c2 = n2;
+    k0 += 0x9E3779B9u;
+    k1 += 0xBB67AE85u;
+  }
+  for (int j = 0; j < 16; ++j) out[j] = (on && ((c0 >> j) & 1u)) ? 0x80000000u : 0u;
+}
+
+// Weyl key schedule of Philox4x32-10 for a 64-bit key, one pair per round.
+inline void philox_round_keys(uint64_t key, uint32_t rk0[10], uint32_t rk1[10]) {
+  uint32_t k0 = static_cast<uint32_t>(key), k1 = static_cast<uint32_t>(key >> 32);
+  for (int i = 0; i < 10; ++i) {
+    rk0[i] = k0;
+    rk1[i] = k1;
+    k0 += 0x9E3779B9u;
+    k1 += 0xBB67AE85u;
+  }
+}
 
 // cuTensorMapEncodeTiled from the driver (null if unavailable).
 PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder();

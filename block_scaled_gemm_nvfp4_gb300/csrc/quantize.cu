@@ -97,20 +97,6 @@ struct TileParams {
   uint32_t* status;
 };
 
-// Philox4x32-10 (Salmon et al., SC'11): ten rounds; the Weyl key schedule is
-// precomputed on the host (sr_rk0 / sr_rk1).
-__device__ __forceinline__ uint4 philox4x32_10_rk(uint4 c, const uint32_t (&rk0)[10], const uint32_t (&rk1)[10]) {
-#pragma unroll
-  for (int i = 0; i < 10; ++i) {
-    const uint64_t p0 = static_cast<uint64_t>(0xD2511F53u) * c.x;
-    const uint64_t p1 = static_cast<uint64_t>(0xCD9E8D57u) * c.z;
-    c = make_uint4(static_cast<uint32_t>(p1 >> 32) ^ c.y ^ rk0[i], static_cast<uint32_t>(p1),
-                   static_cast<uint32_t>(p0 >> 32) ^ c.w ^ rk1[i], static_cast<uint32_t>(p0));
-  }
-  return c;
-}
-
-__device__ __forceinline__ uint32_t abs_bits(float v) { return __float_as_uint(v) & 0x7FFFFFFFu; }
 
 // x' = 1/4 * H16 * (diag(sigma) x) for a run whose signs were applied as it
 // was loaded (load_run with SIGNED: flipping the sign bit is the exact product
@@ -140,31 +126,6 @@ __device__ __forceinline__ uint32_t run_absmax_bits(const float (&v)[16]) {
   return m;
 }
 
-// Stochastic rounding of q onto the E2M1 grid {0, .5, 1, 1.5, 2, 3, 4, 6}:
-// lo, hi the grid points around |q|, f = (|q| - lo) / (hi - lo), round up iff
-// k * 2^-24 < f with k = r >> 8; |q| >= 6 -> 6.  Branch-free:
-//   |q| in [1, 6): the grid points are the values whose 22 mantissa bits
-//     below the top one are zero and f * 2^24 = 4 * (those bits), so
-//     k < f * 2^24 iff adding 2^22 - 1 - (k >> 2) to the bits carries into
-//     the grid bit;
-//   |q| in [0, 1): lo in {0, 1/2} and f * 2^24 = |q| * 2^25 - lo * 2^25,
-//     exact in FP32, compared with k (< 2^24, exact as a float).
-// Returns the grid value with the sign of q.
-__device__ __forceinline__ float sr_round(float q, uint32_t rnd) {
-  const uint32_t b = abs_bits(q);
-  const uint32_t g_hi = (b + ((~rnd) >> 10)) & 0xFFC00000u;
-  const bool half_up = b >= 0x3F000000u;  // |q| >= 1/2: lo = 1/2
-  const float y = __fmaf_rn(__uint_as_float(b), 33554432.0f, half_up ? -16777216.0f : 0.0f);
-  const bool up = __uint2float_rn(rnd >> 8) < y;
-  const uint32_t g_lo = (half_up ? 0x3F000000u : 0u) + (up ? (half_up ? 0x00800000u : 0x3F000000u) : 0u);
-  uint32_t g = b >= 0x3F800000u ? g_hi : g_lo;
-  g = b >= 0x40C00000u ? 0x40C00000u : g;
-  return __uint_as_float(g | (__float_as_uint(q) & 0x80000000u));
-}
-
-// Encode one run of 16 values (already transformed) with block maximum
-// `bamax_bits`; e0 is the linear index of the run's first element in Q, the
-// Philox counter of element e being e >> 2 (word e & 3).
 // Per-output divisor table, built once per CTA: for every nonzero finite
 // scale byte b, d = e4m3(b) * s and rd = RN(1/d) where the fast division is
 // exact for this rounding mode (rd = 0 elsewhere: IEEE division).
@@ -172,6 +133,9 @@ struct DivTable {
   float2 e[128];
 };
 
+// Encode one run of 16 values (already transformed) with block maximum
+// `bamax_bits`; e0 is the linear index of the run's first element in Q, the
+// Philox counter of element e being e >> 2 (word e & 3).
 template <bool SR>
 __device__ __forceinline__ uint2 encode_run(const float (&v)[16], uint32_t bamax_bits, float s_dec, float rs,
                                             const DivTable& dt, uint64_t e0, const OutParams& o, uint32_t& sfb) {
@@ -610,34 +574,8 @@ cudaError_t launch_quantize(const QuantArgs& a, cudaStream_t stream) {
     op.rht_seed = q.rht_seed;
     op.sr_seed = q.sr_seed;
     op.sr_offset = q.sr_offset;
-    {
-      // Weyl key schedule of Philox4x32-10 (Salmon et al., SC'11)
-      uint32_t k0 = static_cast<uint32_t>(q.sr_seed), k1 = static_cast<uint32_t>(q.sr_seed >> 32);
-      for (int i = 0; i < 10; ++i) {
-        op.sr_rk0[i] = k0;
-        op.sr_rk1[i] = k1;
-        k0 += 0x9E3779B9u;
-        k1 += 0xBB67AE85u;
-      }
-    }
-    {
-      // sigma_j = -1 iff bit j of word 0 of Philox4x32-10(key = rht_seed,
-      // counter = 0), the same generator the kernels run
-      uint32_t c0 = 0, c1 = 0, c2 = 0, c3 = 0;
-      uint32_t k0 = static_cast<uint32_t>(q.rht_seed), k1 = static_cast<uint32_t>(q.rht_seed >> 32);
-      for (int i = 0; i < 10; ++i) {
-        const uint64_t p0 = static_cast<uint64_t>(0xD2511F53u) * c0;
-        const uint64_t p1 = static_cast<uint64_t>(0xCD9E8D57u) * c2;
-        const uint32_t n0 = static_cast<uint32_t>(p1 >> 32) ^ c1 ^ k0, n2 = static_cast<uint32_t>(p0 >> 32) ^ c3 ^ k1;
-        c1 = static_cast<uint32_t>(p1);
-        c3 = static_cast<uint32_t>(p0);
-        c0 = n0;
-        c2 = n2;
-        k0 += 0x9E3779B9u;
-        k1 += 0xBB67AE85u;
-      }
-      for (int j = 0; j < 16; ++j) op.rht_sgn[j] = (q.rht && ((c0 >> j) & 1u)) ? 0x80000000u : 0u;
-    }
+    philox_round_keys(q.sr_seed, op.sr_rk0, op.sr_rk1);  // Weyl schedule (Salmon et al., SC'11)
+    rht_sign_words(q.rht_seed, q.rht != 0, op.rht_sgn);
     op.col = q.transpose;
     op.block2d = q.block2d;
     op.sr = q.sr;

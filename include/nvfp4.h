@@ -266,6 +266,46 @@ nvfp4_status nvfp4_gemm_quantize(const nvfp4_tensor* a, const nvfp4_tensor* b, v
                                  nvfp4_stream_t stream);
 
 /*
+ * Quantised AdamW state codec ("Full-Stack FP4: Stable LLM Pretraining with
+ * Quantized Projections, Optimizers, and Attention", section 2.2, Q-AdamW):
+ * the optimizer's moments stored in NVFP4 (codes [rows, cols/2], row-major
+ * block scales [rows, cols/16], one FP32 tensor scale), FP32 states in and out,
+ * all row-major with row stride cols, 16-byte aligned.
+ *
+ * nvfp4_qadamw_m_encode: first moment.  Each run of 16 along a row is mixed by
+ * the 16-point transform 1/4 H16 diag(sigma) (sigma from rht_seed as in
+ * nvfp4_quant_cfg); s = amax / 2688 of the mixed tensor; per run the block
+ * scale maps the run's maximum to 6 or to 4, whichever gives the smaller
+ * round-to-nearest squared error (6 on a tie), and the codes are rounded
+ * stochastically (Philox4x32-10 from sr_seed / sr_offset, element index
+ * row * cols + col, as nvfp4_quantize).  cols % 16 == 0.
+ * nvfp4_qadamw_m_decode: m_hat = diag(sigma) 1/4 H16 (code * scale * s) per run.
+ * nvfp4_qadamw_v_encode: second moment (v >= 0).  r = sqrt(v); per 16x16 tile
+ * the mean of r (row sums added in row order, times 2^-8) is stored as BF16
+ * in tile_mean [rows/16, cols/16]; the residual r - mean is mixed by the
+ * transform and rounded to nearest (1x16 blocks, maximum to 6).  rows % 16 ==
+ * 0 and cols % 16 == 0.  A negative or non-finite v sets NVFP4_ERR_NONFINITE
+ * in the status word and tensor_scale NaN.
+ * nvfp4_qadamw_v_decode: v_hat = (mean + diag(sigma) 1/4 H16 deq)^2.
+ * The encoders need nvfp4_qadamw_workspace_size bytes of workspace (status
+ * word and the amax); the decoders need none.
+ * The pages fix neither the 4/6 decision rule nor the tile size; these are the
+ * readings above.
+ */
+nvfp4_status nvfp4_qadamw_workspace_size(size_t* bytes);
+nvfp4_status nvfp4_qadamw_m_encode(const float* m, int64_t rows, int64_t cols, uint64_t rht_seed, uint64_t sr_seed,
+                                   uint64_t sr_offset, void* codes, void* sf, float* tensor_scale, void* workspace,
+                                   size_t workspace_bytes, nvfp4_stream_t stream);
+nvfp4_status nvfp4_qadamw_m_decode(const void* codes, const void* sf, const float* tensor_scale, int64_t rows,
+                                   int64_t cols, uint64_t rht_seed, float* m_out, nvfp4_stream_t stream);
+nvfp4_status nvfp4_qadamw_v_encode(const float* v, int64_t rows, int64_t cols, uint64_t rht_seed, void* codes,
+                                   void* sf, float* tensor_scale, void* tile_mean, void* workspace,
+                                   size_t workspace_bytes, nvfp4_stream_t stream);
+nvfp4_status nvfp4_qadamw_v_decode(const void* codes, const void* sf, const float* tensor_scale,
+                                   const void* tile_mean, int64_t rows, int64_t cols, uint64_t rht_seed,
+                                   float* v_out, nvfp4_stream_t stream);
+
+/*
  * The linear layer Y = X W^T with X [T, din], W [dout, din], Y [T, dout]
  * (all BF16, row-major, densely packed), and its two backward GEMMs:
  *   fprop:  Y  = Q(X) Q(W)^T           X: 1x16 along din, W: 16x16 along din
