@@ -949,25 +949,37 @@ template <bool OUT_F32, bool PAIR, bool QUANT>
 cudaError_t launch_typed(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& md,
                          const CUtensorMap& mq, GParams p, cudaStream_t stream) {
   using L = Layout<PAIR>;
-  static bool configured = false;
-  static int max_clusters = 0;
   auto kernel = gemm_kernel<OUT_F32, PAIR, QUANT>;
-  if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmemBytes);
-    if (e != cudaSuccess) return e;
-    if (PAIR) {
-      cudaLaunchConfig_t cfg{};
-      cudaLaunchAttribute attr = pair_cluster_attr();
-      cfg.gridDim = dim3(2 * device_sm_count());
-      cfg.blockDim = dim3(kThreads);
-      cfg.dynamicSmemBytes = L::kSmemBytes;
-      cfg.attrs = &attr;
-      cfg.numAttrs = 1;
-      e = cudaOccupancyMaxActiveClusters(&max_clusters, kernel, &cfg);
+  // One-time setup per device (the shared-memory opt-in and, in pair mode,
+  // the number of co-resident clusters), safe against concurrent first calls.
+  static std::mutex setup_mutex;
+  static int clusters_of_device[64] = {0};  // 0: not set up yet
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  int max_clusters = 0;
+  {
+    std::lock_guard<std::mutex> lock(setup_mutex);
+    if (clusters_of_device[dev] == 0) {
+      e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmemBytes);
       if (e != cudaSuccess) return e;
-      if (max_clusters < 1) return cudaErrorInvalidConfiguration;
+      int mc = 1;
+      if (PAIR) {
+        cudaLaunchConfig_t cfg{};
+        cudaLaunchAttribute attr = pair_cluster_attr();
+        cfg.gridDim = dim3(2 * device_sm_count());
+        cfg.blockDim = dim3(kThreads);
+        cfg.dynamicSmemBytes = L::kSmemBytes;
+        cfg.attrs = &attr;
+        cfg.numAttrs = 1;
+        e = cudaOccupancyMaxActiveClusters(&mc, kernel, &cfg);
+        if (e != cudaSuccess) return e;
+        if (mc < 1) return cudaErrorInvalidConfiguration;
+      }
+      clusters_of_device[dev] = mc;
     }
-    configured = true;
+    max_clusters = clusters_of_device[dev];
   }
   if (!PAIR) {
     p.num_units = p.num_tiles;

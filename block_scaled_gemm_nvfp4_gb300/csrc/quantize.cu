@@ -475,20 +475,26 @@ __global__ void __launch_bounds__(kThreads, 2) quant_tiles(const __grid_constant
 
 template <int PASS>
 int tiles_per_sm(cudaError_t* err) {
-  static int per_sm[64] = {0};
+  // One-time setup per device, safe against concurrent first calls.
+  static std::mutex setup_mutex;
+  static int per_sm[64] = {0};  // 0: not set up yet
   int dev = 0;
   *err = cudaGetDevice(&dev);
   if (*err != cudaSuccess) return 0;
-  int& cached = per_sm[(dev >= 0 && dev < 64) ? dev : 0];
-  if (cached == 0) {
+  if (dev < 0 || dev >= 64) {
+    *err = cudaErrorInvalidDevice;
+    return 0;
+  }
+  std::lock_guard<std::mutex> lock(setup_mutex);
+  if (per_sm[dev] == 0) {
     *err = cudaFuncSetAttribute(quant_tiles<PASS>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
     if (*err != cudaSuccess) return 0;
     int b = 0;
     *err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, quant_tiles<PASS>, kThreads, kSmemBytes);
     if (*err != cudaSuccess) return 0;
-    cached = std::max(b, 1);
+    per_sm[dev] = std::max(b, 1);
   }
-  return cached;
+  return per_sm[dev];
 }
 
 // Tensor map over x [rows, cols] BF16: box 64 columns x 128 rows, 128-byte
