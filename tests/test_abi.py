@@ -119,3 +119,80 @@ def test_linear_validation(lib):
     assert lib.nvfp4_linear_dgrad(P(8192), P(8192), 64, 64, 64, None, None, 3, P(8192), P(8192), 1 << 24,
                                   P(0)) == nv.NVFP4_ERR_INVALID_ARG
     assert lib.nvfp4_check_device_status(P(0), P(0)) == nv.NVFP4_ERR_INVALID_ARG
+
+
+def test_given_amax_validation(lib):
+    P = ctypes.c_void_p
+    c = nv.quant_cfg()
+
+    def q(amax=8192, cfg=c, cols=64, ws=8192, wsb=1 << 20):
+        return lib.nvfp4_quantize_given_amax(P(8192), 64, cols, cols, ctypes.byref(cfg), P(amax), P(8192), P(8192),
+                                             P(8192), P(ws), wsb, P(0))
+
+    assert q(amax=0) == nv.NVFP4_ERR_INVALID_ARG
+    assert q(cfg=nv.quant_cfg(block=7)) == nv.NVFP4_ERR_INVALID_ARG
+    assert q(cols=40) == nv.NVFP4_ERR_UNSUPPORTED_SHAPE
+    assert q(ws=0) == nv.NVFP4_ERR_WORKSPACE
+    assert q(wsb=64) == nv.NVFP4_ERR_WORKSPACE
+    assert q(ws=8192 + 64) == nv.NVFP4_ERR_INVALID_ARG  # workspace not 256-byte aligned
+
+
+def test_gemm_quantize_validation(lib):
+    P = ctypes.c_void_p
+
+    def out(amax_in=8192, amax_out=0, codes=8192, sf=8192, scale=8192, layout=nv.NVFP4_SF_MMA, reserved=0):
+        return nv._QuantOut(amax_in, amax_out, codes, sf, scale, layout, reserved)
+
+    def g(a=None, b=None, q=None, d=8192, ldd=64, ws=8192, wsb=4096):
+        a = a if a is not None else _t()
+        b = b if b is not None else _t()
+        qq = ctypes.byref(q) if q is not None else None
+        return lib.nvfp4_gemm_quantize(ctypes.byref(a), ctypes.byref(b), P(d), ldd, qq, P(ws), wsb, P(0))
+
+    assert g(q=None) == nv.NVFP4_ERR_INVALID_ARG
+    assert g(q=out(amax_in=0)) == nv.NVFP4_ERR_INVALID_ARG
+    assert g(q=out(scale=0)) == nv.NVFP4_ERR_INVALID_ARG
+    assert g(q=out(reserved=1)) == nv.NVFP4_ERR_INVALID_ARG
+    assert g(q=out(layout=4)) == nv.NVFP4_ERR_INVALID_ARG
+    assert g(b=_t(rows=48), q=out(), ldd=64) == nv.NVFP4_ERR_UNSUPPORTED_SHAPE   # N % 32
+    assert g(a=_t(k=0), b=_t(k=0), q=out()) == nv.NVFP4_ERR_UNSUPPORTED_SHAPE   # K = 0
+    assert g(a=_t(k=64), b=_t(k=96), q=out()) == nv.NVFP4_ERR_INVALID_ARG
+    assert g(q=out(codes=8200)) == nv.NVFP4_ERR_INVALID_ARG                    # codes not 16-byte aligned
+    assert g(q=out(sf=8200)) == nv.NVFP4_ERR_INVALID_ARG                       # MMA scales not 16-byte aligned
+    assert g(q=out(amax_out=8194)) == nv.NVFP4_ERR_INVALID_ARG                 # amax_out not 4-byte aligned
+    assert g(q=out(), ldd=32) == nv.NVFP4_ERR_INVALID_ARG                      # ldd < N with D stored
+    assert g(q=out(), ws=0) == nv.NVFP4_ERR_WORKSPACE
+    assert g(q=out(), wsb=16) == nv.NVFP4_ERR_WORKSPACE
+
+
+def test_qadamw_validation(lib):
+    P = ctypes.c_void_p
+    n = ctypes.c_size_t(0)
+    assert lib.nvfp4_qadamw_workspace_size(ctypes.byref(n)) == 0 and n.value >= 256
+    assert lib.nvfp4_qadamw_workspace_size(None) == nv.NVFP4_ERR_INVALID_ARG
+
+    def m_enc(m=8192, rows=32, cols=64, codes=8192, sf=8192, scale=8192, ws=8192, wsb=1 << 12):
+        return lib.nvfp4_qadamw_m_encode(P(m), rows, cols, 1, 2, 3, P(codes), P(sf), P(scale), P(ws), wsb, P(0))
+
+    assert m_enc(cols=40) == nv.NVFP4_ERR_UNSUPPORTED_SHAPE
+    assert m_enc(rows=-1) == nv.NVFP4_ERR_INVALID_ARG
+    assert m_enc(m=0) == nv.NVFP4_ERR_INVALID_ARG
+    assert m_enc(m=8196) == nv.NVFP4_ERR_INVALID_ARG          # state not 16-byte aligned
+    assert m_enc(codes=8196) == nv.NVFP4_ERR_INVALID_ARG      # codes not 8-byte aligned
+    assert m_enc(scale=0) == nv.NVFP4_ERR_INVALID_ARG
+    assert m_enc(ws=0) == nv.NVFP4_ERR_WORKSPACE
+    assert m_enc(wsb=8) == nv.NVFP4_ERR_WORKSPACE
+
+    def v_enc(rows=32, cols=64, mean=8192, ws=8192):
+        return lib.nvfp4_qadamw_v_encode(P(8192), rows, cols, 1, P(8192), P(8192), P(8192), P(mean), P(ws),
+                                         1 << 12, P(0))
+
+    assert v_enc(rows=24) == nv.NVFP4_ERR_UNSUPPORTED_SHAPE  # 16x16 tiles
+    assert v_enc(mean=0) == nv.NVFP4_ERR_INVALID_ARG
+    assert v_enc(mean=8193) == nv.NVFP4_ERR_INVALID_ARG      # BF16 means need 2-byte alignment
+    assert v_enc(ws=0) == nv.NVFP4_ERR_WORKSPACE
+    assert lib.nvfp4_qadamw_m_decode(P(8192), P(8192), P(0), 32, 64, 1, P(8192), P(0)) == nv.NVFP4_ERR_INVALID_ARG
+    assert lib.nvfp4_qadamw_v_decode(P(8192), P(8192), P(8192), P(0), 32, 64, 1, P(8192),
+                                     P(0)) == nv.NVFP4_ERR_INVALID_ARG
+    assert lib.nvfp4_qadamw_v_decode(P(8192), P(8192), P(8192), P(8192), 24, 64, 1, P(8192),
+                                     P(0)) == nv.NVFP4_ERR_UNSUPPORTED_SHAPE
