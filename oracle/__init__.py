@@ -93,6 +93,9 @@ def _lib():
         lib.oracle_qadamw_v_encode.argtypes = [P, I64, I64, U64, P, P, P, P]
         lib.oracle_qadamw_v_decode.restype = None
         lib.oracle_qadamw_v_decode.argtypes = [P, P, ctypes.c_float, P, I64, I64, U64, P]
+        lib.oracle_lora_forward.restype = None
+        lib.oracle_lora_forward.argtypes = [P, P, ctypes.c_float, P, P, ctypes.c_float, P, P, P, ctypes.c_double,
+                                            I64, I64, I64, I64, P]
         _LIB = lib
     return _LIB
 
@@ -328,4 +331,23 @@ def qadamw_v_decode(codes, sf, tensor_scale, tile_mean, rows, cols, rht_seed):
     out = np.zeros((rows, cols), dtype=np.float32)
     _lib().oracle_qadamw_v_decode(_ptr(codes), _ptr(sf), float(tensor_scale), _ptr(mu), int(rows), int(cols),
                                   int(rht_seed), _ptr(out))
+    return out
+
+
+# --- LoRA-SVD projection -----------------------------------------------------
+def lora_forward(xq, wq, x_u16, l1_u16, l2_u16, beta):
+    """xq, wq: (codes, sf row-major, tensor_scale) of X [T, din] and W_res
+    [dout, din]; x, l1 [r, din], l2 [dout, r] as BF16 bit patterns.  Returns
+    Y [T, dout] in FP64."""
+    xc, xsf, xs = xq
+    wc, wsf, ws = wq
+    x = np.ascontiguousarray(x_u16, dtype=np.uint16)
+    l1 = np.ascontiguousarray(l1_u16, dtype=np.uint16)
+    l2 = np.ascontiguousarray(l2_u16, dtype=np.uint16)
+    T, din = x.shape
+    dout, r = l2.shape
+    out = np.zeros((T, dout), dtype=np.float64)
+    xc, xsf, wc, wsf = (np.ascontiguousarray(a) for a in (xc, xsf, wc, wsf))
+    _lib().oracle_lora_forward(_ptr(xc), _ptr(xsf), float(xs), _ptr(wc), _ptr(wsf), float(ws), _ptr(x), _ptr(l1),
+                               _ptr(l2), float(beta), int(T), int(din), int(dout), int(r), _ptr(out))
     return out

@@ -621,3 +621,33 @@ void oracle_qadamw_v_decode(const uint8_t* codes, const uint8_t* sf, float tenso
     }
   free(r);
 }
+
+/* ------------------------------------------------------------------------- */
+/* LoRA-SVD projection, forward ("Full-Stack FP4...", section 2.1): the      */
+/* weight is W = W_res + beta * L2 L1, with the residual W_res in NVFP4 and    */
+/* the principal low-rank part L2 [dout, r], L1 [r, din] in BF16.             */
+/* Reading: Y = X W^T = (NVFP4 GEMM of X and W_res) + beta * (U L2^T), with   */
+/* U = BF16_RNE(X L1^T) the branch's intermediate (its product summed in      */
+/* FP64 over the BF16 inputs), U L2^T summed in FP64; Y in FP64.              */
+/* ------------------------------------------------------------------------- */
+void oracle_lora_forward(const uint8_t* xq_codes, const uint8_t* xq_sf, float xq_scale, const uint8_t* wq_codes,
+                         const uint8_t* wq_sf, float wq_scale, const uint16_t* x, const uint16_t* l1,
+                         const uint16_t* l2, double beta, int64_t T, int64_t din, int64_t dout, int64_t r,
+                         double* out) {
+  oracle_gemm_f64(xq_codes, xq_sf, xq_scale, wq_codes, wq_sf, wq_scale, T, dout, din, out);
+  float* u = (float*)malloc((size_t)(T * r + 1) * sizeof(float));
+  if (!u) return;
+  for (int64_t t = 0; t < T; ++t)
+    for (int64_t j = 0; j < r; ++j) {
+      double acc = 0.0;
+      for (int64_t k = 0; k < din; ++k) acc += (double)bf16_to_float(x[t * din + k]) * bf16_to_float(l1[j * din + k]);
+      u[t * r + j] = bf16_to_float(oracle_bf16_rne((float)acc));
+    }
+  for (int64_t t = 0; t < T; ++t)
+    for (int64_t n = 0; n < dout; ++n) {
+      double acc = 0.0;
+      for (int64_t j = 0; j < r; ++j) acc += (double)u[t * r + j] * bf16_to_float(l2[n * r + j]);
+      out[t * dout + n] += beta * acc;
+    }
+  free(u);
+}

@@ -127,6 +127,12 @@ int oracle_qadamw_v_encode(const float* v, int64_t rows, int64_t cols, uint64_t 
 void oracle_qadamw_v_decode(const uint8_t* codes, const uint8_t* sf, float tensor_scale, const uint16_t* tile_mean,
                             int64_t rows, int64_t cols, uint64_t rht_seed, float* v_out);
 
+/* LoRA-SVD projection forward: NVFP4 GEMM of X and W_res plus beta * BF16(X L1^T) L2^T, in FP64. */
+void oracle_lora_forward(const uint8_t* xq_codes, const uint8_t* xq_sf, float xq_scale, const uint8_t* wq_codes,
+                         const uint8_t* wq_sf, float wq_scale, const uint16_t* x, const uint16_t* l1,
+                         const uint16_t* l2, double beta, int64_t T, int64_t din, int64_t dout, int64_t r,
+                         double* out);
+
 #ifdef __cplusplus
 }
 #endif
