@@ -96,6 +96,10 @@ def _lib():
         lib.oracle_lora_forward.restype = None
         lib.oracle_lora_forward.argtypes = [P, P, ctypes.c_float, P, P, ctypes.c_float, P, P, P, ctypes.c_double,
                                             I64, I64, I64, I64, P]
+        lib.oracle_abs_percentile_bf16.restype = ctypes.c_float
+        lib.oracle_abs_percentile_bf16.argtypes = [P, I64, ctypes.c_double]
+        lib.oracle_clip_bf16.restype = None
+        lib.oracle_clip_bf16.argtypes = [P, I64, ctypes.c_float, P]
         _LIB = lib
     return _LIB
 
@@ -350,4 +354,17 @@ def lora_forward(xq, wq, x_u16, l1_u16, l2_u16, beta):
     xc, xsf, wc, wsf = (np.ascontiguousarray(a) for a in (xc, xsf, wc, wsf))
     _lib().oracle_lora_forward(_ptr(xc), _ptr(xsf), float(xs), _ptr(wc), _ptr(wsf), float(ws), _ptr(x), _ptr(l1),
                                _ptr(l2), float(beta), int(T), int(din), int(dout), int(r), _ptr(out))
+    return out
+
+
+# --- p99 clipping ---------------------------------------------------------
+def abs_percentile_bf16(x_u16, p=99.0):
+    x = np.ascontiguousarray(x_u16, dtype=np.uint16)
+    return np.float32(_lib().oracle_abs_percentile_bf16(_ptr(x), int(x.size), float(p)))
+
+
+def clip_bf16(x_u16, c):
+    x = np.ascontiguousarray(x_u16, dtype=np.uint16)
+    out = np.zeros_like(x)
+    _lib().oracle_clip_bf16(_ptr(x), int(x.size), float(c), _ptr(out))
     return out

@@ -651,3 +651,38 @@ void oracle_lora_forward(const uint8_t* xq_codes, const uint8_t* xq_sf, float xq
     }
   free(u);
 }
+
+/* ------------------------------------------------------------------------- */
+/* p99 clipping for the NVFP4 Newton-Schulz products ("Full-Stack FP4...",    */
+/* section 2.3): outliers above the 99th percentile are clipped before       */
+/* quantisation.  Reading: nearest-rank percentile of |x| over the tensor,    */
+/* i.e. the k-th smallest magnitude with k = ceil(p / 100 * n) (k >= 1).      */
+/* ------------------------------------------------------------------------- */
+static int cmp_float(const void* a, const void* b) {
+  float x = *(const float*)a, y = *(const float*)b;
+  return (x > y) - (x < y);
+}
+
+float oracle_abs_percentile_bf16(const uint16_t* x, int64_t n, double p) {
+  if (n <= 0) return 0.0f;
+  float* m = (float*)malloc((size_t)n * sizeof(float));
+  if (!m) return NAN;
+  for (int64_t i = 0; i < n; ++i) m[i] = fabsf(bf16_to_float(x[i]));
+  qsort(m, (size_t)n, sizeof(float), cmp_float);
+  int64_t k = (int64_t)ceil(p / 100.0 * (double)n);
+  if (k < 1) k = 1;
+  if (k > n) k = n;
+  float v = m[k - 1];
+  free(m);
+  return v;
+}
+
+/* x clipped to [-c, c] element-wise (BF16 in, BF16 out; c a BF16 magnitude). */
+void oracle_clip_bf16(const uint16_t* x, int64_t n, float c, uint16_t* out) {
+  for (int64_t i = 0; i < n; ++i) {
+    float v = bf16_to_float(x[i]);
+    if (v > c) v = c;
+    if (v < -c) v = -c;
+    out[i] = oracle_bf16_rne(v);
+  }
+}

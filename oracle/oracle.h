@@ -133,6 +133,10 @@ void oracle_lora_forward(const uint8_t* xq_codes, const uint8_t* xq_sf, float xq
                          const uint16_t* l2, double beta, int64_t T, int64_t din, int64_t dout, int64_t r,
                          double* out);
 
+/* Nearest-rank percentile p (0..100] of |x| over n BF16 values, and clipping to [-c, c]. */
+float oracle_abs_percentile_bf16(const uint16_t* x, int64_t n, double p);
+void oracle_clip_bf16(const uint16_t* x, int64_t n, float c, uint16_t* out);
+
 #ifdef __cplusplus
 }
 #endif
