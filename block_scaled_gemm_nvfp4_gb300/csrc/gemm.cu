@@ -30,9 +30,13 @@
 //              swizzle);
 //   warp 1     TMEM allocation; in the leader (or single) CTA the MMA issuer;
 //   warps 2-9  epilogue, two warps per TMEM lane quarter, each owning 128 of
-//              the 256 columns: TMEM -> registers (tcgen05.ld), times sA * sB,
-//              BF16 (RNE) or FP32, stored to global memory.  In BF16 mode the
-//              accumulator is released before the stores are issued;
+//              the 256 columns: TMEM -> registers (tcgen05.ld, two loads per
+//              wait), times sA * sB, BF16 (RNE) or FP32.  In BF16 mode the
+//              accumulator is released before anything is stored, and D
+//              leaves as 32 x 32 chunks staged in a 2 KB shared-memory buffer
+//              per warp and written by TMA tensor stores; the quantising
+//              variant also encodes D along N (1x16, RNE, supplied amax) and
+//              stores its codes the same way;
 //   warps 10-13 stage each k-block's block scales from the scale ring into a
 //              TMEM slot with tcgen05.st (one warp per lane quarter), keeping
 //              the scale traffic off the tensor pipe, where a tcgen05.cp per
