@@ -37,6 +37,11 @@ class _Cfg(ctypes.Structure):
     ]
 
 
+class _NsTrace(ctypes.Structure):
+    _fields_ = [("qx", ctypes.c_float), ("qa", ctypes.c_float), ("qb", ctypes.c_float)] + [
+        (n, ctypes.c_void_p) for n in ("xc", "a", "ac", "a2", "b", "bc", "bx")]
+
+
 def _lib():
     global _LIB
     if _LIB is None:
@@ -96,6 +101,18 @@ def _lib():
         lib.oracle_lora_forward.restype = None
         lib.oracle_lora_forward.argtypes = [P, P, ctypes.c_float, P, P, ctypes.c_float, P, P, P, ctypes.c_double,
                                             I64, I64, I64, I64, P]
+        lib.oracle_lora_down.restype = None
+        lib.oracle_lora_down.argtypes = [P, P, I64, I64, I64, P, P]
+        lib.oracle_lora_forward_sampled.restype = None
+        lib.oracle_lora_forward_sampled.argtypes = [P, P, ctypes.c_float, P, P, ctypes.c_float, P, P, P,
+                                                    ctypes.c_double, I64, I64, P, P, I64, P]
+        lib.oracle_bf16_rne_f64.restype = ctypes.c_uint16
+        lib.oracle_bf16_rne_f64.argtypes = [ctypes.c_double]
+        lib.oracle_axpby_bf16.restype = None
+        lib.oracle_axpby_bf16.argtypes = [P, P, I64, ctypes.c_float, ctypes.c_float, P]
+        lib.oracle_ns_step.restype = ctypes.c_int
+        lib.oracle_ns_step.argtypes = [P, I64, I64, ctypes.c_float, ctypes.c_float, ctypes.c_float, ctypes.c_double,
+                                       P, ctypes.POINTER(_NsTrace)]
         lib.oracle_abs_percentile_bf16.restype = ctypes.c_float
         lib.oracle_abs_percentile_bf16.argtypes = [P, I64, ctypes.c_double]
         lib.oracle_clip_bf16.restype = None
@@ -355,6 +372,69 @@ def lora_forward(xq, wq, x_u16, l1_u16, l2_u16, beta):
     _lib().oracle_lora_forward(_ptr(xc), _ptr(xsf), float(xs), _ptr(wc), _ptr(wsf), float(ws), _ptr(x), _ptr(l1),
                                _ptr(l2), float(beta), int(T), int(din), int(dout), int(r), _ptr(out))
     return out
+
+
+def lora_down(x_u16, l1_u16):
+    """U = BF16(X L1^T) [T, r] (uint16 bits) and the exact FP64 sums it rounds."""
+    x = np.ascontiguousarray(x_u16, dtype=np.uint16)
+    l1 = np.ascontiguousarray(l1_u16, dtype=np.uint16)
+    T, din = x.shape
+    r = l1.shape[0]
+    u = np.zeros((T, r), dtype=np.uint16)
+    ue = np.zeros((T, r), dtype=np.float64)
+    _lib().oracle_lora_down(_ptr(x), _ptr(l1), int(T), int(din), int(r), _ptr(u), _ptr(ue))
+    return u, ue
+
+
+def lora_forward_sampled(xq, wq, x_u16, l1_u16, l2_u16, beta, t_idx, n_idx):
+    """Y of lora_forward at the coordinates (t_idx[i], n_idx[i]) only."""
+    xc, xsf, xs = xq
+    wc, wsf, ws = wq
+    x = np.ascontiguousarray(x_u16, dtype=np.uint16)
+    l1 = np.ascontiguousarray(l1_u16, dtype=np.uint16)
+    l2 = np.ascontiguousarray(l2_u16, dtype=np.uint16)
+    din = x.shape[1]
+    r = l2.shape[1]
+    ti = np.ascontiguousarray(t_idx, dtype=np.int64)
+    ni = np.ascontiguousarray(n_idx, dtype=np.int64)
+    out = np.zeros(ti.size, dtype=np.float64)
+    xc, xsf, wc, wsf = (np.ascontiguousarray(a) for a in (xc, xsf, wc, wsf))
+    _lib().oracle_lora_forward_sampled(_ptr(xc), _ptr(xsf), float(xs), _ptr(wc), _ptr(wsf), float(ws), _ptr(x),
+                                       _ptr(l1), _ptr(l2), float(beta), int(din), int(r), _ptr(ti), _ptr(ni),
+                                       int(ti.size), _ptr(out))
+    return out
+
+
+# --- Newton-Schulz step with NVFP4 products ----------------------------------
+def bf16_rne_f64(d):
+    return _lib().oracle_bf16_rne_f64(float(d))
+
+
+def axpby_bf16(x_u16, y_u16, a, b):
+    x = np.ascontiguousarray(x_u16, dtype=np.uint16)
+    y = np.ascontiguousarray(y_u16, dtype=np.uint16)
+    out = np.zeros_like(x)
+    _lib().oracle_axpby_bf16(_ptr(x), _ptr(y), int(x.size), float(a), float(b), _ptr(out))
+    return out
+
+
+def ns_step(x_u16, a, b, c, p=99.0):
+    """One Newton-Schulz step (see oracle.c).  Returns (X' as uint16 BF16 bits,
+    trace dict with the clip thresholds qx, qa, qb and the BF16 intermediates
+    xc, a, ac, a2, b, bc, bx)."""
+    x = np.ascontiguousarray(x_u16, dtype=np.uint16)
+    m, n = x.shape
+    out = np.zeros_like(x)
+    bufs = {k: np.zeros((m, n) if k in ("xc", "bx") else (m, m), dtype=np.uint16)
+            for k in ("xc", "a", "ac", "a2", "b", "bc", "bx")}
+    tr = _NsTrace(0.0, 0.0, 0.0, *[bufs[k].ctypes.data for k in ("xc", "a", "ac", "a2", "b", "bc", "bx")])
+    st = _lib().oracle_ns_step(_ptr(x), int(m), int(n), float(a), float(b), float(c), float(p), _ptr(out),
+                               ctypes.byref(tr))
+    if st != OK:
+        raise OracleError(st)
+    trace = dict(bufs)
+    trace.update(qx=np.float32(tr.qx), qa=np.float32(tr.qa), qb=np.float32(tr.qb))
+    return out, trace
 
 
 # --- p99 clipping ---------------------------------------------------------

@@ -630,25 +630,57 @@ void oracle_qadamw_v_decode(const uint8_t* codes, const uint8_t* sf, float tenso
 /* U = BF16_RNE(X L1^T) the branch's intermediate (its product summed in      */
 /* FP64 over the BF16 inputs), U L2^T summed in FP64; Y in FP64.              */
 /* ------------------------------------------------------------------------- */
+
+/* The branch's first product for rows [t0, t1) of X: u_exact = X L1^T summed
+ * in FP64, u_bf16 = its BF16 rounding (through FP32, as the intermediate is
+ * stored).  Either output may be NULL. */
+static void lora_down_rows(const uint16_t* x, const uint16_t* l1, int64_t din, int64_t r, int64_t t0, int64_t t1,
+                           uint16_t* u_bf16, double* u_exact) {
+  for (int64_t t = t0; t < t1; ++t)
+    for (int64_t j = 0; j < r; ++j) {
+      double acc = 0.0;
+      for (int64_t k = 0; k < din; ++k) acc += (double)bf16_to_float(x[t * din + k]) * bf16_to_float(l1[j * din + k]);
+      if (u_exact) u_exact[(t - t0) * r + j] = acc;
+      if (u_bf16) u_bf16[(t - t0) * r + j] = oracle_bf16_rne((float)acc);
+    }
+}
+
+void oracle_lora_down(const uint16_t* x, const uint16_t* l1, int64_t T, int64_t din, int64_t r, uint16_t* u_bf16,
+                      double* u_exact) {
+  lora_down_rows(x, l1, din, r, 0, T, u_bf16, u_exact);
+}
+
 void oracle_lora_forward(const uint8_t* xq_codes, const uint8_t* xq_sf, float xq_scale, const uint8_t* wq_codes,
                          const uint8_t* wq_sf, float wq_scale, const uint16_t* x, const uint16_t* l1,
                          const uint16_t* l2, double beta, int64_t T, int64_t din, int64_t dout, int64_t r,
                          double* out) {
   oracle_gemm_f64(xq_codes, xq_sf, xq_scale, wq_codes, wq_sf, wq_scale, T, dout, din, out);
-  float* u = (float*)malloc((size_t)(T * r + 1) * sizeof(float));
+  uint16_t* u = (uint16_t*)malloc((size_t)(T * r + 1) * sizeof(uint16_t));
   if (!u) return;
-  for (int64_t t = 0; t < T; ++t)
-    for (int64_t j = 0; j < r; ++j) {
-      double acc = 0.0;
-      for (int64_t k = 0; k < din; ++k) acc += (double)bf16_to_float(x[t * din + k]) * bf16_to_float(l1[j * din + k]);
-      u[t * r + j] = bf16_to_float(oracle_bf16_rne((float)acc));
-    }
+  oracle_lora_down(x, l1, T, din, r, u, NULL);
   for (int64_t t = 0; t < T; ++t)
     for (int64_t n = 0; n < dout; ++n) {
       double acc = 0.0;
-      for (int64_t j = 0; j < r; ++j) acc += (double)u[t * r + j] * bf16_to_float(l2[n * r + j]);
+      for (int64_t j = 0; j < r; ++j) acc += (double)bf16_to_float(u[t * r + j]) * bf16_to_float(l2[n * r + j]);
       out[t * dout + n] += beta * acc;
     }
+  free(u);
+}
+
+/* The same Y at the listed (t, n) coordinates only. */
+void oracle_lora_forward_sampled(const uint8_t* xq_codes, const uint8_t* xq_sf, float xq_scale,
+                                 const uint8_t* wq_codes, const uint8_t* wq_sf, float wq_scale, const uint16_t* x,
+                                 const uint16_t* l1, const uint16_t* l2, double beta, int64_t din, int64_t r,
+                                 const int64_t* t_idx, const int64_t* n_idx, int64_t count, double* out) {
+  oracle_gemm_f64_sampled(xq_codes, xq_sf, xq_scale, wq_codes, wq_sf, wq_scale, din, t_idx, n_idx, count, out);
+  uint16_t* u = (uint16_t*)malloc((size_t)(r + 1) * sizeof(uint16_t));
+  if (!u) return;
+  for (int64_t c = 0; c < count; ++c) {
+    lora_down_rows(x, l1, din, r, t_idx[c], t_idx[c] + 1, u, NULL);
+    double acc = 0.0;
+    for (int64_t j = 0; j < r; ++j) acc += (double)bf16_to_float(u[j]) * bf16_to_float(l2[n_idx[c] * r + j]);
+    out[c] += beta * acc;
+  }
   free(u);
 }
 
@@ -685,4 +717,144 @@ void oracle_clip_bf16(const uint16_t* x, int64_t n, float c, uint16_t* out) {
     if (v < -c) v = -c;
     out[i] = oracle_bf16_rne(v);
   }
+}
+
+/* ------------------------------------------------------------------------- */
+/* One Newton-Schulz step of the Root optimizer with its matrix products in   */
+/* NVFP4 ("Full-Stack FP4...", section 2.3: the NS products run directly in   */
+/* NVFP4, stabilised by shape-dependent coefficients a, b, c and p99 outlier  */
+/* clipping).  The pages print no coefficients and no formula; reading: the   */
+/* quintic step on an iterate X [m, n] (m <= n is the caller's orientation),  */
+/*     A = X X^T,   B = b A + c A A^T,   X' = a X + B X,                       */
+/* where every matrix product L R^T is the NVFP4 GEMM of its two operands,    */
+/* each clipped to [-q, q] (q its own p-th percentile magnitude) and then     */
+/* quantised along its K with 1x16 blocks, round to nearest, no transform;    */
+/* the products' results and the iterate are stored in BF16 (round to nearest */
+/* even of the exact FP64 sum), the sums a X + ... and b A + ... in FP32.     */
+/* Clipping applies only to the operands of a product: the linear terms use  */
+/* the unclipped tensors.                                                    */
+/* ------------------------------------------------------------------------- */
+
+/* FP64 -> BF16 bits, one round to nearest even (no intermediate FP32 step):
+ * the value is scaled by a power of two so that the BF16 quantum is 1,
+ * rounded to an integer (ties to even), and scaled back. */
+uint16_t oracle_bf16_rne_f64(double d) {
+  if (isnan(d)) return 0x7FC0u;
+  uint16_t sign = signbit(d) ? 0x8000u : 0u;
+  double a = fabs(d);
+  if (a == 0.0) return sign;
+  int e;
+  frexp(a, &e);           /* a = f 2^e, f in [1/2, 1) */
+  int q = e - 8;          /* quantum of 8 significant bits */
+  if (q < -133) q = -133; /* BF16 subnormal quantum */
+  double v = ldexp(nearbyint(ldexp(a, -q)), q);
+  if (v >= 0x1p128) return (uint16_t)(sign | 0x7F80u);
+  float f = (float)v; /* exact: v has at most 8 significant bits */
+  uint32_t u;
+  memcpy(&u, &f, 4);
+  return (uint16_t)(sign | (u >> 16));
+}
+
+/* out = BF16_RNE(RN(RN(a x) + RN(b y))) elementwise, in FP32. */
+void oracle_axpby_bf16(const uint16_t* x, const uint16_t* y, int64_t n, float a, float b, uint16_t* out) {
+  for (int64_t i = 0; i < n; ++i) {
+    float ax = a * bf16_to_float(x[i]);
+    float by = b * bf16_to_float(y[i]);
+    float s = ax + by;
+    out[i] = oracle_bf16_rne(s);
+  }
+}
+
+/* BF16 result of the NVFP4 product L R^T, L [ml, k], R [nr, k] given as
+ * clipped BF16 tensors, each quantised along k (R given transposed when
+ * r_transposed: R^T [k, nr] row-major, quantised down its columns). */
+static int ns_product(const uint16_t* l, int64_t ml, const uint16_t* rsrc, int64_t nr, int64_t k, int r_transposed,
+                      uint16_t* out) {
+  oracle_cfg cfg;
+  memset(&cfg, 0, sizeof(cfg));
+  uint8_t* lc = (uint8_t*)malloc((size_t)(ml * k / 2 + 1));
+  uint8_t* ls = (uint8_t*)malloc((size_t)(ml * k / 16 + 1));
+  uint8_t* rc = (uint8_t*)malloc((size_t)(nr * k / 2 + 1));
+  uint8_t* rs = (uint8_t*)malloc((size_t)(nr * k / 16 + 1));
+  double* d = (double*)malloc((size_t)(ml * nr + 1) * sizeof(double));
+  int st = ORACLE_ERR_INVALID_ARG;
+  float lsc = 0.0f, rsc = 0.0f;
+  if (lc && ls && rc && rs && d) {
+    st = oracle_quantize(l, ml, k, k, &cfg, lc, ls, &lsc);
+    if (st == ORACLE_OK) {
+      if (r_transposed) {
+        cfg.transpose = 1;
+        st = oracle_quantize(rsrc, k, nr, nr, &cfg, rc, rs, &rsc);
+      } else {
+        st = oracle_quantize(rsrc, nr, k, k, &cfg, rc, rs, &rsc);
+      }
+    }
+    if (st == ORACLE_OK) {
+      oracle_gemm_f64(lc, ls, lsc, rc, rs, rsc, ml, nr, k, d);
+      for (int64_t i = 0; i < ml * nr; ++i) out[i] = oracle_bf16_rne_f64(d[i]);
+    }
+  }
+  free(lc);
+  free(ls);
+  free(rc);
+  free(rs);
+  free(d);
+  return st;
+}
+
+static void clip_to_percentile(const uint16_t* x, int64_t count, double p, float* q, uint16_t* out) {
+  *q = oracle_abs_percentile_bf16(x, count, p);
+  oracle_clip_bf16(x, count, *q, out);
+}
+
+int oracle_ns_step(const uint16_t* x, int64_t m, int64_t n, float a, float b, float c, double p, uint16_t* out,
+                   oracle_ns_trace* trace) {
+  if (m <= 0 || n <= 0 || m % 32 != 0 || n % 32 != 0) return ORACLE_ERR_UNSUPPORTED_SHAPE;
+  size_t mn = (size_t)(m * n), mm = (size_t)(m * m);
+  uint16_t* xc = (uint16_t*)malloc(mn * 2);
+  uint16_t* am = (uint16_t*)malloc(mm * 2);
+  uint16_t* ac = (uint16_t*)malloc(mm * 2);
+  uint16_t* a2 = (uint16_t*)malloc(mm * 2);
+  uint16_t* bm = (uint16_t*)malloc(mm * 2);
+  uint16_t* bc = (uint16_t*)malloc(mm * 2);
+  uint16_t* bx = (uint16_t*)malloc(mn * 2);
+  float qx = 0.0f, qa = 0.0f, qb = 0.0f;
+  int st = ORACLE_ERR_INVALID_ARG;
+  if (xc && am && ac && a2 && bm && bc && bx) {
+    clip_to_percentile(x, (int64_t)mn, p, &qx, xc);
+    st = ns_product(xc, m, xc, m, n, 0, am); /* A = X X^T */
+    if (st == ORACLE_OK) {
+      clip_to_percentile(am, (int64_t)mm, p, &qa, ac);
+      st = ns_product(ac, m, ac, m, m, 0, a2); /* A A^T */
+    }
+    if (st == ORACLE_OK) {
+      oracle_axpby_bf16(am, a2, (int64_t)mm, b, c, bm); /* B = b A + c A A^T */
+      clip_to_percentile(bm, (int64_t)mm, p, &qb, bc);
+      st = ns_product(bc, m, xc, n, m, 1, bx); /* B X: R = X^T, given as X [m, n] */
+    }
+    if (st == ORACLE_OK) {
+      float one = 1.0f;
+      oracle_axpby_bf16(x, bx, (int64_t)mn, a, one, out); /* X' = a X + B X */
+      if (trace) {
+        trace->qx = qx;
+        trace->qa = qa;
+        trace->qb = qb;
+        if (trace->xc) memcpy(trace->xc, xc, mn * 2);
+        if (trace->a) memcpy(trace->a, am, mm * 2);
+        if (trace->ac) memcpy(trace->ac, ac, mm * 2);
+        if (trace->a2) memcpy(trace->a2, a2, mm * 2);
+        if (trace->b) memcpy(trace->b, bm, mm * 2);
+        if (trace->bc) memcpy(trace->bc, bc, mm * 2);
+        if (trace->bx) memcpy(trace->bx, bx, mn * 2);
+      }
+    }
+  }
+  free(xc);
+  free(am);
+  free(ac);
+  free(a2);
+  free(bm);
+  free(bc);
+  free(bx);
+  return st;
 }

@@ -127,7 +127,15 @@ int oracle_qadamw_v_encode(const float* v, int64_t rows, int64_t cols, uint64_t 
 void oracle_qadamw_v_decode(const uint8_t* codes, const uint8_t* sf, float tensor_scale, const uint16_t* tile_mean,
                             int64_t rows, int64_t cols, uint64_t rht_seed, float* v_out);
 
-/* LoRA-SVD projection forward: NVFP4 GEMM of X and W_res plus beta * BF16(X L1^T) L2^T, in FP64. */
+/* LoRA-SVD projection forward: NVFP4 GEMM of X and W_res plus beta * BF16(X L1^T) L2^T, in FP64.
+ * oracle_lora_down gives the branch's intermediate U = BF16(X L1^T) [T, r] and its exact FP64 sums
+ * (either output may be NULL); the sampled form evaluates Y at (t_idx[c], n_idx[c]) only. */
+void oracle_lora_down(const uint16_t* x, const uint16_t* l1, int64_t T, int64_t din, int64_t r, uint16_t* u_bf16,
+                      double* u_exact);
+void oracle_lora_forward_sampled(const uint8_t* xq_codes, const uint8_t* xq_sf, float xq_scale,
+                                 const uint8_t* wq_codes, const uint8_t* wq_sf, float wq_scale, const uint16_t* x,
+                                 const uint16_t* l1, const uint16_t* l2, double beta, int64_t din, int64_t r,
+                                 const int64_t* t_idx, const int64_t* n_idx, int64_t count, double* out);
 void oracle_lora_forward(const uint8_t* xq_codes, const uint8_t* xq_sf, float xq_scale, const uint8_t* wq_codes,
                          const uint8_t* wq_sf, float wq_scale, const uint16_t* x, const uint16_t* l1,
                          const uint16_t* l2, double beta, int64_t T, int64_t din, int64_t dout, int64_t r,
@@ -136,6 +144,24 @@ void oracle_lora_forward(const uint8_t* xq_codes, const uint8_t* xq_sf, float xq
 /* Nearest-rank percentile p (0..100] of |x| over n BF16 values, and clipping to [-c, c]. */
 float oracle_abs_percentile_bf16(const uint16_t* x, int64_t n, double p);
 void oracle_clip_bf16(const uint16_t* x, int64_t n, float c, uint16_t* out);
+
+/* Newton-Schulz step of the Root optimizer with NVFP4 products (see oracle.c for the reading).
+ * x, out: BF16 [m, n]; m % 32 == 0, n % 32 == 0.  trace (may be NULL) receives the clip
+ * thresholds and, where its pointers are not NULL, the step's BF16 intermediates. */
+uint16_t oracle_bf16_rne_f64(double d);
+void oracle_axpby_bf16(const uint16_t* x, const uint16_t* y, int64_t n, float a, float b, uint16_t* out);
+typedef struct oracle_ns_trace {
+  float qx, qa, qb;  /* p-th percentile magnitudes of X, A and B */
+  uint16_t* xc;      /* [m, n]  X clipped                         */
+  uint16_t* a;       /* [m, m]  A = Q(Xc) Q(Xc)^T                 */
+  uint16_t* ac;      /* [m, m]  A clipped                         */
+  uint16_t* a2;      /* [m, m]  Q(Ac) Q(Ac)^T                     */
+  uint16_t* b;       /* [m, m]  B = b A + c A2                    */
+  uint16_t* bc;      /* [m, m]  B clipped                         */
+  uint16_t* bx;      /* [m, n]  Q(Bc) Q(Xc^T)^T                   */
+} oracle_ns_trace;
+int oracle_ns_step(const uint16_t* x, int64_t m, int64_t n, float a, float b, float c, double p, uint16_t* out,
+                   oracle_ns_trace* trace);
 
 #ifdef __cplusplus
 }

@@ -59,3 +59,26 @@ def test_branch_rounds_its_intermediate_to_bf16():
     # and the rounding matters: without it the result differs
     unrounded = 2.0 * ((f(x) @ f(l1).T) @ f(l2).T)
     assert not np.allclose(y, unrounded.numpy(), rtol=1e-9, atol=0)
+
+
+def test_down_step_is_the_bf16_rounded_fp64_product():
+    x = syn.as_u16(syn.normal_bf16((24, 96), seed=9))
+    l1 = syn.as_u16(syn.normal_bf16((40, 96), seed=10))
+    u, ue = oracle.lora_down(x, l1)
+    f = lambda a: torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).double()  # noqa: E731
+    ref = f(x) @ f(l1).T
+    assert np.allclose(ue, ref.numpy(), rtol=1e-13, atol=0)
+    assert np.array_equal(u, _bits(ref.float()))
+
+
+def test_sampled_forward_equals_full_forward():
+    x = syn.as_u16(syn.normal_bf16((48, 64), seed=11))
+    w = syn.as_u16(syn.normal_bf16((80, 64), seed=12, std=0.02))
+    l1 = syn.as_u16(syn.normal_bf16((16, 64), seed=13))
+    l2 = syn.as_u16(syn.normal_bf16((80, 16), seed=14))
+    xq, wq = _quant(x), _quant(w, block=1)
+    full = oracle.lora_forward(xq, wq, x, l1, l2, 0.75)
+    rng = np.random.default_rng(15)
+    t = rng.integers(0, 48, size=200)
+    n = rng.integers(0, 80, size=200)
+    assert np.array_equal(oracle.lora_forward_sampled(xq, wq, x, l1, l2, 0.75, t, n), full[t, n])
