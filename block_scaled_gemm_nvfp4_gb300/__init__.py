@@ -36,7 +36,7 @@ EXPORTS = [
     "nvfp4_quantize_noalloc", "nvfp4_dequantize",
     "nvfp4_gemm_workspace_size", "nvfp4_gemm", "nvfp4_gemm_quantize", "nvfp4_linear_workspace_size",
     "nvfp4_linear_fprop", "nvfp4_linear_dgrad", "nvfp4_linear_wgrad",
-    "nvfp4_check_device_status", "nvfp4_debug_gemm_skip_load",
+    "nvfp4_check_device_status", "nvfp4_debug_gemm_skip_load", "nvfp4_debug_quantize_skip_load",
     "nvfp4_qadamw_workspace_size", "nvfp4_qadamw_m_encode", "nvfp4_qadamw_m_decode", "nvfp4_qadamw_v_encode",
     "nvfp4_qadamw_v_decode",
 ]
@@ -144,6 +144,7 @@ def lib():
             "nvfp4_linear_wgrad": (I32, [P, P, I64, I64, I64, PCFG, PCFG, I32, P, P, SZ, P]),
             "nvfp4_check_device_status": (I32, [P, P]),
             "nvfp4_debug_gemm_skip_load": (None, [I32]),
+            "nvfp4_debug_quantize_skip_load": (None, [I32]),
             "nvfp4_qadamw_workspace_size": (I32, [PSZ]),
             "nvfp4_qadamw_m_encode": (I32, [P, I64, I64, ctypes.c_uint64, ctypes.c_uint64, ctypes.c_uint64, P, P, P, P,
                                             SZ, P]),
@@ -392,6 +393,12 @@ NVFP4_DEFAULT_RHT_SEED = 0x5EEDC0DE0F4
 def nvfp4_debug_gemm_skip_load(enable=True):
     """Failure-detection test hook (see include/nvfp4.h)."""
     lib().nvfp4_debug_gemm_skip_load(1 if enable else 0)
+
+
+def nvfp4_debug_quantize_skip_load(pass_=2):
+    """Quantiser failure-detection test hook (see include/nvfp4.h): 1 = amax
+    pass, 2 = encode pass, 0 = off."""
+    lib().nvfp4_debug_quantize_skip_load(int(pass_))
 
 
 def nvfp4_check_device_status(workspace, stream=None):

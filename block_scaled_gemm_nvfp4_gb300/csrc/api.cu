@@ -25,6 +25,10 @@ int device_sm_count() {
 
 namespace {
 
+// One-shot failure-detection test hooks (nvfp4_debug_*_skip_load).
+std::atomic<int> g_skip_load_once{0};
+std::atomic<int> g_quant_skip_once{0};  // 0 off, 1 amax pass, 2 encode pass
+
 constexpr size_t kAlign = 256;
 size_t align_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
 
@@ -107,6 +111,7 @@ nvfp4_status quantize_into(const void* x, int64_t rows, int64_t cols, int64_t ld
   a.out[0] = make_out(cfg, codes, sf, scale);
   a.status = status;
   a.partials = partials;
+  a.skip_load_pass = g_quant_skip_once.exchange(0);
   return cuda_status(launch_quantize(a, stream));
 }
 
@@ -137,7 +142,6 @@ nvfp4_status check_tensor(const nvfp4_tensor* t) {
   return NVFP4_OK;
 }
 
-std::atomic<int> g_skip_load_once{0};
 
 nvfp4_status gemm_into(const nvfp4_tensor* a, const nvfp4_tensor* b, int32_t out_dtype, void* d, int64_t ldd,
                        uint32_t* status, cudaStream_t stream) {
@@ -253,6 +257,7 @@ nvfp4_status nvfp4_quantize_dual(const void* x, int64_t rows, int64_t cols, int6
   a.out[1] = make_out(*cfg_b, codes_b, sf_b, tensor_scale_b);
   a.status = reinterpret_cast<uint32_t*>(ws);
   a.partials = reinterpret_cast<uint32_t*>(ws + kWsHeaderBytes);
+  a.skip_load_pass = g_quant_skip_once.exchange(0);
   return cuda_status(launch_quantize(a, reinterpret_cast<cudaStream_t>(stream)));
 }
 
@@ -277,6 +282,7 @@ nvfp4_status nvfp4_quantize_given_amax(const void* x, int64_t rows, int64_t cols
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   a.status = reinterpret_cast<uint32_t*>(ws);
   a.partials = reinterpret_cast<uint32_t*>(ws + kWsHeaderBytes);
+  a.skip_load_pass = g_quant_skip_once.exchange(0);
   return cuda_status(launch_quantize(a, reinterpret_cast<cudaStream_t>(stream)));
 }
 
@@ -293,6 +299,7 @@ nvfp4_status nvfp4_quantize_noalloc(const void* x, int64_t rows, int64_t cols, i
   a.ldx = ldx;
   a.n_out = 1;
   a.out[0] = make_out(*cfg, codes, sf, tensor_scale);
+  a.skip_load_pass = g_quant_skip_once.exchange(0);
   return cuda_status(launch_quantize_noalloc(a, reinterpret_cast<cudaStream_t>(stream)));
 }
 
@@ -628,6 +635,8 @@ nvfp4_status nvfp4_linear_wgrad(const void* dy, const void* x, int64_t tokens, i
 }
 
 void nvfp4_debug_gemm_skip_load(int32_t enable) { g_skip_load_once.store(enable ? 1 : 0); }
+
+void nvfp4_debug_quantize_skip_load(int32_t pass) { g_quant_skip_once.store(pass == 1 || pass == 2 ? pass : 0); }
 
 nvfp4_status nvfp4_check_device_status(const void* workspace, nvfp4_stream_t stream) {
   if (!workspace) return NVFP4_ERR_INVALID_ARG;

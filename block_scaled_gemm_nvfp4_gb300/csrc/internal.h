@@ -40,6 +40,10 @@ struct QuantArgs {
   QuantOut out[kMaxQuantOutputs];
   uint32_t* status;    // device status word
   uint32_t* partials;  // kMaxAmaxPartials slots
+  // failure-detection test hook (see nvfp4_debug_quantize_skip_load): 1 or 2
+  // makes CTA 0 of the amax (1) or encode (2) pass leave its first stage
+  // unfilled, so its bounded wait runs out; 0 = off
+  int skip_load_pass;
 };
 
 cudaError_t launch_quantize(const QuantArgs& a, cudaStream_t stream);

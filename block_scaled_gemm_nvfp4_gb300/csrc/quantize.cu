@@ -94,6 +94,7 @@ struct TileParams {
   int n_out;
   int amax_shared;  // two outputs, neither transformed: output 1 reuses output 0's amax
   int num_partials;
+  int skip_first_load;  // test hook: CTA 0 of this pass never loads its first tile
   uint32_t* status;
 };
 
@@ -388,7 +389,11 @@ __global__ void __launch_bounds__(kThreads, 2) quant_tiles(const __grid_constant
     const int64_t it = blockIdx.x + i * G;
     return PASS == 1 ? p.num_tiles - 1 - it : it;
   };
+  // Failure-detection test hook: CTA 0's first stage is never filled, so
+  // its bounded wait runs out and the timeout path below is taken.
+  const bool skip0 = p.skip_first_load && blockIdx.x == 0;
   auto issue = [&](int64_t i) {
+    if (skip0 && i == 0) return;
     const int s = static_cast<int>(i % kStages);
     const int64_t tile = tile_of(i);
     const int32_t x0 = static_cast<int32_t>((tile % p.tiles_c) * kTile);
@@ -410,12 +415,29 @@ __global__ void __launch_bounds__(kThreads, 2) quant_tiles(const __grid_constant
   }
 
   uint32_t tmax[kMaxQuantOutputs] = {0u, 0u};
+  bool timed_out = false;  // block-uniform
   for (int64_t i = 0; i < n_my; ++i) {
     const int s = static_cast<int>(i % kStages);
     const uint32_t parity = static_cast<uint32_t>((i / kStages) & 1);
     const bool ok = ptx::mbar_wait(&full[s], parity, &abort_flag);
     if (__syncthreads_or(!ok)) {
-      if (tid == 0) ptx::set_status(p.status, kDevTimeout);
+      // A wait ran out: record it, let every copy this CTA still has in
+      // flight land (bounded waits) before the CTA leaves, and make the
+      // failure visible in the outputs: pass 0 leaves a NaN-like partial
+      // amax, so pass 1 writes tensor_scale = NaN and encodes nothing;
+      // pass 1 writes tensor_scale = NaN itself.
+      timed_out = true;
+      if (tid == 0) {
+        ptx::set_status(p.status, kDevTimeout);
+        for (int64_t j = i; j < i + kStages && j < n_my; ++j) {
+          if (skip0 && j == 0) continue;  // never issued
+          volatile int never = 0;
+          ptx::mbar_wait(&full[j % kStages], static_cast<uint32_t>((j / kStages) & 1), &never);
+        }
+        if (PASS == 1) {
+          for (int o = 0; o < p.n_out; ++o) *p.out[o].tensor_scale = __uint_as_float(0x7FC00000u);
+        }
+      }
       break;
     }
     const uint8_t* stage = ring + s * kStageBytes;
@@ -467,7 +489,7 @@ __global__ void __launch_bounds__(kThreads, 2) quant_tiles(const __grid_constant
 #pragma unroll
     for (int o = 0; o < kMaxQuantOutputs; ++o) {
       if (o >= p.n_out || (o == 1 && p.amax_shared)) break;
-      const uint32_t m = block_max(tmax[o], red);
+      const uint32_t m = timed_out ? 0xFFFFFFFFu : block_max(tmax[o], red);
       if (tid == 0 && !p.out[o].amax_in) p.out[o].partials[blockIdx.x] = m;
     }
   }
@@ -516,13 +538,42 @@ bool make_x_map(CUtensorMap* map, const uint16_t* x, int64_t rows, int64_t cols,
 // the partial-amax slots of the amax pass, in one file-scope device array.
 // Every GPU that loads the library holds it until the process exits.  In
 // host code `g_noalloc_scratch` only names the symbol; its device address
-// comes from cudaGetSymbolAddress, once per device.
+// comes from cudaGetSymbolAddress, looked up once per CUDA context (with that
+// context current) and cached under the context's unique ID, so a context
+// created after a reset gets its own lookup instead of a stale address.
 constexpr size_t kNoAllocScratchBytes = kWsHeaderBytes + kQuantScratchBytes;
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 
-constexpr int kMaxDevices = 64;
+constexpr int kMaxContexts = 64;
 std::mutex g_noalloc_mutex;
-void* g_noalloc_ptr[kMaxDevices] = {nullptr};
+unsigned long long g_noalloc_ctx_id[kMaxContexts] = {0};
+void* g_noalloc_ptr[kMaxContexts] = {nullptr};
+int g_noalloc_count = 0;
+
+using PfnCtxGetCurrent = CUresult (*)(CUcontext*);
+using PfnCtxGetId = CUresult (*)(CUcontext, unsigned long long*);
+
+template <typename F>
+F driver_fn(const char* name) {
+  void* ptr = nullptr;
+  cudaDriverEntryPointQueryResult q;
+  if (cudaGetDriverEntryPointByVersion(name, &ptr, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+      q != cudaDriverEntryPointSuccess)
+    return nullptr;
+  return reinterpret_cast<F>(ptr);
+}
+
+// Unique ID of the calling thread's current context (0 if there is none).
+cudaError_t current_ctx_id(unsigned long long* id) {
+  static PfnCtxGetCurrent get_current = driver_fn<PfnCtxGetCurrent>("cuCtxGetCurrent");
+  static PfnCtxGetId get_id = driver_fn<PfnCtxGetId>("cuCtxGetId");
+  *id = 0;
+  if (!get_current || !get_id) return cudaErrorNotSupported;
+  CUcontext ctx = nullptr;
+  if (get_current(&ctx) != CUDA_SUCCESS) return cudaErrorDeviceUninitialized;
+  if (ctx && get_id(ctx, id) != CUDA_SUCCESS) return cudaErrorDeviceUninitialized;
+  return cudaSuccess;
+}
 
 }  // namespace
 
@@ -530,15 +581,31 @@ cudaError_t noalloc_scratch(void** ptr) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
   std::lock_guard<std::mutex> lock(g_noalloc_mutex);
-  if (!g_noalloc_ptr[dev]) {
-    void* p = nullptr;
-    e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
-    if (e != cudaSuccess) return e;
-    g_noalloc_ptr[dev] = p;
+  unsigned long long id = 0;
+  e = current_ctx_id(&id);
+  if (e != cudaSuccess) return e;
+  for (int i = 0; id != 0 && i < g_noalloc_count; ++i) {
+    if (g_noalloc_ctx_id[i] == id) {
+      *ptr = g_noalloc_ptr[i];
+      return cudaSuccess;
+    }
   }
-  *ptr = g_noalloc_ptr[dev];
+  // First call in this context (the lookup also makes the device's primary
+  // context current if no context was).
+  void* p = nullptr;
+  e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+  if (e != cudaSuccess) return e;
+  if (id == 0) {
+    e = current_ctx_id(&id);
+    if (e != cudaSuccess) return e;
+  }
+  if (id != 0 && g_noalloc_count < kMaxContexts) {
+    g_noalloc_ctx_id[g_noalloc_count] = id;
+    g_noalloc_ptr[g_noalloc_count] = p;
+    ++g_noalloc_count;
+  }
+  *ptr = p;
   return cudaSuccess;
 }
 
@@ -606,10 +673,12 @@ cudaError_t launch_quantize(const QuantArgs& a, cudaStream_t stream) {
   g = std::max<int64_t>(std::min<int64_t>(g, p.num_tiles), 1);
   p.num_partials = static_cast<int>(g);
   if (scan) {
+    p.skip_first_load = a.skip_load_pass == 1;
     quant_tiles<0><<<static_cast<int>(g), kThreads, kSmemBytes, stream>>>(xmap, p);
     err = cudaGetLastError();
     if (err != cudaSuccess) return err;
   }
+  p.skip_first_load = a.skip_load_pass == 2;
   quant_tiles<1><<<static_cast<int>(g), kThreads, kSmemBytes, stream>>>(xmap, p);
   return cudaGetLastError();
 }

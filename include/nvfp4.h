@@ -124,7 +124,9 @@ size_t nvfp4_sf_bytes(int64_t qr, int64_t qk, int32_t sf_layout);
  * qr % 16 == 0; ldx % 8 == 0 and x 16-byte aligned; codes 8-byte aligned;
  * MMA-layout sf 16-byte aligned.
  * Non-finite input: the device status word is set to NVFP4_ERR_NONFINITE,
- * tensor_scale[0] is set to NaN and codes/sf are left unspecified.
+ * tensor_scale[0] is set to NaN and codes/sf are left unspecified.  A
+ * bounded wait that ran out: NVFP4_ERR_TIMEOUT in the status word and, as
+ * well, tensor_scale[0] = NaN (codes/sf unspecified).
  * Workspace: nvfp4_quantize_workspace_size bytes, device memory.
  * Sources: the encode steps listed at the top of this header.
  */
@@ -191,14 +193,20 @@ nvfp4_status nvfp4_quantize_given_amax(const void* x, int64_t rows, int64_t cols
  * the library interface only.
  * Same arguments, shape rules and outputs as nvfp4_quantize, with a limit of
  * rows * cols <= 2^31 elements (NVFP4_ERR_UNSUPPORTED_SHAPE beyond).
- * Non-finite input is reported only through tensor_scale[0] = NaN.
- * The first call on a device looks up the array's device address
- * (cudaGetSymbolAddress) with that device current; make that first call
- * before any stream capture.  It calls no cudaMalloc, cudaFree or allocating
- * library routine.  All calls share the one array, which keeps the last
- * call's contents (the status word is cleared at the start of every call):
- * calls that overlap on the GPU -- on different streams, or from host
- * threads without ordering between them -- race and must not be issued.
+ * Errors found on the device have one channel here, since the status word
+ * sits in the library's array where the caller cannot read it: after the
+ * call, tensor_scale[0] is NaN if the input held inf or NaN, or if one of
+ * the kernel's bounded waits ran out (codes and sf are then unspecified);
+ * otherwise it is the finite tensor scale.
+ * The first call in a CUDA context looks up the array's device address
+ * (cudaGetSymbolAddress) with that context current and caches it under the
+ * context's unique ID; make that first call before any stream capture.  It
+ * calls no cudaMalloc, cudaFree or allocating library routine.  All calls
+ * share the one array, which keeps the last call's contents (the status
+ * word is cleared at the start of every call, the partial maxima are
+ * rewritten by every call before they are read): calls that overlap on the
+ * GPU -- on different streams, or from host threads without ordering
+ * between them -- race and must not be issued.
  */
 nvfp4_status nvfp4_quantize_noalloc(const void* x, int64_t rows, int64_t cols, int64_t ldx,
                                     const nvfp4_quant_cfg* cfg, void* codes, void* sf, float* tensor_scale,
@@ -359,6 +367,20 @@ nvfp4_status nvfp4_check_device_status(const void* workspace, nvfp4_stream_t str
  * itself when the launch takes it.  Nothing faults, traps or hangs.
  */
 void nvfp4_debug_gemm_skip_load(int32_t enable);
+
+/*
+ * Failure-detection test hook for the quantiser.  pass = 1 (the amax pass)
+ * or 2 (the encode pass): the next quantiser launch made by any entry point
+ * above leaves CTA 0's first tile of that pass unfilled, so its bounded wait
+ * runs out after about one second.  The CTA records NVFP4_ERR_TIMEOUT in
+ * the status word, lets its other copies in flight land, and leaves; the
+ * tensor scale of every output becomes NaN (an amax-pass timeout leaves a
+ * NaN-like partial maximum, so the encode pass writes NaN and encodes
+ * nothing).  Codes and scales of that call are unspecified; the CUDA context
+ * stays usable.  A pass the call does not run (the amax pass under a
+ * supplied amax) is not affected.  One-shot; pass = 0 clears it.
+ */
+void nvfp4_debug_quantize_skip_load(int32_t pass);
 
 #ifdef __cplusplus
 }

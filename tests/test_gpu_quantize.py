@@ -136,3 +136,19 @@ def test_sweep_full_size_sampled(mode, shape_idx):
         r0 = int(gidx) * 16
         ref = oracle.quantize_rows(xs, o, r0, r0 + 16)
         assert_quant_equal(q, ref, rows=np.arange(r0, r0 + 16))
+
+
+@pytest.mark.parametrize("pass_", [1, 2], ids=["amax-pass", "encode-pass"])
+def test_quantize_timeout_is_reported_and_context_survives(pass_):
+    x = syn.normal_bf16((512, 1024), seed=41)
+    g, o = cfgs(rounding=1, rht=1)
+    ws = torch.zeros(nv.nvfp4_quantize_workspace_size(512, 1024, g), dtype=torch.uint8, device=DEV)
+    xd = x.to(DEV)
+    nv.nvfp4_debug_quantize_skip_load(pass_)
+    q = nv.nvfp4_quantize(xd, g, workspace=ws)
+    assert nv.nvfp4_check_device_status(ws) == nv.NVFP4_ERR_TIMEOUT
+    assert np.isnan(q.tensor_scale.cpu().numpy()[0])
+    # one-shot hook; the context is still usable and the next call is exact
+    q = nv.nvfp4_quantize(xd, g, workspace=ws)
+    assert nv.nvfp4_check_device_status(ws) == nv.NVFP4_OK
+    assert_quant_equal(q, oracle.quantize(syn.as_u16(x), o))
