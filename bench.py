@@ -487,6 +487,35 @@ def run_case(args):
         def call():
             nv.nvfp4_gemm_quantize(qa, qb, amax_in, d=d, store_d=store_d, amax_out=amax_out, out=q, workspace=ws)
         work, unit = 2.0 * M * N * K / 1e12, "TFLOP/s"
+    elif kind == "lora":
+        # LoRA-SVD projection forward: U = BF16(X L1^T), then the NVFP4 GEMM with
+        # the rank-r branch in the same accumulator (work counted: the NVFP4
+        # GEMM's 2 M N K plus the branch's 2 T r (din + dout))
+        T, din, dout, r = (int(v) for v in parts[:4])
+        xq = nv.nvfp4_quantize(syn.normal_bf16((T, din), seed=1).to(dev), nv.quant_cfg())
+        wq = nv.nvfp4_quantize(syn.normal_bf16((dout, din), std=0.02, seed=2).to(dev), nv.quant_cfg(block=1))
+        x = syn.normal_bf16((T, din), seed=1).to(dev)
+        l1 = syn.normal_bf16((r, din), std=0.02, seed=3).to(dev)
+        l2 = syn.normal_bf16((dout, r), std=0.02, seed=4).to(dev)
+        y, u = nv.nvfp4_lora_forward(xq, wq, x, l1, l2, 1.0)
+        ws = torch.zeros(nv.nvfp4_lora_workspace_size(T, r), dtype=torch.uint8, device=dev)
+
+        def call():
+            nv.nvfp4_lora_forward(xq, wq, x, l1, l2, 1.0, y=y, u=u, workspace=ws)
+        work, unit = (2.0 * T * dout * din + 2.0 * T * r * (din + dout)) / 1e12, "TFLOP/s"
+    elif kind == "ns":
+        # one Newton-Schulz step with NVFP4 products on an iterate X [m, n]
+        # (quintic coefficients); work counted: the three products'
+        # 2 m m n + 2 m m m + 2 m m n FLOP
+        m, n = int(parts[0]), int(parts[1])
+        g = syn.normal_bf16((m, n), seed=5).float()
+        x = (g / g.norm()).to(torch.bfloat16).to(dev)
+        out = torch.empty_like(x)
+        ws = torch.zeros(nv.nvfp4_ns_workspace_size(m, n), dtype=torch.uint8, device=dev)
+
+        def call():
+            nv.nvfp4_ns_step(x, 15.0 / 8.0, -10.0 / 8.0, 3.0 / 8.0, out=out, workspace=ws)
+        work, unit = (4.0 * m * m * n + 2.0 * m * m * m) / 1e12, "TFLOP/s"
     elif kind == "given":
         R, C = int(parts[0]), int(parts[1])
         cfg = modes[parts[2] if len(parts) > 2 else "row"]

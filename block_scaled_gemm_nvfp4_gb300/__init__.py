@@ -38,7 +38,9 @@ EXPORTS = [
     "nvfp4_linear_fprop", "nvfp4_linear_dgrad", "nvfp4_linear_wgrad",
     "nvfp4_check_device_status", "nvfp4_debug_gemm_skip_load", "nvfp4_debug_quantize_skip_load",
     "nvfp4_qadamw_workspace_size", "nvfp4_qadamw_m_encode", "nvfp4_qadamw_m_decode", "nvfp4_qadamw_v_encode",
-    "nvfp4_qadamw_v_decode",
+    "nvfp4_qadamw_v_decode", "nvfp4_lora_workspace_size", "nvfp4_lora_forward",
+    "nvfp4_abs_percentile_workspace_size", "nvfp4_abs_percentile_bf16", "nvfp4_clip_bf16", "nvfp4_axpby_bf16",
+    "nvfp4_ns_workspace_size", "nvfp4_ns_step",
 ]
 
 
@@ -151,6 +153,15 @@ def lib():
             "nvfp4_qadamw_m_decode": (I32, [P, P, P, I64, I64, ctypes.c_uint64, P, P]),
             "nvfp4_qadamw_v_encode": (I32, [P, I64, I64, ctypes.c_uint64, P, P, P, P, P, SZ, P]),
             "nvfp4_qadamw_v_decode": (I32, [P, P, P, P, I64, I64, ctypes.c_uint64, P, P]),
+            "nvfp4_lora_workspace_size": (I32, [I64, I64, PSZ]),
+            "nvfp4_lora_forward": (I32, [PT, PT, P, I64, P, P, I64, ctypes.c_float, I32, P, I64, P, P, SZ, P]),
+            "nvfp4_abs_percentile_workspace_size": (I32, [PSZ]),
+            "nvfp4_abs_percentile_bf16": (I32, [P, I64, ctypes.c_double, P, P, SZ, P]),
+            "nvfp4_clip_bf16": (I32, [P, I64, P, P, P]),
+            "nvfp4_axpby_bf16": (I32, [P, P, I64, ctypes.c_float, ctypes.c_float, P, P]),
+            "nvfp4_ns_workspace_size": (I32, [I64, I64, PSZ]),
+            "nvfp4_ns_step": (I32, [P, I64, I64, ctypes.c_float, ctypes.c_float, ctypes.c_float, ctypes.c_double, P,
+                                    P, SZ, P]),
         }
         for name, (res, args) in sigs.items():
             fn = getattr(L, name)
@@ -479,4 +490,95 @@ def nvfp4_qadamw_v_decode(state, rht_seed, out=None, stream=None):
                                      _ptr(state.tile_mean), state.rows, state.cols, rht_seed, _ptr(out),
                                      _stream(stream))
     _check(st, "nvfp4_qadamw_v_decode")
+    return out
+
+
+# --- LoRA-SVD projection -----------------------------------------------------
+def nvfp4_lora_workspace_size(tokens, rank):
+    n = ctypes.c_size_t(0)
+    _check(lib().nvfp4_lora_workspace_size(tokens, rank, ctypes.byref(n)), "nvfp4_lora_workspace_size")
+    return n.value
+
+
+def nvfp4_lora_forward(xq, wq, x, l1, l2, beta, out_dtype=NVFP4_OUT_BF16, y=None, u=None, workspace=None,
+                       stream=None):
+    """Y = Q(X) Q(W_res)^T + beta BF16(X L1^T) L2^T (see include/nvfp4.h).
+    x: BF16 [T, din] (unit column stride), l1 BF16 [r, din], l2 BF16 [dout, r]
+    (contiguous).  Returns (y, u)."""
+    assert x.dtype == torch.bfloat16 and x.dim() == 2 and x.stride(1) == 1
+    assert l1.dtype == torch.bfloat16 and l1.is_contiguous() and l2.dtype == torch.bfloat16 and l2.is_contiguous()
+    T, din = x.shape
+    r = l1.shape[0]
+    dout = wq.rows
+    dev = x.device
+    if y is None:
+        dt = torch.float32 if out_dtype == NVFP4_OUT_F32 else torch.bfloat16
+        y = torch.empty((T, dout), dtype=dt, device=dev)
+    if u is None:
+        u = torch.empty((T, r), dtype=torch.bfloat16, device=dev)
+    if workspace is None:
+        workspace = _alloc_ws(nvfp4_lora_workspace_size(T, r), dev)
+    ta, tb = xq._c(), wq._c()
+    ldx = x.stride(0) if T > 1 else din
+    ldy = y.stride(0) if T > 1 else dout
+    st = lib().nvfp4_lora_forward(ctypes.byref(ta), ctypes.byref(tb), _ptr(x), ldx, _ptr(l1), _ptr(l2), r,
+                                  float(beta), out_dtype, _ptr(y), ldy, _ptr(u), _ptr(workspace), workspace.numel(),
+                                  _stream(stream))
+    _check(st, "nvfp4_lora_forward")
+    return y, u
+
+
+# --- Newton-Schulz step (Q-Root) ---------------------------------------------
+def nvfp4_abs_percentile_bf16(x, p=99.0, q=None, workspace=None, stream=None):
+    """q[0] = nearest-rank p-th percentile of |x| (x: BF16 CUDA tensor, any
+    shape, contiguous).  Returns q (float32 CUDA tensor [1])."""
+    assert x.dtype == torch.bfloat16 and x.is_contiguous()
+    if q is None:
+        q = torch.empty(1, dtype=torch.float32, device=x.device)
+    if workspace is None:
+        n = ctypes.c_size_t(0)
+        _check(lib().nvfp4_abs_percentile_workspace_size(ctypes.byref(n)), "nvfp4_abs_percentile_workspace_size")
+        workspace = _alloc_ws(n.value, x.device)
+    st = lib().nvfp4_abs_percentile_bf16(_ptr(x), x.numel(), float(p), _ptr(q), _ptr(workspace), workspace.numel(),
+                                         _stream(stream))
+    _check(st, "nvfp4_abs_percentile_bf16")
+    return q
+
+
+def nvfp4_clip_bf16(x, q, out=None, stream=None):
+    assert x.dtype == torch.bfloat16 and x.is_contiguous()
+    if out is None:
+        out = torch.empty_like(x)
+    _check(lib().nvfp4_clip_bf16(_ptr(x), x.numel(), _ptr(q), _ptr(out), _stream(stream)), "nvfp4_clip_bf16")
+    return out
+
+
+def nvfp4_axpby_bf16(x, y, a, b, out=None, stream=None):
+    assert x.dtype == torch.bfloat16 and y.dtype == torch.bfloat16 and x.is_contiguous() and y.is_contiguous()
+    assert x.numel() == y.numel()
+    if out is None:
+        out = torch.empty_like(x)
+    _check(lib().nvfp4_axpby_bf16(_ptr(x), _ptr(y), x.numel(), float(a), float(b), _ptr(out), _stream(stream)),
+           "nvfp4_axpby_bf16")
+    return out
+
+
+def nvfp4_ns_workspace_size(m, n):
+    s = ctypes.c_size_t(0)
+    _check(lib().nvfp4_ns_workspace_size(m, n, ctypes.byref(s)), "nvfp4_ns_workspace_size")
+    return s.value
+
+
+def nvfp4_ns_step(x, a, b, c, p=99.0, out=None, workspace=None, stream=None):
+    """One Newton-Schulz step with NVFP4 products on the BF16 iterate x
+    [m, n] (see include/nvfp4.h).  Returns X'."""
+    assert x.dtype == torch.bfloat16 and x.dim() == 2 and x.is_contiguous()
+    m, n = x.shape
+    if out is None:
+        out = torch.empty_like(x)
+    if workspace is None:
+        workspace = _alloc_ws(nvfp4_ns_workspace_size(m, n), x.device)
+    st = lib().nvfp4_ns_step(_ptr(x), m, n, float(a), float(b), float(c), float(p), _ptr(out), _ptr(workspace),
+                             workspace.numel(), _stream(stream))
+    _check(st, "nvfp4_ns_step")
     return out

@@ -24,6 +24,8 @@ UNITS = {
     "dequantize.cu": ["-fmad=false"],
     "gemm.cu": [],
     "qadamw.cu": ["-fmad=false"],
+    "lora.cu": ["-fmad=false"],
+    "ns.cu": ["-fmad=false"],
 }
 
 

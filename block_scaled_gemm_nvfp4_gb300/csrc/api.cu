@@ -4,6 +4,7 @@
 #include <cuda_runtime.h>
 
 #include <atomic>
+#include <cmath>
 #include <cstdint>
 #include <cstring>
 
@@ -404,6 +405,269 @@ nvfp4_status nvfp4_gemm_quantize(const nvfp4_tensor* a, const nvfp4_tensor* b, v
   const cudaError_t e = launch_gemm(g, st);
   if (e == cudaErrorInvalidValue) return NVFP4_ERR_INVALID_ARG;
   return cuda_status(e);
+}
+
+// ------------------------------------------------------- LoRA-SVD projection
+static int64_t lora_rpad(int64_t r) { return (r + 63) / 64 * 64; }
+
+nvfp4_status nvfp4_lora_workspace_size(int64_t tokens, int64_t rank, size_t* bytes) {
+  if (!bytes || tokens < 0) return NVFP4_ERR_INVALID_ARG;
+  if (rank < 8 || rank > 256 || rank % 8 != 0) return NVFP4_ERR_UNSUPPORTED_SHAPE;
+  *bytes = kWsHeaderBytes + align_up(static_cast<size_t>(tokens) * 2 * lora_rpad(rank) * 2);
+  return NVFP4_OK;
+}
+
+nvfp4_status nvfp4_lora_forward(const nvfp4_tensor* xq, const nvfp4_tensor* wq, const void* x, int64_t ldx,
+                                const void* l1, const void* l2, int64_t rank, float beta, int32_t out_dtype, void* y,
+                                int64_t ldy, void* u, void* workspace, size_t workspace_bytes,
+                                nvfp4_stream_t stream) {
+  nvfp4_status s = check_tensor(xq);
+  if (s != NVFP4_OK) return s;
+  s = check_tensor(wq);
+  if (s != NVFP4_OK) return s;
+  if (out_dtype != NVFP4_OUT_BF16 && out_dtype != NVFP4_OUT_F32) return NVFP4_ERR_INVALID_ARG;
+  if (xq->k != wq->k) return NVFP4_ERR_INVALID_ARG;
+  const int64_t T = xq->rows, din = xq->k, dout = wq->rows;
+  if (din % 32 != 0 || din == 0) return NVFP4_ERR_UNSUPPORTED_SHAPE;
+  if (rank < 8 || rank > 256 || rank % 8 != 0) return NVFP4_ERR_UNSUPPORTED_SHAPE;
+  if (xq->sf_layout != NVFP4_SF_MMA || wq->sf_layout != NVFP4_SF_MMA) return NVFP4_ERR_UNSUPPORTED_SHAPE;
+  if (T > (int64_t(1) << 31) || dout > (int64_t(1) << 31) || din > (int64_t(1) << 31))
+    return NVFP4_ERR_UNSUPPORTED_SHAPE;
+  if (!(beta == beta) || beta - beta != 0.0f) return NVFP4_ERR_INVALID_ARG;  // NaN or inf
+  if (T == 0 || dout == 0) return NVFP4_OK;
+  if (!x || !l1 || !l2 || !u || !y) return NVFP4_ERR_INVALID_ARG;
+  if (ldx < din || ldx % 8 != 0 || !aligned16(x) || !aligned16(l1) || !aligned16(l2) || !aligned16(u))
+    return NVFP4_ERR_INVALID_ARG;
+  if (ldy < dout) return NVFP4_ERR_INVALID_ARG;
+  if (!aligned16(xq->codes) || !aligned16(wq->codes) || !aligned16(xq->sf) || !aligned16(wq->sf))
+    return NVFP4_ERR_INVALID_ARG;
+  size_t need = 0;
+  s = nvfp4_lora_workspace_size(T, rank, &need);
+  if (s != NVFP4_OK) return s;
+  if (!workspace || workspace_bytes < need) return NVFP4_ERR_WORKSPACE;
+  if (reinterpret_cast<uintptr_t>(workspace) & 255u) return NVFP4_ERR_INVALID_ARG;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  uint32_t* status = reinterpret_cast<uint32_t*>(ws);
+  uint16_t* uhl = reinterpret_cast<uint16_t*>(ws + kWsHeaderBytes);
+  LoraArgs la{};
+  la.x = static_cast<const uint16_t*>(x);
+  la.T = T;
+  la.din = din;
+  la.ldx = ldx;
+  la.l1 = static_cast<const uint16_t*>(l1);
+  la.r = rank;
+  la.beta = beta;
+  la.sx = xq->tensor_scale;
+  la.sw = wq->tensor_scale;
+  la.u = static_cast<uint16_t*>(u);
+  la.uhl = uhl;
+  la.status = status;
+  cudaError_t e = launch_lora_down(la, st);
+  if (e == cudaErrorInvalidValue) return NVFP4_ERR_INVALID_ARG;
+  if (e != cudaSuccess) return NVFP4_ERR_CUDA;
+  GemmArgs g{};
+  g.a_codes = static_cast<const uint8_t*>(xq->codes);
+  g.a_sf = static_cast<const uint8_t*>(xq->sf);
+  g.a_scale = xq->tensor_scale;
+  g.b_codes = static_cast<const uint8_t*>(wq->codes);
+  g.b_sf = static_cast<const uint8_t*>(wq->sf);
+  g.b_scale = wq->tensor_scale;
+  g.M = T;
+  g.N = dout;
+  g.K = din;
+  g.out_f32 = out_dtype == NVFP4_OUT_F32;
+  g.d = y;
+  g.ldd = ldy;
+  g.status = status;
+  g.skip_first_load = g_skip_load_once.exchange(0);
+  g.lora_uhl = uhl;
+  g.lora_l2 = static_cast<const uint16_t*>(l2);
+  g.lora_r = rank;
+  g.lora_rpad = lora_rpad(rank);
+  e = launch_gemm(g, st);
+  if (e == cudaErrorInvalidValue) return NVFP4_ERR_INVALID_ARG;
+  return cuda_status(e);
+}
+
+// ------------------------------------------- Newton-Schulz step (Q-Root)
+static bool percentile_rank(int64_t n, double p, uint64_t* k) {
+  // nearest rank: the k-th smallest of n with k = ceil(p / 100 * n), 1 <= k <= n
+  if (!(p > 0.0 && p <= 100.0)) return false;
+  int64_t r = static_cast<int64_t>(std::ceil(p / 100.0 * static_cast<double>(n)));
+  if (r < 1) r = 1;
+  if (r > n) r = n;
+  *k = static_cast<uint64_t>(r);
+  return true;
+}
+
+static size_t percentile_ws_bytes() { return kWsHeaderBytes + align_up(kPercentileHistBytes); }
+
+nvfp4_status nvfp4_abs_percentile_workspace_size(size_t* bytes) {
+  if (!bytes) return NVFP4_ERR_INVALID_ARG;
+  *bytes = percentile_ws_bytes();
+  return NVFP4_OK;
+}
+
+nvfp4_status nvfp4_abs_percentile_bf16(const void* x, int64_t n, double p, float* q, void* workspace,
+                                       size_t workspace_bytes, nvfp4_stream_t stream) {
+  if (!q || n < 0 || n > (int64_t(1) << 40)) return NVFP4_ERR_INVALID_ARG;
+  uint64_t k = 0;
+  if (n > 0 && !percentile_rank(n, p, &k)) return NVFP4_ERR_INVALID_ARG;
+  if (n > 0 && (!x || !aligned16(x))) return NVFP4_ERR_INVALID_ARG;
+  if (!workspace || workspace_bytes < percentile_ws_bytes()) return NVFP4_ERR_WORKSPACE;
+  if (reinterpret_cast<uintptr_t>(workspace) & 255u) return NVFP4_ERR_INVALID_ARG;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (n == 0) return cuda_status(cudaMemsetAsync(q, 0, sizeof(float), st));
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  return cuda_status(launch_abs_percentile(static_cast<const uint16_t*>(x), n, k,
+                                           reinterpret_cast<uint32_t*>(ws + kWsHeaderBytes), q,
+                                           reinterpret_cast<uint32_t*>(ws), st));
+}
+
+nvfp4_status nvfp4_clip_bf16(const void* x, int64_t n, const float* q, void* out, nvfp4_stream_t stream) {
+  if (!q || n < 0) return NVFP4_ERR_INVALID_ARG;
+  if (n == 0) return NVFP4_OK;
+  if (!x || !out || !aligned16(x) || !aligned16(out)) return NVFP4_ERR_INVALID_ARG;
+  return cuda_status(launch_clip(static_cast<const uint16_t*>(x), n, q, static_cast<uint16_t*>(out),
+                                 reinterpret_cast<cudaStream_t>(stream)));
+}
+
+nvfp4_status nvfp4_axpby_bf16(const void* x, const void* y, int64_t n, float a, float b, void* out,
+                              nvfp4_stream_t stream) {
+  if (n < 0) return NVFP4_ERR_INVALID_ARG;
+  if (n == 0) return NVFP4_OK;
+  if (!x || !y || !out || !aligned16(x) || !aligned16(y) || !aligned16(out)) return NVFP4_ERR_INVALID_ARG;
+  return cuda_status(launch_axpby(static_cast<const uint16_t*>(x), static_cast<const uint16_t*>(y), n, a, b,
+                                  static_cast<uint16_t*>(out), reinterpret_cast<cudaStream_t>(stream)));
+}
+
+namespace {
+// Workspace of nvfp4_ns_step, in order (each part 256-byte aligned): header,
+// three percentile histograms, three clip thresholds, quantiser scratch,
+// Xc [m, n], A, Ac, A A^T, B, Bc [m, m], B X [m, n], and the quantised
+// operands Q(Xc) [m, n], Q(Xc^T) [n, m], Q(Ac), Q(Bc) [m, m].
+struct NsLayout {
+  size_t hist, q, partials, xc, a, ac, a2, b, bc, bx, qx, qxt, qa, qb, total;
+};
+NsLayout ns_layout(int64_t m, int64_t n) {
+  NsLayout L{};
+  size_t off = kWsHeaderBytes;
+  auto take = [&](size_t bytes) {
+    const size_t at = off;
+    off += align_up(bytes);
+    return at;
+  };
+  const size_t mn2 = static_cast<size_t>(m) * n * 2, mm2 = static_cast<size_t>(m) * m * 2;
+  L.hist = take(3 * kPercentileHistBytes);
+  L.q = take(3 * sizeof(float));
+  L.partials = take(kQuantScratchBytes);
+  L.xc = take(mn2);
+  L.a = take(mm2);
+  L.ac = take(mm2);
+  L.a2 = take(mm2);
+  L.b = take(mm2);
+  L.bc = take(mm2);
+  L.bx = take(mn2);
+  L.qx = off;
+  off += operand_bytes(m, n);
+  L.qxt = off;
+  off += operand_bytes(n, m);
+  L.qa = off;
+  off += operand_bytes(m, m);
+  L.qb = off;
+  off += operand_bytes(m, m);
+  L.total = off;
+  return L;
+}
+}  // namespace
+
+nvfp4_status nvfp4_ns_workspace_size(int64_t m, int64_t n, size_t* bytes) {
+  if (!bytes || m < 0 || n < 0) return NVFP4_ERR_INVALID_ARG;
+  if (m == 0 || n == 0 || m % 32 != 0 || n % 32 != 0) return NVFP4_ERR_UNSUPPORTED_SHAPE;
+  if (m > (int64_t(1) << 20) || n > (int64_t(1) << 20)) return NVFP4_ERR_UNSUPPORTED_SHAPE;
+  *bytes = ns_layout(m, n).total;
+  return NVFP4_OK;
+}
+
+nvfp4_status nvfp4_ns_step(const void* x, int64_t m, int64_t n, float a, float b, float c, double p, void* x_out,
+                           void* workspace, size_t workspace_bytes, nvfp4_stream_t stream) {
+  size_t need = 0;
+  nvfp4_status s = nvfp4_ns_workspace_size(m, n, &need);
+  if (s != NVFP4_OK) return s;
+  if (!x || !x_out || !aligned16(x) || !aligned16(x_out)) return NVFP4_ERR_INVALID_ARG;
+  uint64_t kx = 0, ka = 0;
+  if (!percentile_rank(m * n, p, &kx) || !percentile_rank(m * m, p, &ka)) return NVFP4_ERR_INVALID_ARG;
+  if (!workspace || workspace_bytes < need) return NVFP4_ERR_WORKSPACE;
+  if (reinterpret_cast<uintptr_t>(workspace) & 255u) return NVFP4_ERR_INVALID_ARG;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  const NsLayout L = ns_layout(m, n);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  uint32_t* status = reinterpret_cast<uint32_t*>(ws);
+  uint32_t* partials = reinterpret_cast<uint32_t*>(ws + L.partials);
+  uint32_t* hist = reinterpret_cast<uint32_t*>(ws + L.hist);
+  float* q = reinterpret_cast<float*>(ws + L.q);
+  auto bf = [&](size_t off) { return reinterpret_cast<uint16_t*>(ws + off); };
+  uint8_t* cur = ws + L.qx;
+  QuantizedOperand qx = carve_operand(cur, m, n);
+  cur = ws + L.qxt;
+  QuantizedOperand qxt = carve_operand(cur, n, m);
+  cur = ws + L.qa;
+  QuantizedOperand qa = carve_operand(cur, m, m);
+  cur = ws + L.qb;
+  QuantizedOperand qb = carve_operand(cur, m, m);
+  const nvfp4_quant_cfg rows = default_cfg(NVFP4_BLOCK_1x16, NVFP4_ROUND_RNE, 0, 0);
+  nvfp4_quant_cfg cols = rows;
+  cols.transpose = 1;
+  const uint16_t* xin = static_cast<const uint16_t*>(x);
+  cudaError_t e;
+#define NS_TRY(call)                        \
+  do {                                      \
+    e = (call);                             \
+    if (e != cudaSuccess) return NVFP4_ERR_CUDA; \
+  } while (0)
+  // Xc = clip(X); Q(Xc) along n and Q(Xc^T) along m from one read
+  NS_TRY(launch_abs_percentile(xin, m * n, kx, hist, q, status, st));
+  NS_TRY(launch_clip(xin, m * n, q, bf(L.xc), st));
+  {
+    QuantArgs qa2{};
+    qa2.x = bf(L.xc);
+    qa2.rows = m;
+    qa2.cols = n;
+    qa2.ldx = n;
+    qa2.n_out = 2;
+    qa2.out[0] = make_out(rows, qx.codes, qx.sf, qx.scale);
+    qa2.out[1] = make_out(cols, qxt.codes, qxt.sf, qxt.scale);
+    qa2.status = status;
+    qa2.partials = partials;
+    NS_TRY(launch_quantize(qa2, st));
+  }
+  // A = Q(Xc) Q(Xc)^T
+  nvfp4_tensor tx{qx.codes, qx.sf, qx.scale, m, n, NVFP4_SF_MMA, 0};
+  s = gemm_into(&tx, &tx, NVFP4_OUT_BF16, bf(L.a), m, status, st);
+  if (s != NVFP4_OK) return s;
+  // A A^T from Q(clip(A))
+  NS_TRY(launch_abs_percentile(bf(L.a), m * m, ka, hist + 384, q + 1, status, st));
+  NS_TRY(launch_clip(bf(L.a), m * m, q + 1, bf(L.ac), st));
+  s = quantize_into(bf(L.ac), m, m, m, rows, qa.codes, qa.sf, qa.scale, status, partials, st);
+  if (s != NVFP4_OK) return s;
+  nvfp4_tensor ta{qa.codes, qa.sf, qa.scale, m, m, NVFP4_SF_MMA, 0};
+  s = gemm_into(&ta, &ta, NVFP4_OUT_BF16, bf(L.a2), m, status, st);
+  if (s != NVFP4_OK) return s;
+  // B = b A + c A A^T; B X from Q(clip(B)) and Q(Xc^T)
+  NS_TRY(launch_axpby(bf(L.a), bf(L.a2), m * m, b, c, bf(L.b), st));
+  NS_TRY(launch_abs_percentile(bf(L.b), m * m, ka, hist + 768, q + 2, status, st));
+  NS_TRY(launch_clip(bf(L.b), m * m, q + 2, bf(L.bc), st));
+  s = quantize_into(bf(L.bc), m, m, m, rows, qb.codes, qb.sf, qb.scale, status, partials, st);
+  if (s != NVFP4_OK) return s;
+  nvfp4_tensor tb{qb.codes, qb.sf, qb.scale, m, m, NVFP4_SF_MMA, 0};
+  nvfp4_tensor txt{qxt.codes, qxt.sf, qxt.scale, n, m, NVFP4_SF_MMA, 0};
+  s = gemm_into(&tb, &txt, NVFP4_OUT_BF16, bf(L.bx), n, status, st);
+  if (s != NVFP4_OK) return s;
+  // X' = a X + B X
+  NS_TRY(launch_axpby(xin, bf(L.bx), m * n, a, 1.0f, static_cast<uint16_t*>(x_out), st));
+#undef NS_TRY
+  return NVFP4_OK;
 }
 
 // ------------------------------------------------------- optimizer states

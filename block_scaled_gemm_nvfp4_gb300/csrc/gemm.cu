@@ -42,6 +42,12 @@
 //              the scale traffic off the tensor pipe, where a tcgen05.cp per
 //              64-wide K step and 128 rows serialises with the MMAs;
 //   warp 14    bulk-copy producer for the block scales.
+// LoRA-SVD projection ("Full-Stack FP4...", section 2.1, W = W_res +
+// beta L2 L1): the branch beta U L2^T joins the same accumulator as extra
+// k-blocks after the NVFP4 ones -- BF16 operands (U's scaled hi / lo parts
+// and L2, 64 columns per k-block, the byte layout of a k-block of codes) in
+// kind::f16 MMAs; the staging warps only take part in those stages'
+// barriers, and the epilogue's alpha scaling covers both terms.
 // Every mbarrier wait is bounded; on a timeout the CTA records
 // NVFP4_ERR_TIMEOUT in the status word, drains its in-flight copies and MMAs,
 // frees TMEM and exits.
@@ -131,6 +137,12 @@ struct Layout {
   // 24 (M = 256 across the pair in PAIR mode), scale-factor ids 0.
   static constexpr uint32_t kIdesc =
       (1u << 7) | (1u << 10) | ((uint32_t)(BN >> 3) << 17) | ((uint32_t)((PAIR ? 2 * BM : BM) >> 4) << 24);
+  // Instruction descriptor for the LoRA branch's kind::f16 MMAs: F32
+  // accumulator (bit 4), A and B BF16 (format 1 at bits 7 and 10), both
+  // K-major, the same N and M.  A 64-wide BF16 k-block is 128 bytes per row,
+  // the layout of a k-block of E2M1 codes, so it uses the same stages.
+  static constexpr uint32_t kIdescF16 =
+      (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(BN >> 3) << 17) | ((uint32_t)((PAIR ? 2 * BM : BM) >> 4) << 24);
   static_assert(kStageBytes % 1024 == 0, "stages must keep 1024-byte alignment for 128B swizzle");
   static_assert(kSfStageBytes % 16 == 0, "bulk copies need 16-byte alignment");
   static_assert(kEpiStg % 1024 == 0, "staging buffers keep the 64-byte swizzle's 512-byte alignment");
@@ -165,6 +177,10 @@ struct GParams {
   int q_sf_mma;
   int64_t q_kb_count;    // N / 16
   int64_t q_katoms;      // 64-wide N atoms of the MMA scale layout
+  // LoRA-SVD branch: lora_kb BF16 k-blocks after the NVFP4 ones (A from
+  // tmap_lu, B from tmap_l2; kind::f16 MMAs into the same accumulator);
+  // 0 for a plain GEMM
+  int lora_kb;
 };
 
 template <int STAGES, int SF_STAGES>
@@ -514,6 +530,7 @@ template <bool OUT_F32, bool PAIR, bool QUANT>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
                 const __grid_constant__ CUtensorMap tmap_d, const __grid_constant__ CUtensorMap tmap_q,
+                const __grid_constant__ CUtensorMap tmap_lu, const __grid_constant__ CUtensorMap tmap_l2,
                 const GParams p) {
   using L = Layout<PAIR>;
   constexpr int S = L::kStages;
@@ -553,6 +570,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     ptx::prefetch_tensormap(&tmap_b);
     if (p.tma_store) ptx::prefetch_tensormap(&tmap_d);
     if (QUANT) ptx::prefetch_tensormap(&tmap_q);
+    if (p.lora_kb > 0) {
+      ptx::prefetch_tensormap(&tmap_lu);
+      ptx::prefetch_tensormap(&tmap_l2);
+    }
   }
   if (warp == 1) {
     // pair mode: one warp of each CTA of the pair allocates collectively
@@ -580,10 +601,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       int stage = 0;
       uint32_t phase = 0;
       bool ok = true;
+      const int kb_total = p.num_kb + p.lora_kb;
       for (int unit = unit0; unit < p.num_units && ok; unit += ustep) {
         int m_blk, n_blk;
         unit_coords<PAIR>(p, unit, rank, m_blk, n_blk);
-        for (int kb = 0; kb < p.num_kb; ++kb) {
+        for (int kb = 0; kb < kb_total; ++kb) {
           if (!ptx::mbar_wait(&ctl->empty[stage], phase ^ 1u, abort_flag)) {
             fail(&ctl->abort, p, 1);
             ok = false;
@@ -599,7 +621,23 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             continue;
           }
-          if (PAIR) {
+          if (kb >= p.num_kb) {
+            // LoRA branch k-block j: A = hi (j even) or lo (j odd) of the
+            // branch's 64-column chunk j / 2, B = that chunk of L2; the same
+            // box sizes and swizzle as a k-block of codes
+            const int j = kb - p.num_kb;
+            if (PAIR) {
+              const uint32_t bar = full_leader0 + static_cast<uint32_t>(stage * sizeof(uint64_t));
+              if (leader) ptx::mbar_arrive_expect_tx(&ctl->full[stage], 2u * (kABytes + L::kBBytes));
+              ptx::tma_load_2d_pair(st, &tmap_lu, bar, j * 64, m_blk * BM);
+              ptx::tma_load_2d_pair(st + kABytes, &tmap_l2, bar, (j >> 1) * 64,
+                                    n_blk * BN + static_cast<int>(rank) * L::kBRows);
+            } else {
+              ptx::mbar_arrive_expect_tx(&ctl->full[stage], static_cast<uint32_t>(kABytes + L::kBBytes));
+              ptx::tma_load_2d(st, &tmap_lu, &ctl->full[stage], j * 64, m_blk * BM);
+              ptx::tma_load_2d(st + kABytes, &tmap_l2, &ctl->full[stage], (j >> 1) * 64, n_blk * BN);
+            }
+          } else if (PAIR) {
             // both CTAs' code tiles complete on the leader's barrier
             const uint32_t bar = full_leader0 + static_cast<uint32_t>(stage * sizeof(uint64_t));
             if (leader) ptx::mbar_arrive_expect_tx(&ctl->full[stage], 2u * (kABytes + L::kBBytes));
@@ -698,7 +736,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         ptx::tc_fence_after();
-        for (int kb = 0; kb < p.num_kb; ++kb) {
+        for (int kb = 0; kb < p.num_kb + p.lora_kb; ++kb) {
           // One wait per k-block: the stage's barrier completes when its code
           // tiles have landed (pair mode: both CTAs') and every staging warp
           // (both CTAs') has put its scales into the stage's TMEM slot.
@@ -711,10 +749,30 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           ptx::tc_fence_after();
-          const int kk_n = kk_count_for(p, kb);
           const uint32_t st_off = static_cast<uint32_t>(stage * L::kStageBytes);
           const uint64_t adesc0 = a_desc0 + (st_off >> 4);
           const uint64_t bdesc0 = b_desc0 + (st_off >> 4);
+          if (kb >= p.num_kb) {
+            // LoRA branch: four BF16 MMAs of K = 16 (32 bytes along the
+            // swizzled 128-byte rows), added to the NVFP4 accumulation
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+              if (PAIR)
+                ptx::tc_mma_f16_pair(tmem + kAccCol, adesc0 + 2 * kk, bdesc0 + 2 * kk, L::kIdescF16, 1u);
+              else
+                ptx::tc_mma_f16(tmem + kAccCol, adesc0 + 2 * kk, bdesc0 + 2 * kk, L::kIdescF16, 1u);
+            }
+            if (PAIR)
+              ptx::tc_commit_pair_multicast(&ctl->empty[stage], static_cast<uint16_t>(0x3));
+            else
+              ptx::tc_commit(&ctl->empty[stage]);
+            if (++stage == S) {
+              stage = 0;
+              phase ^= 1u;
+            }
+            continue;
+          }
+          const int kk_n = kk_count_for(p, kb);
           const uint32_t sfa_t0 = tmem + kSfaCol + stage * 16;
           const uint32_t sfb_t0 = tmem + kSfbCol + stage * 32;
 #pragma unroll
@@ -815,6 +873,20 @@ __global__ void __launch_bounds__(kThreads, 1)
             slot = 0;
             tphase ^= 1u;
           }
+        }
+      }
+      // LoRA branch k-blocks need no scales: the staging warps only take
+      // part in their stages' barriers, once the stage is free again.
+      for (int j = 0; j < p.lora_kb && ok; ++j) {
+        if (!warp_wait(&ctl->empty[slot], tphase ^ 1u, abort_flag, lane)) {
+          if (lane == 0) fail(&ctl->abort, p, 8);
+          ok = false;
+          break;
+        }
+        if (lane == 0) arrive_full(slot);
+        if (++slot == S) {
+          slot = 0;
+          tphase ^= 1u;
         }
       }
     }
@@ -951,7 +1023,8 @@ cudaLaunchAttribute pair_cluster_attr() {
 
 template <bool OUT_F32, bool PAIR, bool QUANT>
 cudaError_t launch_typed(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& md,
-                         const CUtensorMap& mq, GParams p, cudaStream_t stream) {
+                         const CUtensorMap& mq, const CUtensorMap& mlu, const CUtensorMap& ml2, GParams p,
+                         cudaStream_t stream) {
   using L = Layout<PAIR>;
   auto kernel = gemm_kernel<OUT_F32, PAIR, QUANT>;
   // One-time setup per device (the shared-memory opt-in and, in pair mode,
@@ -988,7 +1061,7 @@ cudaError_t launch_typed(const CUtensorMap& ma, const CUtensorMap& mb, const CUt
   if (!PAIR) {
     p.num_units = p.num_tiles;
     const int grid = std::min(p.num_tiles, device_sm_count());
-    kernel<<<grid, kThreads, L::kSmemBytes, stream>>>(ma, mb, md, mq, p);
+    kernel<<<grid, kThreads, L::kSmemBytes, stream>>>(ma, mb, md, mq, mlu, ml2, p);
     return cudaGetLastError();
   }
   p.num_units = p.tiles_mp * p.tiles_n;
@@ -1001,7 +1074,7 @@ cudaError_t launch_typed(const CUtensorMap& ma, const CUtensorMap& mb, const CUt
   cfg.stream = stream;
   cfg.attrs = &attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kernel, ma, mb, md, mq, p);
+  return cudaLaunchKernelEx(&cfg, kernel, ma, mb, md, mq, mlu, ml2, p);
 }
 
 }  // namespace
@@ -1047,7 +1120,17 @@ cudaError_t launch_gemm(const GemmArgs& a, cudaStream_t stream) {
   }
   const size_t esz = a.out_f32 ? 4 : 2;
   p.vec_store = (reinterpret_cast<uintptr_t>(a.d) % 16 == 0) && ((a.ldd * esz) % 16 == 0);
-  CUtensorMap md{}, mq{};
+  CUtensorMap md{}, mq{}, mlu{}, ml2{};
+  if (a.lora_r > 0) {
+    // LoRA branch: two BF16 k-blocks (hi, lo) per 64 columns of U; boxes of
+    // 64 columns x the code boxes' rows (reads past r are zero)
+    if (a.quant) return cudaErrorInvalidValue;
+    p.lora_kb = static_cast<int>(2 * (a.lora_rpad / 64));
+    if (!make_lora_bf16_map(&mlu, a.lora_uhl, a.M, 2 * a.lora_rpad, 2 * a.lora_rpad, BM) ||
+        !make_lora_bf16_map(&ml2, a.lora_l2, a.N, a.lora_r, a.lora_r,
+                            pair ? Layout<true>::kBRows : Layout<false>::kBRows))
+      return cudaErrorInvalidValue;
+  }
   p.tma_store = !a.out_f32 && a.d != nullptr && p.vec_store;
   if (p.tma_store && !make_d_map(&md, a.d, a.M, a.N, a.ldd)) return cudaErrorInvalidValue;
   if (a.quant) {
@@ -1062,11 +1145,14 @@ cudaError_t launch_gemm(const GemmArgs& a, cudaStream_t stream) {
     p.q_kb_count = a.N / 16;
     p.q_katoms = (p.q_kb_count + 3) / 4;
     if (!make_qcodes_map(&mq, a.q_codes, a.M, a.N)) return cudaErrorInvalidValue;
-    return pair ? launch_typed<false, true, true>(ma, mb, md, mq, p, stream) : launch_typed<false, false, true>(ma, mb, md, mq, p, stream);
+    return pair ? launch_typed<false, true, true>(ma, mb, md, mq, mlu, ml2, p, stream)
+                : launch_typed<false, false, true>(ma, mb, md, mq, mlu, ml2, p, stream);
   }
   if (pair)
-    return a.out_f32 ? launch_typed<true, true, false>(ma, mb, md, mq, p, stream) : launch_typed<false, true, false>(ma, mb, md, mq, p, stream);
-  return a.out_f32 ? launch_typed<true, false, false>(ma, mb, md, mq, p, stream) : launch_typed<false, false, false>(ma, mb, md, mq, p, stream);
+    return a.out_f32 ? launch_typed<true, true, false>(ma, mb, md, mq, mlu, ml2, p, stream)
+                     : launch_typed<false, true, false>(ma, mb, md, mq, mlu, ml2, p, stream);
+  return a.out_f32 ? launch_typed<true, false, false>(ma, mb, md, mq, mlu, ml2, p, stream)
+                   : launch_typed<false, false, false>(ma, mb, md, mq, mlu, ml2, p, stream);
 }
 
 }  // namespace nvfp4

@@ -87,9 +87,34 @@ struct GemmArgs {
   const float* q_amax_in;
   float* q_amax_out;
   int q_sf_mma;
+  // LoRA-SVD branch (nvfp4_lora_forward): extra BF16 k-blocks after the NVFP4
+  // ones, A from lora_uhl [M, 2 lora_rpad] (hi / lo of (beta / alpha) U per 64
+  // columns), B from lora_l2 [N, lora_r]; lora_r == 0: none
+  const uint16_t* lora_uhl;
+  const uint16_t* lora_l2;
+  int64_t lora_r, lora_rpad;
 };
 
 cudaError_t launch_gemm(const GemmArgs& a, cudaStream_t stream);
+
+// LoRA-SVD branch, first half (lora.cu): U = BF16(X L1^T) and the hi / lo
+// split of (beta / (sx sw)) U that the GEMM adds into its accumulator.
+struct LoraArgs {
+  const uint16_t* x;   // BF16 [T, din], row stride ldx
+  int64_t T, din, ldx;
+  const uint16_t* l1;  // BF16 [r, din] dense
+  int64_t r;
+  float beta;
+  const float* sx;     // tensor scales of Q(X) and Q(W_res) (device)
+  const float* sw;
+  uint16_t* u;         // out: U [T, r]
+  uint16_t* uhl;       // out: [T, 2 rpad], rpad = r rounded up to 64
+  uint32_t* status;
+};
+cudaError_t launch_lora_down(const LoraArgs& a, cudaStream_t stream);
+// Tensor map over a BF16 matrix: box 64 columns x box_rows, 128-byte swizzle.
+bool make_lora_bf16_map(CUtensorMap* map, const void* base, int64_t rows, int64_t cols, int64_t ld,
+                        uint32_t box_rows);
 
 // Quantised AdamW state codec (qadamw.cu).
 struct QadamwArgs {
@@ -107,6 +132,15 @@ struct QadamwArgs {
   void* workspace;           // encoders: status word + amax word
 };
 cudaError_t launch_qadamw(const QadamwArgs& a, cudaStream_t stream);
+
+// Newton-Schulz step pieces (ns.cu).  hist: 384 zero-initialised (by the
+// launcher) counters; q receives the k-th smallest |x| (1-based k).
+cudaError_t launch_abs_percentile(const uint16_t* x, int64_t n, uint64_t k, uint32_t* hist, float* q,
+                                  uint32_t* status, cudaStream_t stream);
+constexpr size_t kPercentileHistBytes = 384 * sizeof(uint32_t);
+cudaError_t launch_clip(const uint16_t* x, int64_t n, const float* q, uint16_t* out, cudaStream_t stream);
+cudaError_t launch_axpby(const uint16_t* x, const uint16_t* y, int64_t n, float a, float b, uint16_t* out,
+                         cudaStream_t stream);
 
 int device_sm_count();
 

@@ -274,6 +274,81 @@ nvfp4_status nvfp4_gemm_quantize(const nvfp4_tensor* a, const nvfp4_tensor* b, v
                                  nvfp4_stream_t stream);
 
 /*
+ * nvfp4_lora_forward: the forward GEMM of a LoRA-SVD projection ("Full-Stack
+ * FP4: Stable LLM Pretraining with Quantized Projections, Optimizers, and
+ * Attention", section 2.1: the weight is W = W_res + beta L2 L1, the
+ * residual W_res in NVFP4, the principal low-rank part L2 [dout, r],
+ * L1 [r, din] in BF16; section 3 calls the reparametrisation fusable):
+ *     Y [T, dout] = Q(X) Q(W_res)^T + beta U L2^T,   U = BF16(X L1^T) [T, r].
+ * xq = Q(X) [T, din] and wq = Q(W_res) [dout, din] as for nvfp4_gemm (MMA
+ * scale layout); x is the BF16 X [T, din] they came from (row stride ldx
+ * elements, ldx % 8 == 0, 16-byte aligned); l1 BF16 [r, din] and l2 BF16
+ * [dout, r], both dense row-major and 16-byte aligned; rank r with 8 <= r <=
+ * 256 and r % 8 == 0; beta finite.  Output: y [T, dout] (row stride ldy >=
+ * dout) in BF16 (round to nearest even) or FP32, and u [T, r] (dense BF16,
+ * 16-byte aligned) receives U.
+ * Two kernels: U = X L1^T on the tensor cores (BF16, FP32 accumulation,
+ * rounded to BF16), written with the split hi + lo = (beta / (sX sW)) U into
+ * the workspace; then the NVFP4 GEMM with the branch added into the same
+ * FP32 accumulator as extra BF16 k-blocks (hi and lo against L2), scaled by
+ * sX sW with the NVFP4 part in the epilogue.  The split keeps the branch to
+ * about 2^-16 relative of beta U L2^T; U itself differs from the exactly
+ * rounded BF16(X L1^T) only where the FP32 accumulation lands on the other
+ * side of a BF16 rounding boundary.  Shape rules: din % 32 == 0, din > 0;
+ * T and dout arbitrary.  |beta U / (sX sW)| must stay in BF16 range.
+ * Workspace: nvfp4_lora_workspace_size(T, r) bytes (status word, then the
+ * hi/lo buffer); errors as nvfp4_gemm.
+ */
+nvfp4_status nvfp4_lora_workspace_size(int64_t tokens, int64_t rank, size_t* bytes);
+nvfp4_status nvfp4_lora_forward(const nvfp4_tensor* xq, const nvfp4_tensor* wq, const void* x, int64_t ldx,
+                                const void* l1, const void* l2, int64_t rank, float beta, int32_t out_dtype, void* y,
+                                int64_t ldy, void* u, void* workspace, size_t workspace_bytes,
+                                nvfp4_stream_t stream);
+
+/*
+ * Newton-Schulz step of the Root optimizer with NVFP4 products ("Full-Stack
+ * FP4: Stable LLM Pretraining with Quantized Projections, Optimizers, and
+ * Attention", section 2.3, Q-Root: the NS matrix products run directly in
+ * NVFP4, stabilised by shape-dependent coefficients a, b, c -- not printed on
+ * the page, so they are arguments here -- and clipping of p99 outliers).
+ *
+ * nvfp4_abs_percentile_bf16: q[0] = the p-th percentile of |x| over the n
+ * BF16 values of x (device, 16-byte aligned), nearest rank: the k-th
+ * smallest magnitude with k = ceil(p / 100 * n) clamped to [1, n], exactly
+ * (a radix selection on the magnitude bits); 0 < p <= 100; q[0] = 0 for
+ * n == 0.  x must be finite: a NaN sets NVFP4_ERR_NONFINITE in the status
+ * word and q is then unspecified.  Workspace:
+ * nvfp4_abs_percentile_workspace_size bytes.
+ * nvfp4_clip_bf16: out = x clipped to [-q[0], q[0]] elementwise (q[0] a BF16
+ * magnitude, as the percentile gives; BF16 in and out, exact); out may be x.
+ * nvfp4_axpby_bf16: out = BF16(RN(RN(a x) + RN(b y))) elementwise in FP32,
+ * rounded to nearest even; out may alias x or y.  Needs no workspace.
+ *
+ * nvfp4_ns_step: one step on the BF16 iterate X [m, n] (row-major, dense;
+ * m % 32 == 0, n % 32 == 0; put the shorter side first):
+ *     A = X X^T,   B = b A + c A A^T,   X' = a X + B X,
+ * where each product L R^T is the NVFP4 GEMM of its two operands, each first
+ * clipped to its own p-th percentile magnitude and quantised along its K
+ * (1x16 blocks, round to nearest even, no transform; Q(Xc) and Q(Xc^T) come
+ * from one read), with BF16 results; B and X' are formed by
+ * nvfp4_axpby_bf16 from the unclipped A and X.  x_out may be x.  Workspace:
+ * nvfp4_ns_workspace_size(m, n) bytes (about 6 m^2 + 4 m n bytes plus the
+ * quantised operands; it holds every intermediate).  Device-side errors as
+ * the calls it is made of.  Reading of the page: the coefficients and the
+ * percentile are the caller's; the step's form is the quintic
+ * Newton-Schulz iteration, and clipping applies only to product operands.
+ */
+nvfp4_status nvfp4_abs_percentile_workspace_size(size_t* bytes);
+nvfp4_status nvfp4_abs_percentile_bf16(const void* x, int64_t n, double p, float* q, void* workspace,
+                                       size_t workspace_bytes, nvfp4_stream_t stream);
+nvfp4_status nvfp4_clip_bf16(const void* x, int64_t n, const float* q, void* out, nvfp4_stream_t stream);
+nvfp4_status nvfp4_axpby_bf16(const void* x, const void* y, int64_t n, float a, float b, void* out,
+                              nvfp4_stream_t stream);
+nvfp4_status nvfp4_ns_workspace_size(int64_t m, int64_t n, size_t* bytes);
+nvfp4_status nvfp4_ns_step(const void* x, int64_t m, int64_t n, float a, float b, float c, double p, void* x_out,
+                           void* workspace, size_t workspace_bytes, nvfp4_stream_t stream);
+
+/*
  * Quantised AdamW state codec ("Full-Stack FP4: Stable LLM Pretraining with
  * Quantized Projections, Optimizers, and Attention", section 2.2, Q-AdamW):
  * the optimizer's moments stored in NVFP4 (codes [rows, cols/2], row-major

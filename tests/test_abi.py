@@ -196,3 +196,44 @@ def test_qadamw_validation(lib):
                                      P(0)) == nv.NVFP4_ERR_INVALID_ARG
     assert lib.nvfp4_qadamw_v_decode(P(8192), P(8192), P(8192), P(8192), 24, 64, 1, P(8192),
                                      P(0)) == nv.NVFP4_ERR_UNSUPPORTED_SHAPE
+
+
+def test_lora_validation(lib):
+    P = ctypes.c_void_p
+    n = ctypes.c_size_t(0)
+    assert lib.nvfp4_lora_workspace_size(1000, 64, ctypes.byref(n)) == nv.NVFP4_OK
+    assert n.value >= 256 + 1000 * 128 * 2
+    assert lib.nvfp4_lora_workspace_size(1000, 12, ctypes.byref(n)) == nv.NVFP4_ERR_UNSUPPORTED_SHAPE
+    assert lib.nvfp4_lora_workspace_size(1000, 512, ctypes.byref(n)) == nv.NVFP4_ERR_UNSUPPORTED_SHAPE
+    t = nv._Tensor(8192, 8192, 8192, 64, 64, nv.NVFP4_SF_MMA, 0)
+    w_bad_k = nv._Tensor(8192, 8192, 8192, 64, 96, nv.NVFP4_SF_MMA, 0)
+
+    def call(a=t, b=t, r=64, beta=1.0, ws=1 << 20, ldx=64):
+        return lib.nvfp4_lora_forward(ctypes.byref(a), ctypes.byref(b), P(8192), ldx, P(8192), P(8192), r,
+                                      beta, 0, P(8192), 64, P(8192), P(8192), ws, P(0))
+
+    assert call(b=w_bad_k) == nv.NVFP4_ERR_INVALID_ARG
+    assert call(r=20) == nv.NVFP4_ERR_UNSUPPORTED_SHAPE
+    assert call(beta=float("nan")) == nv.NVFP4_ERR_INVALID_ARG
+    assert call(beta=float("inf")) == nv.NVFP4_ERR_INVALID_ARG
+    assert call(ws=100) == nv.NVFP4_ERR_WORKSPACE
+    assert call(ldx=60) == nv.NVFP4_ERR_INVALID_ARG
+
+
+def test_ns_validation(lib):
+    P = ctypes.c_void_p
+    n = ctypes.c_size_t(0)
+    assert lib.nvfp4_ns_workspace_size(64, 96, ctypes.byref(n)) == nv.NVFP4_OK and n.value > 6 * 64 * 64
+    assert lib.nvfp4_ns_workspace_size(48, 96, ctypes.byref(n)) == nv.NVFP4_ERR_UNSUPPORTED_SHAPE
+    assert lib.nvfp4_ns_workspace_size(64, 0, ctypes.byref(n)) == nv.NVFP4_ERR_UNSUPPORTED_SHAPE
+    assert lib.nvfp4_ns_step(P(8192), 64, 64, 1.0, 0.0, 0.0, 99.0, P(8192), P(8192), 16, P(0)) == \
+        nv.NVFP4_ERR_WORKSPACE
+    assert lib.nvfp4_ns_step(P(8192), 64, 64, 1.0, 0.0, 0.0, 0.0, P(8192), P(8192), 1 << 30, P(0)) == \
+        nv.NVFP4_ERR_INVALID_ARG
+    assert lib.nvfp4_ns_step(P(8192), 64, 64, 1.0, 0.0, 0.0, 101.0, P(8192), P(8192), 1 << 30, P(0)) == \
+        nv.NVFP4_ERR_INVALID_ARG
+    assert lib.nvfp4_abs_percentile_bf16(P(8192), 100, 99.0, P(8192), P(8192), 16, P(0)) == nv.NVFP4_ERR_WORKSPACE
+    assert lib.nvfp4_abs_percentile_bf16(P(8194), 100, 99.0, P(8192), P(8192), 1 << 20, P(0)) == \
+        nv.NVFP4_ERR_INVALID_ARG
+    assert lib.nvfp4_clip_bf16(P(8192), 10, None, P(8192), P(0)) == nv.NVFP4_ERR_INVALID_ARG
+    assert lib.nvfp4_axpby_bf16(P(8192), P(8200), 10, 1.0, 1.0, P(8192), P(0)) == nv.NVFP4_ERR_INVALID_ARG
