@@ -410,9 +410,11 @@ def _oracle_sample(rows=64):
 
 def cpu_baseline(args, rows=64):
     flop, sec = _oracle_sample(rows)
-    return {"value": round(flop / sec / 1e12, 9), "unit": "TFLOP/s", "cores": 1, "kind": "oracle",
+    return {"value": round(flop / sec / 1e12, 9), "unit": "TFLOP/s", "cores": 1, "host_cores": os.cpu_count(),
+            "kind": "oracle",
             "sample": "fprop+dgrad+wgrad, one %dx%d output block each at full K, with the operand rows "
-                      "quantised from the full tensors (single-threaded C, %.1f s)" % (rows, rows, sec)}
+                      "quantised from the full tensors (single-threaded C on one of the host's %d cores, %.1f s)"
+                      % (rows, rows, os.cpu_count() or 1, sec)}
 
 
 def run_reference(args):
@@ -434,7 +436,9 @@ def run_reference(args):
             "scaling": "weak", "vs_baseline": None, "dtype": "nvfp4 (oracle: fp32 encode, fp64 accumulate)",
             "data": "synthetic", "config": _config(), "impl": "reference",
             "cpu_baseline": {"value": round(value, 9), "unit": "TFLOP/s", "kind": "oracle", "cores": 1,
-                             "sample": "per step: fprop+dgrad+wgrad, one 16x16 output block each at full K"},
+                             "host_cores": os.cpu_count(),
+                             "sample": "per step: fprop+dgrad+wgrad, one 16x16 output block each at full K, "
+                                       "single-threaded"},
             "e2e": {"value": round(value, 9), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
@@ -469,7 +473,7 @@ def run_case(args):
         qa = nv.nvfp4_quantize(syn.normal_bf16((M, K), seed=1).to(dev), nv.quant_cfg())
         qb = nv.nvfp4_quantize(syn.normal_bf16((N, K), seed=2).to(dev), nv.quant_cfg())
         d = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
-        ws = torch.zeros(4096, dtype=torch.uint8, device=dev)
+        ws = torch.zeros(nv.nvfp4_gemm_workspace_size(M, N, K), dtype=torch.uint8, device=dev)
 
         def call():
             nv.nvfp4_gemm(qa, qb, nv.NVFP4_OUT_BF16, d=d, workspace=ws)
@@ -583,10 +587,19 @@ def run_case(args):
         call()
     torch.cuda.synchronize()
     stream = torch.cuda.current_stream()
+    run = call
+    if args.graph:
+        # replay a captured CUDA graph of the call: no host launch cost
+        # between calls (short kernels are otherwise host-bound)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            call()
+        torch.cuda.synchronize()
+        run = g.replay
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     t0.record(stream)
     for _ in range(args.steps):
-        call()
+        run()
     t1.record(stream)
     torch.cuda.synchronize()
     ms = t0.elapsed_time(t1) / args.steps
@@ -594,7 +607,232 @@ def run_case(args):
     if st != nv.NVFP4_OK:
         raise RuntimeError("device status %s" % nv.nvfp4_status_string(st))
     print(json.dumps({"case": args.case, "ms": round(ms, 5), "value": round(work / (ms * 1e-3), 1),
-                      "unit": unit, "steps": args.steps, "warmup": args.warmup}), flush=True)
+                      "unit": unit, "steps": args.steps, "warmup": args.warmup, "graph": bool(args.graph)}),
+          flush=True)
+
+
+# ------------------------------------------------------ measurement suite
+def _suite_timer(torch, dev):
+    """Per-call device time with L2 flushed before every call (a 256 MB
+    write), so that inputs smaller than L2 are read from HBM."""
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def timed(call, iters=10, warmup=3):
+        for _ in range(warmup):
+            call()
+        torch.cuda.synchronize()
+        # The call is captured once in a CUDA graph and replayed, so the
+        # timed region holds its kernels only (no host-side launch cost), and
+        # everything is enqueued before the one synchronisation.
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            call()
+        torch.cuda.synchronize()
+        evs = []
+        for _ in range(iters):
+            flush.zero_()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            g.replay()
+            e1.record(stream)
+            evs.append((e0, e1))
+        torch.cuda.synchronize()
+        return sum(a.elapsed_time(b) for a, b in evs) / iters
+
+    return timed
+
+
+def _oracle_quant_slice(args):
+    """Worker: the oracle's encode of rows [r0, r1) of Q under the whole
+    operand's amax (the delayed-scale entry point with amax = the operand's
+    own amax gives the same output as a full quantisation)."""
+    import oracle
+    xs, cfg, amax = args
+    return oracle.quantize_given_amax(xs, cfg, amax)[2]
+
+
+def _oracle_amax_slice(args):
+    import oracle
+    xs, cfg = args
+    return oracle.amax(xs, cfg)
+
+
+def _oracle_suite(emit):
+    """The oracle on full tensors of the quantise sweep's larger shape,
+    single-threaded and on every host core (row slices in a spawn pool), and
+    its FP64 GEMM on an output block of the MLP up-projection, extrapolated."""
+    import multiprocessing as mp
+
+    import oracle
+    from block_scaled_gemm_nvfp4_gb300 import synthetic as syn
+
+    cores = os.cpu_count() or 1
+    x = syn.as_u16(syn.config1(1))  # 8192 x 20480 with outliers
+    R, C = x.shape
+    for name, cfg in (("1x16 rne", oracle.make_cfg()),
+                      ("1x16 sr+rht", oracle.make_cfg(rounding=1, rht=1, rht_seed=1, sr_seed=2))):
+        t0 = time.perf_counter()
+        oracle.quantize(x, cfg)
+        t1 = time.perf_counter() - t0
+        # all cores: amax of row slices, then the encode of row slices (the
+        # transform and blocks run along rows, so slices are independent)
+        step = (R + cores - 1) // cores
+        slices = [(r, min(R, r + step)) for r in range(0, R, step)]
+        with mp.get_context("spawn").Pool(cores) as pool:
+            pool.map(_oracle_amax_slice, [(x[:16], cfg)] * cores)  # start the workers
+            t0 = time.perf_counter()
+            amax = max(pool.map(_oracle_amax_slice, [(x[a:b], cfg) for a, b in slices]))
+            pool.map(_oracle_quant_slice, [(x[a:b], cfg, amax) for a, b in slices])
+            tn = time.perf_counter() - t0
+        gb = R * C * QUANT_BYTES_PER_ELT / 1e9
+        emit({"suite": "oracle_quantize", "mode": name, "shape": [R, C], "threads_1_s": round(t1, 3),
+              "threads_1_GBps": round(gb / t1, 4), "threads_all": cores, "threads_all_s": round(tn, 3),
+              "threads_all_GBps": round(gb / tn, 4), "host_cores": cores})
+    # FP64 GEMM: a 16 x 64 block of the MLP up-projection fprop at full K
+    xw = syn.as_u16(syn.normal_bf16((16, HID), seed=1))
+    ww = syn.as_u16(syn.normal_bf16((64, HID), std=0.02, seed=2))
+    qa = oracle.quantize(xw, oracle.make_cfg())
+    qb = oracle.quantize(ww, oracle.make_cfg(block=1))
+    t0 = time.perf_counter()
+    oracle.gemm_f64(qa, qb, 16, 64, HID)
+    tg = time.perf_counter() - t0
+    flop = 2.0 * 16 * 64 * HID
+    emit({"suite": "oracle_gemm", "sample": "16x64 output block, K=%d, single thread" % HID,
+          "s": round(tg, 4), "TFLOPs": round(flop / tg / 1e12, 9),
+          "full_fprop_s_extrapolated": round(tg * (T * FFN) / (16 * 64), 1), "host_cores": cores})
+
+
+def run_suite(args):
+    """Every measurement the hot path's scope table asks for beyond the
+    benchmark step, one JSON line each: the 16-mode quantise sweep at both
+    sweep shapes (and the one-pass delayed-scale variant of each mode), the
+    large and skinny GEMM probes, the 3B projection chain through the linear
+    wrappers (split into quantise and GEMM), the LoRA-SVD and Newton-Schulz
+    costs, and the oracle on the host cores."""
+    import torch
+
+    import block_scaled_gemm_nvfp4_gb300 as nv
+    from block_scaled_gemm_nvfp4_gb300 import synthetic as syn
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    nv.lib()
+    timed = _suite_timer(torch, dev)
+    peaks, src = _peaks()
+    hbm = peaks["hbm_gbs"]
+    fp4 = peaks["bf16_tflops"] * FP4_OVER_BF16
+
+    def emit(d):
+        print(json.dumps(d), flush=True)
+
+    with ClockSampler(0) as clocks:
+        _suite_gpu(nv, syn, torch, dev, timed, hbm, fp4, emit)
+    emit({"suite": "peaks", "hbm_gbs": hbm, "fp4_tflops": round(fp4, 1), "source": src,
+          "clocks": clocks.summary()})
+    _oracle_suite(emit)
+
+
+def _suite_gpu(nv, syn, torch, dev, timed, hbm, fp4, emit):
+    # quantise sweep: {1x16, 16x16} x {RNE, SR} x {transform off, on} at both shapes
+    for si in range(2):
+        xd = syn.config1(si).to(dev)
+        R, C = xd.shape
+        ws = torch.zeros(nv.nvfp4_quantize_workspace_size(R, C, nv.quant_cfg()), dtype=torch.uint8, device=dev)
+        amax = xd.abs().max().float().reshape(1)
+        for block in (0, 1):
+            for rounding in (0, 1):
+                for rht in (0, 1):
+                    cfg = nv.quant_cfg(block=block, rounding=rounding, rht=rht, rht_seed=11, sr_seed=12)
+                    out = nv.nvfp4_quantize(xd, cfg, workspace=ws)
+                    ms = timed(lambda: nv.nvfp4_quantize(xd, cfg, out=out, workspace=ws))
+                    gbs = R * C * QUANT_BYTES_PER_ELT / (ms * 1e-3) / 1e9
+                    row = {"suite": "quantize", "shape": [R, C], "block": "16x16" if block else "1x16",
+                           "rounding": "sr" if rounding else "rne", "rht": bool(rht), "ms": round(ms, 4),
+                           "GBps": round(gbs, 1), "frac_hbm": round(gbs / hbm, 4),
+                           "actual_two_pass_GBps": round(R * C * (QUANT_BYTES_PER_ELT + 2) / (ms * 1e-3) / 1e9, 1)}
+                    if not rht:  # one pass under a supplied amax (delayed scaling)
+                        ms1 = timed(lambda: nv.nvfp4_quantize_given_amax(xd, cfg, amax, out=out, workspace=ws))
+                        g1 = R * C * QUANT_BYTES_PER_ELT / (ms1 * 1e-3) / 1e9
+                        row.update({"given_amax_ms": round(ms1, 4), "given_amax_GBps": round(g1, 1),
+                                    "given_amax_frac_hbm": round(g1 / hbm, 4)})
+                    emit(row)
+        assert nv.nvfp4_check_device_status(ws) == nv.NVFP4_OK
+        del xd
+
+    # GEMM probes: 16384^3 (tensor-bound) and the skinny decode shape (HBM-bound)
+    for M, N, K in ((16384, 16384, 16384), (128, 8192, 8192)):
+        a, b = syn.config4(M, N, K)
+        qa = nv.nvfp4_quantize(a.to(dev), nv.quant_cfg())
+        qb = nv.nvfp4_quantize(b.to(dev), nv.quant_cfg())
+        d = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+        gws = torch.zeros(nv.nvfp4_gemm_workspace_size(M, N, K), dtype=torch.uint8, device=dev)
+        ms = timed(lambda: nv.nvfp4_gemm(qa, qb, nv.NVFP4_OUT_BF16, d=d, workspace=gws))
+        tf = 2.0 * M * N * K / (ms * 1e-3) / 1e12
+        byts = (M + N) * K * QUANT_OUT_BYTES_PER_ELT + 2.0 * M * N
+        emit({"suite": "gemm", "shape": [M, N, K], "ms": round(ms, 4), "TFLOPs": round(tf, 1),
+              "frac_fp4": round(tf / fp4, 4), "algorithmic_MB": round(byts / 1e6, 1),
+              "GBps": round(byts / (ms * 1e-3) / 1e9, 1), "frac_hbm": round(byts / (ms * 1e-3) / 1e9 / hbm, 4)})
+        del qa, qb, d
+
+    # 3B projection chain through the linear wrappers (quantise both operands + GEMM)
+    for name, din, dout in syn.PROJ3B:
+        x, w, dy = (t.to(dev) for t in syn.config3(name))
+        Tt = x.shape[0]
+        for op, fn, a_src, b_src, shape in (
+                ("fprop", nv.nvfp4_linear_fprop, x, w, (Tt, dout, din)),
+                ("dgrad", nv.nvfp4_linear_dgrad, dy, w, (Tt, din, dout)),
+                ("wgrad", nv.nvfp4_linear_wgrad, dy, x, (dout, din, Tt))):
+            opc = {"fprop": nv.NVFP4_LINEAR_FPROP, "dgrad": nv.NVFP4_LINEAR_DGRAD, "wgrad": nv.NVFP4_LINEAR_WGRAD}[op]
+            ws = torch.zeros(nv.nvfp4_linear_workspace_size(opc, Tt, din, dout), dtype=torch.uint8, device=dev)
+            out = fn(a_src, b_src, workspace=ws)
+            ms = timed(lambda: fn(a_src, b_src, workspace=ws, **{{"fprop": "y", "dgrad": "dx", "wgrad": "dw"}[op]: out}))
+            # the GEMM alone on operands quantised the way the wrapper does
+            M, N, K = shape
+            if op == "fprop":
+                qa = nv.nvfp4_quantize(x, nv.quant_cfg())
+                qb = nv.nvfp4_quantize(w, nv.quant_cfg(block=1))
+            elif op == "dgrad":
+                qa = nv.nvfp4_quantize(dy, nv.quant_cfg())
+                qb = nv.nvfp4_quantize(w, nv.quant_cfg(block=1, transpose=1))
+            else:
+                s = nv.NVFP4_DEFAULT_RHT_SEED
+                qa = nv.nvfp4_quantize(dy, nv.quant_cfg(rounding=1, rht=1, transpose=1, rht_seed=s, sr_seed=5))
+                qb = nv.nvfp4_quantize(x, nv.quant_cfg(rounding=1, rht=1, transpose=1, rht_seed=s, sr_seed=6))
+            msg = timed(lambda: nv.nvfp4_gemm(qa, qb, nv.NVFP4_OUT_BF16, d=out))
+            flop = 2.0 * M * N * K
+            emit({"suite": "linear3b", "proj": name, "op": op, "gemm_shape": [M, N, K], "ms": round(ms, 4),
+                  "TFLOPs": round(flop / (ms * 1e-3) / 1e12, 1), "gemm_ms": round(msg, 4),
+                  "gemm_TFLOPs": round(flop / (msg * 1e-3) / 1e12, 1), "gemm_frac_fp4": round(
+                      flop / (msg * 1e-3) / 1e12 / fp4, 4), "quantize_ms": round(ms - msg, 4)})
+            del qa, qb, out, ws
+        del x, w, dy
+
+    # LoRA-SVD forward (r = 64) against the plain GEMM on the 12B MLP-up fprop shape
+    Tt, din, dout, r = T, HID, FFN, 64
+    x = syn.normal_bf16((Tt, din), seed=1).to(dev)
+    xq = nv.nvfp4_quantize(x, nv.quant_cfg())
+    wq = nv.nvfp4_quantize(syn.normal_bf16((dout, din), std=0.02, seed=2).to(dev), nv.quant_cfg(block=1))
+    l1 = syn.normal_bf16((r, din), std=0.02, seed=3).to(dev)
+    l2 = syn.normal_bf16((dout, r), std=0.02, seed=4).to(dev)
+    y, u = nv.nvfp4_lora_forward(xq, wq, x, l1, l2, 1.0)
+    lws = torch.zeros(nv.nvfp4_lora_workspace_size(Tt, r), dtype=torch.uint8, device=dev)
+    ms_l = timed(lambda: nv.nvfp4_lora_forward(xq, wq, x, l1, l2, 1.0, y=y, u=u, workspace=lws))
+    ms_g = timed(lambda: nv.nvfp4_gemm(xq, wq, nv.NVFP4_OUT_BF16, d=y))
+    emit({"suite": "lora_forward", "shape": [Tt, din, dout, r], "ms": round(ms_l, 4), "gemm_ms": round(ms_g, 4),
+          "branch_overhead": round(ms_l / ms_g - 1.0, 4)})
+    del x, xq, wq, l1, l2, y, u, lws
+
+    # Newton-Schulz step with NVFP4 products
+    for m, n in ((1024, 4096), (3072, 8192), (4096, 4096)):
+        g = syn.normal_bf16((m, n), seed=5).float()
+        xx = (g / g.norm()).to(torch.bfloat16).to(dev)
+        out = torch.empty_like(xx)
+        nws = torch.zeros(nv.nvfp4_ns_workspace_size(m, n), dtype=torch.uint8, device=dev)
+        ms = timed(lambda: nv.nvfp4_ns_step(xx, 15.0 / 8.0, -10.0 / 8.0, 3.0 / 8.0, out=out, workspace=nws))
+        flop = 4.0 * m * m * n + 2.0 * m * m * m
+        emit({"suite": "ns_step", "shape": [m, n], "ms": round(ms, 4), "TFLOPs": round(flop / (ms * 1e-3) / 1e12, 1)})
+        del xx, out, nws
 
 
 def main():
@@ -603,10 +841,16 @@ def main():
     ap.add_argument("--steps", type=int, default=10)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--graph", action="store_true", help="--case: time replays of a captured CUDA graph")
+    ap.add_argument("--suite", action="store_true",
+                    help="every scope-table measurement beyond the step: quantise sweep, GEMM probes, 3B chain, "
+                         "LoRA, Newton-Schulz, oracle on the host cores")
     ap.add_argument("--case", default=None,
                     help="time one call: gemm:M,N,K, quantize:R,C[,mode] or dual:R,C[,act|weight]")
     args = ap.parse_args()
-    if args.case:
+    if args.suite:
+        run_suite(args)
+    elif args.case:
         run_case(args)
     elif args.impl == "reference":
         run_reference(args)

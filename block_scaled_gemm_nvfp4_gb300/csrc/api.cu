@@ -145,7 +145,7 @@ nvfp4_status check_tensor(const nvfp4_tensor* t) {
 
 
 nvfp4_status gemm_into(const nvfp4_tensor* a, const nvfp4_tensor* b, int32_t out_dtype, void* d, int64_t ldd,
-                       uint32_t* status, cudaStream_t stream) {
+                       uint32_t* status, cudaStream_t stream, float* partial = nullptr, size_t partial_bytes = 0) {
   GemmArgs g{};
   g.a_codes = static_cast<const uint8_t*>(a->codes);
   g.a_sf = static_cast<const uint8_t*>(a->sf);
@@ -161,6 +161,8 @@ nvfp4_status gemm_into(const nvfp4_tensor* a, const nvfp4_tensor* b, int32_t out
   g.ldd = ldd;
   g.status = status;
   g.skip_first_load = g_skip_load_once.exchange(0);
+  g.partial = partial;
+  g.partial_bytes = partial_bytes;
   const cudaError_t e = launch_gemm(g, stream);
   if (e == cudaErrorInvalidValue) return NVFP4_ERR_INVALID_ARG;
   return cuda_status(e);
@@ -328,6 +330,8 @@ nvfp4_status nvfp4_gemm_workspace_size(int64_t M, int64_t N, int64_t K, size_t* 
   if (!bytes || M < 0 || N < 0 || K < 0) return NVFP4_ERR_INVALID_ARG;
   if (K % 32 != 0) return NVFP4_ERR_UNSUPPORTED_SHAPE;
   *bytes = kWsHeaderBytes;
+  const int sk = gemm_split_k(M, N, K, nullptr);
+  if (sk > 1) *bytes += align_up(gemm_split_k_bytes(M, N, sk));
   return NVFP4_OK;
 }
 
@@ -350,8 +354,11 @@ nvfp4_status nvfp4_gemm(const nvfp4_tensor* a, const nvfp4_tensor* b, int32_t ou
 
   if (!workspace) return NVFP4_ERR_WORKSPACE;
   if (workspace_bytes < kWsHeaderBytes) return NVFP4_ERR_WORKSPACE;
-  return gemm_into(a, b, out_dtype, d, ldd, static_cast<uint32_t*>(workspace),
-                   reinterpret_cast<cudaStream_t>(stream));
+  // Anything past the header is split-K scratch; a workspace of just the
+  // header runs the GEMM unsplit.
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  return gemm_into(a, b, out_dtype, d, ldd, reinterpret_cast<uint32_t*>(ws), reinterpret_cast<cudaStream_t>(stream),
+                   reinterpret_cast<float*>(ws + kWsHeaderBytes), workspace_bytes - kWsHeaderBytes);
 }
 
 nvfp4_status nvfp4_gemm_quantize(const nvfp4_tensor* a, const nvfp4_tensor* b, void* d, int64_t ldd,

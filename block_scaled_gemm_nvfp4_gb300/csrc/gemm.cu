@@ -181,7 +181,31 @@ struct GParams {
   // tmap_lu, B from tmap_l2; kind::f16 MMAs into the same accumulator);
   // 0 for a plain GEMM
   int lora_kb;
+  // split-K (single mode, FP32 kernel): unit = tile * split_k + s covers
+  // k-blocks [s * kb_per_split, (s + 1) * kb_per_split) and stores its raw
+  // FP32 accumulator (alpha = 1) as a whole column-major 128 x 256 block at
+  // d + (s * num_tiles + tile) * BM * BN (element (r, c) at c * BM + r), so
+  // a warp's 32 lanes write 128 consecutive bytes per column; 1 = no split
+  int split_k;
+  int kb_per_split;
 };
+
+// Tile index and k-block range of a work unit.
+__device__ __forceinline__ void unit_split(const GParams& p, int unit, int& tile, int& kb_lo, int& kb_hi,
+                                           int64_t& d_off) {
+  if (p.split_k > 1) {
+    tile = unit / p.split_k;
+    const int s = unit - tile * p.split_k;
+    kb_lo = s * p.kb_per_split;
+    kb_hi = min(p.num_kb, kb_lo + p.kb_per_split);
+    d_off = (static_cast<int64_t>(s) * p.num_tiles + tile) * (BM * BN);
+  } else {
+    tile = unit;
+    kb_lo = 0;
+    kb_hi = p.num_kb;
+    d_off = 0;
+  }
+}
 
 template <int STAGES, int SF_STAGES>
 struct __align__(8) SmemCtl {
@@ -354,7 +378,7 @@ __device__ __forceinline__ void epilogue_half(const GParams& p, const CUtensorMa
                                               uint8_t* stg,
                                               uint64_t* acc_empty, uint32_t tmem, int m_blk,
                                               int n_blk, int q, int half, int lane, float alpha, uint32_t rank,
-                                              float s_dec, uint32_t& amax_bits) {
+                                              float s_dec, uint32_t& amax_bits, int64_t d_off) {
   const int64_t row = static_cast<int64_t>(m_blk) * BM + q * 32 + lane;
   const int64_t col0 = static_cast<int64_t>(n_blk) * BN + half * kEpiCols;
   const uint32_t taddr = tmem + (static_cast<uint32_t>(q * 32) << 16) + kAccCol + half * kEpiCols;
@@ -455,8 +479,25 @@ __device__ __forceinline__ void epilogue_half(const GParams& p, const CUtensorMa
       store_quantised(p, tmap_q, stg, qh, row, static_cast<int64_t>(m_blk) * BM + q * 32, col0, q, lane);
       amax_bits = max(amax_bits, qh.amax_bits);
     }
+  } else if (p.split_k > 1) {
+    // split-K partial: raw accumulator, column-major block (coalesced across
+    // the warp's lanes, which hold consecutive rows); padding rows and
+    // columns of ragged tiles hold the zeros their out-of-range operands gave
+    float* blk = static_cast<float*>(p.d) + d_off + static_cast<int64_t>(half * kEpiCols) * BM + q * 32 + lane;
+#pragma unroll 1
+    for (int c = 0; c < kEpiCols / 32; ++c) {
+      uint32_t r[32];
+      ptx::tmem_ld_32x32b_x32(taddr + c * 32, r);
+      ptx::tmem_ld_wait();
+      ptx::tmem_ld_regs_ready(r);
+#pragma unroll
+      for (int j = 0; j < 32; ++j) blk[(c * 32 + j) * BM] = __uint_as_float(r[j]);
+    }
+    ptx::tc_fence_before();
+    __syncwarp();
+    if (lane == 0) arrive_leader<PAIR>(acc_empty, rank);
   } else {
-    float* drow = static_cast<float*>(p.d) + row * p.ldd;
+    float* drow = static_cast<float*>(p.d) + d_off + row * p.ldd;
 #pragma unroll 1
     for (int c = 0; c < kEpiCols / 32; ++c) {
       uint32_t r[32];
@@ -601,18 +642,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       int stage = 0;
       uint32_t phase = 0;
       bool ok = true;
-      const int kb_total = p.num_kb + p.lora_kb;
       for (int unit = unit0; unit < p.num_units && ok; unit += ustep) {
-        int m_blk, n_blk;
-        unit_coords<PAIR>(p, unit, rank, m_blk, n_blk);
-        for (int kb = 0; kb < kb_total; ++kb) {
+        int m_blk, n_blk, tile, kb_lo, kb_hi;
+        int64_t d_off;
+        unit_split(p, unit, tile, kb_lo, kb_hi, d_off);
+        unit_coords<PAIR>(p, tile, rank, m_blk, n_blk);
+        for (int kb = kb_lo; kb < kb_hi + p.lora_kb; ++kb) {
           if (!ptx::mbar_wait(&ctl->empty[stage], phase ^ 1u, abort_flag)) {
             fail(&ctl->abort, p, 1);
             ok = false;
             break;
           }
           uint8_t* st = smem + stage * L::kStageBytes;
-          if (p.skip_first_load && blockIdx.x == 0 && unit == unit0 && kb == 0) {
+          if (p.skip_first_load && blockIdx.x == 0 && unit == unit0 && kb == kb_lo) {
             // Failure-detection test hook: this stage is never filled, so the
             // bounded waits on it run out and the CTA reports a timeout.
             if (++stage == S) {
@@ -621,11 +663,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             continue;
           }
-          if (kb >= p.num_kb) {
+          if (kb >= kb_hi) {
             // LoRA branch k-block j: A = hi (j even) or lo (j odd) of the
             // branch's 64-column chunk j / 2, B = that chunk of L2; the same
             // box sizes and swizzle as a k-block of codes
-            const int j = kb - p.num_kb;
+            const int j = kb - kb_hi;
             if (PAIR) {
               const uint32_t bar = full_leader0 + static_cast<uint32_t>(stage * sizeof(uint64_t));
               if (leader) ptx::mbar_arrive_expect_tx(&ctl->full[stage], 2u * (kABytes + L::kBBytes));
@@ -679,14 +721,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t phase = 0;
       bool ok = true;
       for (int unit = unit0; unit < p.num_units && ok; unit += ustep) {
-        int m_blk, n_blk;
-        unit_coords<PAIR>(p, unit, rank, m_blk, n_blk);
+        int m_blk, n_blk, tile, kb_lo, kb_hi;
+        int64_t d_off;
+        unit_split(p, unit, tile, kb_lo, kb_hi, d_off);
+        unit_coords<PAIR>(p, tile, rank, m_blk, n_blk);
         const int64_t n_rows_left = p.N - static_cast<int64_t>(n_blk) * BN;
         const int nb_atoms = static_cast<int>(min(static_cast<int64_t>(2), (n_rows_left + 127) / 128));
         // (a row block past the end -- the odd last half of a pair -- has no
         // scales to load; its rows are never stored)
         const bool a_valid = m_blk < p.tiles_m;
-        for (int kb0 = 0; kb0 < p.num_kb; kb0 += kSfGroup) {
+        for (int kb0 = kb_lo; kb0 < kb_hi; kb0 += kSfGroup) {
           if (!ptx::mbar_wait(&ctl->sf_empty[stage], phase ^ 1u, abort_flag)) {
             fail(&ctl->abort, p, 9);
             ok = false;
@@ -731,12 +775,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t a_desc0 = ptx::smem_desc(ptx::smem_u32(smem), 16, 1024, ptx::kSwizzle128B);
       const uint64_t b_desc0 = ptx::smem_desc(ptx::smem_u32(smem + kABytes), 16, 1024, ptx::kSwizzle128B);
       for (int unit = unit0; unit < p.num_units && ok; unit += ustep) {
+        int tile, kb_lo, kb_hi;
+        int64_t d_off;
+        unit_split(p, unit, tile, kb_lo, kb_hi, d_off);
         if (!ptx::mbar_wait(&ctl->acc_empty, acc_phase ^ 1u, abort_flag)) {
           fail(&ctl->abort, p, 3);
           break;
         }
         ptx::tc_fence_after();
-        for (int kb = 0; kb < p.num_kb + p.lora_kb; ++kb) {
+        for (int kb = kb_lo; kb < kb_hi + p.lora_kb; ++kb) {
           // One wait per k-block: the stage's barrier completes when its code
           // tiles have landed (pair mode: both CTAs') and every staging warp
           // (both CTAs') has put its scales into the stage's TMEM slot.
@@ -752,7 +799,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t st_off = static_cast<uint32_t>(stage * L::kStageBytes);
           const uint64_t adesc0 = a_desc0 + (st_off >> 4);
           const uint64_t bdesc0 = b_desc0 + (st_off >> 4);
-          if (kb >= p.num_kb) {
+          if (kb >= kb_hi) {
             // LoRA branch: four BF16 MMAs of K = 16 (32 bytes along the
             // swizzled 128-byte rows), added to the NVFP4 accumulation
 #pragma unroll
@@ -780,7 +827,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (kk < kk_n) {
               // +32 bytes along K inside the swizzled 128-byte rows
               const uint64_t adesc = adesc0 + 2 * kk, bdesc = bdesc0 + 2 * kk;
-              const uint32_t acc = (kb | kk) != 0 ? 1u : 0u;
+              const uint32_t acc = (kb != kb_lo || kk != 0) ? 1u : 0u;
               if (PAIR)
                 ptx::tc_mma_nvf4_pair(tmem + kAccCol, adesc, bdesc, L::kIdesc, sfa_t0 + kk * 4, sfb_t0 + kk * 8, acc);
               else
@@ -834,8 +881,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::mbar_arrive(&ctl->full[s_]);
     };
     for (int unit = unit0; unit < p.num_units && ok; unit += ustep) {
-      for (int kb = 0; kb < p.num_kb; kb += 2) {
-        const int n2 = min(2, p.num_kb - kb);
+      int tile, kb_lo, kb_hi;
+      int64_t d_off;
+      unit_split(p, unit, tile, kb_lo, kb_hi, d_off);
+      for (int kb = kb_lo; kb < kb_hi; kb += 2) {
+        const int n2 = min(2, kb_hi - kb);
         const int slot1 = slot + 1 == S ? 0 : slot + 1;
         const uint32_t tphase1 = slot + 1 == S ? tphase ^ 1u : tphase;
         // The scales are in the ring (one wait per scale stage), and the MMAs
@@ -858,7 +908,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::tmem_st_wait();
         ptx::tc_fence_before();
         __syncwarp();
-        const bool group_done = j + n2 >= kSfGroup || kb + n2 >= p.num_kb;
+        const bool group_done = j + n2 >= kSfGroup || kb + n2 >= kb_hi;
         if (lane == 0) {
           if (group_done) ptx::mbar_arrive(&ctl->sf_empty[sstage]);
           arrive_full(slot);
@@ -895,7 +945,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int q = warp & 3;              // TMEM lane quarter this warp may access
     const int half = (warp - 2) >> 2;    // which 128 columns of the tile it stores
     uint8_t* stg = smem + L::kEpiStg + (warp - 2) * kEpiStgBytes;  // this warp's output staging
-    const float alpha = __fmul_rn(*p.a_scale, *p.b_scale);
+    // split-K partials are stored unscaled; the reduction applies alpha
+    const float alpha = p.split_k > 1 ? 1.0f : __fmul_rn(*p.a_scale, *p.b_scale);
     // quantising epilogue: tensor scale s = amax_in / 2688 (1 if that is
     // zero); a negative or non-finite amax_in is reported and nothing is
     // encoded
@@ -919,8 +970,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     uint32_t acc_phase = 0;
     for (int unit = unit0; unit < p.num_units; unit += ustep) {
-      int m_blk, n_blk;
-      unit_coords<PAIR>(p, unit, rank, m_blk, n_blk);
+      int m_blk, n_blk, tile, kb_lo, kb_hi;
+      int64_t d_off;
+      unit_split(p, unit, tile, kb_lo, kb_hi, d_off);
+      unit_coords<PAIR>(p, tile, rank, m_blk, n_blk);
       if (!warp_wait(&ctl->acc_full, acc_phase, abort_flag, lane)) {
         if (lane == 0) fail(&ctl->abort, p, 6);
         break;
@@ -929,13 +982,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       if constexpr (QUANT) {
         if (q_live)
           epilogue_half<OUT_F32, PAIR, true>(p, &tmap_d, &tmap_q, stg, &ctl->acc_empty, tmem, m_blk, n_blk, q, half, lane, alpha, rank,
-                                             s_dec, amax_bits);
+                                             s_dec, amax_bits, d_off);
         else
           epilogue_half<OUT_F32, PAIR, false>(p, &tmap_d, &tmap_q, stg, &ctl->acc_empty, tmem, m_blk, n_blk, q, half, lane, alpha, rank,
-                                              s_dec, amax_bits);
+                                              s_dec, amax_bits, d_off);
       } else {
         epilogue_half<OUT_F32, PAIR, false>(p, &tmap_d, &tmap_q, stg, &ctl->acc_empty, tmem, m_blk, n_blk, q, half, lane, alpha, rank,
-                                            s_dec, amax_bits);
+                                            s_dec, amax_bits, d_off);
       }
       acc_phase ^= 1u;
     }
@@ -1012,6 +1065,47 @@ bool make_qcodes_map(CUtensorMap* map, uint8_t* codes, int64_t M, int64_t N) {
   return r == CUDA_SUCCESS;
 }
 
+// Split-K reduction: D[m, n] = RN(alpha * (((P0 + P1) + P2) + ...)) over the
+// split_k partial accumulators, in that fixed order, alpha = RN(sA * sB);
+// BF16 (round to nearest even) or FP32 output, row stride ldd.  Partials are
+// column-major 128 x 256 blocks per (split, tile) (element (r, c) of tile t
+// of split s at ((s * tiles + t) * 256 + c) * 128 + r; M <= 128).  A block of
+// 32 x 8 threads sums a 32-row x 32-column piece reading down columns and
+// writes it along rows through a shared-memory transpose.
+template <bool OUT_F32>
+__global__ void __launch_bounds__(256) splitk_reduce_kernel(const float* __restrict__ part, int split_k, int tiles,
+                                                            int64_t M, int64_t N, const float* a_scale,
+                                                            const float* b_scale, void* d, int64_t ldd) {
+  __shared__ float sm[32][33];
+  const float alpha = __fmul_rn(*a_scale, *b_scale);
+  const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
+  const int64_t n0 = static_cast<int64_t>(blockIdx.x) * 32;  // 32 output columns
+  const int r0 = static_cast<int>(blockIdx.y) * 32;          // 32 output rows
+  const int64_t split_stride = static_cast<int64_t>(tiles) * BN * BM;
+  for (int j = ty; j < 32; j += 8) {
+    const int64_t n = n0 + j;
+    float acc = 0.0f;
+    if (n < N) {
+      const int64_t t = n / BN, c = n - t * BN;
+      const float* src = part + (t * BN + c) * BM + r0 + tx;
+      acc = src[0];
+      for (int sp = 1; sp < split_k; ++sp) acc = __fadd_rn(acc, src[sp * split_stride]);
+    }
+    sm[j][tx] = acc;  // column j, row tx
+  }
+  __syncthreads();
+  for (int i = ty; i < 32; i += 8) {
+    const int64_t m = r0 + i, n = n0 + tx;
+    if (m < M && n < N) {
+      const float v = __fmul_rn(alpha, sm[tx][i]);
+      if (OUT_F32)
+        static_cast<float*>(d)[m * ldd + n] = v;
+      else
+        static_cast<__nv_bfloat16*>(d)[m * ldd + n] = __float2bfloat16_rn(v);
+    }
+  }
+}
+
 cudaLaunchAttribute pair_cluster_attr() {
   cudaLaunchAttribute attr{};
   attr.id = cudaLaunchAttributeClusterDimension;
@@ -1059,8 +1153,8 @@ cudaError_t launch_typed(const CUtensorMap& ma, const CUtensorMap& mb, const CUt
     max_clusters = clusters_of_device[dev];
   }
   if (!PAIR) {
-    p.num_units = p.num_tiles;
-    const int grid = std::min(p.num_tiles, device_sm_count());
+    p.num_units = p.num_tiles * (p.split_k > 1 ? p.split_k : 1);
+    const int grid = std::min(p.num_units, device_sm_count());
     kernel<<<grid, kThreads, L::kSmemBytes, stream>>>(ma, mb, md, mq, mlu, ml2, p);
     return cudaGetLastError();
   }
@@ -1078,6 +1172,31 @@ cudaError_t launch_typed(const CUtensorMap& ma, const CUtensorMap& mb, const CUt
 }
 
 }  // namespace
+
+int gemm_split_k(int64_t M, int64_t N, int64_t K, int* kb_per_split) {
+  // Split-K only where the output has too few tiles to occupy the GPU: one
+  // row block (single mode), fewer than half as many tiles as SMs, and at
+  // least two scale stages (8 k-blocks) of K.  Splits are whole scale stages
+  // (multiples of kSfGroup k-blocks).
+  if (M <= 0 || N <= 0 || M > BM || K <= 0) return 1;
+  const int num_kb = static_cast<int>((K + BK - 1) / BK);
+  const int64_t tiles = (N + BN - 1) / BN;
+  const int sms = device_sm_count();
+  if (tiles * 2 > sms || num_kb < 2 * kSfGroup) return 1;
+  int s = static_cast<int>(std::min<int64_t>(sms / tiles, num_kb / kSfGroup));
+  if (s < 2) return 1;
+  int per = (num_kb + s - 1) / s;
+  per = (per + kSfGroup - 1) / kSfGroup * kSfGroup;
+  s = (num_kb + per - 1) / per;
+  if (s < 2) return 1;
+  if (kb_per_split) *kb_per_split = per;
+  return s;
+}
+
+size_t gemm_split_k_bytes(int64_t M, int64_t N, int split_k) {
+  const int64_t tiles = ((M + BM - 1) / BM) * ((N + BN - 1) / BN);
+  return static_cast<size_t>(split_k) * tiles * BM * BN * sizeof(float);
+}
 
 cudaError_t launch_gemm(const GemmArgs& a, cudaStream_t stream) {
   if (a.M == 0 || a.N == 0) return cudaSuccess;
@@ -1121,6 +1240,33 @@ cudaError_t launch_gemm(const GemmArgs& a, cudaStream_t stream) {
   const size_t esz = a.out_f32 ? 4 : 2;
   p.vec_store = (reinterpret_cast<uintptr_t>(a.d) % 16 == 0) && ((a.ldd * esz) % 16 == 0);
   CUtensorMap md{}, mq{}, mlu{}, ml2{};
+  p.split_k = 1;
+  p.kb_per_split = p.num_kb;
+  if (!a.quant && a.lora_r == 0 && !pair && a.partial) {
+    int per = 0;
+    const int sk = gemm_split_k(a.M, a.N, a.K, &per);
+    if (sk > 1 && a.partial_bytes >= gemm_split_k_bytes(a.M, a.N, sk)) {
+      // partial accumulators [split_k, M, N] FP32 in the workspace, then a
+      // fixed-order reduction that applies alpha and converts
+      GParams q = p;
+      q.split_k = sk;
+      q.kb_per_split = per;
+      q.d = a.partial;
+      q.ldd = a.N;
+      q.vec_store = 0;
+      q.tma_store = 0;
+      cudaError_t e = launch_typed<true, false, false>(ma, mb, md, mq, mlu, ml2, q, stream);
+      if (e != cudaSuccess) return e;
+      const dim3 grid(static_cast<unsigned>((a.N + 31) / 32), static_cast<unsigned>((a.M + 31) / 32));
+      if (a.out_f32)
+        splitk_reduce_kernel<true><<<grid, 256, 0, stream>>>(a.partial, sk, p.num_tiles, a.M, a.N, a.a_scale,
+                                                              a.b_scale, a.d, a.ldd);
+      else
+        splitk_reduce_kernel<false><<<grid, 256, 0, stream>>>(a.partial, sk, p.num_tiles, a.M, a.N, a.a_scale,
+                                                               a.b_scale, a.d, a.ldd);
+      return cudaGetLastError();
+    }
+  }
   if (a.lora_r > 0) {
     // LoRA branch: two BF16 k-blocks (hi, lo) per 64 columns of U; boxes of
     // 64 columns x the code boxes' rows (reads past r are zero)

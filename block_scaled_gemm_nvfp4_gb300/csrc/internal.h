@@ -93,9 +93,18 @@ struct GemmArgs {
   const uint16_t* lora_uhl;
   const uint16_t* lora_l2;
   int64_t lora_r, lora_rpad;
+  // split-K scratch (FP32 partial accumulators) for outputs with too few
+  // tiles; null or too small: no split
+  float* partial;
+  size_t partial_bytes;
 };
 
 cudaError_t launch_gemm(const GemmArgs& a, cudaStream_t stream);
+// Number of K splits launch_gemm uses for a GEMM shape (1: none), and the
+// k-blocks (256 of K) per split.
+int gemm_split_k(int64_t M, int64_t N, int64_t K, int* kb_per_split);
+// Bytes of split-K scratch for that many splits (whole 128 x 256 FP32 blocks).
+size_t gemm_split_k_bytes(int64_t M, int64_t N, int split_k);
 
 // LoRA-SVD branch, first half (lora.cu): U = BF16(X L1^T) and the hi / lo
 // split of (beta / (sx sw)) U that the GEMM adds into its accumulator.

@@ -229,7 +229,13 @@ nvfp4_status nvfp4_dequantize(const nvfp4_tensor* q, int32_t out_dtype, void* ou
  * nearest even) or FP32 store, row stride ldd elements.
  * Shape rules: K % 32 == 0; both operands' scales in NVFP4_SF_MMA layout;
  * codes 16-byte aligned; ldd >= N.  M, N are arbitrary (ragged tiles are
- * handled).  Workspace: nvfp4_gemm_workspace_size bytes (status word).
+ * handled).  Workspace: nvfp4_gemm_workspace_size bytes: the status word,
+ * and, for outputs of one 128-row block with too few tiles to occupy the
+ * GPU (a decode-like M <= 128), FP32 scratch for split-K partial sums: K is
+ * split into whole groups of 1024, each split's accumulator is stored
+ * unscaled, and a reduction adds them in split order, multiplies by
+ * sA * sB and converts.  A workspace holding only the 256-byte header runs
+ * the same GEMM unsplit.
  * Source: "Como o treinamento mixed-precision funciona com NVFP4" (NVFP4
  * operands, FP32 accumulators) on the JAX/MaxText page.
  */

@@ -204,3 +204,30 @@ def test_empty_shapes():
     d = nv.nvfp4_gemm(a, b, out_dtype=nv.NVFP4_OUT_F32)
     torch.cuda.synchronize()
     assert d.shape == (0, 32)
+
+
+@pytest.mark.parametrize("M,N,K", [(128, 8192, 8192), (100, 1000, 4160), (1, 256, 8192), (64, 520, 2048),
+                                   (128, 2304, 16384)])
+@pytest.mark.parametrize("out", ["f32", "bf16"])
+def test_split_k_vs_oracle(M, N, K, out):
+    # one row block with few tiles: the workspace from nvfp4_gemm_workspace_size
+    # holds split-K scratch, and the header-only workspace runs unsplit
+    a = syn.normal_bf16((M, K), seed=M + 7)
+    b = syn.normal_bf16((N, K), seed=N + 8)
+    qa, oa = _quantised(a)
+    qb, ob = _quantised(b, block=0, rounding=1, rht=1)
+    od = nv.NVFP4_OUT_F32 if out == "f32" else nv.NVFP4_OUT_BF16
+    ws = torch.zeros(nv.nvfp4_gemm_workspace_size(M, N, K), dtype=torch.uint8, device=DEV)
+    assert ws.numel() > 256, "this shape is expected to split"
+    d = nv.nvfp4_gemm(qa, qb, out_dtype=od, workspace=ws)
+    d_plain = nv.nvfp4_gemm(qa, qb, out_dtype=od, workspace=torch.zeros(256, dtype=torch.uint8, device=DEV))
+    assert nv.nvfp4_check_device_status(ws) == nv.NVFP4_OK
+    # the oracle's GEMM definition (FP64 sum over its dequantised operands),
+    # summed by a library FP64 matmul for these long shapes
+    ref = oracle.dequantize(*oa, M, K) @ oracle.dequantize(*ob, N, K).T
+    for got in (d, d_plain):
+        g = got.float().cpu().numpy()
+        if out == "f32":
+            assert rel_err(g, ref) <= 1e-3
+        else:
+            assert bf16_within_one_ulp(g, ref)
