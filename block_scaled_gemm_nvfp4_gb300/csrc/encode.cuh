@@ -102,24 +102,29 @@ __device__ __forceinline__ uint4 philox4x32_10_rk(uint4 c, const uint32_t (&rk0)
 
 // Stochastic rounding of q onto the E2M1 grid {0, .5, 1, 1.5, 2, 3, 4, 6}:
 // lo, hi the grid points around |q|, f = (|q| - lo) / (hi - lo), round up iff
-// k * 2^-24 < f with k = r >> 8; |q| >= 6 -> 6.  Branch-free:
+// k * 2^-24 < f with k = r >> 8; |q| >= 6 -> 6.  Branch-free, with b the
+// magnitude bits of q and m its 23 mantissa bits:
 //   |q| in [1, 6): the grid points are the values whose 22 mantissa bits
 //     below the top one are zero and f * 2^24 = 4 * (those bits), so
-//     k < f * 2^24 iff adding 2^22 - 1 - (k >> 2) to the bits carries into
-//     the grid bit;
-//   |q| in [0, 1): lo in {0, 1/2} and f * 2^24 = |q| * 2^25 - lo * 2^25,
-//     exact in FP32, compared with k (< 2^24, exact as a float).
-// Returns the grid value with the sign of q.
+//     k < f * 2^24 iff adding 2^22 - 1 - (r >> 10) to b carries into the
+//     grid bit;
+//   |q| in [1/2, 1): lo = 1/2, hi = 1 and f * 2^24 = 2 m, so k < 2 m iff
+//     adding 2^23 - 1 - (r >> 9) to b carries into the exponent;
+//   |q| in [0, 1/2): lo = 0, f * 2^24 = |q| * 2^25, exact in FP32, compared
+//     with k (< 2^24, exact as a float).
+// The shifts of r are taken as high halves of products (r * 2^(32-s)), and
+// every |q| >= 6 (inf and NaN included) lands at or above the bits of 6, so
+// one unsigned min saturates.  Returns the grid value with the sign of q.
 __device__ __forceinline__ float sr_round(float q, uint32_t rnd) {
-  const uint32_t b = abs_bits(q);
-  const uint32_t g_hi = (b + ((~rnd) >> 10)) & 0xFFC00000u;
-  const bool half_up = b >= 0x3F000000u;  // |q| >= 1/2: lo = 1/2
-  const float y = __fmaf_rn(__uint_as_float(b), 33554432.0f, half_up ? -16777216.0f : 0.0f);
-  const bool up = __uint2float_rn(rnd >> 8) < y;
-  const uint32_t g_lo = (half_up ? 0x3F000000u : 0u) + (up ? (half_up ? 0x00800000u : 0x3F000000u) : 0u);
-  uint32_t g = b >= 0x3F800000u ? g_hi : g_lo;
-  g = b >= 0x40C00000u ? 0x40C00000u : g;
-  return __uint_as_float(g | (__float_as_uint(q) & 0x80000000u));
+  const uint32_t qb = __float_as_uint(q);
+  const uint32_t b = qb & 0x7FFFFFFFu;
+  const uint32_t g_hi = (b + 0x3FFFFFu - __umulhi(rnd, 1u << 22)) & 0xFFC00000u;
+  const uint32_t g_mid = (b + 0x7FFFFFu - __umulhi(rnd, 1u << 23)) & 0xFF800000u;
+  const bool up0 = __uint2float_rn(__umulhi(rnd, 1u << 24)) < __fmul_rn(__uint_as_float(b), 33554432.0f);
+  const uint32_t g_low = up0 ? 0x3F000000u : 0u;
+  uint32_t g = b >= 0x3F800000u ? g_hi : (b >= 0x3F000000u ? g_mid : g_low);
+  g = min(g, 0x40C00000u);
+  return __uint_as_float(g | (qb & 0x80000000u));
 }
 
 }  // namespace nvfp4

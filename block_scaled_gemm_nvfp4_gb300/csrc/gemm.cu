@@ -567,7 +567,10 @@ __device__ __forceinline__ void stage_scales(const uint8_t* sfa, const uint8_t* 
   ptx::tmem_st_32x32b_x32(lane_base + kSfbCol + slot * 32, vb);
 }
 
-template <bool OUT_F32, bool PAIR, bool QUANT>
+// LORA: the kernel also runs the LoRA-SVD branch's BF16 k-blocks.  It is a
+// template parameter because even an untaken per-k-block branch on the MMA
+// issuer's path cost the plain GEMM about 13 % (measured on GB300).
+template <bool OUT_F32, bool PAIR, bool QUANT, bool LORA>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
                 const __grid_constant__ CUtensorMap tmap_d, const __grid_constant__ CUtensorMap tmap_q,
@@ -576,6 +579,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   using L = Layout<PAIR>;
   constexpr int S = L::kStages;
   constexpr int SS = L::kSfStages;
+  const int lora_kb = LORA ? p.lora_kb : 0;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sf_ring = smem + L::kSfRing;
@@ -611,7 +615,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     ptx::prefetch_tensormap(&tmap_b);
     if (p.tma_store) ptx::prefetch_tensormap(&tmap_d);
     if (QUANT) ptx::prefetch_tensormap(&tmap_q);
-    if (p.lora_kb > 0) {
+    if (LORA) {
       ptx::prefetch_tensormap(&tmap_lu);
       ptx::prefetch_tensormap(&tmap_l2);
     }
@@ -647,7 +651,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         int64_t d_off;
         unit_split(p, unit, tile, kb_lo, kb_hi, d_off);
         unit_coords<PAIR>(p, tile, rank, m_blk, n_blk);
-        for (int kb = kb_lo; kb < kb_hi + p.lora_kb; ++kb) {
+        for (int kb = kb_lo; kb < kb_hi + lora_kb; ++kb) {
           if (!ptx::mbar_wait(&ctl->empty[stage], phase ^ 1u, abort_flag)) {
             fail(&ctl->abort, p, 1);
             ok = false;
@@ -663,7 +667,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             continue;
           }
-          if (kb >= kb_hi) {
+          if (LORA && kb >= kb_hi) {
             // LoRA branch k-block j: A = hi (j even) or lo (j odd) of the
             // branch's 64-column chunk j / 2, B = that chunk of L2; the same
             // box sizes and swizzle as a k-block of codes
@@ -783,7 +787,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         ptx::tc_fence_after();
-        for (int kb = kb_lo; kb < kb_hi + p.lora_kb; ++kb) {
+        for (int kb = kb_lo; kb < kb_hi + lora_kb; ++kb) {
           // One wait per k-block: the stage's barrier completes when its code
           // tiles have landed (pair mode: both CTAs') and every staging warp
           // (both CTAs') has put its scales into the stage's TMEM slot.
@@ -799,7 +803,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t st_off = static_cast<uint32_t>(stage * L::kStageBytes);
           const uint64_t adesc0 = a_desc0 + (st_off >> 4);
           const uint64_t bdesc0 = b_desc0 + (st_off >> 4);
-          if (kb >= kb_hi) {
+          if (LORA && kb >= kb_hi) {
             // LoRA branch: four BF16 MMAs of K = 16 (32 bytes along the
             // swizzled 128-byte rows), added to the NVFP4 accumulation
 #pragma unroll
@@ -927,7 +931,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       // LoRA branch k-blocks need no scales: the staging warps only take
       // part in their stages' barriers, once the stage is free again.
-      for (int j = 0; j < p.lora_kb && ok; ++j) {
+      for (int j = 0; LORA && j < lora_kb && ok; ++j) {
         if (!warp_wait(&ctl->empty[slot], tphase ^ 1u, abort_flag, lane)) {
           if (lane == 0) fail(&ctl->abort, p, 8);
           ok = false;
@@ -1115,12 +1119,12 @@ cudaLaunchAttribute pair_cluster_attr() {
   return attr;
 }
 
-template <bool OUT_F32, bool PAIR, bool QUANT>
+template <bool OUT_F32, bool PAIR, bool QUANT, bool LORA = false>
 cudaError_t launch_typed(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& md,
                          const CUtensorMap& mq, const CUtensorMap& mlu, const CUtensorMap& ml2, GParams p,
                          cudaStream_t stream) {
   using L = Layout<PAIR>;
-  auto kernel = gemm_kernel<OUT_F32, PAIR, QUANT>;
+  auto kernel = gemm_kernel<OUT_F32, PAIR, QUANT, LORA>;
   // One-time setup per device (the shared-memory opt-in and, in pair mode,
   // the number of co-resident clusters), safe against concurrent first calls.
   static std::mutex setup_mutex;
@@ -1293,6 +1297,13 @@ cudaError_t launch_gemm(const GemmArgs& a, cudaStream_t stream) {
     if (!make_qcodes_map(&mq, a.q_codes, a.M, a.N)) return cudaErrorInvalidValue;
     return pair ? launch_typed<false, true, true>(ma, mb, md, mq, mlu, ml2, p, stream)
                 : launch_typed<false, false, true>(ma, mb, md, mq, mlu, ml2, p, stream);
+  }
+  if (p.lora_kb > 0) {
+    if (pair)
+      return a.out_f32 ? launch_typed<true, true, false, true>(ma, mb, md, mq, mlu, ml2, p, stream)
+                       : launch_typed<false, true, false, true>(ma, mb, md, mq, mlu, ml2, p, stream);
+    return a.out_f32 ? launch_typed<true, false, false, true>(ma, mb, md, mq, mlu, ml2, p, stream)
+                     : launch_typed<false, false, false, true>(ma, mb, md, mq, mlu, ml2, p, stream);
   }
   if (pair)
     return a.out_f32 ? launch_typed<true, true, false>(ma, mb, md, mq, mlu, ml2, p, stream)

@@ -8,7 +8,8 @@
 // read halves the quantiser's input traffic.
 //
 // Two kernels, both persistent loops over 128 x 128 tiles of x that TMA copies
-// into shared memory (two 64-column boxes, 128-byte swizzle, two-stage ring):
+// into shared memory (two 64-column boxes, 128-byte swizzle; a ring of three
+// stages in the amax pass, two in the encode pass):
 //   pass 0: per-output tensor amax (after the optional random Hadamard
 //           transform, in the output's orientation); one partial per CTA;
 //   pass 1: every CTA reduces the partials, derives s = amax / 2688 and encodes
@@ -60,7 +61,13 @@ constexpr int kThreads = 256;
 constexpr int kTile = 128;                      // tile: 128 rows x 128 columns of x
 constexpr int kBoxBytes = kTile * 128;          // one TMA box: 64 BF16 columns x 128 rows
 constexpr int kStageBytes = 2 * kBoxBytes;      // 32 KB
-constexpr int kStages = 2;
+// TMA ring depth: the encode pass keeps two stages (its staging buffers
+// fill the rest of two CTAs' shared memory per SM); the amax pass has no
+// staging and keeps three tiles in flight.
+template <int PASS>
+__host__ __device__ constexpr int stages_of() {
+  return PASS == 0 ? 3 : 2;
+}
 // Per output, a tile's results are staged in shared memory before they go to
 // global memory in whole 32-byte pieces: codes of position p, run j at
 // p * 72 + 8 j (the 72-byte pitch spreads a warp's stores over the banks);
@@ -69,8 +76,11 @@ constexpr int kStages = 2;
 constexpr int kStgPitch = 72;
 constexpr int kStgCodes = kTile * kStgPitch;    // 9216
 constexpr int kStgBytes = kStgCodes + 2 * 512;  // + scales
-constexpr int kStgOffset = kStages * kStageBytes;
-constexpr int kSmemBytes = kStgOffset + 2 * kMaxQuantOutputs * kStgBytes + 1024;  // + slack to align to 1024 B
+constexpr int kStgOffset = stages_of<1>() * kStageBytes;
+template <int PASS>
+constexpr int smem_bytes() {  // + slack to align to 1024 B
+  return PASS == 0 ? stages_of<0>() * kStageBytes + 1024 : kStgOffset + 2 * kMaxQuantOutputs * kStgBytes + 1024;
+}
 
 struct OutParams {
   uint8_t* codes;
@@ -330,6 +340,7 @@ template <int PASS>
 __global__ void __launch_bounds__(kThreads, 2) quant_tiles(const __grid_constant__ CUtensorMap xmap,
                                                            const TileParams p) {
   extern __shared__ uint8_t smem_raw[];
+  constexpr int kStages = stages_of<PASS>();
   __shared__ __align__(8) uint64_t full[kStages];
   __shared__ uint32_t red[kThreads / 32];
   __shared__ int abort_flag;
@@ -509,10 +520,10 @@ int tiles_per_sm(cudaError_t* err) {
   }
   std::lock_guard<std::mutex> lock(setup_mutex);
   if (per_sm[dev] == 0) {
-    *err = cudaFuncSetAttribute(quant_tiles<PASS>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    *err = cudaFuncSetAttribute(quant_tiles<PASS>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes<PASS>());
     if (*err != cudaSuccess) return 0;
     int b = 0;
-    *err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, quant_tiles<PASS>, kThreads, kSmemBytes);
+    *err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, quant_tiles<PASS>, kThreads, smem_bytes<PASS>());
     if (*err != cudaSuccess) return 0;
     per_sm[dev] = std::max(b, 1);
   }
@@ -674,12 +685,12 @@ cudaError_t launch_quantize(const QuantArgs& a, cudaStream_t stream) {
   p.num_partials = static_cast<int>(g);
   if (scan) {
     p.skip_first_load = a.skip_load_pass == 1;
-    quant_tiles<0><<<static_cast<int>(g), kThreads, kSmemBytes, stream>>>(xmap, p);
+    quant_tiles<0><<<static_cast<int>(g), kThreads, smem_bytes<0>(), stream>>>(xmap, p);
     err = cudaGetLastError();
     if (err != cudaSuccess) return err;
   }
   p.skip_first_load = a.skip_load_pass == 2;
-  quant_tiles<1><<<static_cast<int>(g), kThreads, kSmemBytes, stream>>>(xmap, p);
+  quant_tiles<1><<<static_cast<int>(g), kThreads, smem_bytes<1>(), stream>>>(xmap, p);
   return cudaGetLastError();
 }
 
