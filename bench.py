@@ -39,7 +39,7 @@ WORKLOAD = ("12B-hybrid MLP up-projection fprop+dgrad+wgrad, tokens 8192 (4x2048
 # one ncu capture of each of the step's three GEMM shapes, averaged like the
 # achieved rate), keyed by the SHA-256 prefix of the GEMM kernel's sources: a
 # changed kernel reports null until it is measured again.
-GEMM_TRAFFIC = {"612db1d886fd350a": 438318165}
+GEMM_TRAFFIC = {"612db1d886fd350a": 438318165, "0061b0eb53ba3ef9": 433368405}
 
 
 def _gemm_traffic():
