@@ -634,8 +634,7 @@ nvfp4_status nvfp4_ns_step(const void* x, int64_t m, int64_t n, float a, float b
     if (e != cudaSuccess) return NVFP4_ERR_CUDA; \
   } while (0)
   // Xc = clip(X); Q(Xc) along n and Q(Xc^T) along m from one read
-  NS_TRY(launch_abs_percentile(xin, m * n, kx, hist, q, status, st));
-  NS_TRY(launch_clip(xin, m * n, q, bf(L.xc), st));
+  NS_TRY(launch_percentile_clip(xin, m * n, kx, hist, q, bf(L.xc), status, st));
   {
     QuantArgs qa2{};
     qa2.x = bf(L.xc);
@@ -654,8 +653,7 @@ nvfp4_status nvfp4_ns_step(const void* x, int64_t m, int64_t n, float a, float b
   s = gemm_into(&tx, &tx, NVFP4_OUT_BF16, bf(L.a), m, status, st);
   if (s != NVFP4_OK) return s;
   // A A^T from Q(clip(A))
-  NS_TRY(launch_abs_percentile(bf(L.a), m * m, ka, hist + 384, q + 1, status, st));
-  NS_TRY(launch_clip(bf(L.a), m * m, q + 1, bf(L.ac), st));
+  NS_TRY(launch_percentile_clip(bf(L.a), m * m, ka, hist + 384, q + 1, bf(L.ac), status, st));
   s = quantize_into(bf(L.ac), m, m, m, rows, qa.codes, qa.sf, qa.scale, status, partials, st);
   if (s != NVFP4_OK) return s;
   nvfp4_tensor ta{qa.codes, qa.sf, qa.scale, m, m, NVFP4_SF_MMA, 0};
@@ -663,8 +661,7 @@ nvfp4_status nvfp4_ns_step(const void* x, int64_t m, int64_t n, float a, float b
   if (s != NVFP4_OK) return s;
   // B = b A + c A A^T; B X from Q(clip(B)) and Q(Xc^T)
   NS_TRY(launch_axpby(bf(L.a), bf(L.a2), m * m, b, c, bf(L.b), st));
-  NS_TRY(launch_abs_percentile(bf(L.b), m * m, ka, hist + 768, q + 2, status, st));
-  NS_TRY(launch_clip(bf(L.b), m * m, q + 2, bf(L.bc), st));
+  NS_TRY(launch_percentile_clip(bf(L.b), m * m, ka, hist + 768, q + 2, bf(L.bc), status, st));
   s = quantize_into(bf(L.bc), m, m, m, rows, qb.codes, qb.sf, qb.scale, status, partials, st);
   if (s != NVFP4_OK) return s;
   nvfp4_tensor tb{qb.codes, qb.sf, qb.scale, m, m, NVFP4_SF_MMA, 0};

@@ -687,9 +687,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             // both CTAs' code tiles complete on the leader's barrier
             const uint32_t bar = full_leader0 + static_cast<uint32_t>(stage * sizeof(uint64_t));
             if (leader) ptx::mbar_arrive_expect_tx(&ctl->full[stage], 2u * (kABytes + L::kBBytes));
-            ptx::tma_load_2d_pair(st, &tmap_a, bar, kb * kRowBytes, m_blk * BM);
-            ptx::tma_load_2d_pair(st + kABytes, &tmap_b, bar, kb * kRowBytes,
-                                  n_blk * BN + static_cast<int>(rank) * L::kBRows);
+            ptx::tma_load_2d_pair_hint(st, &tmap_a, bar, kb * kRowBytes, m_blk * BM, l2_keep);
+            ptx::tma_load_2d_pair_hint(st + kABytes, &tmap_b, bar, kb * kRowBytes,
+                                       n_blk * BN + static_cast<int>(rank) * L::kBRows, l2_keep);
           } else {
             ptx::mbar_arrive_expect_tx(&ctl->full[stage], static_cast<uint32_t>(kABytes + L::kBBytes));
             ptx::tma_load_2d_hint(st, &tmap_a, &ctl->full[stage], kb * kRowBytes, m_blk * BM, l2_keep);

@@ -148,6 +148,10 @@ cudaError_t launch_abs_percentile(const uint16_t* x, int64_t n, uint64_t k, uint
                                   uint32_t* status, cudaStream_t stream);
 constexpr size_t kPercentileHistBytes = 384 * sizeof(uint32_t);
 cudaError_t launch_clip(const uint16_t* x, int64_t n, const float* q, uint16_t* out, cudaStream_t stream);
+// Percentile selection and clip together (the selection runs in the clip
+// kernel's blocks; q receives the threshold).
+cudaError_t launch_percentile_clip(const uint16_t* x, int64_t n, uint64_t k, uint32_t* hist, float* q, uint16_t* out,
+                                   uint32_t* status, cudaStream_t stream);
 cudaError_t launch_axpby(const uint16_t* x, const uint16_t* y, int64_t n, float a, float b, uint16_t* out,
                          cudaStream_t stream);
 

@@ -19,7 +19,9 @@
 //     the top 8 bits, one for the low 7 bits inside the selected bin, and a
 //     one-block selection that writes q;
 //   * clipping to [-q, q] (on the bit patterns: a magnitude above q's becomes
-//     q's, with the element's sign), BF16 in and out, exact;
+//     q's, with the element's sign), BF16 in and out, exact; inside the step
+//     the clip kernel also does the selection, so each percentile-and-clip
+//     is two histogram passes and one clip pass;
 //   * out = BF16(RN(RN(a x) + RN(b y))), elementwise in FP32.
 // All three are HBM-bound streaming kernels: 16-byte vector loads and stores,
 // grids of a few CTAs per SM.
@@ -140,13 +142,19 @@ __global__ void __launch_bounds__(kThreads) hist_lo_kernel(const uint16_t* x, in
   }
 }
 
-// q = the k-th smallest magnitude, as the FP32 value of its BF16 pattern.
-__global__ void select_kernel(uint64_t k, const uint32_t* hist_hi, const uint32_t* hist_lo, float* q) {
+// The selected magnitude's bit pattern from the two histograms (one warp).
+__device__ __forceinline__ uint32_t select_bits(uint64_t k, const uint32_t* hist_hi, const uint32_t* hist_lo) {
   int hi, lo;
   uint64_t k_in, k_lo;
   select_bin(hist_hi, kHiBins, k, hi, k_in);
   select_bin(hist_lo, kLoBins, k_in, lo, k_lo);
-  if (threadIdx.x == 0) *q = __uint_as_float(((static_cast<uint32_t>(hi) << 7) | static_cast<uint32_t>(lo)) << 16);
+  return (static_cast<uint32_t>(hi) << 7) | static_cast<uint32_t>(lo);
+}
+
+// q = the k-th smallest magnitude, as the FP32 value of its BF16 pattern.
+__global__ void select_kernel(uint64_t k, const uint32_t* hist_hi, const uint32_t* hist_lo, float* q) {
+  const uint32_t bits = select_bits(k, hist_hi, hist_lo);
+  if (threadIdx.x == 0) *q = __uint_as_float(bits << 16);
 }
 
 __device__ __forceinline__ uint32_t clip_bits(uint32_t b, uint32_t qm) {
@@ -154,8 +162,27 @@ __device__ __forceinline__ uint32_t clip_bits(uint32_t b, uint32_t qm) {
   return (m > qm && m <= 0x7F80u) ? ((b & 0x8000u) | qm) : b;  // NaN passes through
 }
 
-__global__ void __launch_bounds__(kThreads) clip_kernel(const uint16_t* x, int64_t n, const float* q, uint16_t* out) {
-  const uint32_t qm = (__float_as_uint(*q) >> 16) & 0x7FFFu;
+// SELECT: the block's first warp selects the percentile from the histograms
+// itself (block 0 also stores it in q), which saves the one-block selection
+// launch inside the Newton-Schulz step; otherwise q is read.
+template <bool SELECT>
+__global__ void __launch_bounds__(kThreads) clip_kernel(const uint16_t* x, int64_t n, uint64_t k, const uint32_t* hist,
+                                                        float* q, uint16_t* out) {
+  __shared__ uint32_t sel;
+  uint32_t qm;
+  if (SELECT) {
+    if (threadIdx.x < 32) {
+      const uint32_t bits = select_bits(k, hist, hist + kHiBins);
+      if (threadIdx.x == 0) {
+        sel = bits;
+        if (blockIdx.x == 0) *q = __uint_as_float(bits << 16);
+      }
+    }
+    __syncthreads();
+    qm = sel;
+  } else {
+    qm = (__float_as_uint(*q) >> 16) & 0x7FFFu;
+  }
   const int64_t nvec = n / 8;
   const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
   const uint4* xv = reinterpret_cast<const uint4*>(x);
@@ -224,7 +251,18 @@ cudaError_t launch_abs_percentile(const uint16_t* x, int64_t n, uint64_t k, uint
 }
 
 cudaError_t launch_clip(const uint16_t* x, int64_t n, const float* q, uint16_t* out, cudaStream_t stream) {
-  clip_kernel<<<stream_grid(n), kThreads, 0, stream>>>(x, n, q, out);
+  clip_kernel<false><<<stream_grid(n), kThreads, 0, stream>>>(x, n, 0, nullptr, const_cast<float*>(q), out);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_percentile_clip(const uint16_t* x, int64_t n, uint64_t k, uint32_t* hist, float* q, uint16_t* out,
+                                   uint32_t* status, cudaStream_t stream) {
+  cudaError_t e = cudaMemsetAsync(hist, 0, (kHiBins + kLoBins) * sizeof(uint32_t), stream);
+  if (e != cudaSuccess) return e;
+  const int g = stream_grid(n);
+  hist_hi_kernel<<<g, kThreads, 0, stream>>>(x, n, hist, status);
+  hist_lo_kernel<<<g, kThreads, 0, stream>>>(x, n, k, hist, hist + kHiBins);
+  clip_kernel<true><<<g, kThreads, 0, stream>>>(x, n, k, hist, q, out);
   return cudaGetLastError();
 }
 
