@@ -17,13 +17,15 @@
 // Codes and block scales travel in separate rings.  A scale stage holds four
 // k-blocks (three 8 KB copies) and runs ahead of the code ring; the staging
 // warps move each k-block's scales into the TMEM slot of its code stage as
-// soon as the stage's previous MMAs are done, two k-blocks at a time, and
-// arrive on the stage's own barrier, so the scale copies and the staging are
-// hidden behind earlier k-blocks.  The MMA issuer
-// then waits on one barrier and commits once per k-block: the tensor pipe
-// leaves one thread issuing four MMAs per k-block little time to spare, and
-// every extra barrier hop on its path (a separate scale-ready barrier with the
-// peer CTA's remote arrivals cost about a quarter of the throughput) shows up
+// soon as the stage's previous MMAs are done and arrive on the stage's own
+// barrier, so the scale copies and the staging are hidden behind earlier
+// k-blocks.  The MMA issuer then has one barrier per k-block and commits once
+// per k-block.  The tensor pipe holds almost no issued work beyond the MMA in
+// flight, so every cycle the issuing thread spends between MMAs idles it: the
+// issuer tests the next k-block's barrier without blocking, ahead of the
+// current k-block's MMAs, and blocks only when that test failed, and every
+// extra barrier hop on its path (a separate scale-ready barrier with the peer
+// CTA's remote arrivals cost about a quarter of the throughput) shows up
 // directly in the k-block period (measured on GB300 with traces and variants).
 // Warp roles (15 warps):
 //   warp 0     TMA producer for the packed E2M1 codes (tiled TMA, 128-byte
@@ -774,6 +776,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       int stage = 0;
       uint32_t phase = 0, acc_phase = 0;
       bool ok = true, issued = false;
+      // The tensor pipe holds little issued work, so each cycle this thread
+      // spends outside MMA issue between k-blocks idles it; a blocking wait
+      // on an already-completed barrier costs ~150-200 cycles.  Each full
+      // k-block therefore tests the next stage's barrier without blocking,
+      // ahead of its own MMAs, and the next k-block waits only if that test
+      // failed.
+      bool next_ready = false;
       // descriptors of stage 0; other stages and K steps are plain offsets
       // of the 14-bit start-address field (shared-memory addresses < 256 KB)
       const uint64_t a_desc0 = ptx::smem_desc(ptx::smem_u32(smem), 16, 1024, ptx::kSwizzle128B);
@@ -794,7 +803,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           // CTA-scope waits suffice: the peer's arrivals follow completed
           // TMEM writes, and the code tiles are TMA (async-proxy) writes read
           // by the tensor core.
-          if (!ptx::mbar_wait(&ctl->full[stage], phase, abort_flag)) {
+          if (!next_ready && !ptx::mbar_wait(&ctl->full[stage], phase, abort_flag)) {
             fail(&ctl->abort, p, 4);
             ok = false;
             break;
@@ -817,6 +826,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               ptx::tc_commit_pair_multicast(&ctl->empty[stage], static_cast<uint16_t>(0x3));
             else
               ptx::tc_commit(&ctl->empty[stage]);
+            next_ready = false;
             if (++stage == S) {
               stage = 0;
               phase ^= 1u;
@@ -826,17 +836,39 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int kk_n = kk_count_for(p, kb);
           const uint32_t sfa_t0 = tmem + kSfaCol + stage * 16;
           const uint32_t sfb_t0 = tmem + kSfbCol + stage * 32;
+          if (kk_n == 4) {
+            // the next stage's barrier: the phase the next k-block waits for
+            const int nstage = stage + 1 == S ? 0 : stage + 1;
+            const uint32_t nphase = stage + 1 == S ? phase ^ 1u : phase;
+            // +32 bytes along K inside the swizzled 128-byte rows per MMA
+            next_ready = ptx::tc_mma_nvf4_x2_probe<PAIR>(
+                             tmem + kAccCol, adesc0, bdesc0, adesc0 + 2, bdesc0 + 2, L::kIdesc, sfa_t0, sfb_t0,
+                             sfa_t0 + 4, sfb_t0 + 8, kb != kb_lo ? 1u : 0u, ptx::smem_u32(&ctl->full[nstage]),
+                             nphase) != 0u;
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk) {
-            if (kk < kk_n) {
-              // +32 bytes along K inside the swizzled 128-byte rows
-              const uint64_t adesc = adesc0 + 2 * kk, bdesc = bdesc0 + 2 * kk;
-              const uint32_t acc = (kb != kb_lo || kk != 0) ? 1u : 0u;
+            for (int kk = 2; kk < 4; ++kk) {
               if (PAIR)
-                ptx::tc_mma_nvf4_pair(tmem + kAccCol, adesc, bdesc, L::kIdesc, sfa_t0 + kk * 4, sfb_t0 + kk * 8, acc);
+                ptx::tc_mma_nvf4_pair(tmem + kAccCol, adesc0 + 2 * kk, bdesc0 + 2 * kk, L::kIdesc, sfa_t0 + kk * 4,
+                                      sfb_t0 + kk * 8, 1u);
               else
-                ptx::tc_mma_nvf4(tmem + kAccCol, adesc, bdesc, L::kIdesc, sfa_t0 + kk * 4, sfb_t0 + kk * 8, acc);
+                ptx::tc_mma_nvf4(tmem + kAccCol, adesc0 + 2 * kk, bdesc0 + 2 * kk, L::kIdesc, sfa_t0 + kk * 4,
+                                 sfb_t0 + kk * 8, 1u);
             }
+          } else {
+            // the ragged last k-block of K
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+              if (kk < kk_n) {
+                const uint64_t adesc = adesc0 + 2 * kk, bdesc = bdesc0 + 2 * kk;
+                const uint32_t acc = (kb != kb_lo || kk != 0) ? 1u : 0u;
+                if (PAIR)
+                  ptx::tc_mma_nvf4_pair(tmem + kAccCol, adesc, bdesc, L::kIdesc, sfa_t0 + kk * 4, sfb_t0 + kk * 8,
+                                        acc);
+                else
+                  ptx::tc_mma_nvf4(tmem + kAccCol, adesc, bdesc, L::kIdesc, sfa_t0 + kk * 4, sfb_t0 + kk * 8, acc);
+              }
+            }
+            next_ready = false;
           }
           // one commit frees the code stage and its TMEM scale slot
           if (PAIR)
@@ -868,10 +900,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp >= kFirstSfWarp) {
     // ------------------------------------------------------ scale staging
-    // Two k-blocks per iteration: their stores share one wait::st and the
-    // arrivals go out together, which halves this warp's fixed per-k-block
-    // cost (barrier waits, arrivals, a remote one in the follower); staging
-    // had become the slowest stage of the pipeline.
+    // One k-block per iteration: wait until the scales are in the ring (one
+    // wait per scale stage) and the MMAs that last read this TMEM slot (one
+    // ring lap earlier, in the same code stage) have completed, copy this
+    // warp's lane quarter, arrive.  (Staging two k-blocks per pass, with
+    // one shared wait::st, measured about 1.5 % slower once the MMA issuer
+    // probed its barriers ahead.)
     const int q = warp & 3;  // TMEM lane quarter this warp may access
     int sstage = 0, slot = 0;
     uint32_t sphase = 0, tphase = 0;
@@ -888,45 +922,32 @@ __global__ void __launch_bounds__(kThreads, 1)
       int tile, kb_lo, kb_hi;
       int64_t d_off;
       unit_split(p, unit, tile, kb_lo, kb_hi, d_off);
-      for (int kb = kb_lo; kb < kb_hi; kb += 2) {
-        const int n2 = min(2, kb_hi - kb);
-        const int slot1 = slot + 1 == S ? 0 : slot + 1;
-        const uint32_t tphase1 = slot + 1 == S ? tphase ^ 1u : tphase;
-        // The scales are in the ring (one wait per scale stage), and the MMAs
-        // that last read these TMEM slots (one ring lap earlier, in the same
-        // code stages) have completed.
-        if ((kb % kSfGroup == 0 && !warp_wait(&ctl->sf_full[sstage], sphase, abort_flag, lane)) ||
-            !warp_wait(&ctl->empty[slot], tphase ^ 1u, abort_flag, lane) ||
-            (n2 == 2 && !warp_wait(&ctl->empty[slot1], tphase1 ^ 1u, abort_flag, lane))) {
+      for (int kb = kb_lo; kb < kb_hi; ++kb) {
+        const int j = kb % kSfGroup;
+        if ((j == 0 && !warp_wait(&ctl->sf_full[sstage], sphase, abort_flag, lane)) ||
+            !warp_wait(&ctl->empty[slot], tphase ^ 1u, abort_flag, lane)) {
           if (lane == 0) fail(&ctl->abort, p, 7);
           ok = false;
           break;
         }
         ptx::tc_fence_after();
         const uint8_t* st = sf_ring + sstage * kSfStageBytes;
-        const int j = kb % kSfGroup;
         stage_scales(st + j * kSfaBytes, st + kSfaGroupBytes + j * kSfaBytes, kSfaGroupBytes, tmem, slot, q, lane);
-        if (n2 == 2)
-          stage_scales(st + (j + 1) * kSfaBytes, st + kSfaGroupBytes + (j + 1) * kSfaBytes, kSfaGroupBytes, tmem,
-                       slot1, q, lane);
         ptx::tmem_st_wait();
         ptx::tc_fence_before();
         __syncwarp();
-        const bool group_done = j + n2 >= kSfGroup || kb + n2 >= kb_hi;
+        const bool group_done = j + 1 == kSfGroup || kb + 1 == kb_hi;
         if (lane == 0) {
           if (group_done) ptx::mbar_arrive(&ctl->sf_empty[sstage]);
           arrive_full(slot);
-          if (n2 == 2) arrive_full(slot1);
         }
         if (group_done && ++sstage == SS) {
           sstage = 0;
           sphase ^= 1u;
         }
-        for (int i = 0; i < n2; ++i) {
-          if (++slot == S) {
-            slot = 0;
-            tphase ^= 1u;
-          }
+        if (++slot == S) {
+          slot = 0;
+          tphase ^= 1u;
         }
       }
       // LoRA branch k-blocks need no scales: the staging warps only take

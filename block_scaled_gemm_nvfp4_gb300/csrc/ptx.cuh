@@ -275,6 +275,45 @@ __device__ __forceinline__ void tc_mma_nvf4_pair(uint32_t d_tmem, uint64_t adesc
       "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
       : "memory");
 }
+// Two block-scaled MMAs (the second accumulates) with a non-blocking test of
+// another barrier's phase issued ahead of them (mbarrier.test_wait, acquire
+// at CTA scope); the test's result is consumed only after both MMAs, so its
+// latency overlaps their issue.  Returns nonzero if the phase of that barrier
+// with parity `probe_parity` had completed.
+template <bool PAIR>
+__device__ __forceinline__ uint32_t tc_mma_nvf4_x2_probe(uint32_t d_tmem, uint64_t adesc0, uint64_t bdesc0,
+                                                         uint64_t adesc1, uint64_t bdesc1, uint32_t idesc,
+                                                         uint32_t sfa0, uint32_t sfb0, uint32_t sfa1, uint32_t sfb1,
+                                                         uint32_t accumulate0, uint32_t probe_bar,
+                                                         uint32_t probe_parity) {
+  uint32_t ready;
+  if constexpr (PAIR) {
+    asm volatile(
+        "{\n\t.reg .pred p, r;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 r, [%12], %13;\n\t"
+        "setp.ne.u32 p, %11, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::mxf4nvf4.block_scale.scale_vec::4X [%1], %2, %3, %6, [%7], [%8], p;\n\t"
+        "tcgen05.mma.cta_group::2.kind::mxf4nvf4.block_scale.scale_vec::4X [%1], %4, %5, %6, [%9], [%10], 1;\n\t"
+        "selp.u32 %0, 1, 0, r;\n\t}"
+        : "=r"(ready)
+        : "r"(d_tmem), "l"(adesc0), "l"(bdesc0), "l"(adesc1), "l"(bdesc1), "r"(idesc), "r"(sfa0), "r"(sfb0),
+          "r"(sfa1), "r"(sfb1), "r"(accumulate0), "r"(probe_bar), "r"(probe_parity)
+        : "memory");
+  } else {
+    asm volatile(
+        "{\n\t.reg .pred p, r;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 r, [%12], %13;\n\t"
+        "setp.ne.u32 p, %11, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%1], %2, %3, %6, [%7], [%8], p;\n\t"
+        "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%1], %4, %5, %6, [%9], [%10], 1;\n\t"
+        "selp.u32 %0, 1, 0, r;\n\t}"
+        : "=r"(ready)
+        : "r"(d_tmem), "l"(adesc0), "l"(bdesc0), "l"(adesc1), "l"(bdesc1), "r"(idesc), "r"(sfa0), "r"(sfb0),
+          "r"(sfa1), "r"(sfb1), "r"(accumulate0), "r"(probe_bar), "r"(probe_parity)
+        : "memory");
+  }
+  return ready;
+}
 // D (+)= A * B^T with BF16 operands from shared memory (kind::f16, both
 // operands BF16, FP32 accumulator in TMEM); K = 16 per instruction.
 __device__ __forceinline__ void tc_mma_f16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
