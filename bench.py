@@ -39,7 +39,7 @@ WORKLOAD = ("12B-hybrid MLP up-projection fprop+dgrad+wgrad, tokens 8192 (4x2048
 # one ncu capture of each of the step's three GEMM shapes, averaged like the
 # achieved rate), keyed by the SHA-256 prefix of the GEMM kernel's sources: a
 # changed kernel reports null until it is measured again.
-GEMM_TRAFFIC = {"612db1d886fd350a": 438318165, "0061b0eb53ba3ef9": 433368405}
+GEMM_TRAFFIC = {"922b23a45dcc3b46": 438476885}
 
 
 def _gemm_traffic():
@@ -214,6 +214,9 @@ def run_ours(args):
     launches_per_step = 3 * 2 + 3
 
     e2e = run_e2e(args, nv, torch, x_c, w_c, dy_c, dev, world, pg)
+    # the GEMM's own instruction issued back to back in isolation (after the
+    # timed regions): the ceiling its tensor-pipe time can approach
+    mma_tf, mma_cyc = nv.nvfp4_debug_mma_rate(0, 4096)
 
     line = {
         "metric": METRIC, "value": round(value, 3), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
@@ -225,7 +228,12 @@ def run_ours(args):
                      "traffic": _gemm_traffic(),
                      "peak_source": "%s bf16 %.1f TFLOP/s x nominal FP4/BF16 ratio %.1f" % (
                          src, peaks["bf16_tflops"], FP4_OVER_BF16),
-                     "gemm_ms": round(gemm_ms, 4)},
+                     "gemm_ms": round(gemm_ms, 4),
+                     "instruction_ceiling": {
+                         "tflops": round(mma_tf, 1), "frac": round(achieved / mma_tf, 4),
+                         "cycles_per_mma": round(mma_cyc, 2),
+                         "what": "tcgen05.mma kind::mxf4nvf4 scale_vec::4X cta_group::2 256x256x64 issued back to "
+                                 "back in isolation (bench.py --case mma)"}},
         "quantize": {"bound": "hbm", "achieved": round(quant_gbs, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
                      "frac": round(quant_gbs / peaks["hbm_gbs"], 4), "ms_per_step": round(quant_ms, 4),
                      "bytes_model": "per tensor (X, W, dY): read BF16 once + two outputs of codes and scales "
@@ -453,7 +461,9 @@ def run_case(args):
     ``gemmq:M,N,K[,nod]`` (GEMM whose epilogue also quantises D along N under
     a supplied amax; ``nod``: D itself is not stored) or
     ``qadamw:R,C,m|v|mdec|vdec`` (optimizer-state codec on an FP32 state).
-    Prints a JSON line with the mean time per call over --steps calls."""
+    Prints a JSON line with the mean time per call over --steps calls.
+    ``mma[:iters]`` instead prints the isolated tensor-core instruction rates
+    (block-scaled E2M1 and BF16, pair and single CTA)."""
     import torch
 
     import block_scaled_gemm_nvfp4_gb300 as nv
@@ -464,6 +474,16 @@ def run_case(args):
     dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
     nv.lib()
+    if kind == "mma":
+        # the isolated tensor-core instruction rate: the ceiling of the GEMM's
+        # tensor pipe (no counterpart in the pages; a roofline measurement)
+        iters = int(parts[0]) if parts[0] else 4096
+        out = {"case": args.case, "iters": iters, "unit": "TFLOP/s"}
+        for k, name in nv.MMA_RATE_KINDS.items():
+            tf, cyc = nv.nvfp4_debug_mma_rate(k, iters)
+            out[name] = {"tflops": round(tf, 1), "cycles_per_mma": round(cyc, 2)}
+        print(json.dumps(out), flush=True)
+        return
     s = nv.NVFP4_DEFAULT_RHT_SEED
     modes = {"row": nv.quant_cfg(), "col": nv.quant_cfg(transpose=1), "row16": nv.quant_cfg(block=1),
              "col16": nv.quant_cfg(block=1, transpose=1),

@@ -40,7 +40,7 @@ EXPORTS = [
     "nvfp4_qadamw_workspace_size", "nvfp4_qadamw_m_encode", "nvfp4_qadamw_m_decode", "nvfp4_qadamw_v_encode",
     "nvfp4_qadamw_v_decode", "nvfp4_lora_workspace_size", "nvfp4_lora_forward",
     "nvfp4_abs_percentile_workspace_size", "nvfp4_abs_percentile_bf16", "nvfp4_clip_bf16", "nvfp4_axpby_bf16",
-    "nvfp4_ns_workspace_size", "nvfp4_ns_step",
+    "nvfp4_ns_workspace_size", "nvfp4_ns_step", "nvfp4_debug_mma_rate",
 ]
 
 
@@ -147,6 +147,8 @@ def lib():
             "nvfp4_check_device_status": (I32, [P, P]),
             "nvfp4_debug_gemm_skip_load": (None, [I32]),
             "nvfp4_debug_quantize_skip_load": (None, [I32]),
+            "nvfp4_debug_mma_rate": (I32, [I32, I32, ctypes.POINTER(ctypes.c_double),
+                                           ctypes.POINTER(ctypes.c_double)]),
             "nvfp4_qadamw_workspace_size": (I32, [PSZ]),
             "nvfp4_qadamw_m_encode": (I32, [P, I64, I64, ctypes.c_uint64, ctypes.c_uint64, ctypes.c_uint64, P, P, P, P,
                                             SZ, P]),
@@ -410,6 +412,19 @@ def nvfp4_debug_quantize_skip_load(pass_=2):
     """Quantiser failure-detection test hook (see include/nvfp4.h): 1 = amax
     pass, 2 = encode pass, 0 = off."""
     lib().nvfp4_debug_quantize_skip_load(int(pass_))
+
+
+MMA_RATE_KINDS = {0: "nvf4 pair 256x256x64", 1: "nvf4 single 128x256x64", 2: "bf16 pair 256x256x16",
+                  3: "bf16 single 128x256x16"}
+
+
+def nvfp4_debug_mma_rate(kind, iters=4096):
+    """Isolated tensor-core instruction rate on the current device (see
+    include/nvfp4.h): returns (TFLOP/s, cycles per instruction)."""
+    tf, cyc = ctypes.c_double(), ctypes.c_double()
+    _check(lib().nvfp4_debug_mma_rate(int(kind), int(iters), ctypes.byref(tf), ctypes.byref(cyc)),
+           "nvfp4_debug_mma_rate")
+    return tf.value, cyc.value
 
 
 def nvfp4_check_device_status(workspace, stream=None):

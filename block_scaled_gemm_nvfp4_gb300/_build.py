@@ -26,6 +26,7 @@ UNITS = {
     "qadamw.cu": ["-fmad=false"],
     "lora.cu": ["-fmad=false"],
     "ns.cu": ["-fmad=false"],
+    "mma_rate.cu": [],
 }
 
 

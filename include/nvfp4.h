@@ -463,6 +463,26 @@ void nvfp4_debug_gemm_skip_load(int32_t enable);
  */
 void nvfp4_debug_quantize_skip_load(int32_t pass);
 
+/*
+ * Measurement of the tensor-core instruction the GEMM is built on, issued in
+ * isolation: one CTA per SM (kind 0, 2: a CTA pair per two SMs), one thread
+ * issuing `iters` back-to-back MMAs on fixed shared-memory operands into one
+ * TMEM accumulator, five timed launches after two untimed ones.  The pages
+ * have no counterpart: it gives the rate the GEMM's tensor-pipe time is
+ * compared with (the GEMM's roofline).
+ *   kind 0: block-scaled E2M1 (E4M3 scales per 16), cta_group::2, 256x256x64
+ *   kind 1: the same, cta_group::1, 128x256x64
+ *   kind 2: BF16 -> FP32, cta_group::2, 256x256x16
+ *   kind 3: the same, cta_group::1, 128x256x16
+ * Writes *tflops (whole GPU, CUDA events) and *cycles_per_mma (mean
+ * clock64 cycles per instruction in an issuing CTA, the final wait
+ * included).  Synchronous; allocates and frees a few bytes of device
+ * memory; uses the current device.  iters in [16, 2^20] and non-null
+ * outputs, else NVFP4_ERR_INVALID_ARG; NVFP4_ERR_CUDA if a CUDA call fails;
+ * NVFP4_ERR_TIMEOUT if the bounded wait ran out.
+ */
+nvfp4_status nvfp4_debug_mma_rate(int32_t kind, int32_t iters, double* tflops, double* cycles_per_mma);
+
 #ifdef __cplusplus
 }
 #endif

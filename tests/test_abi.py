@@ -237,3 +237,10 @@ def test_ns_validation(lib):
         nv.NVFP4_ERR_INVALID_ARG
     assert lib.nvfp4_clip_bf16(P(8192), 10, None, P(8192), P(0)) == nv.NVFP4_ERR_INVALID_ARG
     assert lib.nvfp4_axpby_bf16(P(8192), P(8200), 10, 1.0, 1.0, P(8192), P(0)) == nv.NVFP4_ERR_INVALID_ARG
+
+
+def test_mma_rate_validation(lib):
+    d = ctypes.c_double()
+    for kind, iters in ((-1, 64), (4, 64), (0, 8), (0, (1 << 20) + 1)):
+        assert lib.nvfp4_debug_mma_rate(kind, iters, ctypes.byref(d), ctypes.byref(d)) == nv.NVFP4_ERR_INVALID_ARG
+    assert lib.nvfp4_debug_mma_rate(0, 64, None, ctypes.byref(d)) == nv.NVFP4_ERR_INVALID_ARG

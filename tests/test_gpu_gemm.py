@@ -231,3 +231,11 @@ def test_split_k_vs_oracle(M, N, K, out):
             assert rel_err(g, ref) <= 1e-3
         else:
             assert bf16_within_one_ulp(g, ref)
+
+
+def test_mma_rate_measurement_runs():
+    # the roofline measurement completes cleanly and gives plausible rates
+    for kind in nv.MMA_RATE_KINDS:
+        tf, cyc = nv.nvfp4_debug_mma_rate(kind, 256)
+        assert 16.0 < cyc < 4096.0, (kind, cyc)
+        assert 50.0 < tf < 50000.0, (kind, tf)
