@@ -105,7 +105,11 @@ constexpr uint32_t kSfbCol = kSfaCol + 16 * kMaxStages;  // + stage * 32 + kk * 
 constexpr int kSfGroup = 4;                   // k-blocks per scale stage
 constexpr int kSfaGroupBytes = kSfGroup * kSfaBytes;     // 8 KB: 16 K atoms of one A row block
 constexpr int kSfStageBytes = 3 * kSfaGroupBytes;        // A + two B row blocks: 24 KB
-constexpr int kGroup = 16;                    // tile raster group (row or column blocks)
+// Operand panels a raster group keeps in L2.  Measured on GB300 (DRAM bytes
+// per launch of the MLP-up GEMMs and 16384^3): 32 MB groups leave fprop and
+// wgrad at their algorithmic operand reads and cut dgrad's from 427 to 321 MB;
+// 64 and 96 MB groups are evicted before their reuse and re-read far more.
+constexpr double kGroupL2Bytes = 32.0e6;
 // BF16 output leaves through shared memory: each epilogue warp stages a
 // 32-row x 32-column chunk (64-byte rows, 64-byte swizzle) and a TMA store
 // writes it, so global writes are whole 64-byte row segments instead of one
@@ -167,6 +171,7 @@ struct GParams {
   int vec_store;
   int tma_store;        // BF16 D leaves by TMA stores (tensor map tmap_d)
   int group_n;          // raster groups column blocks instead of row blocks
+  int group;            // row or column blocks per raster group
   int skip_first_load;  // test hook: CTA 0 never loads its first stage
   uint32_t* status;
   // quantising epilogue (QUANT kernels): D's NVFP4 codes and block scales
@@ -223,17 +228,17 @@ struct __align__(8) SmemCtl {
   int abort;
 };
 
-// Tile raster: tiles are taken in groups of kGroup row blocks (sweeping every
-// column block) or kGroup column blocks (sweeping every row block), whichever
+// Tile raster: tiles are taken in groups of p.group row blocks (sweeping every
+// column block) or p.group column blocks (sweeping every row block), whichever
 // re-reads fewer operand bytes from DRAM; inside a group the fast index runs
 // over the group so concurrent CTAs share operand panels in L2.
 __device__ __forceinline__ void tile_coords(const GParams& p, int tile, int tiles_m, int& m_blk, int& n_blk) {
   const int slow_tiles = p.group_n ? tiles_m : p.tiles_n;
   const int fast_tiles = p.group_n ? p.tiles_n : tiles_m;
-  const int per_group = kGroup * slow_tiles;
+  const int per_group = p.group * slow_tiles;
   const int group = tile / per_group;
-  const int first = group * kGroup;
-  const int g = min(fast_tiles - first, kGroup);
+  const int first = group * p.group;
+  const int g = min(fast_tiles - first, p.group);
   const int local = tile - group * per_group;
   const int fast = first + local % g;
   const int slow = local / g;
@@ -1254,13 +1259,18 @@ cudaError_t launch_gemm(const GemmArgs& a, cudaStream_t stream) {
   p.status = a.status;
   p.skip_first_load = a.skip_first_load;
   {
-    // DRAM operand traffic of the two rasters: the operand swept per group
-    // is read once per group.
+    // DRAM operand traffic of the two rasters: a group holds as many panels
+    // of its own operand (all of K for one row or column block) as fit in
+    // kGroupL2Bytes, which stay in L2 while the other operand is swept past
+    // them; the swept operand is read once per group.
     const double a_bytes = static_cast<double>(a.M) * a.K * 0.5625, b_bytes = static_cast<double>(a.N) * a.K * 0.5625;
     const int m_units = pair ? p.tiles_mp : p.tiles_m;
-    const double by_m = a_bytes + b_bytes * ((m_units + kGroup - 1) / kGroup);
-    const double by_n = b_bytes + a_bytes * ((p.tiles_n + kGroup - 1) / kGroup);
+    const int g_m = static_cast<int>(std::max(1.0, std::min<double>(m_units, kGroupL2Bytes * m_units / a_bytes)));
+    const int g_n = static_cast<int>(std::max(1.0, std::min<double>(p.tiles_n, kGroupL2Bytes * p.tiles_n / b_bytes)));
+    const double by_m = a_bytes + b_bytes * ((m_units + g_m - 1) / g_m);
+    const double by_n = b_bytes + a_bytes * ((p.tiles_n + g_n - 1) / g_n);
     p.group_n = by_n < by_m ? 1 : 0;
+    p.group = p.group_n ? g_n : g_m;
   }
   const size_t esz = a.out_f32 ? 4 : 2;
   p.vec_store = (reinterpret_cast<uintptr_t>(a.d) % 16 == 0) && ((a.ldd * esz) % 16 == 0);

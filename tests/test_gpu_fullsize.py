@@ -7,8 +7,9 @@ the 16384^3 roofline probe.
     quantisation of the whole tensors, every code and scale byte.
   * Whole 256 x 256 output tiles of the fprop, dgrad and wgrad GEMMs and of
     16384^3 -- the first and last tiles, the middle one, and tiles on both
-    sides of the persistent kernel's raster-group boundaries (groups of 16
-    units of 256 rows or columns) -- against the oracle's definition of the
+    sides of the persistent kernel's raster-group boundaries (groups of
+    256-row or 256-column units sized to keep 32 MB of operand panels, the
+    choice `_raster` repeats from the library's launcher) -- against the oracle's definition of the
     GEMM (FP64 sum of the products of its dequantised operands, the sum taken
     by a library FP64 matmul): BF16 output within one BF16 ulp at the floor
     of 1e-3 of the tile's largest value.
@@ -66,15 +67,46 @@ def test_step_quantisation_whole_tensor(step, role):
     assert_quant_equal(gpu[role], ora[role])
 
 
-def _tiles(M, N, limit=12):
+def _raster(M, N, K, budget=32.0e6):
+    """The launcher's raster choice for a pair-mode GEMM: (groups of column
+    blocks?, 256-row or 256-column units per group)."""
+    a, b = M * K * 0.5625, N * K * 0.5625
+    mu, tn = (M // 128 + 1) // 2, (N + 255) // 256
+    gm = int(max(1.0, min(mu, budget * mu / a)))
+    gn = int(max(1.0, min(tn, budget * tn / b)))
+    by_m = a + b * ((mu + gm - 1) // gm)
+    by_n = b + a * ((tn + gn - 1) // gn)
+    return (True, gn) if by_n < by_m else (False, gm)
+
+
+def _tiles(M, N, K, limit=12):
     """Top-left corners of 256 x 256 tiles to check: first, last, middle,
     then tiles on both sides of raster-group boundaries."""
     out = [(0, 0), (M - 256, N - 256), ((M // 2) // 256 * 256, (N // 2) // 256 * 256)]
-    for edge in range(16 * 256, max(M, N), 16 * 256):
-        if edge < M:
-            out += [(edge - 256, min(N - 256, 768)), (edge, min(N - 256, 1024))]
-        if edge < N:
+    by_cols, g = _raster(M, N, K)
+    for edge in range(g * 256, N if by_cols else M, g * 256):
+        if by_cols:
             out += [(min(M - 256, 512), edge - 256), (min(M - 256, 256), edge)]
+        else:
+            out += [(edge - 256, min(N - 256, 768)), (edge, min(N - 256, 1024))]
+    # the tiles on both sides of the end of the first persistent wave (76 CTA
+    # pairs on 152 SMs) and the first tile of the last wave, in the kernel's
+    # tile order: groups of g units along the grouped axis, the grouped axis
+    # fastest inside a group
+    mu, tn = M // 256, N // 256
+    slow_n, fast_n = (mu, tn) if by_cols else (tn, mu)
+    units = mu * tn
+    waves = []
+    for t in (75, 76, (units - 1) // 76 * 76):
+        if t >= units:
+            continue
+        grp, local = divmod(t, g * slow_n)
+        first = grp * g
+        gg = min(fast_n - first, g)
+        fast, slow = first + local % gg, local // gg
+        m, n = (slow, fast) if by_cols else (fast, slow)
+        waves.append((m * 256, n * 256))
+    out = out[:3] + waves + out[3:]
     seen = []
     for t in out:
         if t not in seen:
@@ -99,7 +131,7 @@ def test_step_gemm_whole_tiles(step, gemm):
     a, b, M, N, K = {"fprop": ("x", "w", T, FFN, HID), "dgrad": ("dy", "wt", T, HID, FFN),
                      "wgrad": ("dyt", "xt", FFN, HID, T)}[gemm]
     d = nv.nvfp4_gemm(gpu[a], gpu[b], out_dtype=nv.NVFP4_OUT_BF16)
-    _check_tiles(d, ora[a], ora[b], M, N, K, _tiles(M, N))
+    _check_tiles(d, ora[a], ora[b], M, N, K, _tiles(M, N, K))
 
 
 def test_square_16k_whole_tiles():
@@ -109,7 +141,7 @@ def test_square_16k_whole_tiles():
     qa = nv.nvfp4_quantize(a.to(DEV), g)
     qb = nv.nvfp4_quantize(b.to(DEV), g)
     d = nv.nvfp4_gemm(qa, qb, out_dtype=nv.NVFP4_OUT_BF16)
-    tiles = _tiles(M, N, limit=8)
+    tiles = _tiles(M, N, K, limit=8)
     rows_a = sorted({r for r, _ in tiles})
     rows_b = sorted({c for _, c in tiles})
     oc = oracle.make_cfg()
