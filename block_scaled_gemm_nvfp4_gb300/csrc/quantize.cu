@@ -16,7 +16,10 @@
 //           its tiles.  It walks the tiles in reverse order, so its first
 //           reads hit the part of x that pass 0 left in L2.
 // Under delayed scaling (a supplied amax for every output) pass 0 is not
-// launched and pass 1 takes s from that amax: one read of x.
+// launched and pass 1 takes s from that amax: one read of x.  Two outputs in
+// 16x16 blocks with round-to-nearest, one per orientation (a weight's pair),
+// hold the same codes transposed within each 16x16 tile: the transposed one
+// is copied from the other's staged tile instead of encoded (mirror_tile).
 // Out-of-range parts of a tile read as zero, so ragged tiles need no special
 // case and the padding of the tensor-core scale layout comes out as zeros.
 //
@@ -103,6 +106,7 @@ struct TileParams {
   OutParams out[kMaxQuantOutputs];
   int n_out;
   int amax_shared;  // two outputs, neither transformed: output 1 reuses output 0's amax
+  int mirror;       // -1, or the output copied from the other's staged tile (see mirror_tile)
   int num_partials;
   int skip_first_load;  // test hook: CTA 0 of this pass never loads its first tile
   uint32_t* status;
@@ -285,6 +289,31 @@ __device__ __forceinline__ void encode_tile(const uint8_t* stage, uint8_t* stg, 
   }
 }
 
+// Output Q = x^T from the staged Q = x of the same tile when both use 16x16
+// blocks and round-to-nearest under one tensor scale: element (r, c) then has
+// the same block scale and the same code in both, so position p, run j of the
+// transposed output is nibble p & 15 of run p >> 4 in the sixteen staged rows
+// 16 j .. 16 j + 15 (element k of a run sits in nibble k), and its scale
+// byte is that block's.  Rows and columns past the tensor carry what the
+// zero fill gave the row output, as an encode of them would.
+__device__ __forceinline__ void mirror_tile(const uint8_t* src, uint8_t* dst) {
+  const int p = threadIdx.x & 127, j0 = threadIdx.x >> 7;
+  const int off = 8 * (p >> 4) + ((p & 15) >> 1), sh = 4 * (p & 1);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int j = j0 + 2 * i;
+    const uint8_t* rows = src + 16 * j * kStgPitch + off;
+    uint32_t w0 = 0u, w1 = 0u;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      w0 |= ((static_cast<uint32_t>(rows[e * kStgPitch]) >> sh) & 0xFu) << (4 * e);
+      w1 |= ((static_cast<uint32_t>(rows[(e + 8) * kStgPitch]) >> sh) & 0xFu) << (4 * e);
+    }
+    *reinterpret_cast<uint2*>(dst + p * kStgPitch + 8 * j) = make_uint2(w0, w1);
+    dst[stg_sf_offset(p, j)] = src[stg_sf_offset(16 * j, p >> 4)];
+  }
+}
+
 // Staged tile -> global memory.  Thread t copies the codes of runs 4 (t & 1)
 // .. + 3 of position t >> 1; the first 64 threads copy the two scale atoms.
 // Rows of Q past qr and blocks past kb_count are not written, except that the
@@ -336,9 +365,12 @@ __device__ __forceinline__ uint32_t block_max(uint32_t v, uint32_t* red) {
   return v;
 }
 
-template <int PASS>
+// MIRROR: the encode pass with p.mirror >= 0, a separate instantiation so
+// the other encodes carry none of its code.
+template <int PASS, bool MIRROR = false>
 __global__ void __launch_bounds__(kThreads, 2) quant_tiles(const __grid_constant__ CUtensorMap xmap,
                                                            const TileParams p) {
+  const int mirror = MIRROR ? p.mirror : -1;
   extern __shared__ uint8_t smem_raw[];
   constexpr int kStages = stages_of<PASS>();
   __shared__ __align__(8) uint64_t full[kStages];
@@ -465,7 +497,7 @@ __global__ void __launch_bounds__(kThreads, 2) quant_tiles(const __grid_constant
         // without the transform the orientation does not change the amax
         tmax[o] = max(tmax[o], (op.rht && op.col) ? amax_tile<true>(stage, true, op.rht_sgn)
                                                    : amax_tile<false>(stage, op.rht != 0, op.rht_sgn));
-      } else if (live[o]) {
+      } else if (live[o] && o != mirror) {
         uint8_t* so = stg + o * kStgBytes;
         if (op.col) {
           if (op.sr)
@@ -479,6 +511,10 @@ __global__ void __launch_bounds__(kThreads, 2) quant_tiles(const __grid_constant
             encode_tile<false, false>(stage, so, op, s_dec[o], rs[o], dtab[o], tr, tc, p.status);
         }
       }
+    }
+    if (PASS == 1 && MIRROR && mirror >= 0 && live[mirror]) {
+      __syncthreads();  // the other output's tile is staged
+      mirror_tile(stg + (1 - mirror) * kStgBytes, stg + mirror * kStgBytes);
     }
     // Every thread is done with this stage and, in pass 1, with its staged
     // results.  The staging buffers alternate between tiles, so the copy-out
@@ -522,6 +558,10 @@ int tiles_per_sm(cudaError_t* err) {
   if (per_sm[dev] == 0) {
     *err = cudaFuncSetAttribute(quant_tiles<PASS>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes<PASS>());
     if (*err != cudaSuccess) return 0;
+    if (PASS == 1) {
+      *err = cudaFuncSetAttribute(quant_tiles<1, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes<1>());
+      if (*err != cudaSuccess) return 0;
+    }
     int b = 0;
     *err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, quant_tiles<PASS>, kThreads, smem_bytes<PASS>());
     if (*err != cudaSuccess) return 0;
@@ -668,6 +708,13 @@ cudaError_t launch_quantize(const QuantArgs& a, cudaStream_t stream) {
     op.vec16 = (reinterpret_cast<uintptr_t>(q.codes) % 16 == 0) && (op.code_ld % 16 == 0);
   }
   p.amax_shared = a.n_out == 2 && !a.out[0].rht && !a.out[1].rht && !a.out[0].amax_in && !a.out[1].amax_in;
+  // Two 16x16-block round-to-nearest outputs of opposite orientations under
+  // one tensor scale: the transposed one is copied from the other's staged
+  // tile (mirror_tile) instead of encoded again.
+  p.mirror = -1;
+  if (p.amax_shared && a.out[0].block2d && a.out[1].block2d && !a.out[0].sr && !a.out[1].sr &&
+      a.out[0].transpose != a.out[1].transpose)
+    p.mirror = a.out[0].transpose ? 0 : 1;
   bool scan = false;  // the amax pass runs unless every output has a supplied amax
   for (int o = 0; o < a.n_out; ++o) scan = scan || !a.out[o].amax_in;
 
@@ -690,7 +737,10 @@ cudaError_t launch_quantize(const QuantArgs& a, cudaStream_t stream) {
     if (err != cudaSuccess) return err;
   }
   p.skip_first_load = a.skip_load_pass == 2;
-  quant_tiles<1><<<static_cast<int>(g), kThreads, smem_bytes<1>(), stream>>>(xmap, p);
+  if (p.mirror >= 0)
+    quant_tiles<1, true><<<static_cast<int>(g), kThreads, smem_bytes<1>(), stream>>>(xmap, p);
+  else
+    quant_tiles<1><<<static_cast<int>(g), kThreads, smem_bytes<1>(), stream>>>(xmap, p);
   return cudaGetLastError();
 }
 

@@ -21,6 +21,10 @@ S = nv.NVFP4_DEFAULT_RHT_SEED
 PAIRS = {
     "act-row-rne+col-sr-rht": (dict(), dict(transpose=1, rounding=1, rht=1, rht_seed=S, sr_seed=5)),
     "weight-16x16-both": (dict(block=1), dict(block=1, transpose=1)),
+    # the transposed output listed first, and mixed scale layouts: the kernel
+    # copies the transposed codes from the row output's tile either way
+    "weight-16x16-col-first": (dict(block=1, transpose=1), dict(block=1)),
+    "weight-16x16-mixed-sf": (dict(block=1, sf_layout=nv.NVFP4_SF_ROWMAJOR), dict(block=1, transpose=1)),
     "row-rne+col-rne": (dict(), dict(transpose=1)),
     "row-sr-rht+col-sr-rht": (dict(rounding=1, rht=1, sr_seed=9), dict(transpose=1, rounding=1, rht=1, sr_seed=10)),
     "col-16x16-sr+row-rht": (dict(block=1, transpose=1, rounding=1), dict(rht=1)),
