@@ -107,6 +107,7 @@ struct TileParams {
   int n_out;
   int amax_shared;  // two outputs, neither transformed: output 1 reuses output 0's amax
   int mirror;       // -1, or the output copied from the other's staged tile (see mirror_tile)
+  int amax_pair;    // -1, or the transformed column output whose sweep also gives the other's amax
   int num_partials;
   int skip_first_load;  // test hook: CTA 0 of this pass never loads its first tile
   uint32_t* status;
@@ -248,6 +249,23 @@ __device__ __forceinline__ uint32_t amax_tile(const uint8_t* stage, bool rht, co
   return m;
 }
 
+// Both amaxes of a pair whose output `rht` is transformed down the columns
+// and whose other output is not transformed, from one sweep: the column runs
+// are loaded with the transform's signs folded in, which leaves |x| as it is,
+// so their maximum before the transform is the untransformed amax.
+__device__ __forceinline__ void amax_tile_pair(const uint8_t* stage, const uint32_t* sgn, uint32_t& m_raw,
+                                               uint32_t& m_rht) {
+  const int p = threadIdx.x & 127, j0 = threadIdx.x >> 7;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    float v[16];
+    load_run<true, true>(stage, p, j0 + 2 * i, v, sgn);
+    m_raw = max(m_raw, run_absmax_bits(v));
+    hadamard16(v);
+    m_rht = max(m_rht, run_absmax_bits(v));
+  }
+}
+
 // ------------------------------------------------------------ encode pass
 __device__ __forceinline__ int stg_sf_offset(int p, int j) {
   return kStgCodes + (j >> 2) * 512 + (p & 31) * 16 + (p >> 5) * 4 + (j & 3);
@@ -365,12 +383,15 @@ __device__ __forceinline__ uint32_t block_max(uint32_t v, uint32_t* red) {
   return v;
 }
 
-// MIRROR: the encode pass with p.mirror >= 0, a separate instantiation so
-// the other encodes carry none of its code.
-template <int PASS, bool MIRROR = false>
+// PAIRED: two outputs that share work -- pass 0 takes both amaxes from one
+// sweep (p.amax_pair), pass 1 copies the transposed output from the other's
+// staged tile (p.mirror).  Separate instantiations, so the other calls carry
+// none of that code.
+template <int PASS, bool PAIRED = false>
 __global__ void __launch_bounds__(kThreads, 2) quant_tiles(const __grid_constant__ CUtensorMap xmap,
                                                            const TileParams p) {
-  const int mirror = MIRROR ? p.mirror : -1;
+  const int mirror = PASS == 1 && PAIRED ? p.mirror : -1;
+  const int amax_pair = PASS == 0 && PAIRED ? p.amax_pair : -1;
   extern __shared__ uint8_t smem_raw[];
   constexpr int kStages = stages_of<PASS>();
   __shared__ __align__(8) uint64_t full[kStages];
@@ -487,11 +508,14 @@ __global__ void __launch_bounds__(kThreads, 2) quant_tiles(const __grid_constant
     const int64_t tile = tile_of(i);
     const int64_t tr = tile / p.tiles_c, tc = tile - tr * p.tiles_c;
     uint8_t* stg = ring + kStgOffset + static_cast<int>(i & 1) * (kMaxQuantOutputs * kStgBytes);
+    if (amax_pair == 1) amax_tile_pair(stage, p.out[1].rht_sgn, tmax[0], tmax[1]);
+    if (amax_pair == 0) amax_tile_pair(stage, p.out[0].rht_sgn, tmax[1], tmax[0]);
 #pragma unroll
     for (int o = 0; o < kMaxQuantOutputs; ++o) {
       if (o >= p.n_out) break;
       const OutParams& op = p.out[o];
       if (PASS == 0) {
+        if (amax_pair >= 0) break;
         if (o == 1 && p.amax_shared) break;
         if (op.amax_in) continue;
         // without the transform the orientation does not change the amax
@@ -512,7 +536,7 @@ __global__ void __launch_bounds__(kThreads, 2) quant_tiles(const __grid_constant
         }
       }
     }
-    if (PASS == 1 && MIRROR && mirror >= 0 && live[mirror]) {
+    if (mirror >= 0 && live[mirror]) {
       __syncthreads();  // the other output's tile is staged
       mirror_tile(stg + (1 - mirror) * kStgBytes, stg + mirror * kStgBytes);
     }
@@ -558,10 +582,9 @@ int tiles_per_sm(cudaError_t* err) {
   if (per_sm[dev] == 0) {
     *err = cudaFuncSetAttribute(quant_tiles<PASS>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes<PASS>());
     if (*err != cudaSuccess) return 0;
-    if (PASS == 1) {
-      *err = cudaFuncSetAttribute(quant_tiles<1, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes<1>());
-      if (*err != cudaSuccess) return 0;
-    }
+    *err = cudaFuncSetAttribute(quant_tiles<PASS, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                smem_bytes<PASS>());
+    if (*err != cudaSuccess) return 0;
     int b = 0;
     *err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, quant_tiles<PASS>, kThreads, smem_bytes<PASS>());
     if (*err != cudaSuccess) return 0;
@@ -715,6 +738,13 @@ cudaError_t launch_quantize(const QuantArgs& a, cudaStream_t stream) {
   if (p.amax_shared && a.out[0].block2d && a.out[1].block2d && !a.out[0].sr && !a.out[1].sr &&
       a.out[0].transpose != a.out[1].transpose)
     p.mirror = a.out[0].transpose ? 0 : 1;
+  // One transformed column output and one untransformed output, both
+  // scanned: one sweep gives both amaxes (amax_tile_pair).
+  p.amax_pair = -1;
+  if (a.n_out == 2 && !a.out[0].amax_in && !a.out[1].amax_in) {
+    for (int t = 0; t < 2; ++t)
+      if (a.out[t].rht && a.out[t].transpose && !a.out[1 - t].rht) p.amax_pair = t;
+  }
   bool scan = false;  // the amax pass runs unless every output has a supplied amax
   for (int o = 0; o < a.n_out; ++o) scan = scan || !a.out[o].amax_in;
 
@@ -732,7 +762,10 @@ cudaError_t launch_quantize(const QuantArgs& a, cudaStream_t stream) {
   p.num_partials = static_cast<int>(g);
   if (scan) {
     p.skip_first_load = a.skip_load_pass == 1;
-    quant_tiles<0><<<static_cast<int>(g), kThreads, smem_bytes<0>(), stream>>>(xmap, p);
+    if (p.amax_pair >= 0)
+      quant_tiles<0, true><<<static_cast<int>(g), kThreads, smem_bytes<0>(), stream>>>(xmap, p);
+    else
+      quant_tiles<0><<<static_cast<int>(g), kThreads, smem_bytes<0>(), stream>>>(xmap, p);
     err = cudaGetLastError();
     if (err != cudaSuccess) return err;
   }
