@@ -309,7 +309,7 @@ struct QuantHalf {
 // Encode chunk c (columns col0 + 32 c .. + 31: two runs).  N % 32 == 0, so
 // the chunk is either wholly inside N or wholly outside.
 __device__ __forceinline__ void quantize_chunk(const GParams& p, const uint32_t (&packed)[kEpiCols / 2], int c,
-                                               bool row_ok, int64_t kb0, float s_dec, QuantHalf& qh) {
+                                               bool row_ok, int64_t kb0, float s_dec, float rs, QuantHalf& qh) {
   const bool in = row_ok && kb0 + 2 * c < p.q_kb_count;
 #pragma unroll
   for (int h = 0; h < 2; ++h) {
@@ -322,7 +322,7 @@ __device__ __forceinline__ void quantize_chunk(const GParams& p, const uint32_t 
       v[2 * j + 1] = __uint_as_float(w & 0xFFFF0000u);
     }
     const uint32_t m = run_absmax_nan(v);
-    const uint32_t sfb = in ? block_scale_byte(m, s_dec) : 0u;
+    const uint32_t sfb = in ? block_scale_byte_rcp(m, s_dec, rs) : 0u;
     if (in) qh.amax_bits = max(qh.amax_bits, m);
     qh.codes[2 * r] = 0u;
     qh.codes[2 * r + 1] = 0u;
@@ -385,7 +385,7 @@ __device__ __forceinline__ void epilogue_half(const GParams& p, const CUtensorMa
                                               uint8_t* stg,
                                               uint64_t* acc_empty, uint32_t tmem, int m_blk,
                                               int n_blk, int q, int half, int lane, float alpha, uint32_t rank,
-                                              float s_dec, uint32_t& amax_bits, int64_t d_off) {
+                                              float s_dec, float rs, uint32_t& amax_bits, int64_t d_off) {
   const int64_t row = static_cast<int64_t>(m_blk) * BM + q * 32 + lane;
   const int64_t col0 = static_cast<int64_t>(n_blk) * BN + half * kEpiCols;
   const uint32_t taddr = tmem + (static_cast<uint32_t>(q * 32) << 16) + kAccCol + half * kEpiCols;
@@ -438,7 +438,7 @@ __device__ __forceinline__ void epilogue_half(const GParams& p, const CUtensorMa
       for (int c = 0; c < kEpiCols / kEpiChunkCols; ++c) {
         const int64_t col = col0 + c * kEpiChunkCols;
         if (row0 >= p.M || col >= p.N) {  // warp-uniform
-          if constexpr (QUANT) quantize_chunk(p, packed, c, row < p.M, col0 / 16, s_dec, qh);
+          if constexpr (QUANT) quantize_chunk(p, packed, c, row < p.M, col0 / 16, s_dec, rs, qh);
           continue;
         }
         if (lane == 0) ptx::bulk_wait_group_read0();
@@ -456,7 +456,7 @@ __device__ __forceinline__ void epilogue_half(const GParams& p, const CUtensorMa
           ptx::bulk_commit_group();
         }
         // encode this chunk while the store reads the buffer
-        if constexpr (QUANT) quantize_chunk(p, packed, c, row < p.M, col0 / 16, s_dec, qh);
+        if constexpr (QUANT) quantize_chunk(p, packed, c, row < p.M, col0 / 16, s_dec, rs, qh);
       }
     } else if (row < p.M && p.d != nullptr) {  // D is optional for the quantising epilogue
       __nv_bfloat16* drow = static_cast<__nv_bfloat16*>(p.d) + row * p.ldd;
@@ -481,7 +481,7 @@ __device__ __forceinline__ void epilogue_half(const GParams& p, const CUtensorMa
     if constexpr (QUANT) {
       if (!p.tma_store) {
 #pragma unroll
-        for (int c = 0; c < kEpiCols / kEpiChunkCols; ++c) quantize_chunk(p, packed, c, row < p.M, col0 / 16, s_dec, qh);
+        for (int c = 0; c < kEpiCols / kEpiChunkCols; ++c) quantize_chunk(p, packed, c, row < p.M, col0 / 16, s_dec, rs, qh);
       }
       store_quantised(p, tmap_q, stg, qh, row, static_cast<int64_t>(m_blk) * BM + q * 32, col0, q, lane);
       amax_bits = max(amax_bits, qh.amax_bits);
@@ -981,6 +981,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // zero); a negative or non-finite amax_in is reported and nothing is
     // encoded
     float s_dec = 1.0f;
+    float rs = 0.0f;  // RN(1/s_dec) where the residual-corrected block-scale division applies
     bool q_live = true;
     uint32_t amax_bits = 0;
     if (QUANT) {
@@ -995,6 +996,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       } else {
         s_dec = __fdiv_rn(fabsf(a_in), 2688.0f);
         if (s_dec == 0.0f) s_dec = 1.0f;
+        rs = (s_dec >= 0x1p-70f && s_dec < 0x1p126f) ? __frcp_rn(s_dec) : 0.0f;
         if (first) *p.q_tensor_scale = s_dec;
       }
     }
@@ -1012,13 +1014,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       if constexpr (QUANT) {
         if (q_live)
           epilogue_half<OUT_F32, PAIR, true>(p, &tmap_d, &tmap_q, stg, &ctl->acc_empty, tmem, m_blk, n_blk, q, half, lane, alpha, rank,
-                                             s_dec, amax_bits, d_off);
+                                             s_dec, rs, amax_bits, d_off);
         else
           epilogue_half<OUT_F32, PAIR, false>(p, &tmap_d, &tmap_q, stg, &ctl->acc_empty, tmem, m_blk, n_blk, q, half, lane, alpha, rank,
-                                              s_dec, amax_bits, d_off);
+                                              s_dec, rs, amax_bits, d_off);
       } else {
         epilogue_half<OUT_F32, PAIR, false>(p, &tmap_d, &tmap_q, stg, &ctl->acc_empty, tmem, m_blk, n_blk, q, half, lane, alpha, rank,
-                                            s_dec, amax_bits, d_off);
+                                            s_dec, rs, amax_bits, d_off);
       }
       acc_phase ^= 1u;
     }
