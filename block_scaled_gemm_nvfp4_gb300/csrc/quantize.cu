@@ -16,7 +16,9 @@
 //           its tiles.  It walks the tiles in reverse order, so its first
 //           reads hit the part of x that pass 0 left in L2.
 // Under delayed scaling (a supplied amax for every output) pass 0 is not
-// launched and pass 1 takes s from that amax: one read of x.  Two outputs in
+// launched and pass 1 takes s from that amax: one read of x.  A single
+// untransformed row output in 1x16 blocks with round-to-nearest needs no tile
+// at all: its encode pass is the streaming kernel quant_rows_rne.  Two outputs in
 // 16x16 blocks with round-to-nearest, one per orientation (a weight's pair),
 // hold the same codes transposed within each 16x16 tile: the transposed one
 // is copied from the other's staged tile instead of encoded (mirror_tile).
@@ -383,6 +385,93 @@ __device__ __forceinline__ uint32_t block_max(uint32_t v, uint32_t* red) {
   return v;
 }
 
+// Encode pass for one untransformed row output in 1x16 blocks with
+// round-to-nearest.  Its runs share nothing across rows, so no tile is
+// staged: each thread streams whole runs of 16 straight from global memory
+// (two 16-byte loads) and stores their codes and scale bytes directly, with
+// the whole grid -- as many CTAs as are resident at once -- walking the runs
+// backwards (the amax pass leaves the end of x in L2).  (Two runs per
+// iteration, or a grid of eight CTAs per SM, measured slower.)  The walk covers the tensor-core scale layout's padding rows and
+// blocks too, which receive zero scale bytes.  Same arithmetic, tensor scale
+// and error reporting as the tiled encode pass.
+__global__ void __launch_bounds__(kThreads) quant_rows_rne(const uint16_t* __restrict__ x, int64_t ldx,
+                                                          const TileParams p) {
+  __shared__ uint32_t red[kThreads / 32];
+  __shared__ DivTable dtab;
+  const OutParams& o = p.out[0];
+  const int tid = threadIdx.x;
+  uint32_t m = 0;
+  if (o.amax_in) {
+    const float a = *o.amax_in;
+    m = (a >= 0.0f) ? __float_as_uint(fabsf(a)) : 0x7FC00000u;
+  } else {
+    for (int i = tid; i < p.num_partials; i += kThreads) m = max(m, o.partials[i]);
+    m = block_max(m, red);
+  }
+  if (m >= 0x7F800000u) {  // inf or NaN in the input (or a bad supplied amax)
+    if (blockIdx.x == 0 && tid == 0) {
+      ptx::set_status(p.status, kDevNonFinite);
+      *o.tensor_scale = __uint_as_float(0x7FC00000u);
+    }
+    return;
+  }
+  float s = __fdiv_rn(__uint_as_float(m), 2688.0f);
+  if (s == 0.0f) s = 1.0f;
+  const float rs = (s >= 0x1p-70f && s < 0x1p126f) ? __frcp_rn(s) : 0.0f;
+  if (blockIdx.x == 0 && tid == 0) *o.tensor_scale = s;
+  if (tid >= 1 && tid < 127) {
+    const float d = __fmul_rn(ptx::e4m3_to_float(static_cast<uint32_t>(tid)), s);
+    dtab.e[tid] = make_float2(d, (d >= 0x1p-70f && d < 0x1p126f) ? __frcp_rn(d) : 0.0f);
+  }
+  __syncthreads();
+  const int64_t rows_pad = o.sf_mma ? (o.qr + 127) / 128 * 128 : o.qr;
+  const int64_t kb_pad = o.sf_mma ? o.katoms * 4 : o.kb_count;
+  const int64_t total = rows_pad * kb_pad;
+  if (total == 0) return;
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * kThreads;
+  // Runs are counted from the end: run i sits at r = total - 1 - i, row r /
+  // kb_pad, block r % kb_pad.  One division per thread; each step back by the
+  // grid's stride then subtracts (stride / kb_pad, stride % kb_pad) with a
+  // borrow.
+  const int64_t step_rows = stride / kb_pad, step_kb = stride - step_rows * kb_pad;
+  const int64_t i0 = static_cast<int64_t>(blockIdx.x) * kThreads + tid;
+  int64_t row = (total - 1 - i0) / kb_pad;
+  int64_t kb = (total - 1 - i0) - row * kb_pad;
+  auto finish = [&](int64_t qrow, int64_t qkb, bool in, const uint4& lo, const uint4& hi) {
+    uint32_t sfb = 0u;
+    if (in) {
+      float v[16];
+      unpack8(lo, v);
+      unpack8(hi, v + 8);
+      const uint32_t bm = run_absmax_nan(v);
+      if (bm >= 0x7F800000u) ptx::set_status(p.status, kDevNonFinite);  // codes unspecified
+      const uint2 c = encode_run<false>(v, bm, s, rs, dtab, 0, o, sfb);
+      *reinterpret_cast<uint2*>(o.codes + qrow * o.code_ld + qkb * 8) = c;
+    }
+    if (o.sf_mma)
+      o.sf[((qrow >> 7) * o.katoms + (qkb >> 2)) * 512 + (qrow & 31) * 16 + ((qrow >> 5) & 3) * 4 + (qkb & 3)] =
+          static_cast<uint8_t>(sfb);
+    else if (in)
+      o.sf[qrow * o.kb_count + qkb] = static_cast<uint8_t>(sfb);
+  };
+  for (int64_t i = i0; i < total; i += stride) {
+    const bool in = row < o.qr && kb < o.kb_count;
+    uint4 a = make_uint4(0u, 0u, 0u, 0u), b = a;
+    if (in) {
+      const uint4* src = reinterpret_cast<const uint4*>(x + row * ldx + kb * 16);
+      a = __ldcs(src);
+      b = __ldcs(src + 1);
+    }
+    finish(row, kb, in, a, b);
+    row -= step_rows;
+    kb -= step_kb;
+    if (kb < 0) {
+      kb += kb_pad;
+      --row;
+    }
+  }
+}
+
 // PAIRED: two outputs that share work -- pass 0 takes both amaxes from one
 // sweep (p.amax_pair), pass 1 copies the transposed output from the other's
 // staged tile (p.mirror).  Separate instantiations, so the other calls carry
@@ -593,6 +682,28 @@ int tiles_per_sm(cudaError_t* err) {
   return per_sm[dev];
 }
 
+// Resident CTAs per SM of the streaming row encode (its grid), set up once
+// per device like tiles_per_sm.
+int rows_per_sm(cudaError_t* err) {
+  static std::mutex setup_mutex;
+  static int per_sm[64] = {0};
+  int dev = 0;
+  *err = cudaGetDevice(&dev);
+  if (*err != cudaSuccess) return 0;
+  if (dev < 0 || dev >= 64) {
+    *err = cudaErrorInvalidDevice;
+    return 0;
+  }
+  std::lock_guard<std::mutex> lock(setup_mutex);
+  if (per_sm[dev] == 0) {
+    int b = 0;
+    *err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, quant_rows_rne, kThreads, 0);
+    if (*err != cudaSuccess) return 0;
+    per_sm[dev] = std::max(b, 1);
+  }
+  return per_sm[dev];
+}
+
 // Tensor map over x [rows, cols] BF16: box 64 columns x 128 rows, 128-byte
 // swizzle, out-of-range elements read as zero.
 bool make_x_map(CUtensorMap* map, const uint16_t* x, int64_t rows, int64_t cols, int64_t ldx) {
@@ -770,6 +881,16 @@ cudaError_t launch_quantize(const QuantArgs& a, cudaStream_t stream) {
     if (err != cudaSuccess) return err;
   }
   p.skip_first_load = a.skip_load_pass == 2;
+  const QuantOut& q0 = a.out[0];
+  if (a.n_out == 1 && !q0.transpose && !q0.block2d && !q0.sr && !q0.rht && a.skip_load_pass != 2) {
+    // one untransformed 1x16 round-to-nearest row output: the streaming
+    // encode (the failure-detection hook of the encode pass stays on the
+    // tiled kernel, which has a tile to leave unfilled)
+    const int per_sm = rows_per_sm(&err);
+    if (err != cudaSuccess) return err;
+    quant_rows_rne<<<per_sm * device_sm_count(), kThreads, 0, stream>>>(a.x, a.ldx, p);
+    return cudaGetLastError();
+  }
   if (p.mirror >= 0)
     quant_tiles<1, true><<<static_cast<int>(g), kThreads, smem_bytes<1>(), stream>>>(xmap, p);
   else
