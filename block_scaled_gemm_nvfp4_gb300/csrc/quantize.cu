@@ -16,9 +16,10 @@
 //           its tiles.  It walks the tiles in reverse order, so its first
 //           reads hit the part of x that pass 0 left in L2.
 // Under delayed scaling (a supplied amax for every output) pass 0 is not
-// launched and pass 1 takes s from that amax: one read of x.  A single
-// untransformed row output in 1x16 blocks with round-to-nearest needs no tile
-// at all: its encode pass is the streaming kernel quant_rows_rne.  Two outputs in
+// launched and pass 1 takes s from that amax: one read of x.  A single row
+// output needs no tile at all: its encode pass is the streaming kernel
+// quant_rows (except 16x16 blocks with round-to-nearest and no transform,
+// which the staged tile serves faster).  Two outputs in
 // 16x16 blocks with round-to-nearest, one per orientation (a weight's pair),
 // hold the same codes transposed within each 16x16 tile: the transposed one
 // is copied from the other's staged tile instead of encoded (mirror_tile).
@@ -385,17 +386,21 @@ __device__ __forceinline__ uint32_t block_max(uint32_t v, uint32_t* red) {
   return v;
 }
 
-// Encode pass for one untransformed row output in 1x16 blocks with
-// round-to-nearest.  Its runs share nothing across rows, so no tile is
-// staged: each thread streams whole runs of 16 straight from global memory
-// (two 16-byte loads) and stores their codes and scale bytes directly, with
-// the whole grid -- as many CTAs as are resident at once -- walking the runs
-// backwards (the amax pass leaves the end of x in L2).  (Two runs per
-// iteration, or a grid of eight CTAs per SM, measured slower.)  The walk covers the tensor-core scale layout's padding rows and
-// blocks too, which receive zero scale bytes.  Same arithmetic, tensor scale
-// and error reporting as the tiled encode pass.
-__global__ void __launch_bounds__(kThreads) quant_rows_rne(const uint16_t* __restrict__ x, int64_t ldx,
-                                                          const TileParams p) {
+// Encode pass for a single row output (Q = x).  Its runs share nothing
+// across rows except the maximum of a 16x16 block, so no tile is staged:
+// each thread streams whole runs of 16 straight from global memory (two
+// 16-byte loads, the transform's signs folded in as the tiled loader does)
+// and stores their codes and scale bytes directly, with the whole grid -- as
+// many CTAs as are resident at once -- walking the runs backwards (the amax
+// pass leaves the end of x in L2).  With 16x16 blocks the 16 lanes of a
+// half-warp take the 16 rows of one block and share its maximum by shuffles.
+// The walk covers the tensor-core scale layout's padding rows and blocks
+// too, which receive zero scale bytes.  Same arithmetic, tensor scale and
+// error reporting as the tiled encode pass.  (Two runs per iteration, or a
+// grid of eight CTAs per SM, measured slower.)
+template <bool SR, bool RHT, bool BLOCK2D>
+__global__ void __launch_bounds__(kThreads) quant_rows(const uint16_t* __restrict__ x, int64_t ldx,
+                                                      const TileParams p) {
   __shared__ uint32_t red[kThreads / 32];
   __shared__ DivTable dtab;
   const OutParams& o = p.out[0];
@@ -421,53 +426,62 @@ __global__ void __launch_bounds__(kThreads) quant_rows_rne(const uint16_t* __res
   if (blockIdx.x == 0 && tid == 0) *o.tensor_scale = s;
   if (tid >= 1 && tid < 127) {
     const float d = __fmul_rn(ptx::e4m3_to_float(static_cast<uint32_t>(tid)), s);
-    dtab.e[tid] = make_float2(d, (d >= 0x1p-70f && d < 0x1p126f) ? __frcp_rn(d) : 0.0f);
+    const bool fast = d >= 0x1p-70f && d < (SR ? 0x1p14f : 0x1p126f);
+    dtab.e[tid] = make_float2(d, fast ? __frcp_rn(d) : 0.0f);
   }
   __syncthreads();
+  // Work items: runs (1x16), or 16-row groups of runs (16x16, the group's row
+  // the thread's lane & 15, constant because the stride is a multiple of 16).
+  constexpr int G = BLOCK2D ? 16 : 1;
   const int64_t rows_pad = o.sf_mma ? (o.qr + 127) / 128 * 128 : o.qr;
   const int64_t kb_pad = o.sf_mma ? o.katoms * 4 : o.kb_count;
-  const int64_t total = rows_pad * kb_pad;
+  const int64_t total = rows_pad / G * kb_pad;
   if (total == 0) return;
-  const int64_t stride = static_cast<int64_t>(gridDim.x) * kThreads;
-  // Runs are counted from the end: run i sits at r = total - 1 - i, row r /
-  // kb_pad, block r % kb_pad.  One division per thread; each step back by the
-  // grid's stride then subtracts (stride / kb_pad, stride % kb_pad) with a
-  // borrow.
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * (kThreads / G);
+  const int rr = BLOCK2D ? (tid & 15) : 0;
+  // Items are counted from the end: item i sits at r = total - 1 - i, row
+  // group r / kb_pad, block r % kb_pad.  One division per thread; each step
+  // back by the grid's stride then subtracts (stride / kb_pad, stride %
+  // kb_pad) with a borrow.
   const int64_t step_rows = stride / kb_pad, step_kb = stride - step_rows * kb_pad;
-  const int64_t i0 = static_cast<int64_t>(blockIdx.x) * kThreads + tid;
-  int64_t row = (total - 1 - i0) / kb_pad;
-  int64_t kb = (total - 1 - i0) - row * kb_pad;
-  auto finish = [&](int64_t qrow, int64_t qkb, bool in, const uint4& lo, const uint4& hi) {
+  const int64_t i0 = static_cast<int64_t>(blockIdx.x) * (kThreads / G) + tid / G;
+  int64_t rg = (total - 1 - i0) / kb_pad;
+  int64_t kb = (total - 1 - i0) - rg * kb_pad;
+  const unsigned group_mask = BLOCK2D ? (0xFFFFu << (tid & 16)) : 0xFFFFFFFFu;
+  for (int64_t i = i0; i < total; i += stride) {
+    const int64_t row = rg * G + rr;
+    const bool in = row < o.qr && kb < o.kb_count;  // uniform over a 16x16 block's lanes
     uint32_t sfb = 0u;
     if (in) {
+      const uint4* src = reinterpret_cast<const uint4*>(x + row * ldx + kb * 16);
       float v[16];
-      unpack8(lo, v);
-      unpack8(hi, v + 8);
-      const uint32_t bm = run_absmax_nan(v);
+      unpack8(__ldcs(src), v);
+      unpack8(__ldcs(src + 1), v + 8);
+      if (RHT) {
+#pragma unroll
+        for (int j = 0; j < 16; ++j) v[j] = __uint_as_float(__float_as_uint(v[j]) ^ o.rht_sgn[j]);
+        hadamard16(v);
+      }
+      uint32_t bm = run_absmax_nan(v);
+      if (BLOCK2D) {
+#pragma unroll
+        for (int sh = 1; sh < 16; sh <<= 1) bm = max(bm, __shfl_xor_sync(group_mask, bm, sh));
+      }
       if (bm >= 0x7F800000u) ptx::set_status(p.status, kDevNonFinite);  // codes unspecified
-      const uint2 c = encode_run<false>(v, bm, s, rs, dtab, 0, o, sfb);
-      *reinterpret_cast<uint2*>(o.codes + qrow * o.code_ld + qkb * 8) = c;
+      const uint2 c =
+          encode_run<SR>(v, bm, s, rs, dtab, static_cast<uint64_t>(row * o.qk + kb * 16), o, sfb);
+      *reinterpret_cast<uint2*>(o.codes + row * o.code_ld + kb * 8) = c;
     }
     if (o.sf_mma)
-      o.sf[((qrow >> 7) * o.katoms + (qkb >> 2)) * 512 + (qrow & 31) * 16 + ((qrow >> 5) & 3) * 4 + (qkb & 3)] =
+      o.sf[((row >> 7) * o.katoms + (kb >> 2)) * 512 + (row & 31) * 16 + ((row >> 5) & 3) * 4 + (kb & 3)] =
           static_cast<uint8_t>(sfb);
     else if (in)
-      o.sf[qrow * o.kb_count + qkb] = static_cast<uint8_t>(sfb);
-  };
-  for (int64_t i = i0; i < total; i += stride) {
-    const bool in = row < o.qr && kb < o.kb_count;
-    uint4 a = make_uint4(0u, 0u, 0u, 0u), b = a;
-    if (in) {
-      const uint4* src = reinterpret_cast<const uint4*>(x + row * ldx + kb * 16);
-      a = __ldcs(src);
-      b = __ldcs(src + 1);
-    }
-    finish(row, kb, in, a, b);
-    row -= step_rows;
+      o.sf[row * o.kb_count + kb] = static_cast<uint8_t>(sfb);
+    rg -= step_rows;
     kb -= step_kb;
     if (kb < 0) {
       kb += kb_pad;
-      --row;
+      --rg;
     }
   }
 }
@@ -682,8 +696,9 @@ int tiles_per_sm(cudaError_t* err) {
   return per_sm[dev];
 }
 
-// Resident CTAs per SM of the streaming row encode (its grid), set up once
-// per device like tiles_per_sm.
+// Resident CTAs per SM of a streaming row encode (its grid), set up once per
+// device like tiles_per_sm.
+template <bool SR, bool RHT, bool BLOCK2D>
 int rows_per_sm(cudaError_t* err) {
   static std::mutex setup_mutex;
   static int per_sm[64] = {0};
@@ -697,7 +712,7 @@ int rows_per_sm(cudaError_t* err) {
   std::lock_guard<std::mutex> lock(setup_mutex);
   if (per_sm[dev] == 0) {
     int b = 0;
-    *err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, quant_rows_rne, kThreads, 0);
+    *err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, quant_rows<SR, RHT, BLOCK2D>, kThreads, 0);
     if (*err != cudaSuccess) return 0;
     per_sm[dev] = std::max(b, 1);
   }
@@ -882,14 +897,29 @@ cudaError_t launch_quantize(const QuantArgs& a, cudaStream_t stream) {
   }
   p.skip_first_load = a.skip_load_pass == 2;
   const QuantOut& q0 = a.out[0];
-  if (a.n_out == 1 && !q0.transpose && !q0.block2d && !q0.sr && !q0.rht && a.skip_load_pass != 2) {
-    // one untransformed 1x16 round-to-nearest row output: the streaming
-    // encode (the failure-detection hook of the encode pass stays on the
-    // tiled kernel, which has a tile to leave unfilled)
-    const int per_sm = rows_per_sm(&err);
-    if (err != cudaSuccess) return err;
-    quant_rows_rne<<<per_sm * device_sm_count(), kThreads, 0, stream>>>(a.x, a.ldx, p);
-    return cudaGetLastError();
+  // One row output: the streaming encode, except 16x16 blocks with
+  // round-to-nearest and no transform, where its 16-row loads measured slower
+  // than the staged tile (the failure-detection hook of the encode pass also
+  // stays on the tiled kernel, which has a tile to leave unfilled).
+  if (a.n_out == 1 && !q0.transpose && !(q0.block2d && !q0.sr && !q0.rht) && a.skip_load_pass != 2) {
+    auto run = [&](auto kernel, int per_sm) {
+      kernel<<<per_sm * device_sm_count(), kThreads, 0, stream>>>(a.x, a.ldx, p);
+      return cudaGetLastError();
+    };
+#define NVFP4_ROWS(SR, RHT, B2D)                                            \
+  if (!!q0.sr == SR && !!q0.rht == RHT && !!q0.block2d == B2D) {             \
+    const int per_sm = rows_per_sm<SR, RHT, B2D>(&err);                      \
+    if (err != cudaSuccess) return err;                                      \
+    return run(quant_rows<SR, RHT, B2D>, per_sm);                            \
+  }
+    NVFP4_ROWS(false, false, false)
+    NVFP4_ROWS(false, true, false)
+    NVFP4_ROWS(false, true, true)
+    NVFP4_ROWS(true, false, false)
+    NVFP4_ROWS(true, false, true)
+    NVFP4_ROWS(true, true, false)
+    NVFP4_ROWS(true, true, true)
+#undef NVFP4_ROWS
   }
   if (p.mirror >= 0)
     quant_tiles<1, true><<<static_cast<int>(g), kThreads, smem_bytes<1>(), stream>>>(xmap, p);
