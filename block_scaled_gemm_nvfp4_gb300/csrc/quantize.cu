@@ -318,20 +318,33 @@ __device__ __forceinline__ void encode_tile(const uint8_t* stage, uint8_t* stg, 
 // byte is that block's.  Rows and columns past the tensor carry what the
 // zero fill gave the row output, as an encode of them would.
 __device__ __forceinline__ void mirror_tile(const uint8_t* src, uint8_t* dst) {
-  const int p = threadIdx.x & 127, j0 = threadIdx.x >> 7;
-  const int off = 8 * (p >> 4) + ((p & 15) >> 1), sh = 4 * (p & 1);
+  // Thread t: columns 4 cg .. 4 cg + 3 (cg = t & 31) of row group j = t >> 5,
+  // which are nibbles 4 (cg & 3) .. + 3 of run cg >> 2 of each source row: one
+  // 16-bit load per row gives all four (element k in nibble k, little-endian).
+  const int cg = threadIdx.x & 31, j = threadIdx.x >> 5;
+  const uint8_t* rows = src + 16 * j * kStgPitch + 8 * (cg >> 2) + 2 * (cg & 3);
+  uint32_t w[4][2] = {{0u, 0u}, {0u, 0u}, {0u, 0u}, {0u, 0u}};
+#pragma unroll
+  for (int e = 0; e < 16; ++e) {
+    const uint32_t h = *reinterpret_cast<const uint16_t*>(rows + e * kStgPitch);
+#pragma unroll
+    for (int c = 0; c < 4; ++c) w[c][e >> 3] |= ((h >> (4 * c)) & 0xFu) << (4 * (e & 7));
+  }
+  const uint32_t sf = src[stg_sf_offset(16 * j, cg >> 2)];  // the block's scale byte
+  // stores staggered by cg, so a warp's stores spread over the banks: step i
+  // writes column 4 cg + ((i + cg) & 3), its words picked by selects (a
+  // runtime index into w would put it in local memory)
+  const int r = cg & 3;
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
-    const int j = j0 + 2 * i;
-    const uint8_t* rows = src + 16 * j * kStgPitch + off;
-    uint32_t w0 = 0u, w1 = 0u;
-#pragma unroll
-    for (int e = 0; e < 8; ++e) {
-      w0 |= ((static_cast<uint32_t>(rows[e * kStgPitch]) >> sh) & 0xFu) << (4 * e);
-      w1 |= ((static_cast<uint32_t>(rows[(e + 8) * kStgPitch]) >> sh) & 0xFu) << (4 * e);
-    }
-    *reinterpret_cast<uint2*>(dst + p * kStgPitch + 8 * j) = make_uint2(w0, w1);
-    dst[stg_sf_offset(p, j)] = src[stg_sf_offset(16 * j, p >> 4)];
+    const int c = (i + r) & 3;
+    uint2 v = make_uint2(w[0][0], w[0][1]);
+    if (c == 1) v = make_uint2(w[1][0], w[1][1]);
+    if (c == 2) v = make_uint2(w[2][0], w[2][1]);
+    if (c == 3) v = make_uint2(w[3][0], w[3][1]);
+    const int p = 4 * cg + c;
+    *reinterpret_cast<uint2*>(dst + p * kStgPitch + 8 * j) = v;
+    dst[stg_sf_offset(p, j)] = static_cast<uint8_t>(sf);
   }
 }
 
