@@ -536,6 +536,53 @@ __global__ void __launch_bounds__(kThreads) amax_rows(const uint16_t* __restrict
   if (threadIdx.x == 0) o.partials[blockIdx.x] = m;
 }
 
+// Amax pass of an activation pair (amax_tile_pair's case: output t is
+// transformed down the columns, the other output is not transformed) without
+// a tile: each thread takes two adjacent columns of a 16-row group (one
+// 4-byte load per row, so a warp reads 128 contiguous bytes of each row),
+// folds the transform's signs in, and keeps the largest |x| before the
+// transform (the untransformed amax) and after it (the transformed one).
+// Each CTA writes one partial per output.  Forwards, like amax_rows.
+__global__ void __launch_bounds__(kThreads) amax_cols_pair(const uint16_t* __restrict__ x, int64_t ldx,
+                                                          int64_t rows, int64_t cols, const TileParams p) {
+  __shared__ uint32_t red[kThreads / 32];
+  const int t = p.amax_pair;
+  const uint32_t* sgn = p.out[t].rht_sgn;
+  const int64_t pairs = cols / 2;
+  const int64_t total = rows / 16 * pairs;
+  uint32_t m_raw = 0, m_rht = 0;
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * kThreads;
+  const int64_t step_grp = stride / pairs, step_cp = stride - step_grp * pairs;
+  const int64_t i0 = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x;
+  int64_t grp = i0 / pairs, cp = i0 - grp * pairs;
+  for (int64_t i = i0; i < total; i += stride) {
+    const uint32_t* src = reinterpret_cast<const uint32_t*>(x + grp * 16 * ldx + 2 * cp);
+    float a[16], b[16];
+#pragma unroll
+    for (int e = 0; e < 16; ++e) {
+      const uint32_t w = src[e * (ldx / 2)];
+      a[e] = __uint_as_float((w << 16) ^ sgn[e]);
+      b[e] = __uint_as_float((w & 0xFFFF0000u) ^ sgn[e]);
+    }
+    m_raw = max(m_raw, max(run_absmax_bits(a), run_absmax_bits(b)));
+    hadamard16(a);
+    hadamard16(b);
+    m_rht = max(m_rht, max(run_absmax_bits(a), run_absmax_bits(b)));
+    grp += step_grp;
+    cp += step_cp;
+    if (cp >= pairs) {
+      cp -= pairs;
+      ++grp;
+    }
+  }
+  m_raw = block_max(m_raw, red);
+  m_rht = block_max(m_rht, red);
+  if (threadIdx.x == 0) {
+    p.out[t].partials[blockIdx.x] = m_rht;
+    p.out[1 - t].partials[blockIdx.x] = m_raw;
+  }
+}
+
 // PAIRED: two outputs that share work -- pass 0 takes both amaxes from one
 // sweep (p.amax_pair), pass 1 copies the transposed output from the other's
 // staged tile (p.mirror).  Separate instantiations, so the other calls carry
@@ -769,7 +816,9 @@ int rows_per_sm(cudaError_t* err) {
   return per_sm[dev];
 }
 
-int amax_rows_per_sm(cudaError_t* err) {
+// Resident CTAs per SM of a streaming amax kernel, set up once per device.
+template <int KIND>  // 0: amax_rows, 1: amax_cols_pair
+int amax_stream_per_sm(cudaError_t* err) {
   static std::mutex setup_mutex;
   static int per_sm[64] = {0};
   int dev = 0;
@@ -782,7 +831,10 @@ int amax_rows_per_sm(cudaError_t* err) {
   std::lock_guard<std::mutex> lock(setup_mutex);
   if (per_sm[dev] == 0) {
     int b = 0;
-    *err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, amax_rows, kThreads, 0);
+    if (KIND == 0)
+      *err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, amax_rows, kThreads, 0);
+    else
+      *err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, amax_cols_pair, kThreads, 0);
     if (*err != cudaSuccess) return 0;
     per_sm[dev] = std::max(b, 1);
   }
@@ -964,11 +1016,21 @@ cudaError_t launch_quantize(const QuantArgs& a, cudaStream_t stream) {
   const bool rows_amax = scan && a.skip_load_pass != 1 && p.num_tiles > 0 && a.cols % 16 == 0 &&
                          ((a.n_out == 1 && !a.out[0].rht) || p.amax_shared);
   if (rows_amax) {
-    const int per_sm = amax_rows_per_sm(&err);
+    const int per_sm = amax_stream_per_sm<0>(&err);
     if (err != cudaSuccess) return err;
     const int ga = static_cast<int>(std::min<int64_t>(static_cast<int64_t>(per_sm) * device_sm_count(), kPartialsPerOutput));
     p.num_partials = ga;
     amax_rows<<<ga, kThreads, 0, stream>>>(a.x, a.ldx, p);
+    err = cudaGetLastError();
+    if (err != cudaSuccess) return err;
+  } else if (scan && p.amax_pair >= 0 && a.skip_load_pass != 1 && p.num_tiles > 0 && a.rows % 16 == 0 &&
+             a.cols % 2 == 0) {
+    // an activation pair: both amaxes streamed down the columns
+    const int per_sm = amax_stream_per_sm<1>(&err);
+    if (err != cudaSuccess) return err;
+    const int ga = static_cast<int>(std::min<int64_t>(static_cast<int64_t>(per_sm) * device_sm_count(), kPartialsPerOutput));
+    p.num_partials = ga;
+    amax_cols_pair<<<ga, kThreads, 0, stream>>>(a.x, a.ldx, a.rows, a.cols, p);
     err = cudaGetLastError();
     if (err != cudaSuccess) return err;
   } else if (scan) {
