@@ -7,9 +7,9 @@
 // rows, wgrad uses columns) and of W (fprop, dgrad), so producing both from one
 // read halves the quantiser's input traffic.
 //
-// Two kernels, both persistent loops over 128 x 128 tiles of x that TMA copies
-// into shared memory (two 64-column boxes, 128-byte swizzle; a ring of three
-// stages in the amax pass, two in the encode pass):
+// The general form is two kernels, both persistent loops over 128 x 128 tiles
+// of x that TMA copies into shared memory (two 64-column boxes, 128-byte
+// swizzle; a ring of three stages in the amax pass, two in the encode pass):
 //   pass 0: per-output tensor amax (after the optional random Hadamard
 //           transform, in the output's orientation); one partial per CTA;
 //   pass 1: every CTA reduces the partials, derives s = amax / 2688 and encodes
@@ -23,6 +23,10 @@
 // 16x16 blocks with round-to-nearest, one per orientation (a weight's pair),
 // hold the same codes transposed within each 16x16 tile: the transposed one
 // is copied from the other's staged tile instead of encoded (mirror_tile).
+// Where no tile is needed the passes stream runs of 16 straight from global
+// memory instead, as many CTAs as are resident at once: quant_rows (the
+// encode of a single row output), amax_rows (an amax of x itself) and
+// amax_cols_pair (both amaxes of an activation's pair, down the columns).
 // Out-of-range parts of a tile read as zero, so ragged tiles need no special
 // case and the padding of the tensor-core scale layout comes out as zeros.
 //
