@@ -210,8 +210,11 @@ def run_ours(args):
     quant_gbs = QUANT_STEP_BYTES / (quant_ms * 1e-3) / 1e9
     clock = clocks.summary()
 
-    # launches per step: three dual quantises (amax + encode kernels) and three GEMMs
-    launches_per_step = 3 * 2 + 3
+    # launches per step: three dual quantises (amax + encode kernels), three
+    # GEMMs, and the reduction of each GEMM whose last wave is cut along K
+    tails = sum(nv.nvfp4_gemm_plan(M, N, K, plan["ws"].numel())["tail_tiles"] > 0
+                for M, N, K in ((T, FFN, HID), (T, HID, FFN), (FFN, HID, T)))
+    launches_per_step = 3 * 2 + 3 + tails
 
     e2e = run_e2e(args, nv, torch, x_c, w_c, dy_c, dev, world, pg)
     # the GEMM's own instruction issued back to back in isolation (after the
@@ -267,8 +270,12 @@ def _step_plan(nv, torch, x, w, dy, dev):
     out = {"y": torch.empty((T, FFN), dtype=torch.bfloat16, device=dev),
            "dx": torch.empty((T, HID), dtype=torch.bfloat16, device=dev),
            "dw": torch.empty((FFN, HID), dtype=torch.bfloat16, device=dev)}
-    ws = torch.zeros(nv.nvfp4_quantize_workspace_size(T, FFN, cfg["x"]) + (1 << 16), dtype=torch.uint8,
-                     device=dev)
+    # one workspace for every call of the step: the quantisers' scratch, or
+    # the largest GEMM partial-sum scratch (the last wave's tiles cut along K)
+    ws_bytes = max(nv.nvfp4_quantize_workspace_size(T, FFN, cfg["x"]) + (1 << 16),
+                   *(nv.nvfp4_gemm_workspace_size(M, N, K) for M, N, K in ((T, FFN, HID), (T, HID, FFN),
+                                                                           (FFN, HID, T))))
+    ws = torch.zeros(ws_bytes, dtype=torch.uint8, device=dev)
     return {"cfg": cfg, "q": q, "out": out, "ws": ws, "src": {"x": x, "w": w, "dy": dy}}
 
 

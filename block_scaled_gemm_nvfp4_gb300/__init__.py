@@ -34,7 +34,7 @@ EXPORTS = [
     "nvfp4_status_string", "nvfp4_version", "nvfp4_codes_bytes", "nvfp4_sf_bytes",
     "nvfp4_quantize_workspace_size", "nvfp4_quantize", "nvfp4_quantize_dual", "nvfp4_quantize_given_amax",
     "nvfp4_quantize_noalloc", "nvfp4_dequantize",
-    "nvfp4_gemm_workspace_size", "nvfp4_gemm", "nvfp4_gemm_quantize", "nvfp4_linear_workspace_size",
+    "nvfp4_gemm_workspace_size", "nvfp4_gemm_plan", "nvfp4_gemm", "nvfp4_gemm_quantize", "nvfp4_linear_workspace_size",
     "nvfp4_linear_fprop", "nvfp4_linear_dgrad", "nvfp4_linear_wgrad",
     "nvfp4_check_device_status", "nvfp4_debug_gemm_skip_load", "nvfp4_debug_quantize_skip_load",
     "nvfp4_qadamw_workspace_size", "nvfp4_qadamw_m_encode", "nvfp4_qadamw_m_decode", "nvfp4_qadamw_v_encode",
@@ -138,6 +138,7 @@ def lib():
             "nvfp4_quantize_noalloc": (I32, [P, I64, I64, I64, PCFG, P, P, P, P]),
             "nvfp4_dequantize": (I32, [PT, I32, P, I64, P]),
             "nvfp4_gemm_workspace_size": (I32, [I64, I64, I64, PSZ]),
+            "nvfp4_gemm_plan": (I32, [I64, I64, I64, SZ, ctypes.POINTER(ctypes.c_int64)]),
             "nvfp4_gemm": (I32, [PT, PT, I32, P, I64, P, SZ, P]),
             "nvfp4_gemm_quantize": (I32, [PT, PT, P, I64, ctypes.POINTER(_QuantOut), P, SZ, P]),
             "nvfp4_linear_workspace_size": (I32, [I32, I64, I64, I64, PSZ]),
@@ -205,8 +206,11 @@ def nvfp4_sf_bytes(qr, qk, sf_layout):
 
 
 def _alloc_ws(nbytes, device):
-    # Workspaces are zero-filled once (the status word must start clear).
-    return torch.zeros(max(int(nbytes), 256), dtype=torch.uint8, device=device)
+    # The 256-byte header (the status word) must start clear; the scratch
+    # after it is always written before it is read.
+    ws = torch.empty(max(int(nbytes), 256), dtype=torch.uint8, device=device)
+    ws[:256].zero_()
+    return ws
 
 
 def nvfp4_quantize_workspace_size(rows, cols, cfg):
@@ -308,6 +312,19 @@ def nvfp4_gemm_workspace_size(M, N, K):
     n = ctypes.c_size_t(0)
     _check(lib().nvfp4_gemm_workspace_size(M, N, K, ctypes.byref(n)), "nvfp4_gemm_workspace_size")
     return n.value
+
+
+GEMM_PLAN_KEYS = ("pair", "ctas", "units", "split_k", "kb_per_split", "tail_tiles", "tail_split", "tail_kb")
+
+
+def nvfp4_gemm_plan(M, N, K, workspace_bytes=None):
+    """The schedule nvfp4_gemm uses for this shape with a workspace of that
+    many bytes (default: nvfp4_gemm_workspace_size), as a dict."""
+    if workspace_bytes is None:
+        workspace_bytes = nvfp4_gemm_workspace_size(M, N, K)
+    out = (ctypes.c_int64 * 8)()
+    _check(lib().nvfp4_gemm_plan(M, N, K, workspace_bytes, out), "nvfp4_gemm_plan")
+    return dict(zip(GEMM_PLAN_KEYS, (int(v) for v in out)))
 
 
 def nvfp4_gemm(a, b, out_dtype=NVFP4_OUT_BF16, d=None, workspace=None, stream=None):

@@ -330,8 +330,29 @@ nvfp4_status nvfp4_gemm_workspace_size(int64_t M, int64_t N, int64_t K, size_t* 
   if (!bytes || M < 0 || N < 0 || K < 0) return NVFP4_ERR_INVALID_ARG;
   if (K % 32 != 0) return NVFP4_ERR_UNSUPPORTED_SHAPE;
   *bytes = kWsHeaderBytes;
-  const int sk = gemm_split_k(M, N, K, nullptr);
-  if (sk > 1) *bytes += align_up(gemm_split_k_bytes(M, N, sk));
+  // scratch for the split the GEMM would make with unlimited workspace (none
+  // where no CUDA device can be queried: the GEMM then runs unsplit)
+  GemmPlan g;
+  if (gemm_plan(M, N, K, SIZE_MAX, &g) == cudaSuccess && g.partial_bytes_needed > 0)
+    *bytes += align_up(g.partial_bytes_needed);
+  return NVFP4_OK;
+}
+
+nvfp4_status nvfp4_gemm_plan(int64_t M, int64_t N, int64_t K, size_t workspace_bytes, int64_t* plan) {
+  if (!plan || M < 0 || N < 0 || K < 0) return NVFP4_ERR_INVALID_ARG;
+  if (K % 32 != 0) return NVFP4_ERR_UNSUPPORTED_SHAPE;
+  GemmPlan g;
+  const size_t part = workspace_bytes > kWsHeaderBytes ? workspace_bytes - kWsHeaderBytes : 0;
+  const cudaError_t e = gemm_plan(M, N, K, part, &g);
+  if (e != cudaSuccess) return cuda_status(e);
+  plan[0] = g.pair;
+  plan[1] = g.ctas;
+  plan[2] = g.units;
+  plan[3] = g.split_k;
+  plan[4] = g.kb_per_unit;
+  plan[5] = g.tail_tiles;
+  plan[6] = g.tail_split;
+  plan[7] = g.tail_kb;
   return NVFP4_OK;
 }
 

@@ -110,6 +110,10 @@ constexpr int kSfStageBytes = 3 * kSfaGroupBytes;        // A + two B row blocks
 // wgrad at their algorithmic operand reads and cut dgrad's from 427 to 321 MB;
 // 64 and 96 MB groups are evicted before their reuse and re-read far more.
 constexpr double kGroupL2Bytes = 32.0e6;
+// A tail split pays for its partial stores and the separate reduction (a few
+// microseconds) only when it takes this many k-blocks (~0.3 us each on a
+// 256 x 256 tile) off the last wave.
+constexpr int kTailMinGainKb = 24;
 // BF16 output leaves through shared memory: each epilogue warp stages a
 // 32-row x 32-column chunk (64-byte rows, 64-byte swizzle) and a TMA store
 // writes it, so global writes are whole 64-byte row segments instead of one
@@ -190,27 +194,53 @@ struct GParams {
   int lora_kb;
   // split-K (single mode, FP32 kernel): unit = tile * split_k + s covers
   // k-blocks [s * kb_per_split, (s + 1) * kb_per_split) and stores its raw
-  // FP32 accumulator (alpha = 1) as a whole column-major 128 x 256 block at
-  // d + (s * num_tiles + tile) * BM * BN (element (r, c) at c * BM + r), so
-  // a warp's 32 lanes write 128 consecutive bytes per column; 1 = no split
+  // FP32 accumulator (alpha not applied) as a whole column-major 128 x 256
+  // block at part + (s * num_tiles + tile) * BM * BN (element (r, c) at
+  // c * BM + r), so a warp's 32 lanes write 128 consecutive bytes per
+  // column; 1 = no split
   int split_k;
   int kb_per_split;
+  // Tail split (pair mode): the tail_tiles tiles past the last whole wave of
+  // CTA pairs (tiles tail_first ..) are cut along K into pieces of tail_kb
+  // k-blocks; piece s of tail tile i is unit tail_first + s * tail_tiles + i
+  // and stores its raw accumulator like a split-K partial, one block per CTA
+  // of the pair at part + ((s * tail_tiles + i) * 2 + rank) * BM * BN, and
+  // a reduction launched after the kernel sums them into D.
+  // tail_tiles == 0: none.
+  int tail_first;
+  int tail_tiles;
+  int tail_kb;
+  float* part;  // FP32 partial blocks of split-K units and tail pieces
 };
 
-// Tile index and k-block range of a work unit.
+// Tile index, k-block range and partial block of a work unit; `part` says
+// whether the unit stores a raw partial accumulator instead of D.  SPLIT:
+// the kernel may split K (not with LoRA k-blocks or the quantising epilogue).
+template <bool SPLIT>
 __device__ __forceinline__ void unit_split(const GParams& p, int unit, int& tile, int& kb_lo, int& kb_hi,
-                                           int64_t& d_off) {
-  if (p.split_k > 1) {
+                                           int64_t& d_off, bool& part) {
+  if (SPLIT && p.split_k > 1) {
     tile = unit / p.split_k;
     const int s = unit - tile * p.split_k;
     kb_lo = s * p.kb_per_split;
     kb_hi = min(p.num_kb, kb_lo + p.kb_per_split);
     d_off = (static_cast<int64_t>(s) * p.num_tiles + tile) * (BM * BN);
+    part = true;
+  } else if (SPLIT && p.tail_tiles > 0 && unit >= p.tail_first) {
+    const int idx = unit - p.tail_first;
+    const int s = idx / p.tail_tiles;
+    const int i = idx - s * p.tail_tiles;
+    tile = p.tail_first + i;
+    kb_lo = s * p.tail_kb;
+    kb_hi = min(p.num_kb, kb_lo + p.tail_kb);
+    d_off = (static_cast<int64_t>(s) * p.tail_tiles + i) * (2 * BM * BN);
+    part = true;
   } else {
     tile = unit;
     kb_lo = 0;
     kb_hi = p.num_kb;
     d_off = 0;
+    part = false;
   }
 }
 
@@ -385,11 +415,31 @@ __device__ __forceinline__ void epilogue_half(const GParams& p, const CUtensorMa
                                               uint8_t* stg,
                                               uint64_t* acc_empty, uint32_t tmem, int m_blk,
                                               int n_blk, int q, int half, int lane, float alpha, uint32_t rank,
-                                              float s_dec, float rs, uint32_t& amax_bits, int64_t d_off) {
+                                              float s_dec, float rs, uint32_t& amax_bits, int64_t d_off,
+                                              bool part) {
   const int64_t row = static_cast<int64_t>(m_blk) * BM + q * 32 + lane;
   const int64_t col0 = static_cast<int64_t>(n_blk) * BN + half * kEpiCols;
   const uint32_t taddr = tmem + (static_cast<uint32_t>(q * 32) << 16) + kAccCol + half * kEpiCols;
-  if (!OUT_F32) {
+  if (!QUANT && part) {
+    // split-K partial or tail piece: raw accumulator, column-major block
+    // (coalesced across the warp's lanes, which hold consecutive rows);
+    // padding rows and columns of ragged tiles hold the zeros their
+    // out-of-range operands gave
+    float* blk = p.part + d_off + (PAIR ? static_cast<int64_t>(rank) * (BM * BN) : 0) +
+                 static_cast<int64_t>(half * kEpiCols) * BM + q * 32 + lane;
+#pragma unroll 1
+    for (int c = 0; c < kEpiCols / 32; ++c) {
+      uint32_t r[32];
+      ptx::tmem_ld_32x32b_x32(taddr + c * 32, r);
+      ptx::tmem_ld_wait();
+      ptx::tmem_ld_regs_ready(r);
+#pragma unroll
+      for (int j = 0; j < 32; ++j) blk[(c * 32 + j) * BM] = __uint_as_float(r[j]);
+    }
+    ptx::tc_fence_before();
+    __syncwarp();
+    if (lane == 0) arrive_leader<PAIR>(acc_empty, rank);
+  } else if (!OUT_F32) {
     uint32_t packed[kEpiCols / 2];
     QuantHalf qh;  // used by the quantising epilogue only
     qh.sfw[0] = qh.sfw[1] = 0u;
@@ -486,23 +536,6 @@ __device__ __forceinline__ void epilogue_half(const GParams& p, const CUtensorMa
       store_quantised(p, tmap_q, stg, qh, row, static_cast<int64_t>(m_blk) * BM + q * 32, col0, q, lane);
       amax_bits = max(amax_bits, qh.amax_bits);
     }
-  } else if (p.split_k > 1) {
-    // split-K partial: raw accumulator, column-major block (coalesced across
-    // the warp's lanes, which hold consecutive rows); padding rows and
-    // columns of ragged tiles hold the zeros their out-of-range operands gave
-    float* blk = static_cast<float*>(p.d) + d_off + static_cast<int64_t>(half * kEpiCols) * BM + q * 32 + lane;
-#pragma unroll 1
-    for (int c = 0; c < kEpiCols / 32; ++c) {
-      uint32_t r[32];
-      ptx::tmem_ld_32x32b_x32(taddr + c * 32, r);
-      ptx::tmem_ld_wait();
-      ptx::tmem_ld_regs_ready(r);
-#pragma unroll
-      for (int j = 0; j < 32; ++j) blk[(c * 32 + j) * BM] = __uint_as_float(r[j]);
-    }
-    ptx::tc_fence_before();
-    __syncwarp();
-    if (lane == 0) arrive_leader<PAIR>(acc_empty, rank);
   } else {
     float* drow = static_cast<float*>(p.d) + d_off + row * p.ldd;
 #pragma unroll 1
@@ -617,6 +650,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     ctl->abort = 0;
     ptx::fence_mbar_init();
   }
+  if (threadIdx.x == 0 && (p.split_k > 1 || p.tail_tiles > 0)) {
+    // the partial-sum reduction may be scheduled now: its CTAs take SMs as
+    // this grid's CTAs leave and wait for the whole grid before reading
+    ptx::griddep_launch_dependents();
+  }
   if (warp == 0 && lane == 0) {
     ptx::prefetch_tensormap(&tmap_a);
     ptx::prefetch_tensormap(&tmap_b);
@@ -656,7 +694,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int unit = unit0; unit < p.num_units && ok; unit += ustep) {
         int m_blk, n_blk, tile, kb_lo, kb_hi;
         int64_t d_off;
-        unit_split(p, unit, tile, kb_lo, kb_hi, d_off);
+        bool part;
+        unit_split<!QUANT && !LORA>(p, unit, tile, kb_lo, kb_hi, d_off, part);
         unit_coords<PAIR>(p, tile, rank, m_blk, n_blk);
         for (int kb = kb_lo; kb < kb_hi + lora_kb; ++kb) {
           if (!ptx::mbar_wait(&ctl->empty[stage], phase ^ 1u, abort_flag)) {
@@ -734,7 +773,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int unit = unit0; unit < p.num_units && ok; unit += ustep) {
         int m_blk, n_blk, tile, kb_lo, kb_hi;
         int64_t d_off;
-        unit_split(p, unit, tile, kb_lo, kb_hi, d_off);
+        bool part;
+        unit_split<!QUANT && !LORA>(p, unit, tile, kb_lo, kb_hi, d_off, part);
         unit_coords<PAIR>(p, tile, rank, m_blk, n_blk);
         const int64_t n_rows_left = p.N - static_cast<int64_t>(n_blk) * BN;
         const int nb_atoms = static_cast<int>(min(static_cast<int64_t>(2), (n_rows_left + 127) / 128));
@@ -795,7 +835,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int unit = unit0; unit < p.num_units && ok; unit += ustep) {
         int tile, kb_lo, kb_hi;
         int64_t d_off;
-        unit_split(p, unit, tile, kb_lo, kb_hi, d_off);
+        bool part;
+        unit_split<!QUANT && !LORA>(p, unit, tile, kb_lo, kb_hi, d_off, part);
         if (!ptx::mbar_wait(&ctl->acc_empty, acc_phase ^ 1u, abort_flag)) {
           fail(&ctl->abort, p, 3);
           break;
@@ -926,7 +967,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int unit = unit0; unit < p.num_units && ok; unit += ustep) {
       int tile, kb_lo, kb_hi;
       int64_t d_off;
-      unit_split(p, unit, tile, kb_lo, kb_hi, d_off);
+      bool part;
+      unit_split<!QUANT && !LORA>(p, unit, tile, kb_lo, kb_hi, d_off, part);
       for (int kb = kb_lo; kb < kb_hi; ++kb) {
         const int j = kb % kSfGroup;
         if ((j == 0 && !warp_wait(&ctl->sf_full[sstage], sphase, abort_flag, lane)) ||
@@ -975,8 +1017,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int q = warp & 3;              // TMEM lane quarter this warp may access
     const int half = (warp - 2) >> 2;    // which 128 columns of the tile it stores
     uint8_t* stg = smem + L::kEpiStg + (warp - 2) * kEpiStgBytes;  // this warp's output staging
-    // split-K partials are stored unscaled; the reduction applies alpha
-    const float alpha = p.split_k > 1 ? 1.0f : __fmul_rn(*p.a_scale, *p.b_scale);
+    // (partial accumulators are stored unscaled; their reduction applies alpha)
+    const float alpha = __fmul_rn(*p.a_scale, *p.b_scale);
     // quantising epilogue: tensor scale s = amax_in / 2688 (1 if that is
     // zero); a negative or non-finite amax_in is reported and nothing is
     // encoded
@@ -1004,7 +1046,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int unit = unit0; unit < p.num_units; unit += ustep) {
       int m_blk, n_blk, tile, kb_lo, kb_hi;
       int64_t d_off;
-      unit_split(p, unit, tile, kb_lo, kb_hi, d_off);
+      bool part;
+      unit_split<!QUANT && !LORA>(p, unit, tile, kb_lo, kb_hi, d_off, part);
       unit_coords<PAIR>(p, tile, rank, m_blk, n_blk);
       if (!warp_wait(&ctl->acc_full, acc_phase, abort_flag, lane)) {
         if (lane == 0) fail(&ctl->abort, p, 6);
@@ -1014,13 +1057,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       if constexpr (QUANT) {
         if (q_live)
           epilogue_half<OUT_F32, PAIR, true>(p, &tmap_d, &tmap_q, stg, &ctl->acc_empty, tmem, m_blk, n_blk, q, half, lane, alpha, rank,
-                                             s_dec, rs, amax_bits, d_off);
+                                             s_dec, rs, amax_bits, d_off, part);
         else
           epilogue_half<OUT_F32, PAIR, false>(p, &tmap_d, &tmap_q, stg, &ctl->acc_empty, tmem, m_blk, n_blk, q, half, lane, alpha, rank,
-                                              s_dec, rs, amax_bits, d_off);
+                                              s_dec, rs, amax_bits, d_off, part);
       } else {
         epilogue_half<OUT_F32, PAIR, false>(p, &tmap_d, &tmap_q, stg, &ctl->acc_empty, tmem, m_blk, n_blk, q, half, lane, alpha, rank,
-                                            s_dec, rs, amax_bits, d_off);
+                                            s_dec, rs, amax_bits, d_off, part);
       }
       acc_phase ^= 1u;
     }
@@ -1097,45 +1140,136 @@ bool make_qcodes_map(CUtensorMap* map, uint8_t* codes, int64_t M, int64_t N) {
   return r == CUDA_SUCCESS;
 }
 
-// Split-K reduction: D[m, n] = RN(alpha * (((P0 + P1) + P2) + ...)) over the
-// split_k partial accumulators, in that fixed order, alpha = RN(sA * sB);
-// BF16 (round to nearest even) or FP32 output, row stride ldd.  Partials are
-// column-major 128 x 256 blocks per (split, tile) (element (r, c) of tile t
-// of split s at ((s * tiles + t) * 256 + c) * 128 + r; M <= 128).  A block of
-// 32 x 8 threads sums a 32-row x 32-column piece reading down columns and
-// writes it along rows through a shared-memory transpose.
+// Reduction of partial accumulators: D[m, n] = RN(alpha * (((P0 + P1) + P2)
+// + ...)) over the `split` partial blocks of each output block, in that
+// fixed order, alpha = RN(sA * sB); BF16 (round to nearest even) or FP32
+// output, row stride ldd.  Every 128 x 256 output block h (blockIdx.z) has
+// one column-major partial block per split s at part + (s * blocks + h) *
+// BM * BN (element (r, c) at c * BM + r).  Split-K (single mode, M <= 128):
+// block h is column block h.  Tail pieces (pair mode): block h is the half
+// h & 1 of tail tile h >> 1, placed by the tile raster.  A CTA of 256
+// threads sums a 32-row x 32-column piece: each thread reads four rows of
+// one column from every split with 16-byte loads (eight splits in flight),
+// and the sums leave along rows through a shared-memory transpose.
 template <bool OUT_F32>
-__global__ void __launch_bounds__(256) splitk_reduce_kernel(const float* __restrict__ part, int split_k, int tiles,
-                                                            int64_t M, int64_t N, const float* a_scale,
-                                                            const float* b_scale, void* d, int64_t ldd) {
-  __shared__ float sm[32][33];
-  const float alpha = __fmul_rn(*a_scale, *b_scale);
-  const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
-  const int64_t n0 = static_cast<int64_t>(blockIdx.x) * 32;  // 32 output columns
-  const int r0 = static_cast<int>(blockIdx.y) * 32;          // 32 output rows
-  const int64_t split_stride = static_cast<int64_t>(tiles) * BN * BM;
-  for (int j = ty; j < 32; j += 8) {
-    const int64_t n = n0 + j;
-    float acc = 0.0f;
-    if (n < N) {
-      const int64_t t = n / BN, c = n - t * BN;
-      const float* src = part + (t * BN + c) * BM + r0 + tx;
-      acc = src[0];
-      for (int sp = 1; sp < split_k; ++sp) acc = __fadd_rn(acc, src[sp * split_stride]);
-    }
-    sm[j][tx] = acc;  // column j, row tx
+__global__ void __launch_bounds__(256) partial_reduce_kernel(const float* __restrict__ part, int split, int blocks,
+                                                             const GParams p, void* d, int64_t ldd) {
+  __shared__ float sm[32][33];  // [column][row]
+  const int h = static_cast<int>(blockIdx.z);
+  int m_blk = 0, n_blk = h;
+  if (p.tail_tiles > 0) {
+    int mp;
+    tile_coords(p, p.tail_first + (h >> 1), p.tiles_mp, mp, n_blk);
+    m_blk = 2 * mp + (h & 1);
   }
+  const int r0 = static_cast<int>(blockIdx.y) * 32, c0 = static_cast<int>(blockIdx.x) * 32;
+  const int64_t row0 = static_cast<int64_t>(m_blk) * BM + r0, col0 = static_cast<int64_t>(n_blk) * BN + c0;
+  if (row0 >= p.M || col0 >= p.N) return;  // block-uniform
+  ptx::griddep_wait();  // the GEMM grid's partials (launched as its programmatic dependent)
+  const float alpha = __fmul_rn(*p.a_scale, *p.b_scale);
+  const int t = static_cast<int>(threadIdx.x);
+  const int cc = t >> 3, rq = (t & 7) * 4;  // column cc, rows rq .. rq + 3 of the piece
+  const int64_t split_stride = static_cast<int64_t>(blocks) * BM * BN;
+  const float* src = part + static_cast<int64_t>(h) * BM * BN + static_cast<int64_t>(c0 + cc) * BM + r0 + rq;
+  float4 acc = __ldcg(reinterpret_cast<const float4*>(src));
+  for (int s0 = 1; s0 < split; s0 += 8) {
+    float4 v[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k)
+      if (s0 + k < split) v[k] = __ldcg(reinterpret_cast<const float4*>(src + (s0 + k) * split_stride));
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      if (s0 + k < split) {
+        acc.x = __fadd_rn(acc.x, v[k].x);
+        acc.y = __fadd_rn(acc.y, v[k].y);
+        acc.z = __fadd_rn(acc.z, v[k].z);
+        acc.w = __fadd_rn(acc.w, v[k].w);
+      }
+    }
+  }
+  sm[cc][rq] = acc.x;
+  sm[cc][rq + 1] = acc.y;
+  sm[cc][rq + 2] = acc.z;
+  sm[cc][rq + 3] = acc.w;
   __syncthreads();
-  for (int i = ty; i < 32; i += 8) {
-    const int64_t m = r0 + i, n = n0 + tx;
-    if (m < M && n < N) {
-      const float v = __fmul_rn(alpha, sm[tx][i]);
-      if (OUT_F32)
-        static_cast<float*>(d)[m * ldd + n] = v;
-      else
-        static_cast<__nv_bfloat16*>(d)[m * ldd + n] = __float2bfloat16_rn(v);
+  // thread t writes row t / 8, columns (t % 8) * 4 .. + 3
+  const int r = t >> 3, cs = (t & 7) * 4;
+  const int64_t m = row0 + r, n = col0 + cs;
+  if (m >= p.M || n >= p.N) return;
+  float v[4];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) v[k] = __fmul_rn(alpha, sm[cs + k][r]);
+  const bool whole = n + 4 <= p.N && p.vec_store;
+  if (OUT_F32) {
+    float* drow = static_cast<float*>(d) + m * ldd;
+    if (whole) {
+      *reinterpret_cast<float4*>(drow + n) = make_float4(v[0], v[1], v[2], v[3]);
+    } else {
+#pragma unroll
+      for (int k = 0; k < 4; ++k)
+        if (n + k < p.N) drow[n + k] = v[k];
+    }
+  } else {
+    __nv_bfloat16* drow = static_cast<__nv_bfloat16*>(d) + m * ldd;
+    if (whole) {
+      *reinterpret_cast<uint2*>(drow + n) = make_uint2(pack_bf16(v[0], v[1]), pack_bf16(v[2], v[3]));
+    } else {
+#pragma unroll
+      for (int k = 0; k < 4; ++k)
+        if (n + k < p.N) drow[n + k] = __float2bfloat16_rn(v[k]);
     }
   }
+}
+
+// Launched right after the GEMM kernel as its programmatic dependent, so its
+// launch overlaps the GEMM's last wave.
+template <bool OUT_F32>
+cudaError_t launch_partial_reduce(const GParams& p, int split, int blocks, cudaStream_t stream) {
+  cudaLaunchConfig_t cfg{};
+  cudaLaunchAttribute attr{};
+  attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr.val.programmaticStreamSerializationAllowed = 1;
+  cfg.gridDim = dim3(BN / 32, BM / 32, static_cast<unsigned>(blocks));
+  cfg.blockDim = dim3(256);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cfg.attrs = &attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, partial_reduce_kernel<OUT_F32>, static_cast<const float*>(p.part), split, blocks,
+                            p, p.d, p.ldd);
+}
+
+// Tail split of a pair-mode GEMM run by `clusters` CTA pairs: when the tiles
+// past the last whole wave would leave at least half the pairs idle, each is
+// cut along K into `split` pieces of `kb` k-blocks (whole scale stages), one
+// piece per pair, so the last wave ends after a fraction of a tile's
+// k-blocks; the pieces' partial accumulators are then summed by a separate
+// reduction.  Tiles [first, first + tiles) are the split ones.
+struct TailPlan {
+  int first, tiles, split, kb;
+};
+
+bool plan_tail(int units, int clusters, int num_kb, TailPlan* t) {
+  if (units <= 0 || clusters < 2) return false;
+  const int rem = units % clusters;
+  if (rem == 0 || num_kb < 2 * kSfGroup) return false;
+  int s = std::min(clusters / rem, num_kb / kSfGroup);
+  if (s < 2) return false;
+  int per = (num_kb + s - 1) / s;
+  per = (per + kSfGroup - 1) / kSfGroup * kSfGroup;
+  s = (num_kb + per - 1) / per;
+  if (s < 2 || num_kb - per < kTailMinGainKb) return false;
+  t->first = units - rem;
+  t->tiles = rem;
+  t->split = s;
+  t->kb = per;
+  return true;
+}
+
+// FP32 partial blocks of a tail split: two 128 x 256 blocks (one per CTA of
+// the pair) per piece.
+size_t tail_bytes(const TailPlan& t) {
+  return static_cast<size_t>(t.tiles) * t.split * 2 * BM * BN * sizeof(float);
 }
 
 cudaLaunchAttribute pair_cluster_attr() {
@@ -1147,43 +1281,52 @@ cudaLaunchAttribute pair_cluster_attr() {
   return attr;
 }
 
-template <bool OUT_F32, bool PAIR, bool QUANT, bool LORA = false>
-cudaError_t launch_typed(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& md,
-                         const CUtensorMap& mq, const CUtensorMap& mlu, const CUtensorMap& ml2, GParams p,
-                         cudaStream_t stream) {
+// One-time setup per device of one kernel instantiation (the shared-memory
+// opt-in and, in pair mode, the number of co-resident clusters), safe against
+// concurrent first calls; *max_clusters = co-resident CTA pairs (1 in single
+// mode).
+template <bool OUT_F32, bool PAIR, bool QUANT, bool LORA>
+cudaError_t kernel_setup(int* max_clusters) {
   using L = Layout<PAIR>;
   auto kernel = gemm_kernel<OUT_F32, PAIR, QUANT, LORA>;
-  // One-time setup per device (the shared-memory opt-in and, in pair mode,
-  // the number of co-resident clusters), safe against concurrent first calls.
   static std::mutex setup_mutex;
   static int clusters_of_device[64] = {0};  // 0: not set up yet
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  int max_clusters = 0;
-  {
-    std::lock_guard<std::mutex> lock(setup_mutex);
-    if (clusters_of_device[dev] == 0) {
-      e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmemBytes);
+  std::lock_guard<std::mutex> lock(setup_mutex);
+  if (clusters_of_device[dev] == 0) {
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    int mc = 1;
+    if (PAIR) {
+      cudaLaunchConfig_t cfg{};
+      cudaLaunchAttribute attr = pair_cluster_attr();
+      cfg.gridDim = dim3(2 * device_sm_count());
+      cfg.blockDim = dim3(kThreads);
+      cfg.dynamicSmemBytes = L::kSmemBytes;
+      cfg.attrs = &attr;
+      cfg.numAttrs = 1;
+      e = cudaOccupancyMaxActiveClusters(&mc, kernel, &cfg);
       if (e != cudaSuccess) return e;
-      int mc = 1;
-      if (PAIR) {
-        cudaLaunchConfig_t cfg{};
-        cudaLaunchAttribute attr = pair_cluster_attr();
-        cfg.gridDim = dim3(2 * device_sm_count());
-        cfg.blockDim = dim3(kThreads);
-        cfg.dynamicSmemBytes = L::kSmemBytes;
-        cfg.attrs = &attr;
-        cfg.numAttrs = 1;
-        e = cudaOccupancyMaxActiveClusters(&mc, kernel, &cfg);
-        if (e != cudaSuccess) return e;
-        if (mc < 1) return cudaErrorInvalidConfiguration;
-      }
-      clusters_of_device[dev] = mc;
+      if (mc < 1) return cudaErrorInvalidConfiguration;
     }
-    max_clusters = clusters_of_device[dev];
+    clusters_of_device[dev] = mc;
   }
+  *max_clusters = clusters_of_device[dev];
+  return cudaSuccess;
+}
+
+template <bool OUT_F32, bool PAIR, bool QUANT, bool LORA = false>
+cudaError_t launch_typed(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& md,
+                         const CUtensorMap& mq, const CUtensorMap& mlu, const CUtensorMap& ml2, GParams p,
+                         cudaStream_t stream, size_t part_bytes = 0) {
+  using L = Layout<PAIR>;
+  auto kernel = gemm_kernel<OUT_F32, PAIR, QUANT, LORA>;
+  int max_clusters = 0;
+  cudaError_t e = kernel_setup<OUT_F32, PAIR, QUANT, LORA>(&max_clusters);
+  if (e != cudaSuccess) return e;
   if (!PAIR) {
     p.num_units = p.num_tiles * (p.split_k > 1 ? p.split_k : 1);
     const int grid = std::min(p.num_units, device_sm_count());
@@ -1191,6 +1334,15 @@ cudaError_t launch_typed(const CUtensorMap& ma, const CUtensorMap& mb, const CUt
     return cudaGetLastError();
   }
   p.num_units = p.tiles_mp * p.tiles_n;
+  p.tail_tiles = 0;
+  TailPlan tp;
+  if (!QUANT && !LORA && p.part != nullptr && plan_tail(p.num_units, max_clusters, p.num_kb, &tp) &&
+      tail_bytes(tp) <= part_bytes) {
+    p.tail_first = tp.first;
+    p.tail_tiles = tp.tiles;
+    p.tail_kb = tp.kb;
+    p.num_units = tp.first + tp.tiles * tp.split;
+  }
   const int clusters = std::min(p.num_units, max_clusters);
   cudaLaunchConfig_t cfg{};
   cudaLaunchAttribute attr = pair_cluster_attr();
@@ -1200,7 +1352,10 @@ cudaError_t launch_typed(const CUtensorMap& ma, const CUtensorMap& mb, const CUt
   cfg.stream = stream;
   cfg.attrs = &attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kernel, ma, mb, md, mq, mlu, ml2, p);
+  e = cudaLaunchKernelEx(&cfg, kernel, ma, mb, md, mq, mlu, ml2, p);
+  if (e != cudaSuccess || p.tail_tiles == 0) return e;
+  // the tail tiles' D: their pieces summed in piece order
+  return launch_partial_reduce<OUT_F32>(p, tp.split, 2 * tp.tiles, stream);
 }
 
 }  // namespace
@@ -1228,6 +1383,46 @@ int gemm_split_k(int64_t M, int64_t N, int64_t K, int* kb_per_split) {
 size_t gemm_split_k_bytes(int64_t M, int64_t N, int split_k) {
   const int64_t tiles = ((M + BM - 1) / BM) * ((N + BN - 1) / BN);
   return static_cast<size_t>(split_k) * tiles * BM * BN * sizeof(float);
+}
+
+cudaError_t gemm_plan(int64_t M, int64_t N, int64_t K, size_t partial_bytes, GemmPlan* g) {
+  *g = GemmPlan{};
+  if (M <= 0 || N <= 0 || K <= 0) return cudaSuccess;
+  const int num_kb = static_cast<int>((K + BK - 1) / BK);
+  const int tiles_m = static_cast<int>((M + BM - 1) / BM), tiles_n = static_cast<int>((N + BN - 1) / BN);
+  g->split_k = 1;
+  g->kb_per_unit = num_kb;
+  if (tiles_m < 2) {
+    int per = 0;
+    const int sk = gemm_split_k(M, N, K, &per);
+    g->pair = 0;
+    g->units = tiles_m * tiles_n;
+    g->partial_bytes_needed = sk > 1 ? gemm_split_k_bytes(M, N, sk) : 0;
+    if (sk > 1 && partial_bytes >= g->partial_bytes_needed) {
+      g->split_k = sk;
+      g->kb_per_unit = per;
+      g->units *= sk;
+    }
+    g->ctas = std::min(g->units, device_sm_count());
+    return cudaSuccess;
+  }
+  int max_clusters = 0;
+  const cudaError_t e = kernel_setup<false, true, false, false>(&max_clusters);
+  if (e != cudaSuccess) return e;
+  g->pair = 1;
+  g->units = ((tiles_m + 1) / 2) * tiles_n;
+  TailPlan tp;
+  if (plan_tail(g->units, max_clusters, num_kb, &tp)) {
+    g->partial_bytes_needed = tail_bytes(tp);
+    if (partial_bytes >= g->partial_bytes_needed) {
+      g->tail_tiles = tp.tiles;
+      g->tail_split = tp.split;
+      g->tail_kb = tp.kb;
+      g->units = tp.first + tp.tiles * tp.split;
+    }
+  }
+  g->ctas = 2 * std::min(g->units, max_clusters);
+  return cudaSuccess;
 }
 
 cudaError_t launch_gemm(const GemmArgs& a, cudaStream_t stream) {
@@ -1288,20 +1483,12 @@ cudaError_t launch_gemm(const GemmArgs& a, cudaStream_t stream) {
       GParams q = p;
       q.split_k = sk;
       q.kb_per_split = per;
-      q.d = a.partial;
-      q.ldd = a.N;
-      q.vec_store = 0;
+      q.part = a.partial;
       q.tma_store = 0;
       cudaError_t e = launch_typed<true, false, false>(ma, mb, md, mq, mlu, ml2, q, stream);
       if (e != cudaSuccess) return e;
-      const dim3 grid(static_cast<unsigned>((a.N + 31) / 32), static_cast<unsigned>((a.M + 31) / 32));
-      if (a.out_f32)
-        splitk_reduce_kernel<true><<<grid, 256, 0, stream>>>(a.partial, sk, p.num_tiles, a.M, a.N, a.a_scale,
-                                                              a.b_scale, a.d, a.ldd);
-      else
-        splitk_reduce_kernel<false><<<grid, 256, 0, stream>>>(a.partial, sk, p.num_tiles, a.M, a.N, a.a_scale,
-                                                               a.b_scale, a.d, a.ldd);
-      return cudaGetLastError();
+      return a.out_f32 ? launch_partial_reduce<true>(q, sk, p.num_tiles, stream)
+                       : launch_partial_reduce<false>(q, sk, p.num_tiles, stream);
     }
   }
   if (a.lora_r > 0) {
@@ -1338,9 +1525,12 @@ cudaError_t launch_gemm(const GemmArgs& a, cudaStream_t stream) {
     return a.out_f32 ? launch_typed<true, false, false, true>(ma, mb, md, mq, mlu, ml2, p, stream)
                      : launch_typed<false, false, false, true>(ma, mb, md, mq, mlu, ml2, p, stream);
   }
-  if (pair)
-    return a.out_f32 ? launch_typed<true, true, false>(ma, mb, md, mq, mlu, ml2, p, stream)
-                     : launch_typed<false, true, false>(ma, mb, md, mq, mlu, ml2, p, stream);
+  if (pair) {
+    // the workspace past its header holds the tail split's partial blocks
+    p.part = a.partial;
+    return a.out_f32 ? launch_typed<true, true, false>(ma, mb, md, mq, mlu, ml2, p, stream, a.partial_bytes)
+                     : launch_typed<false, true, false>(ma, mb, md, mq, mlu, ml2, p, stream, a.partial_bytes);
+  }
   return a.out_f32 ? launch_typed<true, false, false>(ma, mb, md, mq, mlu, ml2, p, stream)
                    : launch_typed<false, false, false>(ma, mb, md, mq, mlu, ml2, p, stream);
 }

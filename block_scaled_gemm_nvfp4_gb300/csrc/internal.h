@@ -105,6 +105,20 @@ cudaError_t launch_gemm(const GemmArgs& a, cudaStream_t stream);
 int gemm_split_k(int64_t M, int64_t N, int64_t K, int* kb_per_split);
 // Bytes of split-K scratch for that many splits (whole 128 x 256 FP32 blocks).
 size_t gemm_split_k_bytes(int64_t M, int64_t N, int split_k);
+// How launch_gemm schedules a plain (no LoRA, no quantising epilogue) GEMM
+// shape given that many bytes of partial-sum scratch.
+struct GemmPlan {
+  int pair;                     // 1: CTA pairs on 256 x 256 tiles; 0: single CTAs on 128 x 256
+  int ctas;                     // CTAs launched
+  int units;                    // work units (tiles, split-K pieces or tail pieces)
+  int split_k;                  // single mode: K splits (1: none)
+  int kb_per_unit;              // k-blocks (256 of K) per split-K unit; num_kb otherwise
+  int tail_tiles;               // pair mode: tiles past the last whole wave cut along K (0: none)
+  int tail_split;               // pieces per tail tile
+  int tail_kb;                  // k-blocks per tail piece
+  size_t partial_bytes_needed;  // scratch the split would take (0: no split applies)
+};
+cudaError_t gemm_plan(int64_t M, int64_t N, int64_t K, size_t partial_bytes, GemmPlan* plan);
 
 // LoRA-SVD branch, first half (lora.cu): U = BF16(X L1^T) and the hi / lo
 // split of (beta / (sx sw)) U that the GEMM adds into its accumulator.

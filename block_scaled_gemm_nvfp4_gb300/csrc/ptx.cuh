@@ -77,6 +77,15 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
 }
 
 // ------------------------------------------------------------ TMA / bulk
+// Programmatic dependent launch: the next kernel on the stream (launched
+// with programmatic stream serialization) may be scheduled once every CTA of
+// this grid has issued launch_dependents or exited; griddep_wait in that
+// kernel blocks until this grid has completed and its memory is visible.
+// Both are no-ops for kernels launched without the attribute.
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(map) : "memory");
 }

@@ -230,16 +230,44 @@ nvfp4_status nvfp4_dequantize(const nvfp4_tensor* q, int32_t out_dtype, void* ou
  * Shape rules: K % 32 == 0; both operands' scales in NVFP4_SF_MMA layout;
  * codes 16-byte aligned; ldd >= N.  M, N are arbitrary (ragged tiles are
  * handled).  Workspace: nvfp4_gemm_workspace_size bytes: the status word,
- * and, for outputs of one 128-row block with too few tiles to occupy the
- * GPU (a decode-like M <= 128), FP32 scratch for split-K partial sums: K is
- * split into whole groups of 1024, each split's accumulator is stored
- * unscaled, and a reduction adds them in split order, multiplies by
- * sA * sB and converts.  A workspace holding only the 256-byte header runs
- * the same GEMM unsplit.
+ * and FP32 scratch for partial sums where K is split:
+ *   - outputs of one 128-row block with too few tiles to occupy the GPU (a
+ *     decode-like M <= 128): split-K over the whole output;
+ *   - M > 128 (CTA pairs on 256 x 256 tiles): when the tiles left after the
+ *     last whole wave of CTA pairs would leave at least half the pairs idle
+ *     and the split takes enough of K off that wave, each of those tiles is
+ *     cut along K into pieces, one per pair.
+ * K is split into whole groups of 1024; each piece's accumulator is stored
+ * unscaled, and a reduction adds a tile's pieces in piece order, multiplies
+ * by sA * sB and converts.  A workspace holding only the 256-byte header
+ * (or too small for the split) runs the same GEMM unsplit; nvfp4_gemm_plan
+ * reports the schedule.
  * Source: "Como o treinamento mixed-precision funciona com NVFP4" (NVFP4
  * operands, FP32 accumulators) on the JAX/MaxText page.
  */
 nvfp4_status nvfp4_gemm_workspace_size(int64_t M, int64_t N, int64_t K, size_t* bytes);
+
+/*
+ * nvfp4_gemm_plan: how nvfp4_gemm schedules D [M, N] = A [M, K] * B [N, K]^T
+ * on the current device given a workspace of workspace_bytes (the split
+ * rules are those of nvfp4_gemm above; the schedule does not change the
+ * result beyond the order of the FP32 sums).  Writes eight values to plan:
+ *   plan[0] 1: CTA pairs on 256 x 256 tiles; 0: single CTAs on 128 x 256 tiles
+ *   plan[1] CTAs launched (persistent, at most one per SM)
+ *   plan[2] work units (tiles, split-K pieces or tail pieces)
+ *   plan[3] split-K splits over the whole output (1: none; M <= 128 only)
+ *   plan[4] k-blocks of 256 per split-K unit (all of K when unsplit)
+ *   plan[5] tiles past the last whole wave cut along K (0: none; M > 128 only)
+ *   plan[6] pieces per such tile
+ *   plan[7] k-blocks of 256 per piece
+ * M, N or K == 0 gives all zeros.  The caller owns plan (8 values).  Errors:
+ * plan NULL or a negative size -> NVFP4_ERR_INVALID_ARG; K % 32 != 0 ->
+ * NVFP4_ERR_UNSUPPORTED_SHAPE; no usable CUDA device -> NVFP4_ERR_CUDA.
+ * Sets up the GEMM kernel for the device once (shared-memory opt-in,
+ * occupancy query); launches nothing.  The pages have no counterpart: it
+ * exposes a scheduling decision for tests and measurements.
+ */
+nvfp4_status nvfp4_gemm_plan(int64_t M, int64_t N, int64_t K, size_t workspace_bytes, int64_t* plan);
 nvfp4_status nvfp4_gemm(const nvfp4_tensor* a, const nvfp4_tensor* b, int32_t out_dtype, void* d,
                         int64_t ldd, void* workspace, size_t workspace_bytes, nvfp4_stream_t stream);
 

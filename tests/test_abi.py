@@ -102,6 +102,12 @@ def test_gemm_validation(lib):
     n = ctypes.c_size_t(0)
     assert lib.nvfp4_gemm_workspace_size(128, 128, 80, ctypes.byref(n)) == nv.NVFP4_ERR_UNSUPPORTED_SHAPE
     assert lib.nvfp4_gemm_workspace_size(128, 128, 128, ctypes.byref(n)) == 0 and n.value >= 4
+    plan = (ctypes.c_int64 * 8)(*range(1, 9))
+    assert lib.nvfp4_gemm_plan(256, 256, 1024, 1 << 20, None) == nv.NVFP4_ERR_INVALID_ARG
+    assert lib.nvfp4_gemm_plan(-1, 256, 1024, 1 << 20, plan) == nv.NVFP4_ERR_INVALID_ARG
+    assert lib.nvfp4_gemm_plan(256, 256, 1000, 1 << 20, plan) == nv.NVFP4_ERR_UNSUPPORTED_SHAPE
+    # an empty output has an empty schedule (no device needed)
+    assert lib.nvfp4_gemm_plan(0, 256, 1024, 1 << 20, plan) == 0 and list(plan) == [0] * 8
 
 
 def test_linear_validation(lib):

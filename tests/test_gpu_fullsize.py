@@ -90,14 +90,15 @@ def _tiles(M, N, K, limit=12):
         else:
             out += [(edge - 256, min(N - 256, 768)), (edge, min(N - 256, 1024))]
     # the tiles on both sides of the end of the first persistent wave (76 CTA
-    # pairs on 152 SMs) and the first tile of the last wave, in the kernel's
-    # tile order: groups of g units along the grouped axis, the grouped axis
-    # fastest inside a group
+    # pairs on 152 SMs), the first tile of the last wave and the last tile,
+    # in the kernel's tile order: groups of g units along the grouped axis,
+    # the grouped axis fastest inside a group (the last wave's tiles are the
+    # ones a tail split cuts along K)
     mu, tn = M // 256, N // 256
     slow_n, fast_n = (mu, tn) if by_cols else (tn, mu)
     units = mu * tn
     waves = []
-    for t in (75, 76, (units - 1) // 76 * 76):
+    for t in (75, 76, (units - 1) // 76 * 76, units - 1):
         if t >= units:
             continue
         grp, local = divmod(t, g * slow_n)

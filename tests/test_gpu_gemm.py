@@ -36,8 +36,11 @@ def _operand(codes, sf_rowmajor, scale, rows, k):
 
 
 @pytest.mark.parametrize("M,N,K", [(128, 256, 64), (128, 256, 256), (256, 256, 256), (200, 300, 96),
-                                   (1, 1, 32), (128, 512, 1024), (300, 700, 2080)])
+                                   (1, 1, 32), (128, 512, 1024), (300, 700, 2080), (512, 512, 8192),
+                                   (384, 300, 10240)])
 def test_unit_scales_exact(M, N, K):
+    # (the last two are cut along K into pieces, one per CTA pair: integer
+    # quarters keep every partial sum exact, so any summation order matches)
     rng = np.random.default_rng(M + N + K)
     ca = rng.integers(0, 16, size=(M, K), dtype=np.uint8)
     cb = rng.integers(0, 16, size=(N, K), dtype=np.uint8)
@@ -239,3 +242,64 @@ def test_mma_rate_measurement_runs():
         tf, cyc = nv.nvfp4_debug_mma_rate(kind, 256)
         assert 16.0 < cyc < 4096.0, (kind, cyc)
         assert 50.0 < tf < 50000.0, (kind, tf)
+
+
+def _tail_plan(M, N, K, clusters):
+    """The tail split nvfp4_gemm documents (include/nvfp4.h): tiles past the
+    last whole wave of CTA pairs, when they would leave at least half the
+    pairs idle, cut along K into whole groups of four 256-wide k-blocks, one
+    piece per pair, if that takes at least 24 k-blocks off the last wave."""
+    kb = -(-K // 256)
+    units = -(-M // 256) * -(-N // 256)
+    rem = units % clusters
+    if rem == 0 or kb < 8:
+        return 0, 0, 0
+    s = min(clusters // rem, kb // 4)
+    if s < 2:
+        return 0, 0, 0
+    per = -(-(-(-kb // s)) // 4) * 4
+    s = -(-kb // per)
+    if s < 2 or kb - per < 24:
+        return 0, 0, 0
+    return rem, s, per
+
+
+def _pair_clusters():
+    # CTA pairs the persistent GEMM launches on a shape with many tiles
+    return nv.nvfp4_gemm_plan(16384, 16384, 1024)["ctas"] // 2
+
+
+@pytest.mark.parametrize("shape", ["all-split", "last-wave", "odd-rows"])
+@pytest.mark.parametrize("out", ["f32", "bf16"])
+def test_tail_split_vs_oracle(shape, out):
+    C = _pair_clusters()
+    if shape == "all-split":      # fewer tiles than pairs: every tile cut along K
+        M, N, K = 512, 512, 8192
+    elif shape == "last-wave":    # one whole wave, then a few tiles cut; ragged rows, columns and K
+        M, N, K = 256 * (C // 10 + 1) - 200, 2404, 8320
+    else:                         # odd row blocks: the second pair's follower lies past M
+        M, N, K = 384, 300, 10240
+    tiles, split, per = _tail_plan(M, N, K, C)
+    assert tiles > 0, "this shape is expected to split"
+    plan = nv.nvfp4_gemm_plan(M, N, K)
+    assert plan["pair"] == 1 and (plan["tail_tiles"], plan["tail_split"], plan["tail_kb"]) == (tiles, split, per)
+    assert nv.nvfp4_gemm_plan(M, N, K, 256)["tail_tiles"] == 0  # header-only workspace: unsplit
+    a = syn.normal_bf16((M, K), seed=M + 17)
+    b = syn.normal_bf16((N, K), seed=N + 18)
+    qa, oa = _quantised(a)
+    qb, ob = _quantised(b, block=0, rounding=1, rht=1)
+    od = nv.NVFP4_OUT_F32 if out == "f32" else nv.NVFP4_OUT_BF16
+    ws = torch.zeros(nv.nvfp4_gemm_workspace_size(M, N, K), dtype=torch.uint8, device=DEV)
+    d = nv.nvfp4_gemm(qa, qb, out_dtype=od, workspace=ws)
+    d_plain = nv.nvfp4_gemm(qa, qb, out_dtype=od, workspace=torch.zeros(256, dtype=torch.uint8, device=DEV))
+    assert nv.nvfp4_check_device_status(ws) == nv.NVFP4_OK
+    # the oracle's GEMM definition (FP64 sum over its dequantised operands),
+    # summed by a library FP64 matmul for these long shapes
+    ref = oracle.dequantize(*oa, M, K) @ oracle.dequantize(*ob, N, K).T
+    for got in (d, d_plain):
+        g = got.float().cpu().numpy()
+        if out == "f32":
+            assert rel_err(g, ref) <= 1e-3
+        else:
+            assert bf16_within_one_ulp(g, ref)
+
