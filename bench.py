@@ -35,11 +35,12 @@ WORKLOAD = ("12B-hybrid MLP up-projection fprop+dgrad+wgrad, tokens 8192 (4x2048
             "X N(0,1), W N(0,0.02), dY N(0,1e-3); W 16x16, X/dY 1x16, wgrad operands RHT+SR")
 
 
-# DRAM bytes per GEMM launch (dram__bytes_read.sum + dram__bytes_write.sum from
-# one ncu capture of each of the step's three GEMM shapes, averaged like the
-# achieved rate), keyed by the SHA-256 prefix of the GEMM kernel's sources: a
-# changed kernel reports null until it is measured again.
-GEMM_TRAFFIC = {"b3320e1ce35a0430": 356243797}
+# DRAM bytes per GEMM call (dram__bytes_read.sum + dram__bytes_write.sum from
+# one ncu capture of each of the step's three GEMM shapes -- the GEMM kernel
+# plus, for dgrad and wgrad, the reduction of their last wave's K pieces --
+# averaged like the achieved rate), keyed by the SHA-256 prefix of the GEMM
+# kernel's sources: a changed kernel reports null until it is measured again.
+GEMM_TRAFFIC = {"3d1a2966cf9f94bd": 365575680}
 
 
 def _gemm_traffic():
