@@ -812,9 +812,17 @@ nvfp4_status nvfp4_qadamw_v_decode(const void* codes, const void* sf, const floa
 }
 
 // ------------------------------------------------------------ linear layer
-// Workspace: [header | quantiser scratch | operand A | operand B].
-static size_t linear_ws(int64_t am, int64_t bn, int64_t k) {
+// Workspace: [header | quantiser scratch | operand A | operand B | GEMM
+// partial sums]; the last part is optional (a workspace without it runs the
+// GEMM unsplit), so the minimum is linear_ws_min.
+static size_t linear_ws_min(int64_t am, int64_t bn, int64_t k) {
   return kWsHeaderBytes + kQuantScratchBytes + operand_bytes(am, k) + operand_bytes(bn, k);
+}
+static size_t linear_ws(int64_t am, int64_t bn, int64_t k) {
+  GemmPlan g;
+  size_t part = 0;
+  if (gemm_plan(am, bn, k, SIZE_MAX, &g) == cudaSuccess) part = align_up(g.partial_bytes_needed);
+  return linear_ws_min(am, bn, k) + part;
 }
 
 static nvfp4_status linear_shape(int32_t op, int64_t tokens, int64_t din, int64_t dout, int64_t* M, int64_t* N,
@@ -861,20 +869,22 @@ static nvfp4_status run_linear(int32_t op, const void* a_src, int64_t a_rows, in
   if (s != NVFP4_OK) return s;
   if (!workspace) return NVFP4_ERR_WORKSPACE;
   if (reinterpret_cast<uintptr_t>(workspace) & 255u) return NVFP4_ERR_INVALID_ARG;
-  if (workspace_bytes < linear_ws(M, N, K)) return NVFP4_ERR_WORKSPACE;
+  if (workspace_bytes < linear_ws_min(M, N, K)) return NVFP4_ERR_WORKSPACE;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   uint32_t* status = reinterpret_cast<uint32_t*>(ws);
   uint32_t* partials = reinterpret_cast<uint32_t*>(ws + kWsHeaderBytes);
   uint8_t* cursor = ws + kWsHeaderBytes + kQuantScratchBytes;
   QuantizedOperand qa = carve_operand(cursor, M, K);
   QuantizedOperand qb = carve_operand(cursor, N, K);
+  const size_t used = static_cast<size_t>(cursor - ws);  // the rest holds the GEMM's partial sums
   s = quantize_into(a_src, a_rows, a_cols, a_cols, ca, qa.codes, qa.sf, qa.scale, status, partials, stream);
   if (s != NVFP4_OK) return s;
   s = quantize_into(b_src, b_rows, b_cols, b_cols, cb, qb.codes, qb.sf, qb.scale, status, partials, stream);
   if (s != NVFP4_OK) return s;
   nvfp4_tensor ta{qa.codes, qa.sf, qa.scale, M, K, NVFP4_SF_MMA, 0};
   nvfp4_tensor tb{qb.codes, qb.sf, qb.scale, N, K, NVFP4_SF_MMA, 0};
-  return gemm_into(&ta, &tb, out_dtype, d, N, status, stream);
+  return gemm_into(&ta, &tb, out_dtype, d, N, status, stream, reinterpret_cast<float*>(cursor),
+                   workspace_bytes - used);
 }
 
 static nvfp4_quant_cfg role_cfg(const nvfp4_quant_cfg* user, const nvfp4_quant_cfg& dflt, int transpose) {

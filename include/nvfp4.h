@@ -429,7 +429,10 @@ nvfp4_status nvfp4_qadamw_v_decode(const void* codes, const void* sf, const floa
  *   dgrad:  dX = Q(dY) Q(W^T)^T        dY: 1x16 along dout, W^T: 16x16 along dout
  *   wgrad:  dW = Q(dY^T) Q(X^T)^T      dY^T, X^T: 1x16 along T, RHT + SR
  * Each wrapper quantises its two operands into its workspace, in the
- * orientation its GEMM needs, then runs nvfp4_gemm.  cfg_* may be NULL for
+ * orientation its GEMM needs, then runs nvfp4_gemm (with the rest of the
+ * workspace as its partial-sum scratch: nvfp4_linear_workspace_size includes
+ * what nvfp4_gemm_workspace_size adds for the GEMM's shape; a workspace
+ * without that part runs the GEMM unsplit).  cfg_* may be NULL for
  * the defaults above (seeds: rht_seed NVFP4_DEFAULT_RHT_SEED for every
  * operand, sr_seed 5 for dY^T and 6 for X^T in wgrad, sr_offset 0); a given
  * cfg is used as is except that the wrapper sets `transpose` (by role) and
