@@ -50,6 +50,12 @@
 // and L2, 64 columns per k-block, the byte layout of a k-block of codes) in
 // kind::f16 MMAs; the staging warps only take part in those stages'
 // barriers, and the epilogue's alpha scaling covers both terms.
+// Work units are handed out round-robin to the persistent CTAs (pairs).  When
+// K is split -- over the whole output for one-row-block outputs with too few
+// tiles (split-K), or for the tiles past the last whole wave of CTA pairs
+// (tail split) -- a unit covers whole scale stages of one tile's K and stores
+// its raw FP32 accumulator; partial_reduce_kernel, launched as this kernel's
+// programmatic dependent, sums a tile's partials in K order.
 // Every mbarrier wait is bounded; on a timeout the CTA records
 // NVFP4_ERR_TIMEOUT in the status word, drains its in-flight copies and MMAs,
 // frees TMEM and exits.
