@@ -241,7 +241,11 @@ nvfp4_status nvfp4_dequantize(const nvfp4_tensor* q, int32_t out_dtype, void* ou
  * unscaled, and a reduction adds a tile's pieces in piece order, multiplies
  * by sA * sB and converts.  A workspace holding only the 256-byte header
  * (or too small for the split) runs the same GEMM unsplit; nvfp4_gemm_plan
- * reports the schedule.
+ * reports the schedule.  The split depends on the current device (its SM
+ * count and how many CTA pairs fit at once), so nvfp4_gemm_workspace_size
+ * asks the device (setting the GEMM kernel up for it once, as the first
+ * nvfp4_gemm would); with no usable CUDA device it returns the header size,
+ * which is still valid and runs the GEMM unsplit.
  * Source: "Como o treinamento mixed-precision funciona com NVFP4" (NVFP4
  * operands, FP32 accumulators) on the JAX/MaxText page.
  */
