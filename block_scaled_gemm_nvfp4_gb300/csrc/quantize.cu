@@ -140,6 +140,31 @@ __device__ __forceinline__ void hadamard16(float (&v)[16]) {
   for (int j = 0; j < 16; ++j) v[j] = __fmul_rn(v[j], 0.25f);
 }
 
+// Largest |x'| of x' = 1/4 * H16 * v (v with the transform's signs already
+// applied) as FP32 bits, for the amax passes, without forming x': the last
+// butterfly's two outputs RN(a + b) and RN(a - b) have the larger magnitude
+// RN(|a| + |b|) (rounding to nearest is monotonic and odd), and the exact
+// scaling by 1/4 may follow the maximum because RN(m / 4) is monotonic in m.
+// Equal to run_absmax_bits after hadamard16 bit for bit on finite runs; a run
+// holding an infinity or NaN gives a value at or above the bits of infinity
+// either way, which is all the amax pass tests.
+__device__ __forceinline__ uint32_t hadamard16_absmax_bits(float (&v)[16]) {
+#pragma unroll
+  for (int s = 1; s < 8; s <<= 1) {
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      if (i & s) continue;
+      const float a = v[i], b = v[i + s];
+      v[i] = __fadd_rn(a, b);
+      v[i + s] = __fsub_rn(a, b);
+    }
+  }
+  uint32_t m = 0;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) m = max(m, abs_bits(__fadd_rn(fabsf(v[i]), fabsf(v[i + 8]))));
+  return abs_bits(__fmul_rn(__uint_as_float(m), 0.25f));
+}
+
 // Largest |v| of a run as FP32 bits; inf and NaN sort above every finite
 // value, which is how the amax pass detects them.
 __device__ __forceinline__ uint32_t run_absmax_bits(const float (&v)[16]) {
@@ -247,11 +272,11 @@ __device__ __forceinline__ uint32_t amax_tile(const uint8_t* stage, bool rht, co
     float v[16];
     if (rht) {
       load_run<COL, true>(stage, p, j0 + 2 * i, v, sgn);
-      hadamard16(v);
+      m = max(m, hadamard16_absmax_bits(v));
     } else {
       load_run<COL>(stage, p, j0 + 2 * i, v);
+      m = max(m, run_absmax_bits(v));
     }
-    m = max(m, run_absmax_bits(v));
   }
   return m;
 }
@@ -268,8 +293,7 @@ __device__ __forceinline__ void amax_tile_pair(const uint8_t* stage, const uint3
     float v[16];
     load_run<true, true>(stage, p, j0 + 2 * i, v, sgn);
     m_raw = max(m_raw, run_absmax_bits(v));
-    hadamard16(v);
-    m_rht = max(m_rht, run_absmax_bits(v));
+    m_rht = max(m_rht, hadamard16_absmax_bits(v));
   }
 }
 
@@ -569,9 +593,7 @@ __global__ void __launch_bounds__(kThreads) amax_cols_pair(const uint16_t* __res
       b[e] = __uint_as_float((w & 0xFFFF0000u) ^ sgn[e]);
     }
     m_raw = max(m_raw, max(run_absmax_bits(a), run_absmax_bits(b)));
-    hadamard16(a);
-    hadamard16(b);
-    m_rht = max(m_rht, max(run_absmax_bits(a), run_absmax_bits(b)));
+    m_rht = max(m_rht, max(hadamard16_absmax_bits(a), hadamard16_absmax_bits(b)));
     grp += step_grp;
     cp += step_cp;
     if (cp >= pairs) {
