@@ -303,3 +303,26 @@ def test_tail_split_vs_oracle(shape, out):
         else:
             assert bf16_within_one_ulp(g, ref)
 
+
+
+@pytest.mark.parametrize("pitch", [528, 523], ids=["aligned-rows", "odd-rows"])
+@pytest.mark.parametrize("out", ["f32", "bf16"])
+def test_tail_split_padded_output(pitch, out):
+    # the K-split tiles' reduction writes D through a padded row stride (16-byte
+    # rows: vector stores; odd pitch: element stores) and nothing past M or N
+    M, N, K = 512, 520, 8192
+    assert nv.nvfp4_gemm_plan(M, N, K)["tail_tiles"] > 0, "this shape is expected to split"
+    a = syn.normal_bf16((M, K), seed=31)
+    b = syn.normal_bf16((N, K), seed=32)
+    qa, oa = _quantised(a)
+    qb, ob = _quantised(b)
+    dt = torch.float32 if out == "f32" else torch.bfloat16
+    big = torch.full((M + 8, pitch), 7.0, dtype=dt, device=DEV)
+    nv.nvfp4_gemm(qa, qb, out_dtype=nv.NVFP4_OUT_F32 if out == "f32" else nv.NVFP4_OUT_BF16, d=big[:M, :N])
+    host = big.float().cpu().numpy()
+    assert np.all(host[:, N:] == 7.0) and np.all(host[M:, :] == 7.0)
+    ref = oracle.dequantize(*oa, M, K) @ oracle.dequantize(*ob, N, K).T
+    if out == "f32":
+        assert rel_err(host[:M, :N], ref) <= 1e-3
+    else:
+        assert bf16_within_one_ulp(host[:M, :N], ref)
